@@ -1,0 +1,398 @@
+"""Pins of the CPU oracle to things other than itself (CPU only).
+
+Each test checks the oracle against what the pages and the mathematics fix:
+hand-worked examples (tests/golden, each with its citation), closed forms,
+invariants, brute force on tiny inputs and independent library routines
+(torch's own bf16/e4m3 decoders, numpy's stable sort).  They are chosen so that
+a plausible slip in the oracle -- a dropped ReLU, a weight applied inside the
+ReLU, a transposed operand or index, a wrong mask bound, a wrong tie-break,
+an off-by-one in the paged addressing -- fails at least one of them.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from top_selection_dsa_gb300 import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _num(v):
+    if isinstance(v, str):
+        return {"-inf": -math.inf, "inf": math.inf, "nan": math.nan,
+                "-0.0": -0.0}[v]
+    return float(v)
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def bf16(x):
+    return wl.to_bf16_bits(np.asarray(x, dtype=np.float32))
+
+
+# ------------------------------------------------------------------ decoders
+
+def test_e4m3_decoder_exhaustive_matches_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    mine = oracle.e4m3_to_f64(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(mine[ok], ref[ok])
+    assert np.array_equal(np.signbit(mine[ok]), np.signbit(ref[ok]))
+    assert np.isnan(mine).sum() == 2          # S.1111.111 only
+
+
+def test_e4m3_decoder_golden_codes():
+    g = _load("e4m3_codes.json")
+    for code, val in g["codes"].items():
+        got = oracle.e4m3_to_f64([int(code, 16)])[0]
+        want = _num(val)
+        if math.isnan(want):
+            assert math.isnan(got), code
+        else:
+            assert got == want and math.copysign(1, got) == math.copysign(1, want), code
+
+
+def test_bf16_decoder_matches_torch():
+    rng = np.random.default_rng(1)
+    bits = np.concatenate([
+        rng.integers(0, 1 << 16, 4096).astype(np.uint16),
+        np.array([0x0000, 0x8000, 0x7F80, 0xFF80, 0x0001, 0x7F7F, 0x3F80], np.uint16)])
+    mine = oracle.bf16_to_f64(bits)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(mine[ok], ref[ok])
+
+
+# -------------------------------------------------------------------- logits
+
+def test_logits_hand_example():
+    g = _load("logits_hand_example.json")
+    got = oracle.logits(bf16(g["q"]), bf16(g["k"]), np.array(g["w"], np.float32),
+                        np.array(g["row_starts"], np.int32),
+                        np.array(g["row_ends"], np.int32))
+    want = np.array([[_num(v) for v in r] for r in g["logits"]])
+    assert np.array_equal(got, want)
+
+
+def test_logits_one_hot_is_kronecker_delta():
+    # H=1, w=1, q[t]=e_i(t), k[s]=e_j(s)  =>  logit = [i(t) == j(s)]
+    rng = np.random.default_rng(2)
+    T, S, D = 9, 13, 16
+    it = rng.integers(0, D, T)
+    js = rng.integers(0, D, S)
+    q = np.zeros((T, 1, D), np.float32)
+    q[np.arange(T), 0, it] = 1
+    k = np.zeros((S, D), np.float32)
+    k[np.arange(S), js] = 1
+    rs = np.zeros(T, np.int32)
+    re = np.full(T, S, np.int32)
+    got = oracle.logits(bf16(q), bf16(k), np.ones((T, 1), np.float32), rs, re)
+    assert np.array_equal(got, (it[:, None] == js[None, :]).astype(np.float64))
+
+
+def test_logits_relu_factor_closed_form():
+    # q[t,h,:] = (h+1) e0, k[s,:] = (s-c) e0: all dots share the sign of s-c,
+    # so logit[t,s] = max(0, s-c) * sum_h (h+1) w[t,h]  (zero for s <= c).
+    T, S, H, D, c = 5, 12, 4, 8, 6
+    rng = np.random.default_rng(3)
+    q = np.zeros((T, H, D), np.float32)
+    q[:, :, 0] = np.arange(1, H + 1)[None, :]
+    k = np.zeros((S, D), np.float32)
+    k[:, 0] = np.arange(S) - c
+    w = rng.integers(-8, 9, (T, H)).astype(np.float32) / 4
+    got = oracle.logits(bf16(q), bf16(k), w, np.zeros(T, np.int32), np.full(T, S, np.int32))
+    W = (w.astype(np.float64) * np.arange(1, H + 1)).sum(1)
+    want = np.maximum(0, np.arange(S) - c)[None, :] * W[:, None]
+    assert np.array_equal(got, want)
+
+
+def test_logits_alternating_heads_closed_form():
+    # q[t,h,:] = (-1)^h e0, k[s,:] = b_s e0: the ReLU keeps the even heads when
+    # b_s > 0 and the odd heads when b_s < 0, so
+    # logit = |b_s| * sum_{h even} w  or  |b_s| * sum_{h odd} w.
+    T, S, H, D = 3, 6, 6, 4
+    q = np.zeros((T, H, D), np.float32)
+    q[:, :, 0] = np.array([(-1) ** h for h in range(H)])[None, :]
+    b = np.array([2, -3, 0.5, -1, 0, 4], np.float32)
+    k = np.zeros((S, D), np.float32)
+    k[:, 0] = b
+    w = np.array([[1, 2, 3, 4, 5, 6], [-1, 0, 2, 0, -3, 1], [0.5, -0.5, 1, -1, 2, -2]],
+                 np.float32)
+    got = oracle.logits(bf16(q), bf16(k), w, np.zeros(T, np.int32), np.full(T, S, np.int32))
+    even = w[:, 0::2].astype(np.float64).sum(1)
+    odd = w[:, 1::2].astype(np.float64).sum(1)
+    want = np.where(b[None, :] > 0, b[None, :] * even[:, None],
+                    np.abs(b)[None, :] * odd[:, None])
+    assert np.array_equal(got, want)
+
+
+def test_logits_negative_weights_give_nonpositive_scores():
+    # w < 0 multiplies a ReLU output, so every logit is <= 0 (applying the
+    # weight inside the ReLU would make them >= 0 instead).
+    p = wl.prefill(16, 16, 4, 64, 4, seed=4)
+    w = -np.abs(p.w)
+    got = oracle.logits(p.q, p.k, w, p.row_starts, p.row_ends)
+    fin = np.isfinite(got)
+    assert fin.sum() == p.valid_pairs()
+    assert (got[fin] <= 0).all() and (got[fin] < 0).any()
+
+
+def test_logits_all_negative_dots_are_exact_zero():
+    T, S, H, D = 4, 5, 3, 8
+    q = np.abs(np.random.default_rng(5).standard_normal((T, H, D))).astype(np.float32)
+    k = -np.abs(np.random.default_rng(6).standard_normal((S, D))).astype(np.float32)
+    w = np.random.default_rng(7).standard_normal((T, H)).astype(np.float32)
+    got = oracle.logits(bf16(q), bf16(k), w, np.zeros(T, np.int32), np.full(T, S, np.int32))
+    assert np.array_equal(got, np.zeros((T, S)))
+
+
+def test_logits_masking_and_clamping():
+    T, S = 6, 10
+    p = wl.prefill(T, S, 2, 64, 4, np.zeros(T, np.int32), np.full(T, S, np.int32), seed=8)
+    rs = np.array([0, 3, -4, 7, 5, 2], np.int32)
+    re = np.array([10, 5, 2, 30, 5, 1], np.int32)
+    full = oracle.logits(p.q, p.k, p.w, np.zeros(T, np.int32), np.full(T, S, np.int32))
+    got = oracle.logits(p.q, p.k, p.w, rs, re)
+    for t in range(T):
+        lo, hi = max(rs[t], 0), min(re[t], S)
+        for s in range(S):
+            if lo <= s < hi:
+                assert got[t, s] == full[t, s]
+            else:
+                assert got[t, s] == -math.inf
+    assert np.isneginf(got[4]).all() and np.isneginf(got[5]).all()
+
+
+def test_logits_linear_in_weights():
+    p = wl.prefill(12, 12, 8, 64, 4, seed=9)
+    w2 = np.random.default_rng(10).standard_normal(p.w.shape).astype(np.float32)
+    a = oracle.logits(p.q, p.k, p.w, p.row_starts, p.row_ends)
+    b = oracle.logits(p.q, p.k, w2, p.row_starts, p.row_ends)
+    c = oracle.logits(p.q, p.k, p.w.astype(np.float64) + w2, p.row_starts, p.row_ends)
+    fin = np.isfinite(a)
+    # w1 + w2 is rounded to fp32 by the call; compare within that rounding.
+    assert np.allclose(c[fin], (a + b)[fin], rtol=1e-6, atol=1e-9)
+
+
+def test_logits_positive_homogeneity_in_keys():
+    p = wl.prefill(8, 8, 4, 64, 4, seed=11)
+    k2 = wl.to_bf16_bits(2 * wl.bf16_bits_to_f32(p.k))      # exact in bf16
+    a = oracle.logits(p.q, p.k, p.w, p.row_starts, p.row_ends)
+    b = oracle.logits(p.q, k2, p.w, p.row_starts, p.row_ends)
+    fin = np.isfinite(a)
+    assert np.array_equal(b[fin], 2 * a[fin])
+
+
+def test_logits_e4m3_equals_bf16_of_the_same_values():
+    # Every e4m3 value is exact in bf16; torch converts codes -> bf16
+    # independently of the oracle's decoder.  The block scales enter as the
+    # k_scale/q_scale arguments on both sides.
+    p = wl.prefill(10, 10, 4, 128, 4, seed=12, dtype=wl.E4M3)
+    qb = torch.from_numpy(p.q).view(torch.float8_e4m3fn).to(torch.bfloat16)
+    kb = torch.from_numpy(p.k).view(torch.float8_e4m3fn).to(torch.bfloat16)
+    qb = qb.view(torch.int16).numpy().view(np.uint16)
+    kb = kb.view(torch.int16).numpy().view(np.uint16)
+    sq = np.exp2(np.random.default_rng(13).integers(-3, 3, (10, 4))).astype(np.float32)
+    a = oracle.logits(p.q, p.k, p.w, p.row_starts, p.row_ends, dtype=oracle.E4M3,
+                      q_scale=sq, k_scale=p.k_scale)
+    b = oracle.logits(qb, kb, p.w, p.row_starts, p.row_ends, dtype=oracle.BF16,
+                      q_scale=sq, k_scale=p.k_scale)
+    assert np.array_equal(a, b)
+
+
+def test_logits_scale_commutes_with_relu():
+    # relu(s*x) = s*relu(x) for s > 0: a power-of-two key scale multiplies
+    # the logit exactly.
+    p = wl.prefill(8, 8, 4, 128, 4, seed=14, dtype=wl.E4M3)
+    one = np.ones_like(p.k_scale)
+    a = oracle.logits(p.q, p.k, p.w, p.row_starts, p.row_ends, dtype=oracle.E4M3,
+                      k_scale=one)
+    b = oracle.logits(p.q, p.k, p.w, p.row_starts, p.row_ends, dtype=oracle.E4M3,
+                      k_scale=p.k_scale)
+    fin = np.isfinite(a)
+    sk = np.broadcast_to(p.k_scale[None, :].astype(np.float64), a.shape)
+    assert np.array_equal(b[fin], a[fin] * sk[fin])
+
+
+# --------------------------------------------------------------------- paged
+
+def test_paged_hand_example():
+    g = _load("paged_hand_example.json")
+    kc = bf16(g["k_cache"])
+    got = oracle.logits_paged(bf16(g["q"]), np.array(g["w"], np.float32), kc,
+                              np.array(g["block_table"], np.int32),
+                              np.array(g["context_lens"], np.int32),
+                              next_n=g["next_n"], ld=3)
+    want = np.array([[_num(v) for v in r] for r in g["logits"]])
+    assert np.array_equal(got, want)
+    rs, re = oracle.paged_row_ranges(np.array(g["context_lens"], np.int32), g["next_n"])
+    assert rs.tolist() == g["row_starts"] and re.tolist() == g["row_ends"]
+    for kk, exp in g["topk"].items():
+        assert oracle.topk(got.astype(np.float32), rs, re, int(kk)).tolist() == exp
+
+
+def test_paged_row_ranges_closed_form():
+    rs, re = oracle.paged_row_ranges(np.array([5, 1, 100], np.int32), 3)
+    assert rs.tolist() == [0] * 9
+    assert re.tolist() == [3, 4, 5, 0, 0, 1, 98, 99, 100]
+
+
+def test_paged_equals_contiguous_on_gathered_keys():
+    p = wl.paged_decode(B=3, next_n=2, ctx_lo=40, ctx_hi=300, block_size=16,
+                        H=4, D=64, topk=8, seed=15)
+    ld = p.max_ctx()
+    got = oracle.logits_paged(p.q, p.w, p.k_cache, p.block_table, p.context_lens,
+                              next_n=2, ld=ld)
+    rs, re = oracle.paged_row_ranges(p.context_lens, 2)
+    for b in range(p.B):
+        L = int(p.context_lens[b])
+        pos = np.arange(L)
+        kg = p.k_cache[p.block_table[b, pos // 16], pos % 16]     # [L, D]
+        rows = slice(2 * b, 2 * b + 2)
+        ref = oracle.logits(p.q[rows], kg, p.w[rows], rs[rows], re[rows])
+        assert np.array_equal(got[rows, :L], ref)
+        assert np.isneginf(got[rows, L:]).all()
+
+
+def test_paged_identity_table_equals_contiguous_causal_tail():
+    # One request, identity block table: the next_n rows are the last next_n
+    # rows of a causal prefill over the same keys.
+    L, n, bs = 50, 3, 8
+    p = wl.prefill(L, L, 2, 64, 4, seed=16)
+    nb = -(-L // bs)
+    kc = np.zeros((nb * bs, 64), np.uint16)
+    kc[:L] = p.k
+    got = oracle.logits_paged(p.q[L - n:], p.w[L - n:], kc.reshape(nb, bs, 64),
+                              np.arange(nb, dtype=np.int32)[None, :],
+                              np.array([L], np.int32), next_n=n, ld=L)
+    ref = oracle.logits(p.q, p.k, p.w, p.row_starts, p.row_ends)[L - n:]
+    assert np.array_equal(got, ref)
+
+
+# --------------------------------------------------------------------- top-k
+
+def test_topk_hand_examples():
+    g = _load("topk_semantics.json")
+    for c in g["cases"]:
+        row = np.array([[_num(v) for v in c["logits"]]], np.float32)
+        got = oracle.topk(row, np.array([c["row_start"]], np.int32),
+                          np.array([c["row_end"]], np.int32), c["k"])
+        assert got[0].tolist() == c["expect"], c["why"]
+    h = _load("logits_hand_example.json")
+    lg = np.array([[_num(v) for v in r] for r in h["logits"]], np.float32)
+    for kk, exp in h["topk"].items():
+        got = oracle.topk(lg, np.array(h["row_starts"], np.int32),
+                          np.array(h["row_ends"], np.int32), int(kk))
+        assert got.tolist() == exp
+
+
+def _brute_force_topk(row, lo, hi, k):
+    """Enumerate every subset of the valid columns: keep the one whose values,
+    sorted high to low, are largest, and among equal value lists the one whose
+    columns, sorted, are smallest."""
+    valid = [c for c in range(lo, hi) if not (math.isnan(row[c]) or row[c] == -math.inf)]
+    m = min(k, len(valid))
+    best = None
+    for sub in itertools.combinations(valid, m):
+        vals = sorted((float(row[c]) for c in sub), reverse=True)
+        key = (vals, [-c for c in sorted(sub)])
+        if best is None or key > best[0]:
+            best = (key, sorted(sub))
+    return best[1] + [-1] * (k - m)
+
+
+def test_topk_brute_force_on_tie_heavy_rows():
+    rng = np.random.default_rng(17)
+    pool = np.array([-1.0, 0.0, -0.0, 1.0, 2.0, np.inf, -np.inf, np.nan, 0.5], np.float32)
+    for trial in range(300):
+        n = int(rng.integers(1, 10))
+        row = pool[rng.integers(0, len(pool), n)]
+        lo = int(rng.integers(-2, n))
+        hi = int(rng.integers(lo, n + 3))
+        k = int(rng.integers(1, n + 3))
+        got = oracle.topk(row[None, :], np.array([lo], np.int32),
+                          np.array([hi], np.int32), k)[0].tolist()
+        want = _brute_force_topk(row, max(lo, 0), min(hi, n), k)
+        assert got == want, (row, lo, hi, k)
+
+
+def test_topk_matches_numpy_stable_sort():
+    rng = np.random.default_rng(18)
+    T, S = 40, 300
+    lg = rng.integers(-20, 20, (T, S)).astype(np.float32) / 4   # many ties
+    rs = rng.integers(0, S, T).astype(np.int32)
+    re = (rs + rng.integers(0, S, T)).astype(np.int32)
+    for k in (1, 7, 64, 299):
+        got = oracle.topk(lg, rs, re, k)
+        for t in range(T):
+            lo, hi = rs[t], min(re[t], S)
+            cols = np.arange(lo, hi)
+            order = np.argsort(-lg[t, lo:hi], kind="stable")   # desc, ties by column
+            pick = np.sort(cols[order[:k]])
+            want = np.full(k, -1, np.int32)
+            want[:len(pick)] = pick
+            assert np.array_equal(got[t], want)
+
+
+def test_topk_invariants_random():
+    rng = np.random.default_rng(19)
+    T, S, k = 64, 500, 50
+    lg = rng.standard_normal((T, S)).astype(np.float32)
+    lg[rng.random((T, S)) < 0.05] = -np.inf
+    rs = rng.integers(-10, S, T).astype(np.int32)
+    re = (rs + rng.integers(-5, 120, T)).astype(np.int32)
+    out = oracle.topk(lg, rs, re, k)
+    for t in range(T):
+        lo, hi = max(rs[t], 0), min(max(re[t], 0), S)
+        valid = [c for c in range(lo, hi) if np.isfinite(lg[t, c]) or lg[t, c] == np.inf]
+        sel = [c for c in out[t] if c != -1]
+        assert len(sel) == min(k, len(valid))
+        assert all(c == -1 for c in out[t][len(sel):])             # -1 only at tail
+        assert sel == sorted(set(sel))                              # ascending, unique
+        assert all(lo <= c < hi for c in sel)
+        unsel = set(valid) - set(sel)
+        for i in sel:                                               # exchange property
+            for j in unsel:
+                assert lg[t, i] > lg[t, j] or (lg[t, i] == lg[t, j] and i < j)
+
+
+def test_topk_never_selects_dirty_columns_outside_range():
+    # vime PR #502 review: garbage in invalid columns must not be picked.
+    T, S, k = 8, 64, 16
+    rng = np.random.default_rng(20)
+    lg = rng.standard_normal((T, S)).astype(np.float32)
+    rs = np.arange(T, dtype=np.int32) * 4
+    re = rs + 10
+    dirty = lg.copy()
+    for t in range(T):
+        dirty[t, :rs[t]] = np.inf
+        dirty[t, re[t]:] = 1e30
+    a = oracle.topk(lg, rs, re, k)
+    b = oracle.topk(dirty, rs, re, k)
+    assert np.array_equal(a, b)
+    assert (b[:, 10:] == -1).all()
+
+
+def test_topk_closed_forms():
+    S = 100
+    inc = np.arange(S, dtype=np.float32)[None, :]
+    dec = -inc
+    const = np.zeros((1, S), np.float32)
+    rs, re = np.array([10], np.int32), np.array([90], np.int32)
+    assert oracle.topk(inc, rs, re, 5)[0].tolist() == [85, 86, 87, 88, 89]
+    assert oracle.topk(dec, rs, re, 5)[0].tolist() == [10, 11, 12, 13, 14]
+    assert oracle.topk(const, rs, re, 5)[0].tolist() == [10, 11, 12, 13, 14]
+    assert oracle.topk(inc, rs, re, 80)[0].tolist() == list(range(10, 90))
+    assert oracle.topk(inc, rs, re, 83)[0].tolist() == list(range(10, 90)) + [-1] * 3
