@@ -1,0 +1,219 @@
+/*
+ * dsa.h -- C ABI of the GB300 (sm_103a) DSA lightning-indexer library.
+ *
+ * The library computes the two stages of the DeepSeek sparse-attention
+ * lightning indexer on one GPU:
+ *
+ *   1. index logits   logit[t,s] = sum_h w[t,h] * max(0, q[t,h,:] . k[s,:])
+ *      for the key columns s of query row t's range, -inf elsewhere.  This is
+ *      the quantity KimiK3DSAIndexer.score hands to
+ *      torch.ops.vllm.sparse_attn_indexer (vLLM API docs,
+ *      "vllm.models.kimi_k3.nvidia.dsa"): index_q [T,H,D], one index_k row
+ *      [D] shared by all heads, per-head weights [T,H] into which the query
+ *      scale and the softmax/head scales have already been folded.
+ *   2. masked top-k   for every row, the index_topk best columns inside
+ *      [row_start, row_end), written as int32 and padded with -1 wherever
+ *      fewer valid keys exist -- the semantics of torch_dsa_topk as corrected
+ *      in GitHub "vllm-project/vime" pull request #502 (third review comment),
+ *      written into a caller-owned buffer like the model-level
+ *      topk_indices_buffer of KimiK3DSAAttention.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor pointers are DEVICE memory owned by the caller, dense and
+ *    row-major.  The library keeps no pointer after the call returns, frees
+ *    nothing and allocates no device memory; scratch space is the caller's
+ *    `workspace` (size from dsa_workspace_bytes).
+ *  - Every call is asynchronous on `stream` (NULL = legacy default stream).
+ *  - Element types (dsa_dtype_t): DSA_BF16 -> q and k are bf16 (2 bytes);
+ *    DSA_E4M3 -> q and k are OCP fp8 e4m3 codes (1 byte) with fp32
+ *    power-of-two block scales, one per D-element row (UE8M0 scales,
+ *    quant_block_size = index_head_dim, KimiK3DSAIndexer.__init__).
+ *  - Shapes: H (index heads) is a power of two in [1, 64] (the page's
+ *    DeepGEMM limit of 64 heads); D is 64 or 128 for bf16 and 128 for e4m3.
+ *  - Row ranges are half-open [row_start, row_end) and are clamped to [0, S);
+ *    an empty or inverted range gives an all -1 top-k row.
+ *  - Top-k output rows hold the selected column indices in ascending order,
+ *    then -1 up to k.  Ties go to the lower column; -0.0 equals +0.0; -inf
+ *    and NaN scores are never selected.
+ *  - Errors that can be detected on the host are returned before anything is
+ *    launched and leave every output untouched.  Asynchronous failures (a
+ *    CUDA error, or a device-side wait that gave up) surface as DSA_ERR_CUDA
+ *    from a later call, or from dsa_get_last_device_error().
+ *  - No C++ exception crosses this boundary.  All entry points are safe to
+ *    call from several host threads at once.
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* == cudaStream_t / CUstream */
+typedef struct CUstream_st* dsa_stream_t;
+
+typedef enum {
+    DSA_OK = 0,
+    DSA_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer, small workspace */
+    DSA_ERR_UNSUPPORTED = 2, /* valid request this build does not handle (H, D, dtype) */
+    DSA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
+    DSA_ERR_TIMEOUT = 4      /* a device-side wait gave up (see dsa_get_last_device_error) */
+} dsa_status_t;
+
+typedef enum { DSA_BF16 = 0, DSA_E4M3 = 1 } dsa_dtype_t;
+
+typedef enum {
+    DSA_OP_INDEXER_LOGITS = 0,
+    DSA_OP_TOPK = 1,
+    DSA_OP_INDEXER_TOPK = 2,
+    DSA_OP_INDEXER_LOGITS_PAGED = 3,
+    DSA_OP_INDEXER_TOPK_PAGED = 4
+} dsa_op_t;
+
+/* dsa_indexer_logits flag: also write -inf into every column of [0, S)
+ * outside the row's range (by default only the key tiles the row touches are
+ * written, and columns of skipped tiles keep whatever the buffer held). */
+#define DSA_LOGITS_CLEAN 1u
+
+/*
+ * Index logits, contiguous keys (prefill; packed THD sequences use per-row
+ * ranges in packed coordinates, as the THD packing of the vime "Day-0 Model
+ * Plugins" page and the offset rebase of PR #502's first review comment do).
+ *
+ *   q          [T, H, D] bf16 or e4m3, 16-byte aligned
+ *   q_scale    NULL (scale folded into weights, as KimiK3DSAIndexer.score
+ *              does for fp8 queries) or [T, H] fp32 block scales
+ *   k          [S, D] same element type as q, 16-byte aligned
+ *   k_scale    [S] fp32 power-of-two scales for DSA_E4M3; must be NULL for bf16
+ *   weights    [T, H] fp32
+ *   row_starts, row_ends  [T] int32
+ *   logits     [T, ld] fp32 output, ld >= S.  For every row, the columns of
+ *              every 128-key tile that overlaps the union of the ranges of
+ *              the row's tile group are written (-inf outside the row's own
+ *              range); with DSA_LOGITS_CLEAN every column in [0, S) is.
+ *   flags      0 or DSA_LOGITS_CLEAN
+ * Accumulation is fp32 on tensor cores; the head sum runs in ascending head
+ * order, so dsa_indexer_topk's selection equals dsa_topk applied to these
+ * logits.
+ */
+dsa_status_t dsa_indexer_logits(const void* q, const float* q_scale, const void* k,
+                                const float* k_scale, dsa_dtype_t dtype,
+                                const float* weights, const int32_t* row_starts,
+                                const int32_t* row_ends, int T, int S, int H, int D,
+                                float* logits, int64_t ld, uint32_t flags,
+                                dsa_stream_t stream);
+
+/*
+ * Masked per-row top-k of given fp32 logits (torch_dsa_topk, vime PR #502).
+ *
+ *   logits     [T, ld] fp32, ld >= S; only columns in the clamped row range
+ *              are read, so the rest may hold anything
+ *   row_starts, row_ends  [T] int32
+ *   k          index_topk >= 1
+ *   out        [T, k] int32 output
+ *   workspace  may be NULL when ws_bytes == dsa_workspace_bytes(DSA_OP_TOPK, ...) == 0
+ */
+dsa_status_t dsa_topk(const float* logits, int64_t ld, const int32_t* row_starts,
+                      const int32_t* row_ends, int T, int S, int k, int32_t* out,
+                      void* workspace, size_t ws_bytes, dsa_stream_t stream);
+
+/*
+ * Index logits + masked top-k in one call (the sparse_attn_indexer op of
+ * KimiK3DSAIndexer.score, minus the cache insert).  Arguments as
+ * dsa_indexer_logits plus k/out of dsa_topk.  `workspace` must hold
+ * dsa_workspace_bytes(DSA_OP_INDEXER_TOPK, T, S, k) bytes, 256-byte aligned.
+ * The result equals dsa_topk(dsa_indexer_logits(...)) bit for bit.
+ */
+dsa_status_t dsa_indexer_topk(const void* q, const float* q_scale, const void* k,
+                              const float* k_scale, dsa_dtype_t dtype,
+                              const float* weights, const int32_t* row_starts,
+                              const int32_t* row_ends, int T, int S, int H, int D,
+                              int topk, int32_t* out, void* workspace, size_t ws_bytes,
+                              dsa_stream_t stream);
+
+/*
+ * Index logits of paged decode (the paged indexer K cache of
+ * KimiK3DSAIndexer: KimiK3IndexerCache / DeepseekV32IndexerCache).
+ *
+ *   q            [B*next_n, H, D]; query row r = b*next_n + j is token j of request b
+ *   q_scale      NULL or [B*next_n, H] fp32
+ *   weights      [B*next_n, H] fp32
+ *   k_cache      [num_blocks, block_size, D], 16-byte aligned
+ *   k_scale      NULL (bf16) or [num_blocks, block_size] fp32 (e4m3)
+ *   num_blocks   number of physical blocks in k_cache (>= 1)
+ *   block_table  [B, max_blocks] int32: physical block of each logical block;
+ *                an entry outside [0, num_blocks) is never dereferenced: block
+ *                0 is read in its place and the device error word records it
+ *                (dsa_get_last_device_error -> DSA_ERR_INVALID_ARG)
+ *   context_lens [B] int32, 0 <= L_b <= max_blocks*block_size; L_b counts the
+ *                request's next_n new tokens (a larger L_b is clamped and
+ *                recorded like a bad block id)
+ *   block_size   a power of two in [8, 128]
+ *   logits       [B*next_n, ld] fp32 over LOGICAL key positions,
+ *                ld >= max_blocks*block_size.  Row r = b*next_n + j sees keys
+ *                [0, L_b - next_n + j + 1); the columns of every 128-key tile
+ *                below L_b are written (-inf past the row's end).
+ * Only block-table entries of blocks below ceil(L_b / block_size) are read.
+ */
+dsa_status_t dsa_indexer_logits_paged(const void* q, const float* q_scale,
+                                      const float* weights, const void* k_cache,
+                                      const float* k_scale, int num_blocks,
+                                      dsa_dtype_t dtype,
+                                      const int32_t* block_table, int max_blocks,
+                                      const int32_t* context_lens, int B, int next_n,
+                                      int block_size, int H, int D, float* logits,
+                                      int64_t ld, dsa_stream_t stream);
+
+/*
+ * Paged decode logits + masked top-k.  Indices are logical positions within
+ * the request.  `workspace` must hold
+ * dsa_workspace_bytes(DSA_OP_INDEXER_TOPK_PAGED, B*next_n, max_blocks*block_size, k)
+ * bytes, 256-byte aligned.  out is [B*next_n, k] int32.
+ */
+dsa_status_t dsa_indexer_topk_paged(const void* q, const float* q_scale,
+                                    const float* weights, const void* k_cache,
+                                    const float* k_scale, int num_blocks,
+                                    dsa_dtype_t dtype,
+                                    const int32_t* block_table, int max_blocks,
+                                    const int32_t* context_lens, int B, int next_n,
+                                    int block_size, int H, int D, int topk,
+                                    int32_t* out, void* workspace, size_t ws_bytes,
+                                    dsa_stream_t stream);
+
+/*
+ * Scratch bytes an operation needs.  rows/cols are T/S for the prefill ops and
+ * B*next_n / max_blocks*block_size for the paged ones; k is index_topk.
+ * Returns 0 for operations that need none, and (size_t)-1 for bad arguments.
+ */
+size_t dsa_workspace_bytes(dsa_op_t op, int64_t rows, int64_t cols, int k);
+
+/* Static description of a status code (never NULL). */
+const char* dsa_status_string(dsa_status_t status);
+
+/*
+ * Synchronises the current device, then reports and clears the sticky
+ * device-side error word of the current device: DSA_ERR_TIMEOUT when a
+ * kernel's bounded wait gave up since the last call, DSA_ERR_INVALID_ARG when
+ * a paged call met a block id or context length out of range, DSA_ERR_CUDA
+ * when the synchronisation itself failed, else DSA_OK.
+ */
+dsa_status_t dsa_get_last_device_error(void);
+
+/*
+ * Failure-detection self test: launches one block whose thread waits on a
+ * shared-memory barrier that nothing ever arrives on, giving up after
+ * timeout_ns nanoseconds (clamped to [1e3, 1e9]).  The kernel then records a
+ * timeout in the device error word and returns normally, so the context
+ * stays usable; dsa_get_last_device_error() reports DSA_ERR_TIMEOUT.
+ */
+dsa_status_t dsa_selftest_wait_timeout(uint64_t timeout_ns, dsa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H_ */

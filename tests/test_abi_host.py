@@ -1,0 +1,150 @@
+"""The C-ABI library builds, loads and validates arguments on the host (no GPU).
+
+Only argument-validation paths are exercised: every call here is rejected
+before the library makes any CUDA call, so no device is needed.  Pointers are
+fake addresses that are never dereferenced.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def api():
+    from top_selection_dsa_gb300 import build
+    build.build()
+    from top_selection_dsa_gb300 import api as _api
+    return _api
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "dsa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsa_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for name in ("dsa_indexer_logits", "dsa_topk", "dsa_indexer_topk",
+                 "dsa_indexer_topk_paged", "dsa_workspace_bytes", "dsa_status_string",
+                 "dsa_get_last_device_error"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(api):
+    lib = ctypes.CDLL(api.LIB_PATH)
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    assert set(declared_symbols()) == set(api.EXPORTS)
+
+
+def test_status_strings(api):
+    for s in range(5):
+        assert api.status_string(s)
+    assert api.status_string(99) == "unknown status"
+
+
+def test_workspace_bytes(api):
+    wb = api.lib.dsa_workspace_bytes
+    assert wb(api.DSA_OP_INDEXER_LOGITS, 10, 10, 4) == 0
+    assert wb(api.DSA_OP_TOPK, 10, 10, 4) == 0
+    assert wb(api.DSA_OP_INDEXER_TOPK, 4096, 4096, 2048) == 4096 * 4096 * 4
+    assert wb(api.DSA_OP_INDEXER_TOPK, 3, 5, 1) == 3 * 8 * 4          # rows padded to 16 B
+    assert wb(api.DSA_OP_INDEXER_TOPK_PAGED, 128, 131072, 2048) == 128 * 131072 * 4
+    assert wb(api.DSA_OP_INDEXER_TOPK, 0, 100, 1) == 0
+    bad = ctypes.c_size_t(-1).value
+    assert wb(api.DSA_OP_INDEXER_TOPK, -1, 5, 1) == bad
+    assert wb(17, 1, 1, 1) == bad
+
+
+A = ctypes.c_void_p(0x10000)       # fake, 16-byte aligned, never dereferenced
+MIS = ctypes.c_void_p(0x10004)     # fake, misaligned for TMA
+NUL = None
+
+
+def logits_call(api, q=A, k=A, ks=NUL, dtype=0, w=A, rs=A, re=A, T=8, S=8, H=64, D=128,
+                out=A, ld=8, flags=0):
+    return api.lib.dsa_indexer_logits(q, NUL, k, ks, dtype, w, rs, re, T, S, H, D, out, ld,
+                                      flags, NUL)
+
+
+def test_indexer_logits_validation(api):
+    E, U = api.DSA_ERR_INVALID_ARG, api.DSA_ERR_UNSUPPORTED
+    assert logits_call(api, q=NUL) == E
+    assert logits_call(api, k=NUL) == E
+    assert logits_call(api, w=NUL) == E
+    assert logits_call(api, rs=NUL) == E
+    assert logits_call(api, out=NUL) == E
+    assert logits_call(api, T=-1) == E
+    assert logits_call(api, ld=7) == E                       # ld < S
+    assert logits_call(api, q=MIS) == E                      # TMA needs 16-byte alignment
+    assert logits_call(api, k=MIS) == E
+    assert logits_call(api, flags=2) == E
+    assert logits_call(api, dtype=5) == E
+    assert logits_call(api, H=3) == U
+    assert logits_call(api, H=128) == U                      # > 64 index heads
+    assert logits_call(api, D=96) == U
+    assert logits_call(api, dtype=1, ks=A, D=64) == U        # e4m3 needs D = 128
+    assert logits_call(api, dtype=1, ks=NUL) == E            # e4m3 needs key scales
+    assert logits_call(api, dtype=0, ks=A) == E              # bf16 takes none
+
+
+def test_topk_validation(api):
+    E = api.DSA_ERR_INVALID_ARG
+    f = api.lib.dsa_topk
+    assert f(NUL, 8, A, A, 4, 8, 2, A, NUL, 0, NUL) == E
+    assert f(A, 8, A, A, 4, 8, 0, A, NUL, 0, NUL) == E       # k < 1
+    assert f(A, 4, A, A, 4, 8, 2, A, NUL, 0, NUL) == E       # ld < S
+    assert f(A, 8, A, A, 4, 8, 2, NUL, NUL, 0, NUL) == E
+    assert f(A, 8, NUL, A, 4, 8, 2, A, NUL, 0, NUL) == E
+
+
+def test_indexer_topk_validation(api):
+    E = api.DSA_ERR_INVALID_ARG
+    f = api.lib.dsa_indexer_topk
+    need = api.lib.dsa_workspace_bytes(api.DSA_OP_INDEXER_TOPK, 8, 8, 2)
+    assert f(A, NUL, A, NUL, 0, A, A, A, 8, 8, 64, 128, 2, A, NUL, need, NUL) == E  # no ws
+    assert f(A, NUL, A, NUL, 0, A, A, A, 8, 8, 64, 128, 2, A, A, need - 1, NUL) == E
+    assert f(A, NUL, A, NUL, 0, A, A, A, 8, 8, 64, 128, 2, A, MIS, need, NUL) == E
+    assert f(A, NUL, A, NUL, 0, A, A, A, 8, 8, 64, 128, 0, A, A, need, NUL) == E
+    assert f(A, NUL, A, NUL, 0, A, A, A, 8, 8, 3, 128, 2, A, A, need, NUL) == \
+        api.DSA_ERR_UNSUPPORTED
+
+
+def paged_call(api, q=A, w=A, kc=A, ks=NUL, nblk=10, dtype=0, bt=A, maxb=4, cl=A, B=2,
+               next_n=2, bs=64, H=64, D=128, out=A, ld=256):
+    return api.lib.dsa_indexer_logits_paged(q, NUL, w, kc, ks, nblk, dtype, bt, maxb, cl, B,
+                                            next_n, bs, H, D, out, ld, NUL)
+
+
+def test_paged_validation(api):
+    E, U = api.DSA_ERR_INVALID_ARG, api.DSA_ERR_UNSUPPORTED
+    assert paged_call(api, bt=NUL) == E
+    assert paged_call(api, cl=NUL) == E
+    assert paged_call(api, kc=MIS) == E
+    assert paged_call(api, nblk=0) == E
+    assert paged_call(api, next_n=0) == E
+    assert paged_call(api, ld=255) == E                       # ld < max_blocks * block_size
+    assert paged_call(api, bs=48) == U                        # not a power of two
+    assert paged_call(api, bs=256) == U
+    assert paged_call(api, next_n=5) == U                     # 5 * 64 > 256 MMA columns
+    assert paged_call(api, H=4) == U
+    assert paged_call(api, dtype=1) == E                      # e4m3 without key scales
+    f = api.lib.dsa_indexer_topk_paged
+    need = api.lib.dsa_workspace_bytes(api.DSA_OP_INDEXER_TOPK_PAGED, 4, 256, 8)
+    assert f(A, NUL, A, A, NUL, 10, 0, A, 4, A, 2, 2, 64, 64, 128, 8, A, NUL, need, NUL) == E
+    assert f(A, NUL, A, A, NUL, 10, 0, A, 4, A, 2, 2, 64, 64, 128, 0, A, A, need, NUL) == E
+
+
+def test_binding_refuses_cpu_tensors(api):
+    import torch
+    q = torch.zeros(4, 64, 128, dtype=torch.bfloat16)
+    k = torch.zeros(4, 128, dtype=torch.bfloat16)
+    w = torch.zeros(4, 64)
+    r = torch.zeros(4, dtype=torch.int32)
+    with pytest.raises(ValueError):
+        api.indexer_logits(q, k, w, r, r)

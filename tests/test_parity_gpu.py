@@ -1,0 +1,312 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Two bars, fixed for the lightning-indexer path:
+  * logits: |gpu - oracle| <= 1e-3 + 2e-2 * |oracle| for every finite oracle
+    value, and -inf exactly where the oracle has -inf;
+  * top-k: bit-exact with the oracle's top-k run on the GPU's own logits.
+Full-size workloads compare sampled rows (the oracle computes them one by
+one) and check the top-k of every row the oracle can afford.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from top_selection_dsa_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+RTOL, ATOL = 2e-2, 1e-3
+
+
+@pytest.fixture(scope="module")
+def api():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from top_selection_dsa_gb300 import api as _api
+    return _api
+
+
+def dev(x):
+    t = torch.from_numpy(np.ascontiguousarray(x))
+    return t.cuda()
+
+
+def qk_tensors(p):
+    if p.dtype == wl.BF16:
+        return dev(p.q.view(np.int16)).view(torch.bfloat16), dev(p.k.view(np.int16)).view(torch.bfloat16)
+    return dev(p.q).view(torch.float8_e4m3fn), dev(p.k).view(torch.float8_e4m3fn)
+
+
+def prefill_inputs(p):
+    q, k = qk_tensors(p)
+    ks = dev(p.k_scale) if p.k_scale is not None else None
+    return q, k, dev(p.w), dev(p.row_starts), dev(p.row_ends), ks
+
+
+def assert_logits_close(gpu, ref, what=""):
+    g = np.asarray(gpu, dtype=np.float64)
+    r = np.asarray(ref, dtype=np.float64)
+    assert g.shape == r.shape
+    ninf = np.isneginf(r)
+    bad_inf = np.isneginf(g) != ninf
+    assert not bad_inf.any(), f"{what}: -inf mismatch at {np.argwhere(bad_inf)[:5].tolist()}"
+    fin = ~ninf
+    err = np.abs(g[fin] - r[fin])
+    bound = ATOL + RTOL * np.abs(r[fin])
+    if not (err <= bound).all():
+        i = int(np.argmax(err - bound))
+        raise AssertionError(f"{what}: logits differ: max excess {float((err - bound)[i]):.3g}, "
+                             f"gpu {g[fin][i]!r} oracle {r[fin][i]!r}; "
+                             f"{int((err > bound).sum())} of {err.size} outside tolerance")
+
+
+def oracle_logits(p, rows=None):
+    return oracle.logits(p.q, p.k, p.w, p.row_starts, p.row_ends, dtype=p.dtype,
+                         k_scale=p.k_scale, rows=rows)
+
+
+def sample_rows(T, n, seed=0, always=()):
+    rng = np.random.default_rng(seed)
+    rows = set(int(r) for r in rng.choice(T, size=min(n, T), replace=False))
+    rows.update(r for r in always if 0 <= r < T)
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+# ------------------------------------------------------------ failure detection
+
+def test_bounded_wait_reports_timeout(api):
+    assert api.last_device_error() == api.DSA_OK
+    api.selftest_wait_timeout(2_000_000)          # 2 ms; nothing ever arrives
+    assert api.last_device_error() == api.DSA_ERR_TIMEOUT
+    assert api.last_device_error() == api.DSA_OK  # the word is cleared
+    x = torch.ones(4, device="cuda")              # the context is still usable
+    assert float(x.sum()) == 4.0
+
+
+# ---------------------------------------------------------------- small parity
+
+def test_tiny_causal_logits_and_topk(api):
+    p = wl.tiny_causal()
+    q, k, w, rs, re, ks = prefill_inputs(p)
+    lg = api.indexer_logits(q, k, w, rs, re, clean=True)
+    g = lg.cpu().numpy()
+    assert_logits_close(g, oracle_logits(p), "tiny")
+    ref_idx = oracle.topk(g, p.row_starts, p.row_ends, p.topk)
+    got = api.topk(lg, rs, re, p.topk).cpu().numpy()
+    assert np.array_equal(got, ref_idx)
+    fused = api.indexer_topk(q, k, w, rs, re, p.topk).cpu().numpy()
+    assert np.array_equal(fused, ref_idx)
+    assert (fused[:p.topk - 1, -1] == -1).all()          # early rows padded
+
+
+@pytest.mark.parametrize("H,D", [(64, 128), (32, 128), (16, 64), (8, 128), (4, 64), (2, 128),
+                                 (1, 64)])
+def test_logits_heads_and_dims_ragged(api, H, D):
+    T = S = 333   # several key tiles, ragged tail, partial last token group
+    p = wl.prefill(T, S, H, D, 16, seed=H + D)
+    q, k, w, rs, re, ks = prefill_inputs(p)
+    g = api.indexer_logits(q, k, w, rs, re, clean=True).cpu().numpy()
+    assert_logits_close(g, oracle_logits(p), f"H={H} D={D}")
+    got = api.indexer_topk(q, k, w, rs, re, p.topk).cpu().numpy()
+    assert np.array_equal(got, oracle.topk(g, p.row_starts, p.row_ends, p.topk))
+
+
+def test_logits_non_causal_ranges_and_unclean_buffer(api):
+    T, S = 97, 1000
+    rng = np.random.default_rng(7)
+    rs = rng.integers(-50, S, T).astype(np.int32)
+    re = (rs + rng.integers(-20, 700, T)).astype(np.int32)
+    p = wl.prefill(T, S, 64, 128, 64, rs, re, seed=8)
+    q, k, w, rs_d, re_d, _ = prefill_inputs(p)
+    buf = torch.full((T, S + 3), 7.0, device="cuda")            # ld > S
+    api.indexer_logits(q, k, w, rs_d, re_d, logits=buf)
+    g = buf.cpu().numpy()[:, :S]
+    ref = oracle_logits(p)
+    for t in range(T):                                           # in-range columns only
+        lo, hi = max(rs[t], 0), min(max(re[t], 0), S)
+        if hi > lo:
+            assert_logits_close(g[t, lo:hi], ref[t, lo:hi], f"row {t}")
+    assert (buf.cpu().numpy()[:, S:] == 7.0).all()               # padding columns untouched
+    got = api.topk(buf, rs_d, re_d, p.topk, S=S).cpu().numpy()
+    assert np.array_equal(got, oracle.topk(buf.cpu().numpy(), rs, re, p.topk, S=S))
+
+
+def test_thd_small(api):
+    lens = [130, 1, 400, 257]
+    rs, re = wl.thd_ranges(lens)
+    T = sum(lens)
+    p = wl.prefill(T, T, 64, 128, 100, rs, re, seed=9)
+    q, k, w, rs_d, re_d, _ = prefill_inputs(p)
+    g = api.indexer_logits(q, k, w, rs_d, re_d, clean=True).cpu().numpy()
+    assert_logits_close(g, oracle_logits(p), "thd")
+    got = api.indexer_topk(q, k, w, rs_d, re_d, p.topk).cpu().numpy()
+    ref = oracle.topk(g, rs, re, p.topk)
+    assert np.array_equal(got, ref)
+    sel = got[got >= 0]
+    owner = np.repeat(np.arange(len(lens)), lens)
+    rows = np.nonzero(got >= 0)[0]
+    assert (owner[sel] == owner[rows]).all()                     # indices stay in-sequence
+
+
+def test_fp8_small(api):
+    p = wl.prefill(300, 300, 64, 128, 32, seed=10, dtype=wl.E4M3)
+    q, k, w, rs, re, ks = prefill_inputs(p)
+    g = api.indexer_logits(q, k, w, rs, re, k_scale=ks, clean=True).cpu().numpy()
+    assert_logits_close(g, oracle_logits(p), "fp8")
+    got = api.indexer_topk(q, k, w, rs, re, p.topk, k_scale=ks).cpu().numpy()
+    assert np.array_equal(got, oracle.topk(g, p.row_starts, p.row_ends, p.topk))
+
+
+def test_q_scale_argument(api):
+    p = wl.prefill(130, 130, 16, 128, 8, seed=11)
+    q, k, w, rs, re, _ = prefill_inputs(p)
+    sq = np.exp2(np.random.default_rng(12).integers(-2, 3, (130, 16))).astype(np.float32)
+    g = api.indexer_logits(q, k, w, rs, re, q_scale=dev(sq), clean=True).cpu().numpy()
+    ref = oracle.logits(p.q, p.k, p.w, p.row_starts, p.row_ends, q_scale=sq)
+    assert_logits_close(g, ref, "q_scale")
+
+
+# ---------------------------------------------------------------- top-k alone
+
+def test_topk_edge_cases(api):
+    rng = np.random.default_rng(13)
+    T, S, k = 12, 5000, 64
+    lg = rng.standard_normal((T, S)).astype(np.float32)
+    lg[1] = 0.0                                   # all ties
+    lg[2, ::2] = -0.0                              # signed-zero ties
+    lg[2, 1::2] = 0.0
+    lg[3, :] = -np.inf                             # nothing valid
+    lg[4, rng.random(S) < 0.5] = np.nan            # NaN never selected
+    lg[5] = np.round(lg[5] * 2) / 2                # heavy ties
+    lg[6, 100:200] = np.inf
+    rs = np.array([0, 0, 0, 0, 0, 0, 0, 10, 4000, 30, -5, 2], np.int32)
+    re = np.array([S, S, S, S, S, S, S, 10 + k, 4000 + k - 1, 20, 10 ** 6, 2], np.int32)
+    dirty = lg.copy()
+    for t in range(T):                             # garbage outside the ranges
+        dirty[t, :max(rs[t], 0)] = 1e30
+        dirty[t, min(max(re[t], 0), S):] = np.inf
+    got = api.topk(dev(dirty), dev(rs), dev(re), k).cpu().numpy()
+    ref = oracle.topk(dirty, rs, re, k)
+    assert np.array_equal(got, ref)
+    assert (got[3] == -1).all() and (got[9] == -1).all() and (got[11] == -1).all()
+    assert (got[7] == np.arange(10, 10 + k)).all()
+
+
+@pytest.mark.parametrize("S,k", [(131072, 2048), (60000, 2048), (2049, 2048), (2048, 2048),
+                                 (100, 1), (4096, 4096)])
+def test_topk_row_lengths(api, S, k):
+    rng = np.random.default_rng(S + k)
+    T = 6
+    lg = (rng.standard_normal((T, S)) * 4).round().astype(np.float32)   # many ties
+    rs = np.zeros(T, np.int32)
+    re = np.array([S, S - 1, S // 2, k, k - 1, 1], np.int32)
+    got = api.topk(dev(lg), dev(rs), dev(re), k).cpu().numpy()
+    assert np.array_equal(got, oracle.topk(lg, rs, re, k))
+
+
+# --------------------------------------------------------------------- paged
+
+@pytest.mark.parametrize("next_n,block_size,H,fp8", [(2, 64, 64, False), (1, 16, 64, False),
+                                                     (3, 128, 32, False), (4, 32, 64, False),
+                                                     (2, 64, 64, True), (1, 8, 16, True)])
+def test_paged_small(api, next_n, block_size, H, fp8):
+    ctx = np.array([1, next_n, 129, 500, 1000, 2047, 2048, 2049, 4000], np.int32)
+    ctx = np.maximum(ctx, next_n)
+    p = wl.paged_decode(next_n=next_n, block_size=block_size, H=H, D=128, topk=256,
+                        ctx_hi=4096, seed=next_n * block_size + H, context_lens=ctx,
+                        dtype=wl.E4M3 if fp8 else wl.BF16)
+    check_paged(api, p, rows=None)
+
+
+def paged_tensors(p):
+    if p.dtype == wl.BF16:
+        q = dev(p.q.view(np.int16)).view(torch.bfloat16)
+        kc = dev(p.k_cache.view(np.int16)).view(torch.bfloat16)
+    else:
+        q = dev(p.q).view(torch.float8_e4m3fn)
+        kc = dev(p.k_cache).view(torch.float8_e4m3fn)
+    ks = dev(p.k_scale.reshape(-1)) if p.k_scale is not None else None
+    return q, dev(p.w), kc, dev(p.block_table), dev(p.context_lens), ks
+
+
+def check_paged(api, p, rows=None):
+    q, w, kc, bt, cl, ks = paged_tensors(p)
+    lg = api.indexer_logits_paged(q, w, kc, bt, cl, next_n=p.next_n, k_scale=ks)
+    g = lg.cpu().numpy()
+    ref = oracle.logits_paged(p.q, p.w, p.k_cache, p.block_table, p.context_lens,
+                              next_n=p.next_n, dtype=p.dtype, k_scale=p.k_scale,
+                              ld=p.max_ctx(), rows=rows)
+    gg = g if rows is None else g[rows]
+    rs, re = oracle.paged_row_ranges(p.context_lens, p.next_n)
+    rr = np.arange(p.R) if rows is None else rows
+    for i, r in enumerate(rr):                     # the visited part of each row
+        hi = int(p.context_lens[r // p.next_n])
+        assert_logits_close(gg[i, :hi], ref[i, :hi], f"paged row {r}")
+    got = api.indexer_topk_paged(q, w, kc, bt, cl, p.topk, next_n=p.next_n, k_scale=ks)
+    got = got.cpu().numpy()
+    assert np.array_equal(got, oracle.topk(g, rs, re, p.topk))
+    assert api.last_device_error() == api.DSA_OK
+
+
+def test_paged_bad_block_id_is_reported_not_dereferenced(api):
+    p = wl.paged_decode(B=2, next_n=1, ctx_lo=200, ctx_hi=300, block_size=64, H=64,
+                        topk=16, seed=3)
+    bt = p.block_table.copy()
+    bt[1, 1] = 10 ** 6                              # past the cache
+    q, w, kc, _, cl, _ = paged_tensors(p)
+    api.indexer_logits_paged(q, w, kc, dev(bt), cl, next_n=1)
+    assert api.last_device_error() == api.DSA_ERR_INVALID_ARG
+    assert api.last_device_error() == api.DSA_OK
+
+
+# -------------------------------------------------------- full-size workloads
+
+def test_prefill_causal_4096_full_size(api):
+    p = wl.prefill_causal()
+    q, k, w, rs, re, _ = prefill_inputs(p)
+    lg = api.indexer_logits(q, k, w, rs, re, clean=True)
+    g = lg.cpu().numpy()
+    rows = sample_rows(p.T, 24, seed=1, always=(0, 1, 127, 128, 2047, 2048, 4095))
+    assert_logits_close(g[rows], oracle_logits(p, rows), "prefill 4096")
+    ref = oracle.topk(g, p.row_starts, p.row_ends, p.topk)
+    fused = api.indexer_topk(q, k, w, rs, re, p.topk).cpu().numpy()
+    assert np.array_equal(fused, ref)
+    assert np.array_equal(api.topk(lg, rs, re, p.topk).cpu().numpy(), ref)
+    assert (ref[2047:] != -1).all() and (ref[:2047, -1] == -1).all()
+
+
+def test_prefill_thd_full_size(api):
+    p = wl.prefill_thd()
+    q, k, w, rs, re, _ = prefill_inputs(p)
+    lg = api.indexer_logits(q, k, w, rs, re, clean=True)
+    g = lg.cpu().numpy()
+    offs = np.cumsum([0] + p.seq_lens)
+    edges = [o + d for o in offs[:-1] for d in (0, 1, 2047, 2048)] + [int(offs[-1]) - 1]
+    rows = sample_rows(p.T, 24, seed=2, always=edges)
+    assert_logits_close(g[rows], oracle_logits(p, rows), "thd")
+    fused = api.indexer_topk(q, k, w, rs, re, p.topk).cpu().numpy()
+    ref = oracle.topk(g, p.row_starts, p.row_ends, p.topk)
+    assert np.array_equal(fused, ref)
+
+
+def test_paged_decode_full_size(api):
+    p = wl.paged_decode()
+    check_paged(api, p, rows=sample_rows(p.R, 12, seed=3, always=(0, 1, p.R - 1)))
+
+
+def test_prefill_fp8_32768_full_size(api):
+    p = wl.prefill_fp8()
+    q, k, w, rs, re, ks = prefill_inputs(p)
+    lg = api.indexer_logits(q, k, w, rs, re, k_scale=ks)
+    rows = sample_rows(p.T, 16, seed=4, always=(0, 2047, 2048, 32767))
+    g = lg[torch.from_numpy(rows).cuda()].cpu().numpy()
+    ref = oracle_logits(p, rows)
+    for i, t in enumerate(rows):                   # written part: [0, t + 1)
+        assert_logits_close(g[i, :t + 1], ref[i, :t + 1], f"fp8 row {t}")
+    fused = api.indexer_topk(q, k, w, rs, re, p.topk, k_scale=ks)
+    got = fused[torch.from_numpy(rows).cuda()].cpu().numpy()
+    ref_idx = oracle.topk(g, p.row_starts[rows], p.row_ends[rows], p.topk)
+    assert np.array_equal(got, ref_idx)

@@ -1,0 +1,250 @@
+"""Thin ctypes binding over libdsa.so (include/dsa.h).
+
+Argument marshalling only: every function checks that its torch tensors are
+CUDA, contiguous and of the documented dtype, then passes raw device pointers,
+sizes and the current CUDA stream to the C ABI.  All arithmetic runs in the
+library's kernels.  Importing this module loads libdsa.so and raises if it has
+not been built -- there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdsa.so")
+
+# Mirrors of the enums in include/dsa.h.
+DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_CUDA, DSA_ERR_TIMEOUT = range(5)
+DSA_BF16, DSA_E4M3 = 0, 1
+(DSA_OP_INDEXER_LOGITS, DSA_OP_TOPK, DSA_OP_INDEXER_TOPK, DSA_OP_INDEXER_LOGITS_PAGED,
+ DSA_OP_INDEXER_TOPK_PAGED) = range(5)
+DSA_LOGITS_CLEAN = 1
+
+# Every entry point of include/dsa.h.
+EXPORTS = (
+    "dsa_indexer_logits", "dsa_topk", "dsa_indexer_topk", "dsa_indexer_logits_paged",
+    "dsa_indexer_topk_paged", "dsa_workspace_bytes", "dsa_status_string",
+    "dsa_get_last_device_error", "dsa_selftest_wait_timeout",
+)
+
+
+class DSAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is not built: run `python -m top_selection_dsa_gb300.build` "
+            "(nvcc, sm_103a). There is no CPU fallback.")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, I64, U32, U64, SZ = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint32,
+                               ctypes.c_uint64, ctypes.c_size_t)
+    lib.dsa_indexer_logits.argtypes = [P, P, P, P, I, P, P, P, I, I, I, I, P, I64, U32, P]
+    lib.dsa_topk.argtypes = [P, I64, P, P, I, I, I, P, P, SZ, P]
+    lib.dsa_indexer_topk.argtypes = [P, P, P, P, I, P, P, P, I, I, I, I, I, P, P, SZ, P]
+    lib.dsa_indexer_logits_paged.argtypes = [P, P, P, P, P, I, I, P, I, P, I, I, I, I, I, P,
+                                             I64, P]
+    lib.dsa_indexer_topk_paged.argtypes = [P, P, P, P, P, I, I, P, I, P, I, I, I, I, I, I, P,
+                                           P, SZ, P]
+    lib.dsa_workspace_bytes.argtypes = [I, I64, I64, I]
+    lib.dsa_workspace_bytes.restype = SZ
+    lib.dsa_status_string.argtypes = [I]
+    lib.dsa_status_string.restype = ctypes.c_char_p
+    lib.dsa_get_last_device_error.argtypes = []
+    lib.dsa_selftest_wait_timeout.argtypes = [U64, P]
+    for name in ("dsa_indexer_logits", "dsa_topk", "dsa_indexer_topk",
+                 "dsa_indexer_logits_paged", "dsa_indexer_topk_paged",
+                 "dsa_get_last_device_error", "dsa_selftest_wait_timeout"):
+        getattr(lib, name).restype = I
+    return lib
+
+
+lib = _load()
+
+
+def status_string(status: int) -> str:
+    return lib.dsa_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != DSA_OK:
+        raise DSAError(status, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need(t, name, dtypes, device=None):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} must have dtype in {dtypes}, got {t.dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+_E4M3_TYPES = (torch.float8_e4m3fn, torch.uint8)
+
+
+def _elem_dtype(q, k):
+    if q.dtype == torch.bfloat16 and k.dtype == torch.bfloat16:
+        return DSA_BF16
+    if q.dtype in _E4M3_TYPES and k.dtype in _E4M3_TYPES:
+        return DSA_E4M3
+    raise ValueError(f"q/k must both be bf16 or both e4m3, got {q.dtype}/{k.dtype}")
+
+
+def workspace_bytes(op: int, rows: int, cols: int, k: int) -> int:
+    n = lib.dsa_workspace_bytes(op, rows, cols, k)
+    if n == ctypes.c_size_t(-1).value:
+        raise ValueError("dsa_workspace_bytes: bad arguments")
+    return int(n)
+
+
+def _workspace(nbytes, device, workspace):
+    if nbytes == 0:
+        return workspace
+    if workspace is None:
+        return torch.empty(nbytes, dtype=torch.uint8, device=device)
+    if workspace.numel() * workspace.element_size() < nbytes:
+        raise ValueError(f"workspace holds {workspace.numel() * workspace.element_size()} "
+                         f"bytes, {nbytes} needed")
+    return workspace
+
+
+def indexer_logits(q, k, weights, row_starts, row_ends, *, q_scale=None, k_scale=None,
+                   logits=None, clean=False):
+    """fp32 index logits [T, ld] (ld = logits.shape[1] if given, else S)."""
+    dt = _elem_dtype(q, k)
+    T, H, D = q.shape
+    S = k.shape[0]
+    dev = q.device
+    for t, n, d in ((q, "q", (q.dtype,)), (k, "k", (k.dtype,)), (weights, "weights", (torch.float32,)),
+                    (row_starts, "row_starts", (torch.int32,)), (row_ends, "row_ends", (torch.int32,)),
+                    (q_scale, "q_scale", (torch.float32,)), (k_scale, "k_scale", (torch.float32,))):
+        _need(t, n, d, dev)
+    if logits is None:
+        logits = torch.empty((T, S), dtype=torch.float32, device=dev)
+    _need(logits, "logits", (torch.float32,), dev)
+    st = lib.dsa_indexer_logits(_ptr(q), _ptr(q_scale), _ptr(k), _ptr(k_scale), dt,
+                                _ptr(weights), _ptr(row_starts), _ptr(row_ends), T, S, H, D,
+                                _ptr(logits), logits.shape[1] if logits.dim() == 2 else S,
+                                DSA_LOGITS_CLEAN if clean else 0, _stream(dev))
+    _check(st, "dsa_indexer_logits")
+    return logits
+
+
+def topk(logits, row_starts, row_ends, k, *, S=None, out=None):
+    """Masked top-k [T, k] int32 of fp32 logits [T, ld] over columns [0, S)."""
+    T, ld = logits.shape
+    S = ld if S is None else S
+    dev = logits.device
+    _need(logits, "logits", (torch.float32,), dev)
+    _need(row_starts, "row_starts", (torch.int32,), dev)
+    _need(row_ends, "row_ends", (torch.int32,), dev)
+    if out is None:
+        out = torch.empty((T, k), dtype=torch.int32, device=dev)
+    _need(out, "out", (torch.int32,), dev)
+    st = lib.dsa_topk(_ptr(logits), ld, _ptr(row_starts), _ptr(row_ends), T, S, k, _ptr(out),
+                      None, 0, _stream(dev))
+    _check(st, "dsa_topk")
+    return out
+
+
+def indexer_topk(q, k, weights, row_starts, row_ends, topk_k, *, q_scale=None, k_scale=None,
+                 out=None, workspace=None):
+    """Index logits + masked top-k in one library call: [T, topk_k] int32."""
+    dt = _elem_dtype(q, k)
+    T, H, D = q.shape
+    S = k.shape[0]
+    dev = q.device
+    for t, n, d in ((q, "q", (q.dtype,)), (k, "k", (k.dtype,)), (weights, "weights", (torch.float32,)),
+                    (row_starts, "row_starts", (torch.int32,)), (row_ends, "row_ends", (torch.int32,)),
+                    (q_scale, "q_scale", (torch.float32,)), (k_scale, "k_scale", (torch.float32,))):
+        _need(t, n, d, dev)
+    if out is None:
+        out = torch.empty((T, topk_k), dtype=torch.int32, device=dev)
+    _need(out, "out", (torch.int32,), dev)
+    nbytes = workspace_bytes(DSA_OP_INDEXER_TOPK, T, S, topk_k)
+    ws = _workspace(nbytes, dev, workspace)
+    st = lib.dsa_indexer_topk(_ptr(q), _ptr(q_scale), _ptr(k), _ptr(k_scale), dt, _ptr(weights),
+                              _ptr(row_starts), _ptr(row_ends), T, S, H, D, topk_k, _ptr(out),
+                              _ptr(ws), nbytes, _stream(dev))
+    _check(st, "dsa_indexer_topk")
+    return out
+
+
+def _paged_common(q, weights, k_cache, block_table, context_lens, q_scale, k_scale):
+    dt = _elem_dtype(q, k_cache)
+    dev = q.device
+    for t, n, d in ((q, "q", (q.dtype,)), (k_cache, "k_cache", (k_cache.dtype,)),
+                    (weights, "weights", (torch.float32,)),
+                    (block_table, "block_table", (torch.int32,)),
+                    (context_lens, "context_lens", (torch.int32,)),
+                    (q_scale, "q_scale", (torch.float32,)), (k_scale, "k_scale", (torch.float32,))):
+        _need(t, n, d, dev)
+    return dt, dev
+
+
+def indexer_logits_paged(q, weights, k_cache, block_table, context_lens, *, next_n,
+                         q_scale=None, k_scale=None, logits=None):
+    """Paged-decode logits [B*next_n, ld] over logical key positions."""
+    dt, dev = _paged_common(q, weights, k_cache, block_table, context_lens, q_scale, k_scale)
+    R, H, D = q.shape
+    num_blocks, block_size, _ = k_cache.shape
+    B, max_blocks = block_table.shape
+    if logits is None:
+        logits = torch.empty((R, max_blocks * block_size), dtype=torch.float32, device=dev)
+    _need(logits, "logits", (torch.float32,), dev)
+    st = lib.dsa_indexer_logits_paged(_ptr(q), _ptr(q_scale), _ptr(weights), _ptr(k_cache),
+                                      _ptr(k_scale), num_blocks, dt, _ptr(block_table),
+                                      max_blocks, _ptr(context_lens), B, next_n, block_size, H,
+                                      D, _ptr(logits), logits.shape[1], _stream(dev))
+    _check(st, "dsa_indexer_logits_paged")
+    return logits
+
+
+def indexer_topk_paged(q, weights, k_cache, block_table, context_lens, topk_k, *, next_n,
+                       q_scale=None, k_scale=None, out=None, workspace=None):
+    """Paged-decode logits + masked top-k: [B*next_n, topk_k] logical positions."""
+    dt, dev = _paged_common(q, weights, k_cache, block_table, context_lens, q_scale, k_scale)
+    R, H, D = q.shape
+    num_blocks, block_size, _ = k_cache.shape
+    B, max_blocks = block_table.shape
+    if out is None:
+        out = torch.empty((R, topk_k), dtype=torch.int32, device=dev)
+    _need(out, "out", (torch.int32,), dev)
+    nbytes = workspace_bytes(DSA_OP_INDEXER_TOPK_PAGED, R, max_blocks * block_size, topk_k)
+    ws = _workspace(nbytes, dev, workspace)
+    st = lib.dsa_indexer_topk_paged(_ptr(q), _ptr(q_scale), _ptr(weights), _ptr(k_cache),
+                                    _ptr(k_scale), num_blocks, dt, _ptr(block_table), max_blocks,
+                                    _ptr(context_lens), B, next_n, block_size, H, D, topk_k,
+                                    _ptr(out), _ptr(ws), nbytes, _stream(dev))
+    _check(st, "dsa_indexer_topk_paged")
+    return out
+
+
+def last_device_error() -> int:
+    """Synchronise and return (then clear) the device error word as a status."""
+    return int(lib.dsa_get_last_device_error())
+
+
+def selftest_wait_timeout(timeout_ns: int, device=None):
+    dev = torch.device("cuda") if device is None else device
+    _check(lib.dsa_selftest_wait_timeout(int(timeout_ns), _stream(dev)),
+           "dsa_selftest_wait_timeout")

@@ -1,0 +1,431 @@
+// dsa_api.cu -- the C ABI declared in include/dsa.h: argument validation,
+// TMA descriptor encoding, launches on the caller's stream, and the per-device
+// error word that the kernels' bounded waits report into.
+//
+// Nothing here allocates device memory: outputs and scratch space belong to
+// the caller.  Host-detectable errors return before any CUDA call is made.
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "dsa.h"
+#include "dsa_common.cuh"
+#include "dsa_internal.h"
+
+namespace dsa {
+
+// Sticky error word of each device (bits kErrTimeout / kErrBadIndex).
+__device__ uint32_t g_error_word;
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+constexpr int kMaxDevices = 64;
+
+// Device address of g_error_word on the current device (looked up once per
+// device), or null.
+uint32_t* error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  static std::mutex mu;
+  static uint32_t* addr[kMaxDevices] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_error_word) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<uint32_t*>(a);
+  }
+  return addr[dev];
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+cudaStream_t as_stream(dsa_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+dsa_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
+
+// 128-byte-swizzled tiled map over a row-major [rows, D] matrix (2-D) or a
+// [blocks, block_rows, D] cache (3-D), box = 128 bytes of D x box_rows rows.
+bool encode_map(CUtensorMap* map, const void* base, dsa_dtype_t dtype, int D, int64_t rows,
+                int box_rows, int64_t blocks) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const int esz = dtype == DSA_BF16 ? 2 : 1;
+  const CUtensorMapDataType dt =
+      dtype == DSA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const cuuint32_t box_inner = 128 / esz;
+  CUresult r;
+  if (blocks <= 0) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * esz};
+    const cuuint32_t box[2] = {box_inner, static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(blocks)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * esz,
+                                   static_cast<cuuint64_t>(D) * esz * rows};
+    const cuuint32_t box[3] = {box_inner, static_cast<cuuint32_t>(box_rows), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    r = fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
+  return r == CUDA_SUCCESS;
+}
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+// Shared-memory key cache of the top-k kernel: whole rows up to this length.
+constexpr int kTopkCacheCap = 49152;
+
+int topk_cache_cap(int64_t max_row) {
+  return static_cast<int>(max_row < kTopkCacheCap ? (max_row < 0 ? 0 : max_row) : kTopkCacheCap);
+}
+
+// ---------------------------------------------------------------- validation
+
+dsa_status_t check_elems(dsa_dtype_t dtype, int H, int D, const void* k_scale) {
+  if (dtype != DSA_BF16 && dtype != DSA_E4M3) return DSA_ERR_INVALID_ARG;
+  if (!pow2(H) || H > 64) return DSA_ERR_UNSUPPORTED;
+  if (dtype == DSA_BF16 && D != 64 && D != 128) return DSA_ERR_UNSUPPORTED;
+  if (dtype == DSA_E4M3 && D != 128) return DSA_ERR_UNSUPPORTED;
+  if ((dtype == DSA_E4M3) != (k_scale != nullptr)) return DSA_ERR_INVALID_ARG;
+  return DSA_OK;
+}
+
+dsa_status_t check_logits_args(const void* q, const float* q_scale, const void* k,
+                               const float* k_scale, dsa_dtype_t dtype, const float* weights,
+                               const int32_t* row_starts, const int32_t* row_ends, int T, int S,
+                               int H, int D) {
+  if (!q || !k || !weights || !row_starts || !row_ends) return DSA_ERR_INVALID_ARG;
+  if (T < 0 || S < 0 || H < 1 || D < 1) return DSA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(weights, 4) || !aligned(row_starts, 4) ||
+      !aligned(row_ends, 4) || (q_scale && !aligned(q_scale, 4)) ||
+      (k_scale && !aligned(k_scale, 4)))
+    return DSA_ERR_INVALID_ARG;
+  dsa_status_t st = check_elems(dtype, H, D, k_scale);
+  if (st != DSA_OK) return st;
+  if (static_cast<int64_t>(T) * H >= (int64_t(1) << 31)) return DSA_ERR_UNSUPPORTED;
+  return DSA_OK;
+}
+
+// Validated, unchecked launch of the prefill scoring kernel.
+dsa_status_t run_logits(const void* q, const float* q_scale, const void* k, const float* k_scale,
+                        dsa_dtype_t dtype, const float* weights, const int32_t* row_starts,
+                        const int32_t* row_ends, int T, int S, int H, int D, float* logits,
+                        int64_t ld, cudaStream_t st) {
+  if (T == 0 || S == 0) return DSA_OK;
+  ScoreParams p = {};
+  if (!encode_map(&p.tmap_q, q, dtype, D, static_cast<int64_t>(T) * H, 256, 0) ||
+      !encode_map(&p.tmap_k, k, dtype, D, S, 128, 0))
+    return DSA_ERR_CUDA;
+  p.weights = weights;
+  p.q_scale = q_scale;
+  p.k_scale = k_scale;
+  p.row_starts = row_starts;
+  p.row_ends = row_ends;
+  p.logits = logits;
+  p.ld = ld;
+  p.R = T;
+  p.S = S;
+  p.err = error_word();
+  if (!p.err) return DSA_ERR_CUDA;
+  cudaError_t e = dtype == DSA_BF16 ? launch_score_prefill_bf16(p, H, D, st)
+                                    : launch_score_prefill_fp8(p, H, D, st);
+  return from_cuda(e);
+}
+
+dsa_status_t run_topk(const float* logits, int64_t ld, const int32_t* row_starts,
+                      const int32_t* row_ends, const int32_t* context_lens, int next_n, int R,
+                      int S, int k, int32_t* out, cudaStream_t st) {
+  if (R == 0) return DSA_OK;
+  TopkParams p = {};
+  p.logits = logits;
+  p.ld = ld;
+  p.row_starts = row_starts;
+  p.row_ends = row_ends;
+  p.context_lens = context_lens;
+  p.next_n = next_n;
+  p.R = R;
+  p.S = S;
+  p.k = k;
+  p.cache_cap = topk_cache_cap(S);
+  p.out = out;
+  return from_cuda(launch_topk(p, st));
+}
+
+struct PagedShape {
+  int B, next_n, block_size, max_blocks, num_blocks, H, D;
+};
+
+dsa_status_t check_paged_args(const void* q, const float* q_scale, const float* weights,
+                              const void* k_cache, const float* k_scale, dsa_dtype_t dtype,
+                              const int32_t* block_table, const int32_t* context_lens,
+                              const PagedShape& s) {
+  if (!q || !weights || !k_cache || !block_table || !context_lens) return DSA_ERR_INVALID_ARG;
+  if (s.B < 0 || s.next_n < 1 || s.max_blocks < 1 || s.num_blocks < 1 || s.H < 1 || s.D < 1)
+    return DSA_ERR_INVALID_ARG;
+  if (!pow2(s.block_size) || s.block_size < 8 || s.block_size > 128) return DSA_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(weights, 4) ||
+      !aligned(block_table, 4) || !aligned(context_lens, 4) || (q_scale && !aligned(q_scale, 4)) ||
+      (k_scale && !aligned(k_scale, 4)))
+    return DSA_ERR_INVALID_ARG;
+  dsa_status_t st = check_elems(dtype, s.H, s.D, k_scale);
+  if (st != DSA_OK) return st;
+  if (!score_paged_supported(dtype == DSA_E4M3, s.H, s.D, s.next_n)) return DSA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(s.max_blocks) * s.block_size >= (int64_t(1) << 30) ||
+      static_cast<int64_t>(s.B) * s.next_n * s.H >= (int64_t(1) << 31))
+    return DSA_ERR_UNSUPPORTED;
+  return DSA_OK;
+}
+
+constexpr int kPagedChunkKeys = 2048;
+
+dsa_status_t run_logits_paged(const void* q, const float* q_scale, const float* weights,
+                              const void* k_cache, const float* k_scale, dsa_dtype_t dtype,
+                              const int32_t* block_table, const int32_t* context_lens,
+                              const PagedShape& s, float* logits, int64_t ld, cudaStream_t st) {
+  if (s.B == 0) return DSA_OK;
+  const int64_t R = static_cast<int64_t>(s.B) * s.next_n;
+  const int max_ctx = s.max_blocks * s.block_size;
+  ScoreParams p = {};
+  if (!encode_map(&p.tmap_q, q, dtype, s.D, R * s.H, 256, 0) ||
+      !encode_map(&p.tmap_k, k_cache, dtype, s.D, s.block_size, s.block_size, s.num_blocks))
+    return DSA_ERR_CUDA;
+  p.weights = weights;
+  p.q_scale = q_scale;
+  p.k_scale = k_scale;
+  p.block_table = block_table;
+  p.context_lens = context_lens;
+  p.logits = logits;
+  p.ld = ld;
+  p.R = static_cast<int>(R);
+  p.S = max_ctx;
+  p.max_blocks = s.max_blocks;
+  p.next_n = s.next_n;
+  p.block_size = s.block_size;
+  p.num_blocks = s.num_blocks;
+  p.chunk_keys = kPagedChunkKeys;
+  p.chunks_per_req = (max_ctx + kPagedChunkKeys - 1) / kPagedChunkKeys;
+  p.err = error_word();
+  if (!p.err) return DSA_ERR_CUDA;
+  return from_cuda(launch_score_paged(p, dtype == DSA_E4M3, s.H, s.D, st));
+}
+
+// ------------------------------------------------------------ small kernels
+
+__global__ void fill_kernel(float* dst, int64_t rows, int64_t cols, int64_t ld, float v) {
+  const int64_t total = rows * cols;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    dst[(i / cols) * ld + (i % cols)] = v;
+}
+
+__global__ void wait_timeout_selftest_kernel(uint32_t* err, uint64_t timeout_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  // Nothing ever arrives on `bar`: the bounded wait must give up.
+  if (threadIdx.x == 0 && !mbar_wait_bounded(&bar, 0u, nullptr, timeout_ns))
+    record_error(err, kErrTimeout);
+}
+
+}  // namespace
+
+cudaError_t launch_fill(float* dst, int64_t rows, int64_t cols, int64_t ld, float value,
+                        cudaStream_t s) {
+  if (rows <= 0 || cols <= 0) return cudaSuccess;
+  const int64_t total = rows * cols;
+  const int64_t want = (total + 255) / 256;
+  const int grid = static_cast<int>(want < 152 * 16 ? want : 152 * 16);
+  fill_kernel<<<grid, 256, 0, s>>>(dst, rows, cols, ld, value);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint64_t timeout_ns, cudaStream_t s) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, s>>>(err, timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" {
+
+dsa_status_t dsa_indexer_logits(const void* q, const float* q_scale, const void* k,
+                                const float* k_scale, dsa_dtype_t dtype, const float* weights,
+                                const int32_t* row_starts, const int32_t* row_ends, int T, int S,
+                                int H, int D, float* logits, int64_t ld, uint32_t flags,
+                                dsa_stream_t stream) {
+  dsa_status_t st = check_logits_args(q, q_scale, k, k_scale, dtype, weights, row_starts,
+                                      row_ends, T, S, H, D);
+  if (st != DSA_OK) return st;
+  if (!logits || !aligned(logits, 4) || ld < S || ld < 1) return DSA_ERR_INVALID_ARG;
+  if (flags & ~DSA_LOGITS_CLEAN) return DSA_ERR_INVALID_ARG;
+  if (T == 0) return DSA_OK;
+  if (flags & DSA_LOGITS_CLEAN) {
+    st = from_cuda(launch_fill(logits, T, S, ld, -INFINITY, as_stream(stream)));
+    if (st != DSA_OK) return st;
+  }
+  return run_logits(q, q_scale, k, k_scale, dtype, weights, row_starts, row_ends, T, S, H, D,
+                    logits, ld, as_stream(stream));
+}
+
+dsa_status_t dsa_topk(const float* logits, int64_t ld, const int32_t* row_starts,
+                      const int32_t* row_ends, int T, int S, int k, int32_t* out, void* workspace,
+                      size_t ws_bytes, dsa_stream_t stream) {
+  (void)workspace;
+  (void)ws_bytes;
+  if (!logits || !row_starts || !row_ends || !out) return DSA_ERR_INVALID_ARG;
+  if (T < 0 || S < 0 || k < 1 || ld < S || ld < 1) return DSA_ERR_INVALID_ARG;
+  if (!aligned(logits, 4) || !aligned(out, 4) || !aligned(row_starts, 4) ||
+      !aligned(row_ends, 4))
+    return DSA_ERR_INVALID_ARG;
+  return run_topk(logits, ld, row_starts, row_ends, nullptr, 1, T, S, k, out, as_stream(stream));
+}
+
+dsa_status_t dsa_indexer_topk(const void* q, const float* q_scale, const void* k,
+                              const float* k_scale, dsa_dtype_t dtype, const float* weights,
+                              const int32_t* row_starts, const int32_t* row_ends, int T, int S,
+                              int H, int D, int topk, int32_t* out, void* workspace,
+                              size_t ws_bytes, dsa_stream_t stream) {
+  dsa_status_t st = check_logits_args(q, q_scale, k, k_scale, dtype, weights, row_starts,
+                                      row_ends, T, S, H, D);
+  if (st != DSA_OK) return st;
+  if (!out || !aligned(out, 4) || topk < 1) return DSA_ERR_INVALID_ARG;
+  const size_t need = dsa_workspace_bytes(DSA_OP_INDEXER_TOPK, T, S, topk);
+  if (need > 0 && (!workspace || ws_bytes < need || !aligned(workspace, 256)))
+    return DSA_ERR_INVALID_ARG;
+  if (T == 0) return DSA_OK;
+  const int64_t ld = round_up(S > 0 ? S : 1, 4);
+  float* lg = static_cast<float*>(workspace);
+  st = run_logits(q, q_scale, k, k_scale, dtype, weights, row_starts, row_ends, T, S, H, D, lg, ld,
+                  as_stream(stream));
+  if (st != DSA_OK) return st;
+  return run_topk(lg, ld, row_starts, row_ends, nullptr, 1, T, S, topk, out, as_stream(stream));
+}
+
+dsa_status_t dsa_indexer_logits_paged(const void* q, const float* q_scale, const float* weights,
+                                      const void* k_cache, const float* k_scale, int num_blocks,
+                                      dsa_dtype_t dtype, const int32_t* block_table,
+                                      int max_blocks, const int32_t* context_lens, int B,
+                                      int next_n, int block_size, int H, int D, float* logits,
+                                      int64_t ld, dsa_stream_t stream) {
+  const PagedShape s = {B, next_n, block_size, max_blocks, num_blocks, H, D};
+  dsa_status_t st = check_paged_args(q, q_scale, weights, k_cache, k_scale, dtype, block_table,
+                                     context_lens, s);
+  if (st != DSA_OK) return st;
+  if (!logits || !aligned(logits, 4) || ld < static_cast<int64_t>(max_blocks) * block_size)
+    return DSA_ERR_INVALID_ARG;
+  return run_logits_paged(q, q_scale, weights, k_cache, k_scale, dtype, block_table, context_lens,
+                          s, logits, ld, as_stream(stream));
+}
+
+dsa_status_t dsa_indexer_topk_paged(const void* q, const float* q_scale, const float* weights,
+                                    const void* k_cache, const float* k_scale, int num_blocks,
+                                    dsa_dtype_t dtype, const int32_t* block_table, int max_blocks,
+                                    const int32_t* context_lens, int B, int next_n,
+                                    int block_size, int H, int D, int topk, int32_t* out,
+                                    void* workspace, size_t ws_bytes, dsa_stream_t stream) {
+  const PagedShape s = {B, next_n, block_size, max_blocks, num_blocks, H, D};
+  dsa_status_t st = check_paged_args(q, q_scale, weights, k_cache, k_scale, dtype, block_table,
+                                     context_lens, s);
+  if (st != DSA_OK) return st;
+  if (!out || !aligned(out, 4) || topk < 1) return DSA_ERR_INVALID_ARG;
+  const int64_t R = static_cast<int64_t>(B) * next_n;
+  const int64_t max_ctx = static_cast<int64_t>(max_blocks) * block_size;
+  const size_t need = dsa_workspace_bytes(DSA_OP_INDEXER_TOPK_PAGED, R, max_ctx, topk);
+  if (need > 0 && (!workspace || ws_bytes < need || !aligned(workspace, 256)))
+    return DSA_ERR_INVALID_ARG;
+  if (B == 0) return DSA_OK;
+  const int64_t ld = round_up(max_ctx, 4);
+  float* lg = static_cast<float*>(workspace);
+  st = run_logits_paged(q, q_scale, weights, k_cache, k_scale, dtype, block_table, context_lens, s,
+                        lg, ld, as_stream(stream));
+  if (st != DSA_OK) return st;
+  return run_topk(lg, ld, nullptr, nullptr, context_lens, next_n, static_cast<int>(R),
+                  static_cast<int>(max_ctx), topk, out, as_stream(stream));
+}
+
+size_t dsa_workspace_bytes(dsa_op_t op, int64_t rows, int64_t cols, int k) {
+  if (rows < 0 || cols < 0 || k < 0) return static_cast<size_t>(-1);
+  switch (op) {
+    case DSA_OP_INDEXER_LOGITS:
+    case DSA_OP_TOPK:
+    case DSA_OP_INDEXER_LOGITS_PAGED:
+      return 0;
+    case DSA_OP_INDEXER_TOPK:
+    case DSA_OP_INDEXER_TOPK_PAGED:
+      if (rows == 0) return 0;
+      return static_cast<size_t>(rows) * static_cast<size_t>(round_up(cols > 0 ? cols : 1, 4)) *
+             sizeof(float);
+    default:
+      return static_cast<size_t>(-1);
+  }
+}
+
+const char* dsa_status_string(dsa_status_t status) {
+  switch (status) {
+    case DSA_OK:
+      return "ok";
+    case DSA_ERR_INVALID_ARG:
+      return "invalid argument";
+    case DSA_ERR_UNSUPPORTED:
+      return "unsupported shape or dtype";
+    case DSA_ERR_CUDA:
+      return "CUDA error";
+    case DSA_ERR_TIMEOUT:
+      return "device-side wait timed out";
+    default:
+      return "unknown status";
+  }
+}
+
+dsa_status_t dsa_get_last_device_error(void) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return DSA_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_error_word, sizeof(word)) != cudaSuccess) return DSA_ERR_CUDA;
+  const uint32_t zero = 0;
+  if (word && cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  if (word & kErrTimeout) return DSA_ERR_TIMEOUT;
+  if (word & kErrBadIndex) return DSA_ERR_INVALID_ARG;
+  return DSA_OK;
+}
+
+dsa_status_t dsa_selftest_wait_timeout(uint64_t timeout_ns, dsa_stream_t stream) {
+  if (timeout_ns < 1000) timeout_ns = 1000;
+  if (timeout_ns > 1000000000ull) timeout_ns = 1000000000ull;
+  uint32_t* err = error_word();
+  if (!err) return DSA_ERR_CUDA;
+  return from_cuda(launch_wait_timeout_selftest(err, timeout_ns, as_stream(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,66 @@
+// dsa_internal.h -- parameter blocks and launchers shared between the kernel
+// translation units and the C-ABI unit (dsa_api.cu).  Not part of the ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dsa {
+
+// Scoring kernel parameters.  Passed by value as a __grid_constant__ kernel
+// argument, so the two TMA descriptors live in parameter space.
+struct ScoreParams {
+  CUtensorMap tmap_q;  // q viewed as [R*H, D] elements, 128-byte swizzled boxes
+  CUtensorMap tmap_k;  // prefill: k [S, D]; paged: k_cache [num_blocks, block_size, D]
+  const float* weights;       // [R, H]
+  const float* q_scale;       // [R, H] or null
+  const float* k_scale;       // prefill [S]; paged [num_blocks*block_size]; or null
+  const int32_t* row_starts;  // prefill [R]
+  const int32_t* row_ends;    // prefill [R]
+  const int32_t* block_table;   // paged [B, max_blocks]
+  const int32_t* context_lens;  // paged [B]
+  float* logits;              // [R, ld]
+  int64_t ld;
+  int R;            // query rows (prefill T, paged B*next_n)
+  int S;            // prefill: number of keys; paged: ld bound on columns written
+  int max_blocks;   // paged
+  int next_n;       // paged
+  int block_size;   // paged
+  int num_blocks;   // paged
+  int chunk_keys;   // paged: keys per CTA (multiple of 128)
+  int chunks_per_req;  // paged
+  uint32_t* err;    // device error word
+};
+
+struct TopkParams {
+  const float* logits;  // [R, ld]
+  int64_t ld;
+  const int32_t* row_starts;    // [R] (prefill) or null
+  const int32_t* row_ends;      // [R] (prefill) or null
+  const int32_t* context_lens;  // [B] (paged) or null
+  int next_n;                   // paged
+  int R;
+  int S;          // column bound: prefill S, paged max context
+  int k;
+  int cache_cap;  // keys of a row cached in shared memory
+  int32_t* out;   // [R, k]
+};
+
+// Launchers (return the launch error, if any).  Shapes were validated by the
+// caller; `supported` variants report whether a template instance exists.
+bool score_prefill_bf16_supported(int H, int D);
+cudaError_t launch_score_prefill_bf16(const ScoreParams& p, int H, int D, cudaStream_t s);
+bool score_prefill_fp8_supported(int H, int D);
+cudaError_t launch_score_prefill_fp8(const ScoreParams& p, int H, int D, cudaStream_t s);
+bool score_paged_supported(bool fp8, int H, int D, int next_n);
+cudaError_t launch_score_paged(const ScoreParams& p, bool fp8, int H, int D, cudaStream_t s);
+// Tokens (query rows) per prefill tile group for a head count.
+int score_tokens_per_group(int H);
+
+cudaError_t launch_topk(const TopkParams& p, cudaStream_t s);
+cudaError_t launch_fill(float* dst, int64_t rows, int64_t cols, int64_t ld, float value,
+                        cudaStream_t s);
+cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint64_t timeout_ns, cudaStream_t s);
+
+}  // namespace dsa
