@@ -1,0 +1,481 @@
+"""Benchmark of the DSA lightning-indexer hot path (index logits + masked top-k).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-e2e] [--no-cpu-baseline]
+
+One step = one pass of the whole path over one batch of synthetic input that
+is resident in HBM: the tcgen05 scoring kernel writes the fp32 logits of every
+in-range key tile, then the radix-select kernel takes the per-row top-k.  The
+default workload is the single-sequence causal prefill T=S=4096, H=64, D=128,
+index_topk=2048 (bf16 q/k, fp32 weights).  L2 is flushed (a 256 MiB write)
+before every timed step, outside the step's own event pair.
+
+Under torchrun (N > 1) every rank runs an independent replica of the workload
+on its own GPU (the path has no exchange step): the K steps are bracketed by a
+barrier + synchronize, the per-step time is the max over ranks, and `value`
+is the rows all ranks processed divided by that time.
+
+--impl reference times the CPU oracle (the only other implementation of this
+path) on the host cores, on a bounded row sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = ("indexer+top-k query rows/sec and TFLOP/s (prefill), GB/s (decode) "
+          "vs GB300 roofline")
+L2_FLUSH_BYTES = 256 << 20
+PROFILE = os.path.join(ROOT, "profiles", "score_prefill_bf16_T4096_H64_D128.md")
+KERNEL_SOURCES = ("top_selection_dsa_gb300/csrc/dsa_score.cuh",
+                  "top_selection_dsa_gb300/csrc/dsa_common.cuh",
+                  "top_selection_dsa_gb300/csrc/dsa_score_prefill_bf16.cu")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="prefill_causal",
+                    choices=("prefill_causal", "prefill_thd", "prefill_fp8", "paged_decode",
+                             "tiny_causal"))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true",
+                    help="skip the clock-sampling load window (for profiler runs)")
+    ap.add_argument("--oracle-rows", type=int, default=512,
+                    help="rows of the CPU oracle sample (cpu_baseline / reference arm)")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------- helpers
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def kernel_sha():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """dram read+write bytes per launch of the scoring kernel from the committed
+    ncu summary, or None when that summary was taken on other kernel sources."""
+    if not os.path.exists(PROFILE):
+        return None
+    text = open(PROFILE).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    s = re.search(r"kernel_sources_sha:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != kernel_sha():
+        return None
+    return int(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.lines:
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def reduce_max(values, world, device):
+    """Element-wise max over ranks of a list of floats."""
+    if world == 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def make_workload(name):
+    from top_selection_dsa_gb300 import workloads as wl
+    return wl.WORKLOADS[name]()
+
+
+def step_flops(p):
+    return 2.0 * p.valid_pairs() * p.H * p.D
+
+
+# ------------------------------------------------------- CPU oracle timing
+
+def oracle_sample_rate(p, nrows, seed=0):
+    """Time the CPU oracle (logits + top-k) on a seeded row sample: rows/s."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    if hasattr(p, "row_starts"):
+        rows = np.sort(rng.choice(p.T, size=min(nrows, p.T), replace=False)).astype(np.int64)
+        t0 = time.perf_counter()
+        lg = oracle.logits(p.q, p.k, p.w, p.row_starts, p.row_ends, dtype=p.dtype,
+                           k_scale=p.k_scale, rows=rows)
+        oracle.topk(lg.astype(np.float32), p.row_starts[rows], p.row_ends[rows], p.topk,
+                    S=p.S)
+        dt = time.perf_counter() - t0
+        sample = f"{len(rows)} of {p.T} rows, uniform without replacement (seed {seed})"
+    else:
+        rows = np.sort(rng.choice(p.R, size=min(nrows, p.R), replace=False)).astype(np.int64)
+        t0 = time.perf_counter()
+        lg = oracle.logits_paged(p.q, p.w, p.k_cache, p.block_table, p.context_lens,
+                                 next_n=p.next_n, dtype=p.dtype, k_scale=p.k_scale,
+                                 ld=p.max_ctx(), rows=rows)
+        rs, re_ = oracle.paged_row_ranges(p.context_lens, p.next_n)
+        oracle.topk(lg.astype(np.float32), rs[rows], re_[rows], p.topk)
+        dt = time.perf_counter() - t0
+        sample = f"{len(rows)} of {p.R} query rows, uniform (seed {seed})"
+    return len(rows) / dt, dt, sample, oracle.max_threads()
+
+
+def run_reference(args):
+    world, rank, local = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0
+    if rank != 0:
+        return 0
+    p = make_workload(args.workload)
+    rows = max(8, args.oracle_rows // 8)
+    for _ in range(args.warmup):
+        oracle_sample_rate(p, rows, seed=1)
+    times, rates = [], []
+    sample = cores = None
+    for i in range(args.steps):
+        rate, dt, sample, cores = oracle_sample_rate(p, rows, seed=2 + i)
+        times.append(dt)
+        rates.append(rate)
+    value = float(np.mean(rates))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * float(np.mean(times)), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": p.name},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": cores, "kind": "oracle",
+                         "sample": f"each step: {sample}"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------- our path
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    from top_selection_dsa_gb300 import api
+
+    p = make_workload(args.workload)
+    paged = not hasattr(p, "row_starts")
+    cuda = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
+
+    def elems(x):
+        if p.dtype == 0:
+            return cuda(x.view(np.int16)).view(torch.bfloat16)
+        return cuda(x).view(torch.float8_e4m3fn)
+
+    stream = torch.cuda.current_stream(device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    if not paged:
+        q, k, w = elems(p.q), elems(p.k), cuda(p.w)
+        rs, re_ = cuda(p.row_starts), cuda(p.row_ends)
+        ks = cuda(p.k_scale) if p.k_scale is not None else None
+        rows_per_step = p.T
+        ld = (p.S + 3) // 4 * 4
+        logits = torch.empty((p.T, ld), dtype=torch.float32, device=device)
+        out = torch.empty((p.T, p.topk), dtype=torch.int32, device=device)
+
+        def score():
+            api.indexer_logits(q, k, w, rs, re_, k_scale=ks, logits=logits)
+
+        def select():
+            api.topk(logits, rs, re_, p.topk, S=p.S, out=out)
+
+        def fused(o):
+            return api.indexer_topk(q, k, w, rs, re_, p.topk, k_scale=ks, out=o, workspace=logits)
+    else:
+        q, w, kc = elems(p.q), cuda(p.w), elems(p.k_cache)
+        bt, cl = cuda(p.block_table), cuda(p.context_lens)
+        ks = cuda(p.k_scale.reshape(-1)) if p.k_scale is not None else None
+        rows_per_step = p.R
+        ld = p.max_ctx()
+        logits = torch.empty((p.R, ld), dtype=torch.float32, device=device)
+        out = torch.empty((p.R, p.topk), dtype=torch.int32, device=device)
+        rs_np, re_np = (np.zeros(p.R, np.int32),
+                        np.array([max(int(p.context_lens[r // p.next_n]) - p.next_n
+                                      + r % p.next_n + 1, 0) for r in range(p.R)], np.int32))
+        rs, re_ = cuda(rs_np), cuda(re_np)
+
+        def score():
+            api.indexer_logits_paged(q, w, kc, bt, cl, next_n=p.next_n, k_scale=ks,
+                                     logits=logits)
+
+        def select():
+            api.topk(logits, rs, re_, p.topk, out=out)
+
+        def fused(o):
+            return api.indexer_topk_paged(q, w, kc, bt, cl, p.topk, next_n=p.next_n,
+                                          k_scale=ks, out=o, workspace=logits)
+
+    # The fused entry point is the same two kernels: check bit-identity once.
+    score()
+    select()
+    ref_out = out.clone()
+    o2 = torch.empty_like(out)
+    fused(o2)
+    torch.cuda.synchronize(device)
+    if not torch.equal(o2, ref_out):
+        raise RuntimeError("fused entry point differs from logits + top-k")
+    if api.last_device_error() != api.DSA_OK:
+        raise RuntimeError("device error word set during warm-up")
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        score()
+        select()
+    torch.cuda.synchronize(device)
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(device)
+    with ClockSampler(local) as clocks:
+        # nvidia-smi samples every 100 ms while the timed region lasts only a
+        # few ms: keep the same load running for ~1 s right before it, so the
+        # samples describe the clocks this step runs at.
+        t_end = time.perf_counter() + (0.0 if args.no_clocks else 1.0)
+        while time.perf_counter() < t_end:
+            for _ in range(8):
+                flush.zero_()
+                score()
+                select()
+            torch.cuda.synchronize(device)
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            score()
+            ev[i][1].record(stream)
+            select()
+            ev[i][2].record(stream)
+        torch.cuda.synchronize(device)
+        wall = time.perf_counter() - wall0
+    barrier(world)
+    score_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    topk_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    if api.last_device_error() != api.DSA_OK:
+        raise RuntimeError("device error word set during the timed steps")
+    ms, s_ms, t_ms = reduce_max([statistics.mean(step_ms), statistics.mean(score_ms),
+                                 statistics.mean(topk_ms)], world, device)
+
+    # End to end through the C ABI: pinned host inputs -> device, fused call,
+    # indices -> pinned host, every step.
+    e2e = None
+    if not args.no_e2e:
+        if not paged:
+            host_in = [torch.from_numpy(np.ascontiguousarray(a)).pin_memory() for a in
+                       (p.q.view(np.uint8), p.k.view(np.uint8), p.w, p.row_starts, p.row_ends)]
+            dev_in = [q.view(torch.uint8), k.view(torch.uint8), w, rs, re_]
+        else:
+            host_in = [torch.from_numpy(np.ascontiguousarray(a)).pin_memory() for a in
+                       (p.q.view(np.uint8), p.w, p.block_table, p.context_lens)]
+            dev_in = [q.view(torch.uint8), w, bt, cl]
+            # the K cache stays resident: it is the serving system's state, not an input
+        if ks is not None:
+            host_in.append(torch.from_numpy(np.ascontiguousarray(
+                p.k_scale.reshape(-1) if paged else p.k_scale)).pin_memory())
+            dev_in.append(ks)
+        host_out = torch.empty(out.shape, dtype=torch.int32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
+        d2h = host_out.numel() * 4
+        e2e_ms = []
+        for i in range(args.warmup + args.steps):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for d, h in zip(dev_in, host_in):
+                d.view(-1).copy_(h.view(-1), non_blocking=True)
+            fused(out)
+            host_out.copy_(out, non_blocking=True)
+            b.record(stream)
+            b.synchronize()
+            if i >= args.warmup:
+                e2e_ms.append(a.elapsed_time(b))
+        if not torch.equal(host_out, ref_out.cpu()):
+            raise RuntimeError("end-to-end result differs from the resident-input result")
+        (em,) = reduce_max([statistics.mean(e2e_ms)], world, device)
+        e2e = {"value": world * rows_per_step / (em / 1e3), "unit": "rows/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": em}
+
+    if rank != 0:
+        return 0
+
+    peaks, peak_src = measured_peaks()
+    flops = step_flops(p)
+    if not paged:
+        peak = peaks["bf16_tflops"] * (2.0 if p.dtype == 1 else 1.0)
+        achieved = flops / (s_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": profiled_traffic(),
+                "kernel": "score_kernel (tcgen05 scoring, writes fp32 logits)",
+                "algorithmic_flops_per_launch": flops,
+                "peak_source": f"{peak_src} {'bf16 burst x2 (fp8 nominal ratio)' if p.dtype == 1 else 'bf16 burst'}"}
+    else:
+        kbytes = int(sum(int(L) for L in p.context_lens)) * p.D * (2 if p.dtype == 0 else 1)
+        other = p.R * p.H * p.D * (2 if p.dtype == 0 else 1) + p.R * p.H * 4 \
+            + int(sum(-(-int(L) // p.block_size) for L in p.context_lens)) * 4 \
+            + p.valid_pairs() * 4
+        alg = kbytes + other
+        achieved = alg / (s_ms / 1e3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": None,
+                "kernel": "score_kernel (paged, writes fp32 logits)",
+                "algorithmic_bytes_per_launch": alg, "peak_source": f"{peak_src} hbm copy"}
+    # top-k pass: reads each valid logit once, writes the indices.
+    topk_bytes = p.valid_pairs() * 4 + rows_per_step * p.topk * 4
+    line = {
+        "metric": METRIC,
+        "value": world * rows_per_step / (ms / 1e3),
+        "unit": "rows/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if p.dtype == 0 else "e4m3",
+        "data": "synthetic",
+        "config": {"workload": p.name, "rows_per_step": rows_per_step,
+                   "valid_pairs": p.valid_pairs(), "index_topk": p.topk, "H": p.H, "D": p.D,
+                   "l2": "flushed before every step (256 MiB write, outside the step events)",
+                   "parallelism": f"replicas x{world}",
+                   "clock_window": "nvidia-smi every 100 ms over a 1 s window of the same "
+                                   "steps that ends where the timed steps begin"},
+        "tflops": flops / (ms / 1e3) / 1e12,
+        "kernels": {"score_ms": s_ms, "topk_ms": t_ms,
+                    "topk_gbs": topk_bytes / (t_ms / 1e3) / 1e9,
+                    "topk_hbm_frac": topk_bytes / (t_ms / 1e3) / 1e9 / peaks["hbm_gbs"]},
+        "roofline": roof,
+        "gpu_launches": 2 * args.steps,
+        "wall_s_timed_region": wall,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    cs = clocks.summary()
+    line["clocks"] = cs
+    if not args.no_cpu_baseline and world == 1:
+        rate, dt, sample, cores = oracle_sample_rate(p, args.oracle_rows)
+        line["cpu_baseline"] = {"value": rate, "unit": "rows/s", "cores": cores,
+                                "kind": "oracle", "sample": sample, "seconds": dt}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -98,13 +98,6 @@ bool encode_map(CUtensorMap* map, const void* base, dsa_dtype_t dtype, int D, in
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
-// Shared-memory key cache of the top-k kernel: whole rows up to this length.
-constexpr int kTopkCacheCap = 49152;
-
-int topk_cache_cap(int64_t max_row) {
-  return static_cast<int>(max_row < kTopkCacheCap ? (max_row < 0 ? 0 : max_row) : kTopkCacheCap);
-}
-
 // ---------------------------------------------------------------- validation
 
 dsa_status_t check_elems(dsa_dtype_t dtype, int H, int D, const void* k_scale) {
@@ -172,7 +165,7 @@ dsa_status_t run_topk(const float* logits, int64_t ld, const int32_t* row_starts
   p.R = R;
   p.S = S;
   p.k = k;
-  p.cache_cap = topk_cache_cap(S);
+  p.bitmap_words = topk_bitmap_words(S);
   p.out = out;
   return from_cuda(launch_topk(p, st));
 }
@@ -212,7 +205,10 @@ dsa_status_t run_logits_paged(const void* q, const float* q_scale, const float* 
   const int64_t R = static_cast<int64_t>(s.B) * s.next_n;
   const int max_ctx = s.max_blocks * s.block_size;
   ScoreParams p = {};
-  if (!encode_map(&p.tmap_q, q, dtype, s.D, R * s.H, 256, 0) ||
+  // The q box must be exactly the kernel's N rows: the stage accounting
+  // (expect_tx) and the shared-memory q region are sized for N.
+  const int ncols = score_paged_cols(s.H, s.next_n);
+  if (!encode_map(&p.tmap_q, q, dtype, s.D, R * s.H, ncols, 0) ||
       !encode_map(&p.tmap_k, k_cache, dtype, s.D, s.block_size, s.block_size, s.num_blocks))
     return DSA_ERR_CUDA;
   p.weights = weights;

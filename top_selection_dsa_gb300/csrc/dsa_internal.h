@@ -43,8 +43,8 @@ struct TopkParams {
   int R;
   int S;          // column bound: prefill S, paged max context
   int k;
-  int cache_cap;  // keys of a row cached in shared memory
-  int32_t* out;   // [R, k]
+  int bitmap_words;  // ceil(S / 32): shared-memory selection bitmaps per row
+  int32_t* out;      // [R, k]
 };
 
 // Launchers (return the launch error, if any).  Shapes were validated by the
@@ -54,11 +54,14 @@ cudaError_t launch_score_prefill_bf16(const ScoreParams& p, int H, int D, cudaSt
 bool score_prefill_fp8_supported(int H, int D);
 cudaError_t launch_score_prefill_fp8(const ScoreParams& p, int H, int D, cudaStream_t s);
 bool score_paged_supported(bool fp8, int H, int D, int next_n);
+// MMA columns (and q-tile rows) of the paged kernel: next_n*H rounded up to 64/128/256.
+int score_paged_cols(int H, int next_n);
 cudaError_t launch_score_paged(const ScoreParams& p, bool fp8, int H, int D, cudaStream_t s);
 // Tokens (query rows) per prefill tile group for a head count.
 int score_tokens_per_group(int H);
 
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t s);
+int topk_bitmap_words(int max_row);
 cudaError_t launch_fill(float* dst, int64_t rows, int64_t cols, int64_t ld, float value,
                         cudaStream_t s);
 cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint64_t timeout_ns, cudaStream_t s);

@@ -7,15 +7,16 @@
 #include "dsa_score.cuh"
 
 namespace dsa {
-namespace {
 
-int paged_cols(int H, int next_n) {
+int score_paged_cols(int H, int next_n) {
   const int need = H * next_n;
   if (need <= 64) return 64;
   if (need <= 128) return 128;
   if (need <= 256) return 256;
   return 0;
 }
+
+namespace {
 
 template <bool kFp8, int H>
 cudaError_t by_cols(const ScoreParams& p, int N, int grid, cudaStream_t s) {
@@ -52,12 +53,12 @@ cudaError_t by_heads(const ScoreParams& p, int H, int N, int grid, cudaStream_t 
 bool score_paged_supported(bool fp8, int H, int D, int next_n) {
   (void)fp8;
   return D == 128 && (H == 8 || H == 16 || H == 32 || H == 64) && next_n >= 1 &&
-         paged_cols(H, next_n) != 0;
+         score_paged_cols(H, next_n) != 0;
 }
 
 cudaError_t launch_score_paged(const ScoreParams& p, bool fp8, int H, int D, cudaStream_t s) {
   (void)D;
-  const int N = paged_cols(H, p.next_n);
+  const int N = score_paged_cols(H, p.next_n);
   const int B = p.R / p.next_n;
   const int grid = B * p.chunks_per_req;
   return fp8 ? by_heads<true>(p, H, N, grid, s) : by_heads<false>(p, H, N, grid, s);

@@ -7,26 +7,29 @@
 // page is silent: ties go to the lower column (-0.0 equals +0.0), NaN is never
 // selected, and the selected columns are written in ascending column order.
 //
-// One CTA per row:
+// One 256-thread CTA per row; several rows share an SM, so the per-row
+// barriers of one CTA overlap with the memory traffic of the others.
 //   1. every logit becomes an order-preserving 32-bit key (larger float ->
 //      larger key; -0.0 folded onto +0.0; -inf and NaN -> 0, which no valid
-//      score maps to) and, when the row fits, is cached in shared memory;
-//   2. if at most k keys are valid, all of them are taken;
-//   3. otherwise an exact radix select over the key bits (11 + 11 + 10) finds
-//      the k-th largest key tau and how many keys equal to tau must be taken
-//      (need_eq) after every key greater than tau;
-//   4. one ordered pass over the row writes every key > tau and the first
-//      need_eq keys == tau, at positions given by a block-wide prefix count,
-//      which yields ascending column order directly; -1 fills the tail.
+//      score maps to); pass 1 streams the row from HBM with 16-byte loads and
+//      histograms the top 11 key bits;
+//   2. if at most k keys are valid, every valid key is taken; otherwise two
+//      more histogram passes (11 and 10 bits, re-reading the row, which is
+//      now in L2) find the exact k-th largest key tau and how many keys equal
+//      to tau to take (need_eq) after all keys greater than tau;
+//   3. a last pass turns the row into two bitmaps (key > tau, key == tau) with
+//      warp ballots; one prefix scan over the words gives every selected
+//      column its output position, so indices come out in column order; the
+//      first need_eq ties (in column order) are the ones kept; -1 fills the
+//      tail of the output row.
 #include "dsa_common.cuh"
 #include "dsa_internal.h"
 
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kItems = 4;  // consecutive columns per thread in the ordered pass
 constexpr int kHistBins = 2048;
 
 __device__ __forceinline__ uint32_t order_key(float x) {
@@ -37,47 +40,50 @@ __device__ __forceinline__ uint32_t order_key(float x) {
   return invalid ? 0u : key;
 }
 
-// Exclusive prefix sum of one value per thread over the block; *total gets
-// the block sum.  Contains barriers: every thread must call it.
-__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* warp_sums,
-                                                         uint32_t* total) {
+// Exclusive prefix sums of two counters per thread over the block.  Contains
+// barriers: every thread must call it.
+__device__ __forceinline__ uint2 block_exclusive_scan2(uint2 v, uint2* warp_sums, uint2* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t x = v;
+  uint2 x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
+    const uint32_t a = __shfl_up_sync(0xffffffffu, x.x, o);
+    const uint32_t b = __shfl_up_sync(0xffffffffu, x.y, o);
+    if (lane >= o) {
+      x.x += a;
+      x.y += b;
+    }
   }
   if (lane == 31) warp_sums[warp] = x;
   __syncthreads();
-  if (warp == 0) {
-    uint32_t w = lane < kWarps ? warp_sums[lane] : 0u;
+  uint2 before = make_uint2(0u, 0u), all = make_uint2(0u, 0u);
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
+  for (int w = 0; w < kWarps; ++w) {
+    const uint2 s = warp_sums[w];
+    if (w < warp) {
+      before.x += s.x;
+      before.y += s.y;
     }
-    if (lane < kWarps) warp_sums[lane] = w;
+    all.x += s.x;
+    all.y += s.y;
   }
+  *total = all;
   __syncthreads();
-  const uint32_t before = warp ? warp_sums[warp - 1] : 0u;
-  *total = warp_sums[kWarps - 1];
-  __syncthreads();
-  return before + x - v;
+  return make_uint2(before.x + x.x - v.x, before.y + x.y - v.y);
 }
 
-// Over hist[0..nbins), find the bin b holding the r-th largest element
-// (r >= 1): above = sum of bins > b satisfies above < r <= above + hist[b].
-// Every thread returns the same (b, above).
+// Over hist[0..nbins), the bin b holding the r-th largest element (r >= 1):
+// above = sum of bins > b satisfies above < r <= above + hist[b].  Every thread
+// returns the same (b, above).
 __device__ __forceinline__ void find_bin(const uint32_t* hist, int nbins, uint32_t r,
-                                         uint32_t* warp_sums, uint32_t* sel, uint32_t* bin,
+                                         uint2* warp_sums, uint32_t* sel, uint32_t* bin,
                                          uint32_t* above) {
   const int per = nbins / kThreads;  // bins per thread, highest bins first
   const int top = nbins - 1 - threadIdx.x * per;
   uint32_t local = 0;
   for (int i = 0; i < per; ++i) local += hist[top - i];
-  uint32_t total;
-  const uint32_t excl = block_exclusive_scan(local, warp_sums, &total);
+  uint2 total;
+  const uint32_t excl = block_exclusive_scan2(make_uint2(local, 0u), warp_sums, &total).x;
   if (excl < r && r <= excl + local) {
     uint32_t acc = excl;
     for (int i = 0; i < per; ++i) {
@@ -93,18 +99,18 @@ __device__ __forceinline__ void find_bin(const uint32_t* hist, int nbins, uint32
   __syncthreads();
   *bin = sel[0];
   *above = sel[1];
-  __syncthreads();
 }
 
 __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
   extern __shared__ uint32_t sm[];
-  uint32_t* hist = sm;                 // kHistBins
-  uint32_t* cache = sm + kHistBins;    // p.cache_cap keys
-  __shared__ uint32_t warp_sums[32];
+  uint32_t* hist = sm;                   // kHistBins
+  uint32_t* gt_bits = sm + kHistBins;    // ceil(S/32) words: key > tau
+  uint32_t* eq_bits = gt_bits + p.bitmap_words;  // key == tau
+  __shared__ uint2 warp_sums[kWarps];
   __shared__ uint32_t sel[2];
 
   const int row = blockIdx.x;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int lo, hi;
   if (p.context_lens) {
     const int b = row / p.next_n, j = row % p.next_n;
@@ -119,42 +125,54 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
   const int n = hi - lo;
   const float* src = p.logits + static_cast<int64_t>(row) * p.ld + lo;
   int32_t* dst = p.out + static_cast<int64_t>(row) * p.k;
-  const bool cached = n <= p.cache_cap;
 
-  // Pass 1: keys (+ cache) and the histogram of their top 11 bits.
+  // ---- pass 1: histogram of the top 11 key bits, 16-byte loads from HBM.
   for (int i = tid; i < kHistBins; i += kThreads) hist[i] = 0u;
   __syncthreads();
-  for (int i = tid; i < n; i += kThreads) {
-    const uint32_t key = order_key(src[i]);
-    if (cached) cache[i] = key;
-    atomicAdd(&hist[key >> 21], 1u);
+  {
+    const uintptr_t addr = reinterpret_cast<uintptr_t>(src);
+    int head = (addr & 3u) ? n : static_cast<int>(((16u - (addr & 15u)) & 15u) >> 2);
+    head = min(head, n);
+    const int body = (n - head) >> 2;
+    for (int i = tid; i < head; i += kThreads) atomicAdd(&hist[order_key(src[i]) >> 21], 1u);
+    const float4* src4 = reinterpret_cast<const float4*>(src + head);
+    for (int i = tid; i < body; i += kThreads) {
+      const float4 v = __ldg(src4 + i);
+      atomicAdd(&hist[order_key(v.x) >> 21], 1u);
+      atomicAdd(&hist[order_key(v.y) >> 21], 1u);
+      atomicAdd(&hist[order_key(v.z) >> 21], 1u);
+      atomicAdd(&hist[order_key(v.w) >> 21], 1u);
+    }
+    for (int i = head + 4 * body + tid; i < n; i += kThreads)
+      atomicAdd(&hist[order_key(src[i]) >> 21], 1u);
   }
   __syncthreads();
   // Bin 0 holds exactly the invalid keys: the smallest valid key is 0x00800000.
   const int nvalid = n - static_cast<int>(hist[0]);
-  __syncthreads();
 
-  uint32_t tau = 0u;   // take every key > tau ...
-  uint32_t need_eq = 0u;  // ... and the first need_eq keys == tau (column order)
+  uint32_t tau = 0u;      // take every key > tau ...
+  uint32_t need_eq = 0u;  // ... and the first need_eq keys == tau, in column order
   if (nvalid > p.k) {
     uint32_t rem = static_cast<uint32_t>(p.k);
     uint32_t b1, a1, b2, a2, b3, a3;
     find_bin(hist, kHistBins, rem, warp_sums, sel, &b1, &a1);
     rem -= a1;
+    __syncthreads();
     for (int i = tid; i < kHistBins; i += kThreads) hist[i] = 0u;
     __syncthreads();
     for (int i = tid; i < n; i += kThreads) {
-      const uint32_t key = cached ? cache[i] : order_key(src[i]);
+      const uint32_t key = order_key(src[i]);
       if ((key >> 21) == b1) atomicAdd(&hist[(key >> 10) & 0x7FFu], 1u);
     }
     __syncthreads();
     find_bin(hist, kHistBins, rem, warp_sums, sel, &b2, &a2);
     rem -= a2;
     const uint32_t prefix = (b1 << 11) | b2;
+    __syncthreads();
     for (int i = tid; i < 1024; i += kThreads) hist[i] = 0u;
     __syncthreads();
     for (int i = tid; i < n; i += kThreads) {
-      const uint32_t key = cached ? cache[i] : order_key(src[i]);
+      const uint32_t key = order_key(src[i]);
       if ((key >> 10) == prefix) atomicAdd(&hist[key & 0x3FFu], 1u);
     }
     __syncthreads();
@@ -164,37 +182,47 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
     need_eq = rem;
   }
 
-  // Ordered pass: ascending columns, positions from a block-wide prefix count.
-  uint32_t base_gt = 0u, base_eq = 0u;
-  for (int c0 = 0; c0 < n; c0 += kThreads * kItems) {
-    const int i0 = c0 + tid * kItems;
-    uint32_t keys[kItems];
-    uint32_t n_gt = 0u, n_eq = 0u;
-#pragma unroll
-    for (int u = 0; u < kItems; ++u) {
-      const int i = i0 + u;
-      const uint32_t key = i < n ? (cached ? cache[i] : order_key(src[i])) : 0u;
-      keys[u] = key;
-      n_gt += key > tau ? 1u : 0u;
-      n_eq += (need_eq > 0u && key == tau) ? 1u : 0u;
+  // ---- last pass: bitmaps of (key > tau) and (key == tau), one word per
+  // 32 consecutive columns, written by warp ballots.
+  const int nwords = (n + 31) >> 5;
+  for (int w = warp; w < nwords; w += kWarps) {
+    const int i = (w << 5) + lane;
+    const uint32_t key = i < n ? order_key(src[i]) : 0u;
+    const uint32_t g = __ballot_sync(0xffffffffu, key > tau);
+    const uint32_t e = __ballot_sync(0xffffffffu, need_eq > 0u && key == tau);
+    if (lane == 0) {
+      gt_bits[w] = g;
+      eq_bits[w] = e;
     }
-    uint32_t total;
-    const uint32_t excl = block_exclusive_scan(n_gt | (n_eq << 16), warp_sums, &total);
-    uint32_t gb = base_gt + (excl & 0xFFFFu);
-    uint32_t eb = base_eq + (excl >> 16);
-#pragma unroll
-    for (int u = 0; u < kItems; ++u) {
-      const uint32_t key = keys[u];
-      if (key > tau) {
-        dst[gb + min(eb, need_eq)] = lo + i0 + u;
+  }
+  __syncthreads();
+
+  // ---- positions: prefix counts over words (each thread owns a run of words).
+  const int per = (nwords + kThreads - 1) / kThreads;
+  const int w0 = min(tid * per, nwords), w1 = min(w0 + per, nwords);
+  uint2 mine = make_uint2(0u, 0u);
+  for (int w = w0; w < w1; ++w) {
+    mine.x += __popc(gt_bits[w]);
+    mine.y += __popc(eq_bits[w]);
+  }
+  uint2 total;
+  const uint2 before = block_exclusive_scan2(mine, warp_sums, &total);
+  uint32_t gb = before.x, eb = before.y;
+  for (int w = w0; w < w1; ++w) {
+    uint32_t g = gt_bits[w], e = eq_bits[w];
+    uint32_t m = g | e;
+    while (m) {
+      const int bit = __ffs(m) - 1;
+      m &= m - 1;
+      const int col = lo + (w << 5) + bit;
+      if ((g >> bit) & 1u) {
+        dst[gb + min(eb, need_eq)] = col;
         ++gb;
-      } else if (need_eq > 0u && key == tau) {
-        if (eb < need_eq) dst[gb + eb] = lo + i0 + u;
+      } else {
+        if (eb < need_eq) dst[gb + eb] = col;
         ++eb;
       }
     }
-    base_gt += total & 0xFFFFu;
-    base_eq += total >> 16;
   }
   const int nsel = nvalid < p.k ? nvalid : p.k;
   for (int i = nsel + tid; i < p.k; i += kThreads) dst[i] = -1;
@@ -202,12 +230,14 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
 
 }  // namespace
 
+int topk_bitmap_words(int max_row) { return (max_row + 31) / 32; }
+
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t s) {
   if (p.R <= 0) return cudaSuccess;
-  const size_t smem = sizeof(uint32_t) * (static_cast<size_t>(kHistBins) + p.cache_cap);
-  cudaError_t e =
-      cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem));
+  const size_t smem =
+      sizeof(uint32_t) * (static_cast<size_t>(kHistBins) + 2 * static_cast<size_t>(p.bitmap_words));
+  cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   topk_kernel<<<p.R, kThreads, smem, s>>>(p);
   return cudaGetLastError();
