@@ -57,6 +57,23 @@ uint32_t* error_word() {
   return addr[dev];
 }
 
+}  // namespace
+
+// SM count of the current device (queried once per device).
+int device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  static std::mutex mu;
+  static int count[kMaxDevices] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  if (count[dev] == 0 &&
+      cudaDeviceGetAttribute(&count[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    count[dev] = 0;
+  return count[dev];
+}
+
+namespace {
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 cudaStream_t as_stream(dsa_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }

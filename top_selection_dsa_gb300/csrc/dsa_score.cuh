@@ -7,19 +7,27 @@
 // row's range, -inf for the other columns of the key tiles it visits.
 //
 // Layout of the contraction: keys sit on the MMA M dimension (128 TMEM lanes
-// = 128 keys of a tile) and the group's query tokens x heads on N (up to 256
+// = 128 keys of a tile) and a group of query tokens x heads on N (up to 256
 // columns, e.g. 4 tokens x 64 heads).  Each epilogue thread therefore owns
 // one key and reduces over the heads of its own TMEM lane in registers.
 //
-// CTA roles (one CTA per SM; 192 or 320 threads):
-//   warp 0      TMA producer: the group's q tile once, then K tiles into an
-//               NST-deep ring of shared-memory stages (prefill: 2-D boxes of
-//               the [S, D] key matrix; paged: 3-D boxes of
+// Persistent CTAs (one per SM) walk a static list of work items -- a group of
+// TOK query rows (prefill) or one chunk of one request's keys (paged decode)
+// -- in snake order, so that the long causal groups spread evenly.  Roles:
+//   warp 0      TMA producer: each group's q tile into one of two q buffers,
+//               then its K tiles into an NST-deep ring of shared-memory stages
+//               (prefill: 2-D boxes of [S, D]; paged: 3-D boxes of
 //               [num_blocks, block_size, D] through the block table)
 //   warp 1      TMEM allocator + single-thread tcgen05.mma issuer into one of
-//               two TMEM accumulators (double buffer)
-//   warps 2..   epilogue: tcgen05.ld of the accumulator, ReLU, head-weighted
-//               sum in ascending head order, key scale, range mask, store
+//               two TMEM accumulators
+//   warps 2..   EPI_WG epilogue warpgroups, each owning EPI_COLS accumulator
+//               columns (whole tokens): one batched tcgen05.ld per tile, ReLU,
+//               head-weighted sum, key scale, range mask, store
+//
+// The head sum uses min(8, H) interleaved fp32 partial sums (head h goes to
+// partial h % 8, each accumulated in ascending h) combined pairwise.  The
+// order is fixed, so every entry point that scores the same inputs produces
+// bit-identical logits.
 #pragma once
 
 #include "dsa_common.cuh"
@@ -36,38 +44,114 @@ struct ScoreCfg {
   static constexpr int KSTEPS = ROW_BYTES / 32;     // one MMA consumes 32 bytes of K
   static constexpr int TILE = 128;                  // keys per tile = MMA M
   static constexpr int TOK = N / H;                 // query rows per group
-  static constexpr int EPI_WG = (N / 2 >= H) ? 2 : 1;
+  static constexpr int MINCOLS = H > 32 ? H : 32;
+  static constexpr int EPI_WG = (N / MINCOLS) < 4 ? (N / MINCOLS) : 4;
   static constexpr int EPI_COLS = N / EPI_WG;       // accumulator columns per epilogue thread
   static constexpr int EPI_TOK = EPI_COLS / H;
+  static constexpr int NPART = H < 8 ? H : 8;       // partial sums of the head reduction
   static constexpr int THREADS = 64 + 128 * EPI_WG;
   static constexpr int Q_BYTES = ATOMS * N * 128;
   static constexpr int STAGE_BYTES = ATOMS * TILE * 128;
-  static constexpr int MISC_BYTES = 4096;
+  // misc: w_s[N] | rs_s[TOK] | re_s[TOK] | 24 barriers | tmem slot + abort
+  static constexpr int MISC_W = 0;
+  static constexpr int MISC_RS = N * 4;
+  static constexpr int MISC_RE = MISC_RS + TOK * 4;
+  static constexpr int MISC_BARS = (MISC_RE + TOK * 4 + 7) / 8 * 8;
+  static constexpr int MISC_SLOT = MISC_BARS + 24 * 8;
+  static constexpr int MISC_BYTES = (MISC_SLOT + 16 + 127) / 128 * 128;
   static constexpr int SMEM_LIMIT = 232448;
-  static constexpr int NST_FIT = (SMEM_LIMIT - 1024 - MISC_BYTES - Q_BYTES) / STAGE_BYTES;
+  static constexpr int NST_FIT = (SMEM_LIMIT - 1024 - MISC_BYTES - 2 * Q_BYTES) / STAGE_BYTES;
   static constexpr int NST = NST_FIT > 8 ? 8 : NST_FIT;
-  static constexpr int SMEM = 1024 + Q_BYTES + NST * STAGE_BYTES + MISC_BYTES;
+  static constexpr int SMEM = 1024 + 2 * Q_BYTES + NST * STAGE_BYTES + MISC_BYTES;
   static constexpr uint32_t TMEM_COLS = 2u * N;
   static constexpr uint32_t IDESC = mma_idesc(kFp8 ? 0u : 1u, TILE, N);
 
   static_assert(ROW_BYTES % 128 == 0, "a key row must be a whole number of swizzle atoms");
   static_assert(N % 16 == 0 && N >= 32 && N <= 256, "MMA N for M=128");
-  static_assert(N % H == 0 && EPI_COLS % H == 0 && EPI_COLS % 32 == 0, "column split");
+  static_assert(N % H == 0 && EPI_COLS % H == 0 && (EPI_COLS == 32 || EPI_COLS == 64 ||
+                EPI_COLS == 128), "column split");
   static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM allocation");
   static_assert(NST >= 2 && NST <= 8, "pipeline depth");
   static_assert(SMEM <= SMEM_LIMIT, "shared memory");
 };
 
-// Shared-memory carve-up of the MISC region.
-struct ScoreMisc {
-  static constexpr int W = 0;           // float w_s[N]      (<= 1024 B)
-  static constexpr int RS = 1024;       // int rs_s[TOK]     (<= 1024 B)
-  static constexpr int RE = 2048;       // int re_s[TOK]     (<= 1024 B)
-  static constexpr int BARS = 3072;     // full[8], empty[8], qfull, accf[2], acce[2]
-  static constexpr int TMEM_SLOT = 3072 + 256;
-  static constexpr int INFO = 3072 + 272;   // int[4]: kt_begin, kt_end
-  static constexpr int ABORT = 3072 + 304;  // uint32 abort flag
+// One work item, as every role derives it.
+struct ScoreGroup {
+  int row0;      // first query row
+  int ntok;      // valid query rows (<= TOK)
+  int kt_begin;  // first key tile (prefill: absolute; paged: logical within the request)
+  int kt_end;    // one past the last key tile; kt_end <= kt_begin means nothing to do
+  int b;         // paged: request
+  int L;         // paged: clamped context length
+  bool bad_len;  // paged: context length was out of range
 };
+
+// Work item `slot`.  Must be called by all 32 lanes of a warp.
+template <int TOK, bool kPaged>
+__device__ __forceinline__ ScoreGroup score_group(const ScoreParams& p, int slot, int lane) {
+  ScoreGroup g;
+  g.bad_len = false;
+  if constexpr (kPaged) {
+    const int B = p.R / p.next_n;
+    const int c = slot / B;
+    g.b = slot % B;
+    const int Lraw = p.context_lens[g.b];
+    const int cap = p.max_blocks * p.block_size;
+    g.L = Lraw < 0 ? 0 : (Lraw > cap ? cap : Lraw);
+    g.bad_len = (c == 0) && (Lraw < 0 || Lraw > cap);
+    const int lo = c * p.chunk_keys;
+    const int hi = min(g.L, lo + p.chunk_keys);
+    g.row0 = g.b * p.next_n;
+    g.ntok = p.next_n;
+    g.kt_begin = lo / 128;
+    g.kt_end = hi > lo ? (hi + 127) / 128 : g.kt_begin;
+  } else {
+    const int G = (p.R + TOK - 1) / TOK;
+    const int grp = G - 1 - slot;  // later causal groups carry more keys: start with them
+    g.b = 0;
+    g.L = 0;
+    g.row0 = grp * TOK;
+    g.ntok = min(TOK, p.R - g.row0);
+    int lo = 0x7fffffff, hi = 0;
+    for (int i = lane; i < g.ntok; i += 32) {
+      const int a = min(max(p.row_starts[g.row0 + i], 0), p.S);
+      const int e = min(max(p.row_ends[g.row0 + i], 0), p.S);
+      if (e > a) {
+        lo = min(lo, a);
+        hi = max(hi, e);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+      hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    g.kt_begin = hi > lo ? lo / 128 : 0;
+    g.kt_end = hi > lo ? (hi + 127) / 128 : 0;
+  }
+  return g;
+}
+
+// Snake order over work items: round r visits CTAs 0..P-1 forward when r is
+// even and backward when r is odd.
+__device__ __forceinline__ int snake_slot(int r, int P, int cta) {
+  return r * P + ((r & 1) ? (P - 1 - cta) : cta);
+}
+
+template <int COLS>
+__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, float (&v)[COLS]) {
+  static_assert(COLS == 32 || COLS == 64 || COLS == 128, "tcgen05.ld width");
+  if constexpr (COLS == 32) {
+    tmem_load32(taddr, v);
+  } else if constexpr (COLS == 64) {
+    tmem_load64(taddr, v);
+  } else {
+    float* lo = v;
+    float* hi = v + 64;
+    tmem_load64(taddr, *reinterpret_cast<float(*)[64]>(lo));
+    tmem_load64(taddr + 64, *reinterpret_cast<float(*)[64]>(hi));
+  }
+}
 
 template <int H, int N, int D, bool kFp8, bool kPaged>
 __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
@@ -76,282 +160,289 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* q_s = smem;
-  uint8_t* k_s = smem + C::Q_BYTES;
+  uint8_t* q_s = smem;                         // 2 x Q_BYTES
+  uint8_t* k_s = smem + 2 * C::Q_BYTES;        // NST x STAGE_BYTES
   uint8_t* misc = k_s + C::NST * C::STAGE_BYTES;
-  float* w_s = reinterpret_cast<float*>(misc + ScoreMisc::W);
-  int* rs_s = reinterpret_cast<int*>(misc + ScoreMisc::RS);
-  int* re_s = reinterpret_cast<int*>(misc + ScoreMisc::RE);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(misc + ScoreMisc::BARS);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + 8;
-  uint64_t* qfull = bars + 16;
-  uint64_t* accf = bars + 17;
-  uint64_t* acce = bars + 19;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + ScoreMisc::TMEM_SLOT);
-  int* info = reinterpret_cast<int*>(misc + ScoreMisc::INFO);
-  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(misc + ScoreMisc::ABORT);
+  float* w_s = reinterpret_cast<float*>(misc + C::MISC_W);
+  int* rs_s = reinterpret_cast<int*>(misc + C::MISC_RS);
+  int* re_s = reinterpret_cast<int*>(misc + C::MISC_RE);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(misc + C::MISC_BARS);
+  uint64_t* full = bars;         // [8]
+  uint64_t* empty = bars + 8;    // [8]
+  uint64_t* qfull = bars + 16;   // [2]
+  uint64_t* qempty = bars + 18;  // [2]
+  uint64_t* accf = bars + 20;    // [2]
+  uint64_t* acce = bars + 22;    // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + C::MISC_SLOT);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(misc + C::MISC_SLOT + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  // ---------------------------------------------------------------- work item
-  int row0, ntok, b = 0, L = 0, key_lo = 0, key_hi = 0;
+  const int P = gridDim.x;
+  const int cta = blockIdx.x;
+  int nslots;
   if constexpr (kPaged) {
-    b = blockIdx.x / p.chunks_per_req;
-    const int c = blockIdx.x % p.chunks_per_req;
-    const int Lraw = p.context_lens[b];
-    const int cap = p.max_blocks * p.block_size;
-    L = Lraw < 0 ? 0 : (Lraw > cap ? cap : Lraw);
-    key_lo = c * p.chunk_keys;
-    key_hi = min(L, key_lo + p.chunk_keys);
-    if (c == 0 && threadIdx.x == 0 && (Lraw < 0 || Lraw > cap)) record_error(p.err, kErrBadIndex);
-    if (key_lo >= key_hi) return;  // whole CTA, before any barrier or TMEM use
-    row0 = b * p.next_n;
-    ntok = p.next_n;
+    nslots = (p.R / p.next_n) * p.chunks_per_req;
   } else {
-    const int g = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);
-    row0 = g * C::TOK;
-    ntok = min(C::TOK, p.R - row0);
+    nslots = (p.R + C::TOK - 1) / C::TOK;
   }
+  const int rounds = (nslots + P - 1) / P;
 
   // -------------------------------------------------------------------- setup
-  for (int i = threadIdx.x; i < N; i += C::THREADS) {
-    const int tok = i / H, h = i % H;
-    float wv = 0.f;
-    if (tok < ntok) {
-      const int64_t r = row0 + tok;
-      wv = p.weights[r * H + h];
-      if (p.q_scale) wv *= p.q_scale[r * H + h];
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::NST; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
     }
-    w_s[i] = wv;
-  }
-  for (int i = threadIdx.x; i < C::TOK; i += C::THREADS) {
-    int lo = 0, hi = 0;
-    if (i < ntok) {
-      if constexpr (kPaged) {
-        const int end = L - p.next_n + i + 1;
-        hi = end < 0 ? 0 : end;
-      } else {
-        lo = min(max(p.row_starts[row0 + i], 0), p.S);
-        hi = min(max(p.row_ends[row0 + i], 0), p.S);
-        if (hi < lo) hi = lo;
-      }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&qfull[i], 1);
+      mbar_init(&qempty[i], 1);
+      mbar_init(&accf[i], 1);
+      mbar_init(&acce[i], 128 * C::EPI_WG);
     }
-    rs_s[i] = lo;
-    re_s[i] = hi;
-  }
-  if (warp == 0) {
-    // Union of the group's key ranges -> tile range.
-    int lo = 0x7fffffff, hi = 0;
-    if constexpr (kPaged) {
-      lo = key_lo;
-      hi = key_hi;
-    } else {
-      for (int i = lane; i < ntok; i += 32) {
-        const int a = min(max(p.row_starts[row0 + i], 0), p.S);
-        const int e = min(max(p.row_ends[row0 + i], 0), p.S);
-        if (e > a) {
-          lo = min(lo, a);
-          hi = max(hi, e);
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
-      }
-    }
-    if (lane == 0) {
-      if (hi > lo) {
-        info[0] = lo / C::TILE;
-        info[1] = (hi + C::TILE - 1) / C::TILE;
-      } else {
-        info[0] = 0;
-        info[1] = 0;
-      }
-      for (int s = 0; s < C::NST; ++s) {
-        mbar_init(&full[s], 1);
-        mbar_init(&empty[s], 1);
-      }
-      mbar_init(qfull, 1);
-      for (int i = 0; i < 2; ++i) {
-        mbar_init(&accf[i], 1);
-        mbar_init(&acce[i], 128 * C::EPI_WG);
-      }
-      *abort_flag = 0;
-      fence_barrier_init();
-    }
+    *abort_flag = 0;
+    fence_barrier_init();
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
-  const int kt_begin = info[0], kt_end = info[1];
 
-  // -------------------------------------------------------------------- roles
   if (warp == 0) {
-    if (lane == 0 && kt_end > kt_begin) {
+    // ------------------------------------------------------------- producer
+    int kiter = 0, ngroups = 0, qissued = 0;
+    bool ok = true;
+    if (lane == 0) {
       tma_prefetch_desc(&p.tmap_q);
       tma_prefetch_desc(&p.tmap_k);
-      mbar_arrive_expect_tx(qfull, C::Q_BYTES);
-#pragma unroll
-      for (int a = 0; a < C::ATOMS; ++a)
-        tma_load_2d(q_s + a * N * 128, &p.tmap_q, qfull, a * C::ATOM_ELEMS, row0 * H);
-      int stage = 0;
-      uint32_t phase = 0;
-      int issued = 0;
-      bool ok = true;
-      for (int kt = kt_begin; kt < kt_end; ++kt) {
-        if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag)) {
+    }
+    for (int r = 0; r < rounds && ok; ++r) {
+      const int slot = snake_slot(r, P, cta);
+      if (slot >= nslots) continue;
+      const ScoreGroup g = score_group<C::TOK, kPaged>(p, slot, lane);
+      if (g.kt_end <= g.kt_begin) continue;
+      if (lane == 0) {
+        const int qb = ngroups & 1;
+        if (!mbar_wait_bounded(&qempty[qb], ((ngroups >> 1) & 1u) ^ 1u, abort_flag)) {
           ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-        uint8_t* dst = k_s + stage * C::STAGE_BYTES;
-        if constexpr (!kPaged) {
+        } else {
+          mbar_arrive_expect_tx(&qfull[qb], C::Q_BYTES);
 #pragma unroll
           for (int a = 0; a < C::ATOMS; ++a)
-            tma_load_2d(dst + a * C::TILE * 128, &p.tmap_k, &full[stage], a * C::ATOM_ELEMS,
-                        kt * C::TILE);
-        } else {
-          const int bs = p.block_size;
-          const int nblk = (L + bs - 1) / bs;
-          const int per_tile = C::TILE / bs;
-          for (int i = 0; i < per_tile; ++i) {
-            int lb = kt * per_tile + i;
-            if (lb > nblk - 1) lb = nblk - 1;
-            int pb = p.block_table[static_cast<int64_t>(b) * p.max_blocks + lb];
-            if (pb < 0 || pb >= p.num_blocks) {
-              record_error(p.err, kErrBadIndex);
-              pb = 0;
+            tma_load_2d(q_s + qb * C::Q_BYTES + a * N * 128, &p.tmap_q, &qfull[qb],
+                        a * C::ATOM_ELEMS, g.row0 * H);
+          ++qissued;
+          for (int kt = g.kt_begin; kt < g.kt_end; ++kt) {
+            const int stage = kiter % C::NST;
+            const uint32_t phase = static_cast<uint32_t>(kiter / C::NST) & 1u;
+            if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag)) {
+              ok = false;
+              break;
             }
+            mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+            uint8_t* dst = k_s + stage * C::STAGE_BYTES;
+            if constexpr (!kPaged) {
 #pragma unroll
-            for (int a = 0; a < C::ATOMS; ++a)
-              tma_load_3d(dst + a * C::TILE * 128 + i * bs * 128, &p.tmap_k, &full[stage],
-                          a * C::ATOM_ELEMS, 0, pb);
+              for (int a = 0; a < C::ATOMS; ++a)
+                tma_load_2d(dst + a * C::TILE * 128, &p.tmap_k, &full[stage],
+                            a * C::ATOM_ELEMS, kt * C::TILE);
+            } else {
+              const int bs = p.block_size;
+              const int nblk = (g.L + bs - 1) / bs;
+              const int per_tile = C::TILE / bs;
+              for (int i = 0; i < per_tile; ++i) {
+                int lb = kt * per_tile + i;
+                if (lb > nblk - 1) lb = nblk - 1;
+                int pb = p.block_table[static_cast<int64_t>(g.b) * p.max_blocks + lb];
+                if (pb < 0 || pb >= p.num_blocks) {
+                  record_error(p.err, kErrBadIndex);
+                  pb = 0;
+                }
+#pragma unroll
+                for (int a = 0; a < C::ATOMS; ++a)
+                  tma_load_3d(dst + a * C::TILE * 128 + i * bs * 128, &p.tmap_k, &full[stage],
+                              a * C::ATOM_ELEMS, 0, pb);
+              }
+            }
+            ++kiter;
           }
         }
-        ++issued;
-        if (++stage == C::NST) {
-          stage = 0;
-          phase ^= 1u;
-        }
+        ++ngroups;
       }
-      if (!ok) {
-        *abort_flag = 1;
-        record_error(p.err, kErrTimeout);
-        // Let the copies already in flight land before the CTA retires.
-        mbar_wait_bounded(qfull, 0, nullptr, 100000000ull);
-        const int first = issued > C::NST ? issued - C::NST : 0;
-        for (int i = first; i < issued; ++i)
-          mbar_wait_bounded(&full[i % C::NST], (i / C::NST) & 1u, nullptr, 100000000ull);
-      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    }
+    if (lane == 0 && !ok) {
+      *abort_flag = 1;
+      record_error(p.err, kErrTimeout);
+      // Let the copies already in flight land before the CTA retires.
+      const int first = kiter > C::NST ? kiter - C::NST : 0;
+      for (int i = first; i < kiter; ++i)
+        mbar_wait_bounded(&full[i % C::NST], static_cast<uint32_t>(i / C::NST) & 1u, nullptr,
+                          100000000ull);
+      for (int j = qissued > 2 ? qissued - 2 : 0; j < qissued; ++j)
+        mbar_wait_bounded(&qfull[j & 1], static_cast<uint32_t>(j >> 1) & 1u, nullptr,
+                          100000000ull);
     }
   } else if (warp == 1) {
-    if (lane == 0 && kt_end > kt_begin) {
-      bool ok = mbar_wait_bounded(qfull, 0, abort_flag);
-      int stage = 0;
-      uint32_t phase = 0;
-      int issued = 0;
-      const uint32_t q_addr = smem_u32(q_s);
-      for (int kt = kt_begin; ok && kt < kt_end; ++kt) {
-        const int it = kt - kt_begin;
-        const int buf = it & 1;
-        const uint32_t aphase = static_cast<uint32_t>(it >> 1) & 1u;
-        if (!mbar_wait_bounded(&acce[buf], aphase ^ 1u, abort_flag) ||
-            !mbar_wait_bounded(&full[stage], phase, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * N);
-        const uint32_t k_addr = smem_u32(k_s + stage * C::STAGE_BYTES);
+    // ----------------------------------------------------------- MMA issuer
+    int kiter = 0, ngroups = 0, tcount = 0;
+    bool ok = true;
+    for (int r = 0; r < rounds && ok; ++r) {
+      const int slot = snake_slot(r, P, cta);
+      if (slot >= nslots) continue;
+      const ScoreGroup g = score_group<C::TOK, kPaged>(p, slot, lane);
+      if (g.kt_end <= g.kt_begin) continue;
+      if (lane == 0) {
+        const int qb = ngroups & 1;
+        ok = mbar_wait_bounded(&qfull[qb], static_cast<uint32_t>(ngroups >> 1) & 1u, abort_flag);
+        const uint32_t q_addr = smem_u32(q_s + qb * C::Q_BYTES);
+        for (int kt = g.kt_begin; ok && kt < g.kt_end; ++kt) {
+          const int stage = kiter % C::NST;
+          const uint32_t phase = static_cast<uint32_t>(kiter / C::NST) & 1u;
+          const int buf = tcount & 1;
+          const uint32_t aphase = static_cast<uint32_t>(tcount >> 1) & 1u;
+          if (!mbar_wait_bounded(&acce[buf], aphase ^ 1u, abort_flag) ||
+              !mbar_wait_bounded(&full[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * N);
+          const uint32_t k_addr = smem_u32(k_s + stage * C::STAGE_BYTES);
 #pragma unroll
-        for (int ks = 0; ks < C::KSTEPS; ++ks) {
-          const int atom = ks / 4, within = ks % 4;
-          const uint64_t adesc = sw128_kmajor_desc(k_addr + atom * C::TILE * 128 + within * 32);
-          const uint64_t bdesc = sw128_kmajor_desc(q_addr + atom * N * 128 + within * 32);
-          mma_ss<kFp8>(d_tmem, adesc, bdesc, C::IDESC, ks > 0 ? 1u : 0u);
+          for (int ks = 0; ks < C::KSTEPS; ++ks) {
+            const int atom = ks / 4, within = ks % 4;
+            const uint64_t adesc =
+                sw128_kmajor_desc(k_addr + atom * C::TILE * 128 + within * 32);
+            const uint64_t bdesc = sw128_kmajor_desc(q_addr + atom * N * 128 + within * 32);
+            mma_ss<kFp8>(d_tmem, adesc, bdesc, C::IDESC, ks > 0 ? 1u : 0u);
+          }
+          mma_commit(&empty[stage]);
+          mma_commit(&accf[buf]);
+          ++kiter;
+          ++tcount;
         }
-        mma_commit(&empty[stage]);
-        mma_commit(&accf[buf]);
-        ++issued;
-        if (++stage == C::NST) {
-          stage = 0;
-          phase ^= 1u;
-        }
+        if (ok) mma_commit(&qempty[qb]);  // q buffer free once this group's MMAs are done
+        ++ngroups;
       }
-      if (!ok) {
-        *abort_flag = 1;
-        record_error(p.err, kErrTimeout);
-        if (issued > 0) {
-          // The last commit covers every MMA issued before it.
-          const int last = issued - 1;
-          mbar_wait_bounded(&accf[last & 1], static_cast<uint32_t>(last >> 1) & 1u, nullptr,
-                            100000000ull);
-        }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    }
+    if (lane == 0 && !ok) {
+      *abort_flag = 1;
+      record_error(p.err, kErrTimeout);
+      if (tcount > 0) {
+        // The last commit covers every MMA issued before it.
+        const int last = tcount - 1;
+        mbar_wait_bounded(&accf[last & 1], static_cast<uint32_t>(last >> 1) & 1u, nullptr,
+                          100000000ull);
       }
     }
   } else {
-    // ---------------------------------------------------------------- epilogue
+    // ------------------------------------------------------------- epilogue
     const int ew = warp - 2;
-    const int wg = ew >> 2;       // which column half
+    const int wg = ew >> 2;        // column group of this warpgroup
     const int quarter = warp & 3;  // the TMEM lane quarter this warp may access
     const int key_in_tile = quarter * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-    for (int kt = kt_begin; kt < kt_end; ++kt) {
-      const int it = kt - kt_begin;
-      const int buf = it & 1;
-      const uint32_t aphase = static_cast<uint32_t>(it >> 1) & 1u;
-      if (!mbar_wait_bounded(&accf[buf], aphase, abort_flag)) {
-        *abort_flag = 1;
-        record_error(p.err, kErrTimeout);
-        break;
+    const int etid = threadIdx.x - 64;  // 0 .. 128*EPI_WG-1
+    int tcount = 0;
+    bool ok = true;
+    // No early exit from this loop: every epilogue warp must reach the same
+    // named barriers.  After an abort the tile waits fail at once instead.
+    for (int r = 0; r < rounds; ++r) {
+      const int slot = snake_slot(r, P, cta);
+      if (slot >= nslots) continue;
+      const ScoreGroup g = score_group<C::TOK, kPaged>(p, slot, lane);
+      if (etid == 0 && g.bad_len) record_error(p.err, kErrBadIndex);
+      if (g.kt_end <= g.kt_begin) continue;
+      // Stage this group's weights and row ranges (every epilogue thread has
+      // finished the previous group when the named barrier opens).
+      asm volatile("bar.sync 1, %0;" ::"r"(128 * C::EPI_WG) : "memory");
+      for (int i = etid; i < N; i += 128 * C::EPI_WG) {
+        const int tok = i / H, h = i % H;
+        float wv = 0.f;
+        if (tok < g.ntok) {
+          const int64_t row = g.row0 + tok;
+          wv = p.weights[row * H + h];
+          if (p.q_scale) wv *= p.q_scale[row * H + h];
+        }
+        w_s[i] = wv;
       }
-      tc_fence_after_sync();
-      float v[C::EPI_COLS];
-#pragma unroll
-      for (int c = 0; c < C::EPI_COLS; c += 32) {
-        float chunk[32];
-        tmem_load32(tmem_base + lane_addr + static_cast<uint32_t>(buf * N + wg * C::EPI_COLS + c),
-                    chunk);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[c + i] = chunk[i];
+      for (int i = etid; i < C::TOK; i += 128 * C::EPI_WG) {
+        int lo = 0, hi = 0;
+        if (i < g.ntok) {
+          if constexpr (kPaged) {
+            const int end = g.L - p.next_n + i + 1;
+            hi = end < 0 ? 0 : end;
+          } else {
+            lo = min(max(p.row_starts[g.row0 + i], 0), p.S);
+            hi = min(max(p.row_ends[g.row0 + i], 0), p.S);
+            if (hi < lo) hi = lo;
+          }
+        }
+        rs_s[i] = lo;
+        re_s[i] = hi;
       }
-      tc_fence_before_sync();
-      mbar_arrive(&acce[buf]);
+      asm volatile("bar.sync 1, %0;" ::"r"(128 * C::EPI_WG) : "memory");
 
-      const int s = kt * C::TILE + key_in_tile;
-      float kscale = 1.f;
-      if constexpr (kFp8) {
-        if constexpr (kPaged) {
-          const int bs = p.block_size;
-          const int nblk = (L + bs - 1) / bs;
-          int lb = s / bs;
-          if (lb > nblk - 1) lb = nblk - 1;
-          int pb = p.block_table[static_cast<int64_t>(b) * p.max_blocks + lb];
-          if (pb < 0 || pb >= p.num_blocks) pb = 0;
-          kscale = p.k_scale[static_cast<int64_t>(pb) * bs + (s % bs)];
-        } else {
-          kscale = s < p.S ? p.k_scale[s] : 0.f;
+      for (int kt = g.kt_begin; ok && kt < g.kt_end; ++kt) {
+        const int buf = tcount & 1;
+        const uint32_t aphase = static_cast<uint32_t>(tcount >> 1) & 1u;
+        // Warp-uniform outcome: tcgen05.ld below needs every lane.
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&accf[buf], aphase, abort_flag) ? 1 : 0);
+        if (!ok) break;
+        tc_fence_after_sync();
+        float v[C::EPI_COLS];
+        tmem_load_cols<C::EPI_COLS>(
+            tmem_base + lane_addr + static_cast<uint32_t>(buf * N + wg * C::EPI_COLS), v);
+        tc_fence_before_sync();
+        mbar_arrive(&acce[buf]);
+        ++tcount;
+
+        const int s = kt * C::TILE + key_in_tile;
+        float kscale = 1.f;
+        if constexpr (kFp8) {
+          if constexpr (kPaged) {
+            const int bs = p.block_size;
+            const int nblk = (g.L + bs - 1) / bs;
+            int lb = s / bs;
+            if (lb > nblk - 1) lb = nblk - 1;
+            int pb = p.block_table[static_cast<int64_t>(g.b) * p.max_blocks + lb];
+            if (pb < 0 || pb >= p.num_blocks) pb = 0;
+            kscale = p.k_scale[static_cast<int64_t>(pb) * bs + (s % bs)];
+          } else {
+            kscale = s < p.S ? p.k_scale[s] : 0.f;
+          }
+        }
+        const bool col_ok = s < p.S;
+#pragma unroll
+        for (int j = 0; j < C::EPI_TOK; ++j) {
+          const int tok = wg * C::EPI_TOK + j;
+          const float* wt = w_s + tok * H;
+          float part[C::NPART];
+#pragma unroll
+          for (int i = 0; i < C::NPART; ++i) part[i] = 0.f;
+#pragma unroll
+          for (int h = 0; h < H; ++h)
+            part[h % C::NPART] = fmaf(wt[h], fmaxf(v[j * H + h], 0.f), part[h % C::NPART]);
+#pragma unroll
+          for (int w = C::NPART / 2; w > 0; w >>= 1) {
+#pragma unroll
+            for (int i = 0; i < w; ++i) part[i] = part[i] + part[i + w];
+          }
+          float acc = part[0];
+          if constexpr (kFp8) acc *= kscale;
+          if (tok < g.ntok && col_ok) {
+            const float val = (s >= rs_s[tok] && s < re_s[tok]) ? acc : -INFINITY;
+            p.logits[static_cast<int64_t>(g.row0 + tok) * p.ld + s] = val;
+          }
         }
       }
-      const bool col_ok = s < p.S;
-#pragma unroll
-      for (int j = 0; j < C::EPI_TOK; ++j) {
-        const int tok = wg * C::EPI_TOK + j;
-        const float* wt = w_s + tok * H;
-        float acc = 0.f;
-#pragma unroll
-        for (int h = 0; h < H; ++h) acc = fmaf(wt[h], fmaxf(v[j * H + h], 0.f), acc);
-        if constexpr (kFp8) acc *= kscale;
-        if (tok < ntok && col_ok) {
-          const float val = (s >= rs_s[tok] && s < re_s[tok]) ? acc : -INFINITY;
-          p.logits[static_cast<int64_t>(row0 + tok) * p.ld + s] = val;
-        }
-      }
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      record_error(p.err, kErrTimeout);
     }
   }
 
@@ -364,13 +455,18 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
   }
 }
 
+int device_sm_count();
+
 template <int H, int N, int D, bool kFp8, bool kPaged>
-cudaError_t launch_score_instance(const ScoreParams& p, int grid, cudaStream_t st) {
+cudaError_t launch_score_instance(const ScoreParams& p, int work_items, cudaStream_t st) {
   using C = ScoreCfg<H, N, D, kFp8, kPaged>;
   auto kern = score_kernel<H, N, D, kFp8, kPaged>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  if (grid <= 0) return cudaSuccess;
+  if (work_items <= 0) return cudaSuccess;
+  const int sms = device_sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const int grid = work_items < sms ? work_items : sms;
   kern<<<grid, C::THREADS, C::SMEM, st>>>(p);
   return cudaGetLastError();
 }
