@@ -195,14 +195,18 @@ def test_topk_edge_cases(api):
     assert (got[7] == np.arange(10, 10 + k)).all()
 
 
-@pytest.mark.parametrize("S,k", [(131072, 2048), (60000, 2048), (2049, 2048), (2048, 2048),
-                                 (100, 1), (4096, 4096)])
+# Row lengths that reach every top-k kernel variant: register-resident CTAs
+# of 4K/8K/16K/32K keys, clusters of 2/4/8 CTAs, and the streaming kernel.
+@pytest.mark.parametrize("S,k", [(100, 1), (2048, 2048), (2049, 2048), (4096, 4096),
+                                 (8000, 2048), (16384, 3000), (30000, 2048), (60000, 2048),
+                                 (131072, 2048), (200000, 5000), (300000, 2048)])
 def test_topk_row_lengths(api, S, k):
     rng = np.random.default_rng(S + k)
-    T = 6
+    T = 7
     lg = (rng.standard_normal((T, S)) * 4).round().astype(np.float32)   # many ties
-    rs = np.zeros(T, np.int32)
-    re = np.array([S, S - 1, S // 2, k, k - 1, 1], np.int32)
+    lg[6] = rng.standard_normal(S).astype(np.float32)                   # few ties
+    rs = np.array([0, 0, 0, 0, 0, 0, S // 3], np.int32)
+    re = np.array([S, S - 1, S // 2, k, k - 1, 1, S], np.int32)
     got = api.topk(dev(lg), dev(rs), dev(re), k).cpu().numpy()
     assert np.array_equal(got, oracle.topk(lg, rs, re, k))
 

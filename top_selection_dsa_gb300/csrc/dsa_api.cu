@@ -321,6 +321,7 @@ dsa_status_t dsa_topk(const float* logits, int64_t ld, const int32_t* row_starts
   if (!aligned(logits, 4) || !aligned(out, 4) || !aligned(row_starts, 4) ||
       !aligned(row_ends, 4))
     return DSA_ERR_INVALID_ARG;
+  if (!topk_supported(S)) return DSA_ERR_UNSUPPORTED;
   return run_topk(logits, ld, row_starts, row_ends, nullptr, 1, T, S, k, out, as_stream(stream));
 }
 
@@ -333,6 +334,7 @@ dsa_status_t dsa_indexer_topk(const void* q, const float* q_scale, const void* k
                                       row_ends, T, S, H, D);
   if (st != DSA_OK) return st;
   if (!out || !aligned(out, 4) || topk < 1) return DSA_ERR_INVALID_ARG;
+  if (!topk_supported(S)) return DSA_ERR_UNSUPPORTED;
   const size_t need = dsa_workspace_bytes(DSA_OP_INDEXER_TOPK, T, S, topk);
   if (need > 0 && (!workspace || ws_bytes < need || !aligned(workspace, 256)))
     return DSA_ERR_INVALID_ARG;
@@ -374,6 +376,7 @@ dsa_status_t dsa_indexer_topk_paged(const void* q, const float* q_scale, const f
   if (!out || !aligned(out, 4) || topk < 1) return DSA_ERR_INVALID_ARG;
   const int64_t R = static_cast<int64_t>(B) * next_n;
   const int64_t max_ctx = static_cast<int64_t>(max_blocks) * block_size;
+  if (!topk_supported(static_cast<int>(max_ctx))) return DSA_ERR_UNSUPPORTED;
   const size_t need = dsa_workspace_bytes(DSA_OP_INDEXER_TOPK_PAGED, R, max_ctx, topk);
   if (need > 0 && (!workspace || ws_bytes < need || !aligned(workspace, 256)))
     return DSA_ERR_INVALID_ARG;

@@ -62,6 +62,8 @@ int score_tokens_per_group(int H);
 
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t s);
 int topk_bitmap_words(int max_row);
+// Whether rows of up to max_row columns fit the top-k kernels.
+bool topk_supported(int max_row);
 cudaError_t launch_fill(float* dst, int64_t rows, int64_t cols, int64_t ld, float value,
                         cudaStream_t s);
 cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint64_t timeout_ns, cudaStream_t s);

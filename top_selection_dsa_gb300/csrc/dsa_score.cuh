@@ -187,6 +187,18 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
     nslots = (p.R + C::TOK - 1) / C::TOK;
   }
   const int rounds = (nslots + P - 1) / P;
+  if constexpr (kPaged) {
+    // Paged decode launches one CTA per work item: a CTA whose chunk lies past
+    // its request's context leaves before touching barriers or TMEM.
+    if (rounds == 1) {
+      const int slot = snake_slot(0, P, cta);
+      const ScoreGroup g0 = score_group<C::TOK, kPaged>(p, slot, lane);
+      if (slot >= nslots || g0.kt_end <= g0.kt_begin) {
+        if (threadIdx.x == 0 && slot < nslots && g0.bad_len) record_error(p.err, kErrBadIndex);
+        return;
+      }
+    }
+  }
 
   // -------------------------------------------------------------------- setup
   if (threadIdx.x == 0) {
@@ -457,6 +469,8 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
 
 int device_sm_count();
 
+// Prefill runs persistent CTAs (one per SM); paged decode runs one CTA per
+// work item, most of which exit at once, and lets the hardware balance them.
 template <int H, int N, int D, bool kFp8, bool kPaged>
 cudaError_t launch_score_instance(const ScoreParams& p, int work_items, cudaStream_t st) {
   using C = ScoreCfg<H, N, D, kFp8, kPaged>;
@@ -464,9 +478,12 @@ cudaError_t launch_score_instance(const ScoreParams& p, int work_items, cudaStre
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   if (work_items <= 0) return cudaSuccess;
-  const int sms = device_sm_count();
-  if (sms <= 0) return cudaErrorInvalidDevice;
-  const int grid = work_items < sms ? work_items : sms;
+  int grid = work_items;
+  if constexpr (!kPaged) {
+    const int sms = device_sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    grid = work_items < sms ? work_items : sms;
+  }
   kern<<<grid, C::THREADS, C::SMEM, st>>>(p);
   return cudaGetLastError();
 }

@@ -7,29 +7,29 @@
 // page is silent: ties go to the lower column (-0.0 equals +0.0), NaN is never
 // selected, and the selected columns are written in ascending column order.
 //
-// One 256-thread CTA per row; several rows share an SM, so the per-row
-// barriers of one CTA overlap with the memory traffic of the others.
-//   1. every logit becomes an order-preserving 32-bit key (larger float ->
-//      larger key; -0.0 folded onto +0.0; -inf and NaN -> 0, which no valid
-//      score maps to); pass 1 streams the row from HBM with 16-byte loads and
-//      histograms the top 11 key bits;
-//   2. if at most k keys are valid, every valid key is taken; otherwise two
-//      more histogram passes (11 and 10 bits, re-reading the row, which is
-//      now in L2) find the exact k-th largest key tau and how many keys equal
-//      to tau to take (need_eq) after all keys greater than tau;
-//   3. a last pass turns the row into two bitmaps (key > tau, key == tau) with
-//      warp ballots; one prefix scan over the words gives every selected
-//      column its output position, so indices come out in column order; the
-//      first need_eq ties (in column order) are the ones kept; -1 fills the
-//      tail of the output row.
+// Every logit becomes an order-preserving 32-bit key (larger float -> larger
+// key; -0.0 folded onto +0.0; -inf and NaN -> 0, which no valid score maps
+// to).  The exact k-th largest key tau is found by a radix select over the key
+// bits (11 + 11 + 10), after which every key > tau and the first need_eq keys
+// == tau (in column order) are taken.  The output order comes from warp-ballot
+// bitmaps of (key > tau) and (key == tau) and one prefix count over their
+// words, so selected columns are written in ascending order directly.
+//
+// Two kernels:
+//   topk_reg_kernel<THREADS, ITEMS, CL>  a row of up to CL*THREADS*ITEMS keys
+//       is read once from memory into registers (ITEMS per thread, striped so
+//       that each warp's loads are contiguous); the radix passes and the
+//       bitmaps work on registers only.  CL > 1 spreads a row over a
+//       thread-block cluster whose CTAs merge their histograms and counts
+//       through distributed shared memory.
+//   topk_stream_kernel  rows longer than the largest cluster: one CTA per row,
+//       histogram passes re-read the row from memory.
 #include "dsa_common.cuh"
 #include "dsa_internal.h"
 
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
 constexpr int kHistBins = 2048;
 
 __device__ __forceinline__ uint32_t order_key(float x) {
@@ -40,9 +40,46 @@ __device__ __forceinline__ uint32_t order_key(float x) {
   return invalid ? 0u : key;
 }
 
-// Exclusive prefix sums of two counters per thread over the block.  Contains
-// barriers: every thread must call it.
-__device__ __forceinline__ uint2 block_exclusive_scan2(uint2 v, uint2* warp_sums, uint2* total) {
+// ---------------------------------------------------------------- clusters
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of every CTA of the cluster arrives and waits (release/acquire
+// ordering of shared memory across the cluster).
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of `p` (this CTA's shared memory) in the shared memory of CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_map(const void* p, uint32_t rank) {
+  uint32_t out;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(smem_u32(p)), "r"(rank));
+  return out;
+}
+
+__device__ __forceinline__ void cluster_add(uint32_t addr, uint32_t v) {
+  asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_load(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// ------------------------------------------------------------- block scans
+
+// Exclusive prefix sums of two counters per thread over the block; *total
+// gets the block sums.  Contains barriers: every thread must call it.
+template <int THREADS>
+__device__ __forceinline__ uint2 block_scan2(uint2 v, uint2* warp_sums, uint2* total) {
+  constexpr int NW = THREADS / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint2 x = v;
 #pragma unroll
@@ -58,7 +95,7 @@ __device__ __forceinline__ uint2 block_exclusive_scan2(uint2 v, uint2* warp_sums
   __syncthreads();
   uint2 before = make_uint2(0u, 0u), all = make_uint2(0u, 0u);
 #pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
+  for (int w = 0; w < NW; ++w) {
     const uint2 s = warp_sums[w];
     if (w < warp) {
       before.x += s.x;
@@ -72,18 +109,20 @@ __device__ __forceinline__ uint2 block_exclusive_scan2(uint2 v, uint2* warp_sums
   return make_uint2(before.x + x.x - v.x, before.y + x.y - v.y);
 }
 
-// Over hist[0..nbins), the bin b holding the r-th largest element (r >= 1):
-// above = sum of bins > b satisfies above < r <= above + hist[b].  Every thread
-// returns the same (b, above).
-__device__ __forceinline__ void find_bin(const uint32_t* hist, int nbins, uint32_t r,
-                                         uint2* warp_sums, uint32_t* sel, uint32_t* bin,
-                                         uint32_t* above) {
-  const int per = nbins / kThreads;  // bins per thread, highest bins first
-  const int top = nbins - 1 - threadIdx.x * per;
+// Over hist[0..nbins), the bin b holding the r-th largest element: above =
+// sum of bins > b satisfies above < r <= above + hist[b].  Returns the sum of
+// all bins; (b, above) are valid when r <= that sum.  Every thread gets the
+// same values.
+template <int THREADS>
+__device__ __forceinline__ uint32_t find_bin(const uint32_t* hist, int nbins, uint32_t r,
+                                             uint2* warp_sums, uint32_t* sel, uint32_t* bin,
+                                             uint32_t* above) {
+  const int per = nbins / THREADS;  // bins per thread, highest bins first
+  const int top = nbins - 1 - static_cast<int>(threadIdx.x) * per;
   uint32_t local = 0;
   for (int i = 0; i < per; ++i) local += hist[top - i];
   uint2 total;
-  const uint32_t excl = block_exclusive_scan2(make_uint2(local, 0u), warp_sums, &total).x;
+  const uint32_t excl = block_scan2<THREADS>(make_uint2(local, 0u), warp_sums, &total).x;
   if (excl < r && r <= excl + local) {
     uint32_t acc = excl;
     for (int i = 0; i < per; ++i) {
@@ -99,106 +138,230 @@ __device__ __forceinline__ void find_bin(const uint32_t* hist, int nbins, uint32
   __syncthreads();
   *bin = sel[0];
   *above = sel[1];
+  return total.x;
 }
 
-__global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
+__device__ __forceinline__ void row_range(const TopkParams& p, int row, int* lo, int* hi) {
+  if (p.context_lens) {
+    const int b = row / p.next_n, j = row % p.next_n;
+    const int end = p.context_lens[b] - p.next_n + j + 1;
+    *lo = 0;
+    *hi = min(max(end, 0), p.S);
+  } else {
+    *lo = min(max(p.row_starts[row], 0), p.S);
+    *hi = min(max(p.row_ends[row], 0), p.S);
+    if (*hi < *lo) *hi = *lo;
+  }
+}
+
+// ------------------------------------------------------ register-resident
+
+template <int THREADS, int ITEMS, int CL>
+__global__ void __launch_bounds__(THREADS, 1) topk_reg_kernel(const TopkParams p) {
+  constexpr int NW = THREADS / 32;
+  constexpr int SEG = THREADS * ITEMS;  // keys per CTA
+  constexpr int WORDS = SEG / 32;
+  __shared__ uint32_t hist[kHistBins];
+  __shared__ uint32_t merged[CL > 1 ? kHistBins : 1];
+  __shared__ uint32_t gt_bits[WORDS];
+  __shared__ uint32_t eq_bits[WORDS];
+  __shared__ uint2 warp_sums[NW];
+  __shared__ uint32_t sel[2];
+  __shared__ uint2 cta_total;
+  __shared__ uint2 cta_base;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t rank = CL > 1 ? cluster_rank() : 0u;
+  const int row = CL > 1 ? static_cast<int>(blockIdx.x) / CL : static_cast<int>(blockIdx.x);
+  int lo, hi;
+  row_range(p, row, &lo, &hi);
+  const int n = hi - lo;
+  const int seg0 = static_cast<int>(rank) * SEG;
+  const float* src = p.logits + static_cast<int64_t>(row) * p.ld + lo;
+  int32_t* dst = p.out + static_cast<int64_t>(row) * p.k;
+
+  // One read of the row segment: element seg0 + u*THREADS + tid.
+  float val[ITEMS];
+#pragma unroll
+  for (int u = 0; u < ITEMS; ++u) {
+    const int e = seg0 + u * THREADS + tid;
+    val[u] = e < n ? src[e] : -INFINITY;
+  }
+  uint32_t key[ITEMS];
+#pragma unroll
+  for (int u = 0; u < ITEMS; ++u) key[u] = order_key(val[u]);
+
+  // Radix select over digits of 11, 11 and 10 bits.
+  uint32_t prefix = 0u, rem = static_cast<uint32_t>(p.k), nvalid = 0u;
+  bool take_all = false;
+#pragma unroll 1
+  for (int d = 0; d < 3; ++d) {
+    const int shift = d == 0 ? 21 : (d == 1 ? 10 : 0);
+    const int pshift = d == 1 ? 21 : 10;  // prefix of the keys still in play (d > 0)
+    const int nbins = d == 2 ? 1024 : 2048;
+    for (int i = tid; i < nbins; i += THREADS) {
+      hist[i] = 0u;
+      if (CL > 1 && rank == 0) merged[i] = 0u;
+    }
+    if constexpr (CL > 1) cluster_barrier(); else __syncthreads();
+#pragma unroll
+    for (int u = 0; u < ITEMS; ++u) {
+      const uint32_t kk = key[u];
+      const bool live = kk != 0u && (d == 0 || (kk >> pshift) == prefix);
+      if (live) atomicAdd(&hist[(kk >> shift) & static_cast<uint32_t>(nbins - 1)], 1u);
+    }
+    __syncthreads();
+    if constexpr (CL > 1) {
+      // Merge into the leader's histogram, then every CTA takes a copy.
+      const uint32_t leader = cluster_map(merged, 0);
+      for (int i = tid; i < nbins; i += THREADS) {
+        const uint32_t v = hist[i];
+        if (v) cluster_add(leader + 4u * i, v);
+      }
+      cluster_barrier();
+      for (int i = tid; i < nbins; i += THREADS) hist[i] = cluster_load(leader + 4u * i);
+      cluster_barrier();
+    }
+    uint32_t b, above;
+    const uint32_t total = find_bin<THREADS>(hist, nbins, rem, warp_sums, sel, &b, &above);
+    if (d == 0) {
+      nvalid = total;
+      if (nvalid <= static_cast<uint32_t>(p.k)) {
+        take_all = true;
+        break;
+      }
+    }
+    rem -= above;
+    prefix = d == 0 ? b : ((prefix << (d == 1 ? 11 : 10)) | b);
+    __syncthreads();
+  }
+  const uint32_t tau = take_all ? 0u : prefix;      // take every key > tau ...
+  const uint32_t need_eq = take_all ? 0u : rem;     // ... and the first need_eq keys == tau
+
+  // Bitmaps: word u*NW + warp holds columns seg0 + (u*NW + warp)*32 + lane.
+#pragma unroll
+  for (int u = 0; u < ITEMS; ++u) {
+    const uint32_t g = __ballot_sync(0xffffffffu, key[u] > tau);
+    const uint32_t e = __ballot_sync(0xffffffffu, need_eq > 0u && key[u] == tau);
+    if (lane == 0) {
+      gt_bits[u * NW + warp] = g;
+      eq_bits[u * NW + warp] = e;
+    }
+  }
+  __syncthreads();
+  constexpr int PER = (WORDS + THREADS - 1) / THREADS;
+  const int w0 = min(tid * PER, WORDS), w1 = min(w0 + PER, WORDS);
+  uint2 mine = make_uint2(0u, 0u);
+  for (int w = w0; w < w1; ++w) {
+    mine.x += __popc(gt_bits[w]);
+    mine.y += __popc(eq_bits[w]);
+  }
+  uint2 total;
+  const uint2 before = block_scan2<THREADS>(mine, warp_sums, &total);
+  uint2 base = make_uint2(0u, 0u);
+  if constexpr (CL > 1) {
+    // Counts of the lower-ranked CTAs of the cluster come first.
+    if (tid == 0) cta_total = total;
+    cluster_barrier();
+    if (tid == 0) {
+      uint2 acc = make_uint2(0u, 0u);
+      for (uint32_t r = 0; r < rank; ++r) {
+        const uint32_t a = cluster_map(&cta_total, r);
+        acc.x += cluster_load(a);
+        acc.y += cluster_load(a + 4u);
+      }
+      cta_base = acc;
+    }
+    __syncthreads();
+    base = cta_base;
+    cluster_barrier();  // no CTA leaves while another may still read its shared memory
+  }
+  uint32_t gb = base.x + before.x, eb = base.y + before.y;
+  for (int w = w0; w < w1; ++w) {
+    const uint32_t g = gt_bits[w], e = eq_bits[w];
+    uint32_t m = g | e;
+    while (m) {
+      const int bit = __ffs(m) - 1;
+      m &= m - 1;
+      const int col = lo + seg0 + (w << 5) + bit;
+      if ((g >> bit) & 1u) {
+        dst[gb + min(eb, need_eq)] = col;
+        ++gb;
+      } else {
+        if (eb < need_eq) dst[gb + eb] = col;
+        ++eb;
+      }
+    }
+  }
+  if (rank == 0) {
+    const int nsel = nvalid < static_cast<uint32_t>(p.k) ? static_cast<int>(nvalid) : p.k;
+    for (int i = nsel + tid; i < p.k; i += THREADS) dst[i] = -1;
+  }
+}
+
+// --------------------------------------------------------------- streaming
+
+constexpr int kStreamThreads = 1024;
+
+__global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const TopkParams p) {
   extern __shared__ uint32_t sm[];
   uint32_t* hist = sm;                   // kHistBins
-  uint32_t* gt_bits = sm + kHistBins;    // ceil(S/32) words: key > tau
-  uint32_t* eq_bits = gt_bits + p.bitmap_words;  // key == tau
-  __shared__ uint2 warp_sums[kWarps];
+  uint32_t* gt_bits = sm + kHistBins;    // ceil(S/32) words
+  uint32_t* eq_bits = gt_bits + p.bitmap_words;
+  __shared__ uint2 warp_sums[kStreamThreads / 32];
   __shared__ uint32_t sel[2];
 
   const int row = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int lo, hi;
-  if (p.context_lens) {
-    const int b = row / p.next_n, j = row % p.next_n;
-    const int end = p.context_lens[b] - p.next_n + j + 1;
-    lo = 0;
-    hi = min(max(end, 0), p.S);
-  } else {
-    lo = min(max(p.row_starts[row], 0), p.S);
-    hi = min(max(p.row_ends[row], 0), p.S);
-    if (hi < lo) hi = lo;
-  }
+  row_range(p, row, &lo, &hi);
   const int n = hi - lo;
   const float* src = p.logits + static_cast<int64_t>(row) * p.ld + lo;
   int32_t* dst = p.out + static_cast<int64_t>(row) * p.k;
 
-  // ---- pass 1: histogram of the top 11 key bits, 16-byte loads from HBM.
-  for (int i = tid; i < kHistBins; i += kThreads) hist[i] = 0u;
-  __syncthreads();
-  {
-    const uintptr_t addr = reinterpret_cast<uintptr_t>(src);
-    int head = (addr & 3u) ? n : static_cast<int>(((16u - (addr & 15u)) & 15u) >> 2);
-    head = min(head, n);
-    const int body = (n - head) >> 2;
-    for (int i = tid; i < head; i += kThreads) atomicAdd(&hist[order_key(src[i]) >> 21], 1u);
-    const float4* src4 = reinterpret_cast<const float4*>(src + head);
-    for (int i = tid; i < body; i += kThreads) {
-      const float4 v = __ldg(src4 + i);
-      atomicAdd(&hist[order_key(v.x) >> 21], 1u);
-      atomicAdd(&hist[order_key(v.y) >> 21], 1u);
-      atomicAdd(&hist[order_key(v.z) >> 21], 1u);
-      atomicAdd(&hist[order_key(v.w) >> 21], 1u);
+  uint32_t prefix = 0u, rem = static_cast<uint32_t>(p.k), nvalid = 0u;
+  bool take_all = false;
+  for (int d = 0; d < 3; ++d) {
+    const int shift = d == 0 ? 21 : (d == 1 ? 10 : 0);
+    const int pshift = d == 1 ? 21 : 10;
+    const int nbins = d == 2 ? 1024 : 2048;
+    for (int i = tid; i < nbins; i += kStreamThreads) hist[i] = 0u;
+    __syncthreads();
+    for (int i = tid; i < n; i += kStreamThreads) {
+      const uint32_t kk = order_key(src[i]);
+      const bool live = kk != 0u && (d == 0 || (kk >> pshift) == prefix);
+      if (live) atomicAdd(&hist[(kk >> shift) & static_cast<uint32_t>(nbins - 1)], 1u);
     }
-    for (int i = head + 4 * body + tid; i < n; i += kThreads)
-      atomicAdd(&hist[order_key(src[i]) >> 21], 1u);
+    __syncthreads();
+    uint32_t b, above;
+    const uint32_t total = find_bin<kStreamThreads>(hist, nbins, rem, warp_sums, sel, &b, &above);
+    if (d == 0) {
+      nvalid = total;
+      if (nvalid <= static_cast<uint32_t>(p.k)) {
+        take_all = true;
+        break;
+      }
+    }
+    rem -= above;
+    prefix = d == 0 ? b : ((prefix << (d == 1 ? 11 : 10)) | b);
+    __syncthreads();
   }
-  __syncthreads();
-  // Bin 0 holds exactly the invalid keys: the smallest valid key is 0x00800000.
-  const int nvalid = n - static_cast<int>(hist[0]);
+  const uint32_t tau = take_all ? 0u : prefix;
+  const uint32_t need_eq = take_all ? 0u : rem;
 
-  uint32_t tau = 0u;      // take every key > tau ...
-  uint32_t need_eq = 0u;  // ... and the first need_eq keys == tau, in column order
-  if (nvalid > p.k) {
-    uint32_t rem = static_cast<uint32_t>(p.k);
-    uint32_t b1, a1, b2, a2, b3, a3;
-    find_bin(hist, kHistBins, rem, warp_sums, sel, &b1, &a1);
-    rem -= a1;
-    __syncthreads();
-    for (int i = tid; i < kHistBins; i += kThreads) hist[i] = 0u;
-    __syncthreads();
-    for (int i = tid; i < n; i += kThreads) {
-      const uint32_t key = order_key(src[i]);
-      if ((key >> 21) == b1) atomicAdd(&hist[(key >> 10) & 0x7FFu], 1u);
-    }
-    __syncthreads();
-    find_bin(hist, kHistBins, rem, warp_sums, sel, &b2, &a2);
-    rem -= a2;
-    const uint32_t prefix = (b1 << 11) | b2;
-    __syncthreads();
-    for (int i = tid; i < 1024; i += kThreads) hist[i] = 0u;
-    __syncthreads();
-    for (int i = tid; i < n; i += kThreads) {
-      const uint32_t key = order_key(src[i]);
-      if ((key >> 10) == prefix) atomicAdd(&hist[key & 0x3FFu], 1u);
-    }
-    __syncthreads();
-    find_bin(hist, 1024, rem, warp_sums, sel, &b3, &a3);
-    rem -= a3;
-    tau = (prefix << 10) | b3;
-    need_eq = rem;
-  }
-
-  // ---- last pass: bitmaps of (key > tau) and (key == tau), one word per
-  // 32 consecutive columns, written by warp ballots.
   const int nwords = (n + 31) >> 5;
-  for (int w = warp; w < nwords; w += kWarps) {
+  for (int w = warp; w < nwords; w += kStreamThreads / 32) {
     const int i = (w << 5) + lane;
-    const uint32_t key = i < n ? order_key(src[i]) : 0u;
-    const uint32_t g = __ballot_sync(0xffffffffu, key > tau);
-    const uint32_t e = __ballot_sync(0xffffffffu, need_eq > 0u && key == tau);
+    const uint32_t kk = i < n ? order_key(src[i]) : 0u;
+    const uint32_t g = __ballot_sync(0xffffffffu, kk > tau);
+    const uint32_t e = __ballot_sync(0xffffffffu, need_eq > 0u && kk == tau);
     if (lane == 0) {
       gt_bits[w] = g;
       eq_bits[w] = e;
     }
   }
   __syncthreads();
-
-  // ---- positions: prefix counts over words (each thread owns a run of words).
-  const int per = (nwords + kThreads - 1) / kThreads;
+  const int per = (nwords + kStreamThreads - 1) / kStreamThreads;
   const int w0 = min(tid * per, nwords), w1 = min(w0 + per, nwords);
   uint2 mine = make_uint2(0u, 0u);
   for (int w = w0; w < w1; ++w) {
@@ -206,10 +369,10 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
     mine.y += __popc(eq_bits[w]);
   }
   uint2 total;
-  const uint2 before = block_exclusive_scan2(mine, warp_sums, &total);
+  const uint2 before = block_scan2<kStreamThreads>(mine, warp_sums, &total);
   uint32_t gb = before.x, eb = before.y;
   for (int w = w0; w < w1; ++w) {
-    uint32_t g = gt_bits[w], e = eq_bits[w];
+    const uint32_t g = gt_bits[w], e = eq_bits[w];
     uint32_t m = g | e;
     while (m) {
       const int bit = __ffs(m) - 1;
@@ -224,22 +387,64 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
       }
     }
   }
-  const int nsel = nvalid < p.k ? nvalid : p.k;
-  for (int i = nsel + tid; i < p.k; i += kThreads) dst[i] = -1;
+  const int nsel = nvalid < static_cast<uint32_t>(p.k) ? static_cast<int>(nvalid) : p.k;
+  for (int i = nsel + tid; i < p.k; i += kStreamThreads) dst[i] = -1;
+}
+
+template <int THREADS, int ITEMS, int CL>
+cudaError_t launch_reg(const TopkParams& p, cudaStream_t s) {
+  auto kern = topk_reg_kernel<THREADS, ITEMS, CL>;
+  if constexpr (CL == 1) {
+    kern<<<p.R, THREADS, 0, s>>>(p);
+    return cudaGetLastError();
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.R) * CL);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+  }
 }
 
 }  // namespace
 
 int topk_bitmap_words(int max_row) { return (max_row + 31) / 32; }
 
+bool topk_supported(int max_row) {
+  const size_t stream_smem = sizeof(uint32_t) *
+      (static_cast<size_t>(kHistBins) + 2 * static_cast<size_t>(topk_bitmap_words(max_row)));
+  return max_row >= 0 && stream_smem <= 232448;
+}
+
+// Longest row (in keys) the register-resident kernel takes.
+constexpr int kTopkRegMaxRow = 1024 * 32 * 8;
+
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t s) {
   if (p.R <= 0) return cudaSuccess;
+  const int S = p.S;
+  if (S <= 4096) return launch_reg<256, 16, 1>(p, s);
+  if (S <= 8192) return launch_reg<512, 16, 1>(p, s);
+  if (S <= 16384) return launch_reg<512, 32, 1>(p, s);
+  if (S <= 32768) return launch_reg<1024, 32, 1>(p, s);
+  if (S <= 65536) return launch_reg<1024, 32, 2>(p, s);
+  if (S <= 131072) return launch_reg<1024, 32, 4>(p, s);
+  if (S <= kTopkRegMaxRow) return launch_reg<1024, 32, 8>(p, s);
   const size_t smem =
       sizeof(uint32_t) * (static_cast<size_t>(kHistBins) + 2 * static_cast<size_t>(p.bitmap_words));
-  cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (smem > 232448) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(topk_stream_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  topk_kernel<<<p.R, kThreads, smem, s>>>(p);
+  topk_stream_kernel<<<p.R, kStreamThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 
