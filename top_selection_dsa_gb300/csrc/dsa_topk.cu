@@ -156,17 +156,55 @@ __device__ __forceinline__ void row_range(const TopkParams& p, int row, int* lo,
 
 // ------------------------------------------------------ register-resident
 
+// Histogram slots are padded by one word every 32 bins, so that a thread
+// reading a run of consecutive bins never shares a bank with its neighbours.
+__device__ __forceinline__ int hpad(int bin) { return bin + (bin >> 5); }
+constexpr int kHistSlots = kHistBins + kHistBins / 32;
+
+// find_bin over a padded histogram (see find_bin).  Three barriers.
+template <int THREADS>
+__device__ __forceinline__ void find_bin_padded(const uint32_t* hist, int nbins, uint32_t r,
+                                                uint2* warp_sums, uint32_t* sel, uint32_t* bin,
+                                                uint32_t* above, uint32_t* count) {
+  const int per = nbins / THREADS;  // consecutive bins per thread, highest first
+  const int top = nbins - 1 - static_cast<int>(threadIdx.x) * per;
+  uint32_t local = 0;
+  for (int i = 0; i < per; ++i) local += hist[hpad(top - i)];
+  uint2 total;
+  const uint32_t excl = block_scan2<THREADS>(make_uint2(local, 0u), warp_sums, &total).x;
+  if (excl < r && r <= excl + local) {
+    uint32_t acc = excl;
+    for (int i = 0; i < per; ++i) {
+      const uint32_t h = hist[hpad(top - i)];
+      if (acc + h >= r) {
+        sel[0] = static_cast<uint32_t>(top - i);
+        sel[1] = acc;
+        sel[2] = h;
+        break;
+      }
+      acc += h;
+    }
+  }
+  __syncthreads();
+  *bin = sel[0];
+  *above = sel[1];
+  *count = sel[2];
+}
+
 template <int THREADS, int ITEMS, int CL>
 __global__ void __launch_bounds__(THREADS, 1) topk_reg_kernel(const TopkParams p) {
   constexpr int NW = THREADS / 32;
   constexpr int SEG = THREADS * ITEMS;  // keys per CTA
   constexpr int WORDS = SEG / 32;
-  __shared__ uint32_t hist[kHistBins];
-  __shared__ uint32_t merged[CL > 1 ? kHistBins : 1];
+  static_assert(kHistBins % THREADS == 0 || THREADS <= kHistBins, "bins per thread");
+  __shared__ uint32_t hist[2][kHistSlots];   // double buffer: one pass fills, the next is cleared
+  // Cluster merge targets (read on the leader), double-buffered like hist.
+  __shared__ uint32_t merged[CL > 1 ? 2 : 1][CL > 1 ? kHistSlots : 1];
   __shared__ uint32_t gt_bits[WORDS];
   __shared__ uint32_t eq_bits[WORDS];
   __shared__ uint2 warp_sums[NW];
-  __shared__ uint32_t sel[2];
+  __shared__ uint32_t sel[4];
+  __shared__ uint32_t valid_count;
   __shared__ uint2 cta_total;
   __shared__ uint2 cta_base;
 
@@ -177,80 +215,129 @@ __global__ void __launch_bounds__(THREADS, 1) topk_reg_kernel(const TopkParams p
   row_range(p, row, &lo, &hi);
   const int n = hi - lo;
   const int seg0 = static_cast<int>(rank) * SEG;
-  const float* src = p.logits + static_cast<int64_t>(row) * p.ld + lo;
+  const int mine_n = min(max(n - seg0, 0), SEG);  // keys of this CTA's segment
+  const float* src = p.logits + static_cast<int64_t>(row) * p.ld + lo + seg0;
   int32_t* dst = p.out + static_cast<int64_t>(row) * p.k;
 
-  // One read of the row segment: element seg0 + u*THREADS + tid.
-  float val[ITEMS];
-#pragma unroll
-  for (int u = 0; u < ITEMS; ++u) {
-    const int e = seg0 + u * THREADS + tid;
-    val[u] = e < n ? src[e] : -INFINITY;
+  for (int i = tid; i < kHistSlots; i += THREADS) {
+    hist[0][i] = 0u;
+    hist[1][i] = 0u;
+    if (CL > 1) merged[0][i] = 0u;
   }
+  if (tid == 0) {
+    valid_count = 0u;
+    sel[3] = 0u;
+  }
+
+  // One read of the segment: element u*THREADS + tid; slots past the row end
+  // are skipped a whole item at a time.
   uint32_t key[ITEMS];
 #pragma unroll
-  for (int u = 0; u < ITEMS; ++u) key[u] = order_key(val[u]);
+  for (int u = 0; u < ITEMS; ++u) {
+    const int e = u * THREADS + tid;
+    key[u] = 0u;
+    if (u * THREADS < mine_n && e < mine_n) key[u] = order_key(src[e]);
+  }
+  uint32_t nv = 0;
+#pragma unroll
+  for (int u = 0; u < ITEMS; ++u) nv += key[u] != 0u ? 1u : 0u;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) nv += __shfl_xor_sync(0xffffffffu, nv, o);
+  // Histograms cleared (in every CTA of the cluster, before any merge).
+  if constexpr (CL > 1) cluster_barrier(); else __syncthreads();
+  if (lane == 0 && nv) atomicAdd(&valid_count, nv);
 
-  // Radix select over digits of 11, 11 and 10 bits.
-  uint32_t prefix = 0u, rem = static_cast<uint32_t>(p.k), nvalid = 0u;
-  bool take_all = false;
+  // Pass 0 histogram (top 11 bits): lanes that hit the same bin add once.
+#pragma unroll
+  for (int u = 0; u < ITEMS; ++u) {
+    if (u * THREADS < mine_n) {
+      const uint32_t kk = key[u];
+      const uint32_t b = kk != 0u ? (kk >> 21) : 0xFFFFFFFFu;
+      const uint32_t peers = __match_any_sync(0xffffffffu, b);
+      if (kk != 0u && lane == __ffs(peers) - 1) atomicAdd(&hist[0][hpad(b)], __popc(peers));
+    }
+  }
+
+  uint32_t prefix = 0u, rem = static_cast<uint32_t>(p.k);
+  uint32_t tau = 0u, need_eq = 0u;  // take every key > tau, then the first need_eq == tau
+  uint32_t nvalid = 0u;
 #pragma unroll 1
   for (int d = 0; d < 3; ++d) {
-    const int shift = d == 0 ? 21 : (d == 1 ? 10 : 0);
-    const int pshift = d == 1 ? 21 : 10;  // prefix of the keys still in play (d > 0)
+    uint32_t* hcur = hist[d & 1];
     const int nbins = d == 2 ? 1024 : 2048;
-    for (int i = tid; i < nbins; i += THREADS) {
-      hist[i] = 0u;
-      if (CL > 1 && rank == 0) merged[i] = 0u;
-    }
-    if constexpr (CL > 1) cluster_barrier(); else __syncthreads();
+    if (d > 0) {
+      const int shift = d == 1 ? 10 : 0;
+      const int pshift = d == 1 ? 21 : 10;
 #pragma unroll
-    for (int u = 0; u < ITEMS; ++u) {
-      const uint32_t kk = key[u];
-      const bool live = kk != 0u && (d == 0 || (kk >> pshift) == prefix);
-      if (live) atomicAdd(&hist[(kk >> shift) & static_cast<uint32_t>(nbins - 1)], 1u);
+      for (int u = 0; u < ITEMS; ++u) {
+        if (u * THREADS < mine_n) {
+          const uint32_t kk = key[u];
+          if (kk != 0u && (kk >> pshift) == prefix)
+            atomicAdd(&hcur[hpad(static_cast<int>((kk >> shift) & static_cast<uint32_t>(nbins - 1)))], 1u);
+        }
+      }
     }
     __syncthreads();
     if constexpr (CL > 1) {
-      // Merge into the leader's histogram, then every CTA takes a copy.
-      const uint32_t leader = cluster_map(merged, 0);
-      for (int i = tid; i < nbins; i += THREADS) {
-        const uint32_t v = hist[i];
+      // Merge into the leader's histogram, then every CTA takes a copy.  The
+      // leader zeroes the other merge buffer for the next pass meanwhile; the
+      // second barrier orders that before anyone adds into it.
+      const uint32_t leader = cluster_map(merged[d & 1], 0);
+      for (int i = tid; i < kHistSlots; i += THREADS) {
+        const uint32_t v = hcur[i];
         if (v) cluster_add(leader + 4u * i, v);
       }
+      if (d == 0 && tid == 0 && valid_count) cluster_add(cluster_map(&sel[3], 0), valid_count);
       cluster_barrier();
-      for (int i = tid; i < nbins; i += THREADS) hist[i] = cluster_load(leader + 4u * i);
+      for (int i = tid; i < kHistSlots; i += THREADS) hcur[i] = cluster_load(leader + 4u * i);
+      if (d == 0 && tid == 0) valid_count = cluster_load(cluster_map(&sel[3], 0));
+      if (rank == 0)
+        for (int i = tid; i < kHistSlots; i += THREADS) merged[(d + 1) & 1][i] = 0u;
       cluster_barrier();
     }
-    uint32_t b, above;
-    const uint32_t total = find_bin<THREADS>(hist, nbins, rem, warp_sums, sel, &b, &above);
     if (d == 0) {
-      nvalid = total;
-      if (nvalid <= static_cast<uint32_t>(p.k)) {
-        take_all = true;
-        break;
-      }
+      nvalid = valid_count;
+      if (nvalid <= static_cast<uint32_t>(p.k)) break;  // every valid key is taken
     }
+    uint32_t b, above, cnt;
+    find_bin_padded<THREADS>(hcur, nbins, rem, warp_sums, sel, &b, &above, &cnt);
     rem -= above;
     prefix = d == 0 ? b : ((prefix << (d == 1 ? 11 : 10)) | b);
+    if (rem == cnt || d == 2) {
+      // Either the whole bin is taken (every key whose top bits are >= prefix)
+      // or the key is complete.
+      const int used = d == 0 ? 11 : (d == 1 ? 22 : 32);
+      if (d == 2) {
+        tau = prefix;
+        need_eq = rem;
+      } else {
+        tau = (prefix << (32 - used)) - 1u;
+        need_eq = 0u;
+      }
+      break;
+    }
+    // Clear the other buffer for the next pass (it held pass d-1).
+    uint32_t* hnext = hist[(d + 1) & 1];
+    for (int i = tid; i < kHistSlots; i += THREADS) hnext[i] = 0u;
     __syncthreads();
   }
-  const uint32_t tau = take_all ? 0u : prefix;      // take every key > tau ...
-  const uint32_t need_eq = take_all ? 0u : rem;     // ... and the first need_eq keys == tau
 
   // Bitmaps: word u*NW + warp holds columns seg0 + (u*NW + warp)*32 + lane.
 #pragma unroll
   for (int u = 0; u < ITEMS; ++u) {
-    const uint32_t g = __ballot_sync(0xffffffffu, key[u] > tau);
-    const uint32_t e = __ballot_sync(0xffffffffu, need_eq > 0u && key[u] == tau);
-    if (lane == 0) {
-      gt_bits[u * NW + warp] = g;
-      eq_bits[u * NW + warp] = e;
+    if (u * THREADS < mine_n) {
+      const uint32_t g = __ballot_sync(0xffffffffu, key[u] > tau);
+      const uint32_t e = __ballot_sync(0xffffffffu, need_eq > 0u && key[u] == tau);
+      if (lane == 0) {
+        gt_bits[u * NW + warp] = g;
+        eq_bits[u * NW + warp] = e;
+      }
     }
   }
   __syncthreads();
-  constexpr int PER = (WORDS + THREADS - 1) / THREADS;
-  const int w0 = min(tid * PER, WORDS), w1 = min(w0 + PER, WORDS);
+  const int nwords = (mine_n + 31) >> 5;
+  const int per = (nwords + THREADS - 1) / THREADS;
+  const int w0 = min(tid * per, nwords), w1 = min(w0 + per, nwords);
   uint2 mine = make_uint2(0u, 0u);
   for (int w = w0; w < w1; ++w) {
     mine.x += __popc(gt_bits[w]);
@@ -430,8 +517,8 @@ constexpr int kTopkRegMaxRow = 1024 * 32 * 8;
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t s) {
   if (p.R <= 0) return cudaSuccess;
   const int S = p.S;
-  if (S <= 4096) return launch_reg<256, 16, 1>(p, s);
-  if (S <= 8192) return launch_reg<512, 16, 1>(p, s);
+  if (S <= 4096) return launch_reg<128, 32, 1>(p, s);
+  if (S <= 8192) return launch_reg<256, 32, 1>(p, s);
   if (S <= 16384) return launch_reg<512, 32, 1>(p, s);
   if (S <= 32768) return launch_reg<1024, 32, 1>(p, s);
   if (S <= 65536) return launch_reg<1024, 32, 2>(p, s);
