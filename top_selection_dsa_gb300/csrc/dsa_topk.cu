@@ -19,11 +19,14 @@
 //   topk_reg_kernel<THREADS, ITEMS, CL>  a row of up to CL*THREADS*ITEMS keys
 //       is read once from memory into registers (ITEMS per thread, striped so
 //       that each warp's loads are contiguous); the radix passes and the
-//       bitmaps work on registers only.  CL > 1 spreads a row over a
+//       ordered writes work on registers.  CL > 1 spreads a row over a
 //       thread-block cluster whose CTAs merge their histograms and counts
-//       through distributed shared memory.
-//   topk_stream_kernel  rows longer than the largest cluster: one CTA per row,
-//       histogram passes re-read the row from memory.
+//       through distributed shared memory (few, very long rows).
+//   topk_stream_kernel  256 threads per row, several rows per SM: the first
+//       pass streams the row with 16-byte loads, later passes re-read it
+//       (from L2).
+// A row whose columns are all valid and that has at most k of them is
+// written directly as lo, lo+1, ..., hi-1.
 #include "dsa_common.cuh"
 #include "dsa_internal.h"
 
@@ -192,7 +195,7 @@ __device__ __forceinline__ void find_bin_padded(const uint32_t* hist, int nbins,
 }
 
 template <int THREADS, int ITEMS, int CL>
-__global__ void __launch_bounds__(THREADS, 1) topk_reg_kernel(const TopkParams p) {
+__global__ void __launch_bounds__(THREADS, 65536 / (THREADS * 64)) topk_reg_kernel(const TopkParams p) {
   constexpr int NW = THREADS / 32;
   constexpr int SEG = THREADS * ITEMS;  // keys per CTA
   constexpr int WORDS = SEG / 32;
@@ -247,14 +250,12 @@ __global__ void __launch_bounds__(THREADS, 1) topk_reg_kernel(const TopkParams p
   if constexpr (CL > 1) cluster_barrier(); else __syncthreads();
   if (lane == 0 && nv) atomicAdd(&valid_count, nv);
 
-  // Pass 0 histogram (top 11 bits): lanes that hit the same bin add once.
+  // Pass 0 histogram of the top 11 bits (invalid keys are left out).
 #pragma unroll
   for (int u = 0; u < ITEMS; ++u) {
     if (u * THREADS < mine_n) {
       const uint32_t kk = key[u];
-      const uint32_t b = kk != 0u ? (kk >> 21) : 0xFFFFFFFFu;
-      const uint32_t peers = __match_any_sync(0xffffffffu, b);
-      if (kk != 0u && lane == __ffs(peers) - 1) atomicAdd(&hist[0][hpad(b)], __popc(peers));
+      if (kk != 0u) atomicAdd(&hist[0][hpad(static_cast<int>(kk >> 21))], 1u);
     }
   }
 
@@ -271,8 +272,10 @@ __global__ void __launch_bounds__(THREADS, 1) topk_reg_kernel(const TopkParams p
 #pragma unroll
       for (int u = 0; u < ITEMS; ++u) {
         if (u * THREADS < mine_n) {
+          // prefix >= 4 here (the smallest valid key is 0x00800000), so an
+          // invalid key (0) never matches.
           const uint32_t kk = key[u];
-          if (kk != 0u && (kk >> pshift) == prefix)
+          if ((kk >> pshift) == prefix)
             atomicAdd(&hcur[hpad(static_cast<int>((kk >> shift) & static_cast<uint32_t>(nbins - 1)))], 1u);
         }
       }
@@ -322,73 +325,89 @@ __global__ void __launch_bounds__(THREADS, 1) topk_reg_kernel(const TopkParams p
     __syncthreads();
   }
 
-  // Bitmaps: word u*NW + warp holds columns seg0 + (u*NW + warp)*32 + lane.
+  const int nsel = nvalid < static_cast<uint32_t>(p.k) ? static_cast<int>(nvalid) : p.k;
+  if (nvalid <= static_cast<uint32_t>(p.k) && nvalid == static_cast<uint32_t>(n)) {
+    // Every column of the row is valid and taken: indices lo .. hi-1, in order.
+    for (int i = tid; i < mine_n; i += THREADS) dst[seg0 + i] = lo + seg0 + i;
+  } else {
+    // Ballot words: word u*NW + warp holds columns seg0 + (u*NW + warp)*32 + lane.
 #pragma unroll
-  for (int u = 0; u < ITEMS; ++u) {
-    if (u * THREADS < mine_n) {
-      const uint32_t g = __ballot_sync(0xffffffffu, key[u] > tau);
-      const uint32_t e = __ballot_sync(0xffffffffu, need_eq > 0u && key[u] == tau);
-      if (lane == 0) {
-        gt_bits[u * NW + warp] = g;
-        eq_bits[u * NW + warp] = e;
+    for (int u = 0; u < ITEMS; ++u) {
+      if (u * THREADS < mine_n) {
+        const uint32_t g = __ballot_sync(0xffffffffu, key[u] > tau);
+        const uint32_t e = __ballot_sync(0xffffffffu, need_eq > 0u && key[u] == tau);
+        if (lane == 0) {
+          gt_bits[u * NW + warp] = g;
+          eq_bits[u * NW + warp] = e;
+        }
       }
-    }
-  }
-  __syncthreads();
-  const int nwords = (mine_n + 31) >> 5;
-  const int per = (nwords + THREADS - 1) / THREADS;
-  const int w0 = min(tid * per, nwords), w1 = min(w0 + per, nwords);
-  uint2 mine = make_uint2(0u, 0u);
-  for (int w = w0; w < w1; ++w) {
-    mine.x += __popc(gt_bits[w]);
-    mine.y += __popc(eq_bits[w]);
-  }
-  uint2 total;
-  const uint2 before = block_scan2<THREADS>(mine, warp_sums, &total);
-  uint2 base = make_uint2(0u, 0u);
-  if constexpr (CL > 1) {
-    // Counts of the lower-ranked CTAs of the cluster come first.
-    if (tid == 0) cta_total = total;
-    cluster_barrier();
-    if (tid == 0) {
-      uint2 acc = make_uint2(0u, 0u);
-      for (uint32_t r = 0; r < rank; ++r) {
-        const uint32_t a = cluster_map(&cta_total, r);
-        acc.x += cluster_load(a);
-        acc.y += cluster_load(a + 4u);
-      }
-      cta_base = acc;
     }
     __syncthreads();
-    base = cta_base;
-    cluster_barrier();  // no CTA leaves while another may still read its shared memory
-  }
-  uint32_t gb = base.x + before.x, eb = base.y + before.y;
-  for (int w = w0; w < w1; ++w) {
-    const uint32_t g = gt_bits[w], e = eq_bits[w];
-    uint32_t m = g | e;
-    while (m) {
-      const int bit = __ffs(m) - 1;
-      m &= m - 1;
-      const int col = lo + seg0 + (w << 5) + bit;
-      if ((g >> bit) & 1u) {
-        dst[gb + min(eb, need_eq)] = col;
-        ++gb;
-      } else {
-        if (eb < need_eq) dst[gb + eb] = col;
-        ++eb;
+    // Prefix counts over the words, in column order (each thread a run of words).
+    const int nwords = (mine_n + 31) >> 5;
+    const int per = (nwords + THREADS - 1) / THREADS;
+    const int w0 = min(tid * per, nwords), w1 = min(w0 + per, nwords);
+    uint2 mine = make_uint2(0u, 0u);
+    for (int w = w0; w < w1; ++w) {
+      mine.x += __popc(gt_bits[w]);
+      mine.y += __popc(eq_bits[w]);
+    }
+    uint2 total;
+    const uint2 before = block_scan2<THREADS>(mine, warp_sums, &total);
+    uint2 base = make_uint2(0u, 0u);
+    if constexpr (CL > 1) {
+      // Counts of the lower-ranked CTAs of the cluster come first.
+      if (tid == 0) cta_total = total;
+      cluster_barrier();
+      if (tid == 0) {
+        uint2 acc = make_uint2(0u, 0u);
+        for (uint32_t r = 0; r < rank; ++r) {
+          const uint32_t a = cluster_map(&cta_total, r);
+          acc.x += cluster_load(a);
+          acc.y += cluster_load(a + 4u);
+        }
+        cta_base = acc;
+      }
+      __syncthreads();
+      base = cta_base;
+      cluster_barrier();  // no CTA leaves while another may still read its shared memory
+    }
+    // Word prefixes (gt count, eq count) replace the ballot words in place.
+    uint32_t gp = base.x + before.x, ep = base.y + before.y;
+    for (int w = w0; w < w1; ++w) {
+      const uint32_t g = gt_bits[w], e = eq_bits[w];
+      gt_bits[w] = gp;
+      eq_bits[w] = ep;
+      gp += __popc(g);
+      ep += __popc(e);
+    }
+    __syncthreads();
+    // Every lane writes its own column: position = selected columns before it.
+    const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+    for (int u = 0; u < ITEMS; ++u) {
+      if (u * THREADS < mine_n) {
+        const int w = u * NW + warp;
+        const uint32_t kk = key[u];
+        const bool g = kk > tau;
+        const bool e = need_eq > 0u && kk == tau;
+        const uint32_t gm = __ballot_sync(0xffffffffu, g);
+        const uint32_t em = __ballot_sync(0xffffffffu, e);
+        const uint32_t gb = gt_bits[w] + __popc(gm & lt);
+        const uint32_t eb = eq_bits[w] + __popc(em & lt);
+        const int col = lo + seg0 + u * THREADS + tid;
+        if (g) dst[gb + min(eb, need_eq)] = col;
+        else if (e && eb < need_eq) dst[gb + eb] = col;
       }
     }
   }
-  if (rank == 0) {
-    const int nsel = nvalid < static_cast<uint32_t>(p.k) ? static_cast<int>(nvalid) : p.k;
+  if (rank == 0)
     for (int i = nsel + tid; i < p.k; i += THREADS) dst[i] = -1;
-  }
 }
 
 // --------------------------------------------------------------- streaming
 
-constexpr int kStreamThreads = 1024;
+constexpr int kStreamThreads = 256;
 
 __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const TopkParams p) {
   extern __shared__ uint32_t sm[];
@@ -396,7 +415,8 @@ __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const TopkP
   uint32_t* gt_bits = sm + kHistBins;    // ceil(S/32) words
   uint32_t* eq_bits = gt_bits + p.bitmap_words;
   __shared__ uint2 warp_sums[kStreamThreads / 32];
-  __shared__ uint32_t sel[2];
+  __shared__ uint32_t sel[4];
+  __shared__ uint32_t valid_count;
 
   const int row = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -406,75 +426,114 @@ __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const TopkP
   const float* src = p.logits + static_cast<int64_t>(row) * p.ld + lo;
   int32_t* dst = p.out + static_cast<int64_t>(row) * p.k;
 
-  uint32_t prefix = 0u, rem = static_cast<uint32_t>(p.k), nvalid = 0u;
-  bool take_all = false;
-  for (int d = 0; d < 3; ++d) {
-    const int shift = d == 0 ? 21 : (d == 1 ? 10 : 0);
-    const int pshift = d == 1 ? 21 : 10;
-    const int nbins = d == 2 ? 1024 : 2048;
-    for (int i = tid; i < nbins; i += kStreamThreads) hist[i] = 0u;
-    __syncthreads();
-    for (int i = tid; i < n; i += kStreamThreads) {
-      const uint32_t kk = order_key(src[i]);
-      const bool live = kk != 0u && (d == 0 || (kk >> pshift) == prefix);
-      if (live) atomicAdd(&hist[(kk >> shift) & static_cast<uint32_t>(nbins - 1)], 1u);
+  // Pass 0: histogram of the top 11 key bits, 16-byte loads from memory.
+  for (int i = tid; i < kHistBins; i += kStreamThreads) hist[i] = 0u;
+  if (tid == 0) valid_count = 0u;
+  __syncthreads();
+  {
+    uint32_t nv = 0;
+    const uintptr_t addr = reinterpret_cast<uintptr_t>(src);
+    const int head = min(static_cast<int>(((16u - (addr & 15u)) & 15u) >> 2), n);
+    const int body = (n - head) >> 2;
+    auto add = [&](float x) {
+      const uint32_t kk = order_key(x);
+      if (kk != 0u) {
+        atomicAdd(&hist[kk >> 21], 1u);
+        ++nv;
+      }
+    };
+    for (int i = tid; i < head; i += kStreamThreads) add(src[i]);
+    const float4* src4 = reinterpret_cast<const float4*>(src + head);
+    for (int i = tid; i < body; i += kStreamThreads) {
+      const float4 v = __ldg(src4 + i);
+      add(v.x);
+      add(v.y);
+      add(v.z);
+      add(v.w);
     }
-    __syncthreads();
-    uint32_t b, above;
-    const uint32_t total = find_bin<kStreamThreads>(hist, nbins, rem, warp_sums, sel, &b, &above);
-    if (d == 0) {
-      nvalid = total;
-      if (nvalid <= static_cast<uint32_t>(p.k)) {
-        take_all = true;
+    for (int i = head + 4 * body + tid; i < n; i += kStreamThreads) add(src[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) nv += __shfl_xor_sync(0xffffffffu, nv, o);
+    if (lane == 0 && nv) atomicAdd(&valid_count, nv);
+  }
+  __syncthreads();
+  const uint32_t nvalid = valid_count;
+  const int nsel = nvalid < static_cast<uint32_t>(p.k) ? static_cast<int>(nvalid) : p.k;
+
+  uint32_t prefix = 0u, rem = static_cast<uint32_t>(p.k), tau = 0u, need_eq = 0u;
+  if (nvalid > static_cast<uint32_t>(p.k)) {
+#pragma unroll 1
+    for (int d = 0; d < 3; ++d) {
+      const int nbins = d == 2 ? 1024 : 2048;
+      if (d > 0) {
+        const int shift = d == 1 ? 10 : 0;
+        const int pshift = d == 1 ? 21 : 10;
+        for (int i = tid; i < nbins; i += kStreamThreads) hist[i] = 0u;
+        __syncthreads();
+        for (int i = tid; i < n; i += kStreamThreads) {
+          const uint32_t kk = order_key(src[i]);
+          if ((kk >> pshift) == prefix)
+            atomicAdd(&hist[(kk >> shift) & static_cast<uint32_t>(nbins - 1)], 1u);
+        }
+        __syncthreads();
+      }
+      uint32_t b, above;
+      find_bin<kStreamThreads>(hist, nbins, rem, warp_sums, sel, &b, &above);
+      const uint32_t cnt = hist[b];
+      rem -= above;
+      prefix = d == 0 ? b : ((prefix << (d == 1 ? 11 : 10)) | b);
+      __syncthreads();
+      if (rem == cnt || d == 2) {
+        const int used = d == 0 ? 11 : (d == 1 ? 22 : 32);
+        tau = d == 2 ? prefix : (prefix << (32 - used)) - 1u;
+        need_eq = d == 2 ? rem : 0u;
         break;
       }
     }
-    rem -= above;
-    prefix = d == 0 ? b : ((prefix << (d == 1 ? 11 : 10)) | b);
-    __syncthreads();
   }
-  const uint32_t tau = take_all ? 0u : prefix;
-  const uint32_t need_eq = take_all ? 0u : rem;
 
-  const int nwords = (n + 31) >> 5;
-  for (int w = warp; w < nwords; w += kStreamThreads / 32) {
-    const int i = (w << 5) + lane;
-    const uint32_t kk = i < n ? order_key(src[i]) : 0u;
-    const uint32_t g = __ballot_sync(0xffffffffu, kk > tau);
-    const uint32_t e = __ballot_sync(0xffffffffu, need_eq > 0u && kk == tau);
-    if (lane == 0) {
-      gt_bits[w] = g;
-      eq_bits[w] = e;
+  if (nvalid <= static_cast<uint32_t>(p.k) && nvalid == static_cast<uint32_t>(n)) {
+    for (int i = tid; i < n; i += kStreamThreads) dst[i] = lo + i;
+  } else {
+    const int nwords = (n + 31) >> 5;
+    for (int w = warp; w < nwords; w += kStreamThreads / 32) {
+      const int i = (w << 5) + lane;
+      const uint32_t kk = i < n ? order_key(src[i]) : 0u;
+      const uint32_t g = __ballot_sync(0xffffffffu, kk > tau);
+      const uint32_t e = __ballot_sync(0xffffffffu, need_eq > 0u && kk == tau);
+      if (lane == 0) {
+        gt_bits[w] = g;
+        eq_bits[w] = e;
+      }
     }
-  }
-  __syncthreads();
-  const int per = (nwords + kStreamThreads - 1) / kStreamThreads;
-  const int w0 = min(tid * per, nwords), w1 = min(w0 + per, nwords);
-  uint2 mine = make_uint2(0u, 0u);
-  for (int w = w0; w < w1; ++w) {
-    mine.x += __popc(gt_bits[w]);
-    mine.y += __popc(eq_bits[w]);
-  }
-  uint2 total;
-  const uint2 before = block_scan2<kStreamThreads>(mine, warp_sums, &total);
-  uint32_t gb = before.x, eb = before.y;
-  for (int w = w0; w < w1; ++w) {
-    const uint32_t g = gt_bits[w], e = eq_bits[w];
-    uint32_t m = g | e;
-    while (m) {
-      const int bit = __ffs(m) - 1;
-      m &= m - 1;
-      const int col = lo + (w << 5) + bit;
-      if ((g >> bit) & 1u) {
-        dst[gb + min(eb, need_eq)] = col;
-        ++gb;
-      } else {
-        if (eb < need_eq) dst[gb + eb] = col;
-        ++eb;
+    __syncthreads();
+    const int per = (nwords + kStreamThreads - 1) / kStreamThreads;
+    const int w0 = min(tid * per, nwords), w1 = min(w0 + per, nwords);
+    uint2 mine = make_uint2(0u, 0u);
+    for (int w = w0; w < w1; ++w) {
+      mine.x += __popc(gt_bits[w]);
+      mine.y += __popc(eq_bits[w]);
+    }
+    uint2 total;
+    const uint2 before = block_scan2<kStreamThreads>(mine, warp_sums, &total);
+    uint32_t gb = before.x, eb = before.y;
+    for (int w = w0; w < w1; ++w) {
+      const uint32_t g = gt_bits[w], e = eq_bits[w];
+      uint32_t m = g | e;
+      while (m) {
+        const int bit = __ffs(m) - 1;
+        m &= m - 1;
+        const int col = lo + (w << 5) + bit;
+        if ((g >> bit) & 1u) {
+          dst[gb + min(eb, need_eq)] = col;
+          ++gb;
+        } else {
+          if (eb < need_eq) dst[gb + eb] = col;
+          ++eb;
+        }
       }
     }
   }
-  const int nsel = nvalid < static_cast<uint32_t>(p.k) ? static_cast<int>(nvalid) : p.k;
   for (int i = nsel + tid; i < p.k; i += kStreamThreads) dst[i] = -1;
 }
 
@@ -517,13 +576,14 @@ constexpr int kTopkRegMaxRow = 1024 * 32 * 8;
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t s) {
   if (p.R <= 0) return cudaSuccess;
   const int S = p.S;
+  // Short rows: keys in registers, one CTA per row, several rows per SM.
   if (S <= 4096) return launch_reg<128, 32, 1>(p, s);
   if (S <= 8192) return launch_reg<256, 32, 1>(p, s);
   if (S <= 16384) return launch_reg<512, 32, 1>(p, s);
-  if (S <= 32768) return launch_reg<1024, 32, 1>(p, s);
-  if (S <= 65536) return launch_reg<1024, 32, 2>(p, s);
-  if (S <= 131072) return launch_reg<1024, 32, 4>(p, s);
-  if (S <= kTopkRegMaxRow) return launch_reg<1024, 32, 8>(p, s);
+  // Very long rows (decode): a cluster of register-resident CTAs per row.
+  if (S > 65536 && S <= 131072) return launch_reg<1024, 32, 4>(p, s);
+  if (S > 131072 && S <= kTopkRegMaxRow) return launch_reg<1024, 32, 8>(p, s);
+  // Otherwise: 256-thread CTAs that stream the row (8 rows in flight per SM).
   const size_t smem =
       sizeof(uint32_t) * (static_cast<size_t>(kHistBins) + 2 * static_cast<size_t>(p.bitmap_words));
   if (smem > 232448) return cudaErrorInvalidValue;
