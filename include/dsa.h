@@ -185,6 +185,39 @@ dsa_status_t dsa_indexer_topk_paged(const void* q, const float* q_scale,
                                     dsa_stream_t stream);
 
 /*
+ * dsa_indexer_topk for callers that cannot allocate device memory.  The pages
+ * have no counterpart to this entry point; it is an addition of this library.
+ *
+ * Some callers have no way to obtain a scratch buffer when they need one:
+ * code that runs while a stream is being captured into a CUDA graph without a
+ * graph-safe allocator, plugins inside a host framework that owns every
+ * device allocation, or latency-critical serving loops that must not pay for
+ * cudaMalloc's implicit synchronisation.  This variant keeps its fp32 logits
+ * in a fixed device array inside the library instead of a caller workspace;
+ * it calls no allocator of any kind.
+ *   - The array holds DSA_NOALLOC_SCRATCH_BYTES (64 MiB) on every GPU that
+ *     loads the library, for the life of the process.
+ *   - It covers T * round_up(S, 4) fp32 logits, i.e. at most
+ *     DSA_NOALLOC_SCRATCH_BYTES / 4 of them (T = S = 4096 fits); a larger
+ *     request returns DSA_ERR_UNSUPPORTED before anything is launched.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, under a lock); make that first call before capturing a
+ *     stream.
+ *   - Every call on a device uses the same array and leaves its logits there.
+ *     Calls whose work overlaps on the GPU (several streams, or several host
+ *     threads) race on it and corrupt each other's results: order them on one
+ *     stream or with events.
+ *   - Arguments and result are those of dsa_indexer_topk without the
+ *     workspace; the indices are bit-identical to it.
+ */
+#define DSA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+dsa_status_t dsa_indexer_topk_noalloc(const void* q, const float* q_scale, const void* k,
+                                      const float* k_scale, dsa_dtype_t dtype,
+                                      const float* weights, const int32_t* row_starts,
+                                      const int32_t* row_ends, int T, int S, int H, int D,
+                                      int topk, int32_t* out, dsa_stream_t stream);
+
+/*
  * Scratch bytes an operation needs.  rows/cols are T/S for the prefill ops and
  * B*next_n / max_blocks*block_size for the paged ones; k is index_topk.
  * Returns 0 for operations that need none, and (size_t)-1 for bad arguments.

@@ -27,7 +27,7 @@ DSA_LOGITS_CLEAN = 1
 EXPORTS = (
     "dsa_indexer_logits", "dsa_topk", "dsa_indexer_topk", "dsa_indexer_logits_paged",
     "dsa_indexer_topk_paged", "dsa_workspace_bytes", "dsa_status_string",
-    "dsa_get_last_device_error", "dsa_selftest_wait_timeout",
+    "dsa_get_last_device_error", "dsa_selftest_wait_timeout", "dsa_indexer_topk_noalloc",
 )
 
 

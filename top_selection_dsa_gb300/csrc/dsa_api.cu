@@ -445,3 +445,59 @@ dsa_status_t dsa_selftest_wait_timeout(uint64_t timeout_ns, dsa_stream_t stream)
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------
+// dsa_indexer_topk_noalloc: the logits scratch is a fixed device array of the
+// library, for callers that cannot allocate device memory at call time.
+
+namespace dsa {
+namespace {
+
+constexpr size_t kNoallocScratchFloats = DSA_NOALLOC_SCRATCH_BYTES / sizeof(float);
+
+// Shared by every call on a device; held for the life of the process.
+static __device__ __align__(256) float g_noalloc_scratch[kNoallocScratchFloats];
+
+// Device address of g_noalloc_scratch on the current device.  In host code the
+// array's name only stands in for the symbol; the address is looked up once
+// per device, with that device current, and cached.
+float* noalloc_scratch() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  static std::mutex mu;
+  static float* addr[kMaxDevices] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_noalloc_scratch) != cudaSuccess || !a) return nullptr;
+    addr[dev] = static_cast<float*>(a);
+  }
+  return addr[dev];
+}
+
+}  // namespace
+}  // namespace dsa
+
+extern "C" dsa_status_t dsa_indexer_topk_noalloc(const void* q, const float* q_scale,
+                                                 const void* k, const float* k_scale,
+                                                 dsa_dtype_t dtype, const float* weights,
+                                                 const int32_t* row_starts,
+                                                 const int32_t* row_ends, int T, int S, int H,
+                                                 int D, int topk, int32_t* out,
+                                                 dsa_stream_t stream) {
+  dsa_status_t st = check_logits_args(q, q_scale, k, k_scale, dtype, weights, row_starts,
+                                      row_ends, T, S, H, D);
+  if (st != DSA_OK) return st;
+  if (!out || !aligned(out, 4) || topk < 1) return DSA_ERR_INVALID_ARG;
+  if (!topk_supported(S)) return DSA_ERR_UNSUPPORTED;
+  if (T == 0) return DSA_OK;
+  const int64_t ld = round_up(S > 0 ? S : 1, 4);
+  if (static_cast<uint64_t>(T) * static_cast<uint64_t>(ld) > kNoallocScratchFloats)
+    return DSA_ERR_UNSUPPORTED;
+  float* lg = noalloc_scratch();
+  if (!lg) return DSA_ERR_CUDA;
+  st = run_logits(q, q_scale, k, k_scale, dtype, weights, row_starts, row_ends, T, S, H, D, lg, ld,
+                  as_stream(stream));
+  if (st != DSA_OK) return st;
+  return run_topk(lg, ld, row_starts, row_ends, nullptr, 1, T, S, topk, out, as_stream(stream));
+}
