@@ -60,6 +60,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true",
                     help="skip the clock-sampling load window (for profiler runs)")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override T = S of the prefill workloads (smaller profiler captures)")
     ap.add_argument("--oracle-rows", type=int, default=512,
                     help="rows of the CPU oracle sample (cpu_baseline / reference arm)")
     return ap.parse_args(argv)
@@ -185,8 +187,10 @@ def barrier(world):
         dist.barrier()
 
 
-def make_workload(name):
+def make_workload(name, tokens=0):
     from top_selection_dsa_gb300 import workloads as wl
+    if tokens and name in ("prefill_causal", "prefill_fp8"):
+        return wl.WORKLOADS[name](T=tokens)
     return wl.WORKLOADS[name]()
 
 
@@ -226,7 +230,7 @@ def run_reference(args):
     world, rank, local = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0
     if rank != 0:
         return 0
-    p = make_workload(args.workload)
+    p = make_workload(args.workload, args.tokens)
     rows = max(8, args.oracle_rows // 8)
     for _ in range(args.warmup):
         oracle_sample_rate(p, rows, seed=1)
@@ -261,7 +265,7 @@ def run_ours(args):
     device = torch.device("cuda", local)
     from top_selection_dsa_gb300 import api
 
-    p = make_workload(args.workload)
+    p = make_workload(args.workload, args.tokens)
     paged = not hasattr(p, "row_starts")
     cuda = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
 

@@ -96,9 +96,10 @@ typedef enum {
  *              the row's tile group are written (-inf outside the row's own
  *              range); with DSA_LOGITS_CLEAN every column in [0, S) is.
  *   flags      0 or DSA_LOGITS_CLEAN
- * Accumulation is fp32 on tensor cores; the head sum runs in ascending head
- * order, so dsa_indexer_topk's selection equals dsa_topk applied to these
- * logits.
+ * Accumulation is fp32 on tensor cores; the head sum runs in one fixed order
+ * (eight interleaved fp32 partial sums, combined pairwise), so every entry
+ * point produces the same logits bit for bit and dsa_indexer_topk's
+ * selection equals dsa_topk applied to these logits.
  */
 dsa_status_t dsa_indexer_logits(const void* q, const float* q_scale, const void* k,
                                 const float* k_scale, dsa_dtype_t dtype,
