@@ -52,11 +52,15 @@ struct ScoreCfg {
   static constexpr int THREADS = 64 + 128 * EPI_WG;
   static constexpr int Q_BYTES = ATOMS * N * 128;
   static constexpr int STAGE_BYTES = ATOMS * TILE * 128;
-  // misc: w_s[N] | rs_s[TOK] | re_s[TOK] | 24 barriers | tmem slot + abort
+  // misc: w_s[N] | rs_s[TOK] | re_s[TOK] | paged block-table slices for the
+  // producer and the epilogue (BT entries each) | 24 barriers | tmem slot + abort
+  static constexpr int BT = kPaged ? 256 : 0;  // >= chunk keys / smallest block (2048 / 8)
   static constexpr int MISC_W = 0;
   static constexpr int MISC_RS = N * 4;
   static constexpr int MISC_RE = MISC_RS + TOK * 4;
-  static constexpr int MISC_BARS = (MISC_RE + TOK * 4 + 7) / 8 * 8;
+  static constexpr int MISC_BTP = MISC_RE + TOK * 4;
+  static constexpr int MISC_BTE = MISC_BTP + BT * 4;
+  static constexpr int MISC_BARS = (MISC_BTE + BT * 4 + 7) / 8 * 8;
   static constexpr int MISC_SLOT = MISC_BARS + 24 * 8;
   static constexpr int MISC_BYTES = (MISC_SLOT + 16 + 127) / 128 * 128;
   static constexpr int SMEM_LIMIT = 232448;
@@ -68,8 +72,8 @@ struct ScoreCfg {
 
   static_assert(ROW_BYTES % 128 == 0, "a key row must be a whole number of swizzle atoms");
   static_assert(N % 16 == 0 && N >= 32 && N <= 256, "MMA N for M=128");
-  static_assert(N % H == 0 && EPI_COLS % H == 0 && (EPI_COLS == 32 || EPI_COLS == 64 ||
-                EPI_COLS == 128), "column split");
+  static_assert(N % H == 0 && EPI_COLS % H == 0 && (EPI_COLS == 32 || EPI_COLS == 64),
+                "column split");
   static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM allocation");
   static_assert(NST >= 2 && NST <= 8, "pipeline depth");
   static_assert(SMEM <= SMEM_LIMIT, "shared memory");
@@ -153,8 +157,13 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, float (&v)[COLS])
   }
 }
 
+// One CTA per SM: every thread may use its share of the 64K registers
+// (rounded down to a multiple of 8); the epilogue's in-flight TMEM loads must
+// not be spilled.
 template <int H, int N, int D, bool kFp8, bool kPaged>
-__global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
+__global__ void __maxnreg__((65536 / ScoreCfg<H, N, D, kFp8, kPaged>::THREADS) / 8 * 8 > 255
+                                ? 255
+                                : (65536 / ScoreCfg<H, N, D, kFp8, kPaged>::THREADS) / 8 * 8)
     score_kernel(const __grid_constant__ ScoreParams p) {
   using C = ScoreCfg<H, N, D, kFp8, kPaged>;
   extern __shared__ uint8_t smem_raw[];
@@ -173,6 +182,8 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
   uint64_t* qempty = bars + 18;  // [2]
   uint64_t* accf = bars + 20;    // [2]
   uint64_t* acce = bars + 22;    // [2]
+  int* bt_p = reinterpret_cast<int*>(misc + C::MISC_BTP);  // producer's block-table slice
+  int* bt_e = reinterpret_cast<int*>(misc + C::MISC_BTE);  // epilogue's block-table slice
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + C::MISC_SLOT);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(misc + C::MISC_SLOT + 4);
 
@@ -234,6 +245,26 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
       if (slot >= nslots) continue;
       const ScoreGroup g = score_group<C::TOK, kPaged>(p, slot, lane);
       if (g.kt_end <= g.kt_begin) continue;
+      if constexpr (kPaged) {
+        // The group's physical block ids, read once with coalesced loads
+        // (validated: an id outside the cache is recorded and replaced by 0).
+        const int bs = p.block_size;
+        const int nblk = (g.L + bs - 1) / bs;
+        const int lb0 = g.kt_begin * (C::TILE / bs);
+        const int cnt = (g.kt_end - g.kt_begin) * (C::TILE / bs);
+        __syncwarp();
+        for (int i = lane; i < cnt; i += 32) {
+          int lb = lb0 + i;
+          if (lb > nblk - 1) lb = nblk - 1;
+          int pb = p.block_table[static_cast<int64_t>(g.b) * p.max_blocks + lb];
+          if (pb < 0 || pb >= p.num_blocks) {
+            record_error(p.err, kErrBadIndex);
+            pb = 0;
+          }
+          bt_p[i] = pb;
+        }
+        __syncwarp();
+      }
       if (lane == 0) {
         const int qb = ngroups & 1;
         if (!mbar_wait_bounded(&qempty[qb], ((ngroups >> 1) & 1u) ^ 1u, abort_flag)) {
@@ -261,16 +292,9 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
                             a * C::ATOM_ELEMS, kt * C::TILE);
             } else {
               const int bs = p.block_size;
-              const int nblk = (g.L + bs - 1) / bs;
               const int per_tile = C::TILE / bs;
               for (int i = 0; i < per_tile; ++i) {
-                int lb = kt * per_tile + i;
-                if (lb > nblk - 1) lb = nblk - 1;
-                int pb = p.block_table[static_cast<int64_t>(g.b) * p.max_blocks + lb];
-                if (pb < 0 || pb >= p.num_blocks) {
-                  record_error(p.err, kErrBadIndex);
-                  pb = 0;
-                }
+                const int pb = bt_p[(kt - g.kt_begin) * per_tile + i];
 #pragma unroll
                 for (int a = 0; a < C::ATOMS; ++a)
                   tma_load_3d(dst + a * C::TILE * 128 + i * bs * 128, &p.tmap_k, &full[stage],
@@ -381,6 +405,19 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
         }
         w_s[i] = wv;
       }
+      if constexpr (kPaged && kFp8) {
+        const int bs = p.block_size;
+        const int nblk = (g.L + bs - 1) / bs;
+        const int lb0 = g.kt_begin * (C::TILE / bs);
+        const int cnt = (g.kt_end - g.kt_begin) * (C::TILE / bs);
+        for (int i = etid; i < cnt; i += 128 * C::EPI_WG) {
+          int lb = lb0 + i;
+          if (lb > nblk - 1) lb = nblk - 1;
+          int pb = p.block_table[static_cast<int64_t>(g.b) * p.max_blocks + lb];
+          if (pb < 0 || pb >= p.num_blocks) pb = 0;
+          bt_e[i] = pb;
+        }
+      }
       for (int i = etid; i < C::TOK; i += 128 * C::EPI_WG) {
         int lo = 0, hi = 0;
         if (i < g.ntok) {
@@ -398,57 +435,116 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
       }
       asm volatile("bar.sync 1, %0;" ::"r"(128 * C::EPI_WG) : "memory");
 
-      for (int kt = g.kt_begin; ok && kt < g.kt_end; ++kt) {
-        const int buf = tcount & 1;
-        const uint32_t aphase = static_cast<uint32_t>(tcount >> 1) & 1u;
-        // Warp-uniform outcome: tcgen05.ld below needs every lane.
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&accf[buf], aphase, abort_flag) ? 1 : 0);
-        if (!ok) break;
-        tc_fence_after_sync();
-        float v[C::EPI_COLS];
-        tmem_load_cols<C::EPI_COLS>(
-            tmem_base + lane_addr + static_cast<uint32_t>(buf * N + wg * C::EPI_COLS), v);
-        tc_fence_before_sync();
-        mbar_arrive(&acce[buf]);
-        ++tcount;
-
+      // Key scale of this thread's key in tile kt (fp8 only).
+      auto key_scale = [&](int kt) -> float {
         const int s = kt * C::TILE + key_in_tile;
-        float kscale = 1.f;
-        if constexpr (kFp8) {
-          if constexpr (kPaged) {
-            const int bs = p.block_size;
-            const int nblk = (g.L + bs - 1) / bs;
-            int lb = s / bs;
-            if (lb > nblk - 1) lb = nblk - 1;
-            int pb = p.block_table[static_cast<int64_t>(g.b) * p.max_blocks + lb];
-            if (pb < 0 || pb >= p.num_blocks) pb = 0;
-            kscale = p.k_scale[static_cast<int64_t>(pb) * bs + (s % bs)];
-          } else {
-            kscale = s < p.S ? p.k_scale[s] : 0.f;
-          }
+        if constexpr (kPaged) {
+          const int bs = p.block_size;
+          const int nblk = (g.L + bs - 1) / bs;
+          int lb = s / bs;
+          if (lb > nblk - 1) lb = nblk - 1;
+          const int pb = bt_e[lb - g.kt_begin * (C::TILE / bs)];
+          return p.k_scale[static_cast<int64_t>(pb) * bs + (s % bs)];
+        } else {
+          return s < p.S ? p.k_scale[s] : 0.f;
         }
+      };
+      // Reduce 32 accumulator columns (chunk CH of this thread's EPI_COLS):
+      // column c is head c % H of token c / H; head h feeds partial h % NPART
+      // in ascending h; a token is stored once its last head is in.
+      float part[C::NPART];
+      auto consume = [&](const uint32_t (&x)[32], int chunk, int kt, float kscale) {
+        const int s = kt * C::TILE + key_in_tile;
         const bool col_ok = s < p.S;
 #pragma unroll
-        for (int j = 0; j < C::EPI_TOK; ++j) {
-          const int tok = wg * C::EPI_TOK + j;
-          const float* wt = w_s + tok * H;
-          float part[C::NPART];
+        for (int i = 0; i < 32; ++i) {
+          const int col = chunk * 32 + i;
+          const int tl = col / H;           // token within this warpgroup
+          const int h = col % H;
+          if (h == 0) {
 #pragma unroll
-          for (int i = 0; i < C::NPART; ++i) part[i] = 0.f;
-#pragma unroll
-          for (int h = 0; h < H; ++h)
-            part[h % C::NPART] = fmaf(wt[h], fmaxf(v[j * H + h], 0.f), part[h % C::NPART]);
-#pragma unroll
-          for (int w = C::NPART / 2; w > 0; w >>= 1) {
-#pragma unroll
-            for (int i = 0; i < w; ++i) part[i] = part[i] + part[i + w];
+            for (int q = 0; q < C::NPART; ++q) part[q] = 0.f;
           }
-          float acc = part[0];
-          if constexpr (kFp8) acc *= kscale;
-          if (tok < g.ntok && col_ok) {
-            const float val = (s >= rs_s[tok] && s < re_s[tok]) ? acc : -INFINITY;
-            p.logits[static_cast<int64_t>(g.row0 + tok) * p.ld + s] = val;
+          const int tok = wg * C::EPI_TOK + tl;
+          part[h % C::NPART] =
+              fmaf(w_s[tok * H + h], fmaxf(__uint_as_float(x[i]), 0.f), part[h % C::NPART]);
+          if (h == H - 1) {
+#pragma unroll
+            for (int w = C::NPART / 2; w > 0; w >>= 1) {
+#pragma unroll
+              for (int q = 0; q < w; ++q) part[q] = part[q] + part[q + w];
+            }
+            float acc = part[0];
+            if constexpr (kFp8) acc *= kscale;
+            if (tok < g.ntok && col_ok) {
+              const float val = (s >= rs_s[tok] && s < re_s[tok]) ? acc : -INFINITY;
+              p.logits[static_cast<int64_t>(g.row0 + tok) * p.ld + s] = val;
+            }
           }
+        }
+      };
+      const uint32_t col0 = lane_addr + static_cast<uint32_t>(wg * C::EPI_COLS);
+      uint32_t xa[32], xb[32];
+      if constexpr (C::EPI_COLS == 64) {
+        // Software pipeline over 32-column chunks: the load of the next chunk
+        // (the second half of this tile, or the first half of the next tile)
+        // is in flight while the current chunk is reduced.
+        int kt = g.kt_begin;
+        {
+          const int buf = tcount & 1;
+          const uint32_t aphase = static_cast<uint32_t>(tcount >> 1) & 1u;
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&accf[buf], aphase, abort_flag) ? 1 : 0);
+          if (ok) {
+            tc_fence_after_sync();
+            tmem_ld32_async(tmem_base + col0 + static_cast<uint32_t>(buf * N), xa);
+            tmem_wait_ld(xa);
+          }
+        }
+        float ks_cur = 1.f;
+        if constexpr (kFp8) ks_cur = key_scale(kt);
+        for (; ok && kt < g.kt_end; ++kt) {
+          const int buf = tcount & 1;
+          tmem_ld32_async(tmem_base + col0 + static_cast<uint32_t>(buf * N + 32), xb);
+          float ks_next = 1.f;
+          if constexpr (kFp8) {
+            if (kt + 1 < g.kt_end) ks_next = key_scale(kt + 1);
+          }
+          consume(xa, 0, kt, ks_cur);
+          tmem_wait_ld(xb);
+          tc_fence_before_sync();
+          mbar_arrive(&acce[buf]);
+          ++tcount;
+          const bool more = kt + 1 < g.kt_end;
+          if (more) {
+            const int nbuf = tcount & 1;
+            const uint32_t nphase = static_cast<uint32_t>(tcount >> 1) & 1u;
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait_bounded(&accf[nbuf], nphase, abort_flag) ? 1 : 0);
+            if (ok) {
+              tc_fence_after_sync();
+              tmem_ld32_async(tmem_base + col0 + static_cast<uint32_t>(nbuf * N), xa);
+            }
+          }
+          consume(xb, 1, kt, ks_cur);
+          if (more && ok) tmem_wait_ld(xa);
+          ks_cur = ks_next;
+        }
+      } else {
+        for (int kt = g.kt_begin; ok && kt < g.kt_end; ++kt) {
+          const int buf = tcount & 1;
+          const uint32_t aphase = static_cast<uint32_t>(tcount >> 1) & 1u;
+          // Warp-uniform outcome: tcgen05.ld below needs every lane.
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&accf[buf], aphase, abort_flag) ? 1 : 0);
+          if (!ok) break;
+          tc_fence_after_sync();
+          tmem_ld32_async(tmem_base + col0 + static_cast<uint32_t>(buf * N), xa);
+          float kscale = 1.f;
+          if constexpr (kFp8) kscale = key_scale(kt);
+          tmem_wait_ld(xa);
+          tc_fence_before_sync();
+          mbar_arrive(&acce[buf]);
+          ++tcount;
+          consume(xa, 0, kt, kscale);
         }
       }
     }
