@@ -157,13 +157,8 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, float (&v)[COLS])
   }
 }
 
-// One CTA per SM: every thread may use its share of the 64K registers
-// (rounded down to a multiple of 8); the epilogue's in-flight TMEM loads must
-// not be spilled.
 template <int H, int N, int D, bool kFp8, bool kPaged>
-__global__ void __maxnreg__((65536 / ScoreCfg<H, N, D, kFp8, kPaged>::THREADS) / 8 * 8 > 255
-                                ? 255
-                                : (65536 / ScoreCfg<H, N, D, kFp8, kPaged>::THREADS) / 8 * 8)
+__global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
     score_kernel(const __grid_constant__ ScoreParams p) {
   using C = ScoreCfg<H, N, D, kFp8, kPaged>;
   extern __shared__ uint8_t smem_raw[];
