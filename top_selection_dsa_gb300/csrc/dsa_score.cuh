@@ -72,8 +72,8 @@ struct ScoreCfg {
 
   static_assert(ROW_BYTES % 128 == 0, "a key row must be a whole number of swizzle atoms");
   static_assert(N % 16 == 0 && N >= 32 && N <= 256, "MMA N for M=128");
-  static_assert(N % H == 0 && EPI_COLS % H == 0 && (EPI_COLS == 32 || EPI_COLS == 64),
-                "column split");
+  static_assert(N % H == 0 && EPI_COLS % H == 0 && (EPI_COLS == 32 || EPI_COLS == 64 ||
+                EPI_COLS == 128), "column split");
   static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM allocation");
   static_assert(NST >= 2 && NST <= 8, "pipeline depth");
   static_assert(SMEM <= SMEM_LIMIT, "shared memory");
@@ -134,6 +134,16 @@ __device__ __forceinline__ ScoreGroup score_group(const ScoreParams& p, int slot
     g.kt_end = hi > lo ? (hi + 127) / 128 : 0;
   }
   return g;
+}
+
+// ReLU of head h's dot product, as the epilogue takes it.  Three heads in four
+// use max(x, 0) (ALU pipe); every fourth uses x + |x| = 2 max(x, 0) (one add
+// on the FMA pipe), and its weight is staged halved, so that both forms give
+// the same products w * relu(x) bit for bit while the two pipes share the work.
+__host__ __device__ constexpr bool relu_by_add(int h) { return (h & 3) == 3; }
+
+__device__ __forceinline__ float relu_term(int h, float x) {
+  return relu_by_add(h) ? x + fabsf(x) : fmaxf(x, 0.f);
 }
 
 // Snake order over work items: round r visits CTAs 0..P-1 forward when r is
@@ -398,7 +408,9 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
           wv = p.weights[row * H + h];
           if (p.q_scale) wv *= p.q_scale[row * H + h];
         }
-        w_s[i] = wv;
+        // Heads that take their ReLU as x + |x| (= 2 relu(x)) get a halved
+        // weight: (w/2)(x + |x|) = w relu(x) exactly.
+        w_s[i] = relu_by_add(h) ? 0.5f * wv : wv;
       }
       if constexpr (kPaged && kFp8) {
         const int bs = p.block_size;
@@ -430,7 +442,7 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
       }
       asm volatile("bar.sync 1, %0;" ::"r"(128 * C::EPI_WG) : "memory");
 
-      // Key scale of this thread's key in tile kt (fp8 only).
+      // fp8: this thread's key scale, loaded one tile ahead of its use.
       auto key_scale = [&](int kt) -> float {
         const int s = kt * C::TILE + key_in_tile;
         if constexpr (kPaged) {
@@ -444,102 +456,68 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
           return s < p.S ? p.k_scale[s] : 0.f;
         }
       };
-      // Reduce 32 accumulator columns (chunk CH of this thread's EPI_COLS):
-      // column c is head c % H of token c / H; head h feeds partial h % NPART
-      // in ascending h; a token is stored once its last head is in.
-      float part[C::NPART];
-      auto consume = [&](const uint32_t (&x)[32], int chunk, int kt, float kscale) {
+      float ks_next = 1.f;
+      if constexpr (kFp8) ks_next = key_scale(g.kt_begin);
+      for (int kt = g.kt_begin; ok && kt < g.kt_end; ++kt) {
+        const int buf = tcount & 1;
+        const uint32_t aphase = static_cast<uint32_t>(tcount >> 1) & 1u;
+        // Warp-uniform outcome: tcgen05.ld below needs every lane.
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&accf[buf], aphase, abort_flag) ? 1 : 0);
+        if (!ok) break;
+        tc_fence_after_sync();
+        float v[C::EPI_COLS];
+        tmem_load_cols<C::EPI_COLS>(
+            tmem_base + lane_addr + static_cast<uint32_t>(buf * N + wg * C::EPI_COLS), v);
+        tc_fence_before_sync();
+        mbar_arrive(&acce[buf]);
+        ++tcount;
+
         const int s = kt * C::TILE + key_in_tile;
+        const float kscale = ks_next;
+        if constexpr (kFp8) {
+          if (kt + 1 < g.kt_end) ks_next = key_scale(kt + 1);
+        }
         const bool col_ok = s < p.S;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int col = chunk * 32 + i;
-          const int tl = col / H;           // token within this warpgroup
-          const int h = col % H;
-          if (h == 0) {
+        for (int j = 0; j < C::EPI_TOK; ++j) {
+          const int tok = wg * C::EPI_TOK + j;
+          const float* wt = w_s + tok * H;
+          float part[C::NPART];
 #pragma unroll
-            for (int q = 0; q < C::NPART; ++q) part[q] = 0.f;
-          }
-          const int tok = wg * C::EPI_TOK + tl;
-          part[h % C::NPART] =
-              fmaf(w_s[tok * H + h], fmaxf(__uint_as_float(x[i]), 0.f), part[h % C::NPART]);
-          if (h == H - 1) {
+          for (int i = 0; i < C::NPART; ++i) part[i] = 0.f;
+          if constexpr (C::NPART == 8) {
+            // Heads in pairs: one packed FMA per pair, same partials and order.
+            float2 part2[4];
 #pragma unroll
-            for (int w = C::NPART / 2; w > 0; w >>= 1) {
+            for (int i = 0; i < 4; ++i) part2[i] = make_float2(0.f, 0.f);
 #pragma unroll
-              for (int q = 0; q < w; ++q) part[q] = part[q] + part[q + w];
+            for (int h = 0; h < H; h += 2) {
+              const float2 w2 = *reinterpret_cast<const float2*>(wt + h);
+              const float2 y2 = make_float2(relu_term(h, v[j * H + h]),
+                                            relu_term(h + 1, v[j * H + h + 1]));
+              part2[(h % 8) / 2] = __ffma2_rn(w2, y2, part2[(h % 8) / 2]);
             }
-            float acc = part[0];
-            if constexpr (kFp8) acc *= kscale;
-            if (tok < g.ntok && col_ok) {
-              const float val = (s >= rs_s[tok] && s < re_s[tok]) ? acc : -INFINITY;
-              p.logits[static_cast<int64_t>(g.row0 + tok) * p.ld + s] = val;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              part[2 * i] = part2[i].x;
+              part[2 * i + 1] = part2[i].y;
             }
+          } else {
+#pragma unroll
+            for (int h = 0; h < H; ++h)
+              part[h % C::NPART] = fmaf(wt[h], relu_term(h, v[j * H + h]), part[h % C::NPART]);
           }
-        }
-      };
-      const uint32_t col0 = lane_addr + static_cast<uint32_t>(wg * C::EPI_COLS);
-      uint32_t xa[32], xb[32];
-      if constexpr (C::EPI_COLS == 64) {
-        // Software pipeline over 32-column chunks: the load of the next chunk
-        // (the second half of this tile, or the first half of the next tile)
-        // is in flight while the current chunk is reduced.
-        int kt = g.kt_begin;
-        {
-          const int buf = tcount & 1;
-          const uint32_t aphase = static_cast<uint32_t>(tcount >> 1) & 1u;
-          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&accf[buf], aphase, abort_flag) ? 1 : 0);
-          if (ok) {
-            tc_fence_after_sync();
-            tmem_ld32_async(tmem_base + col0 + static_cast<uint32_t>(buf * N), xa);
-            tmem_wait_ld(xa);
+#pragma unroll
+          for (int w = C::NPART / 2; w > 0; w >>= 1) {
+#pragma unroll
+            for (int i = 0; i < w; ++i) part[i] = part[i] + part[i + w];
           }
-        }
-        float ks_cur = 1.f;
-        if constexpr (kFp8) ks_cur = key_scale(kt);
-        for (; ok && kt < g.kt_end; ++kt) {
-          const int buf = tcount & 1;
-          tmem_ld32_async(tmem_base + col0 + static_cast<uint32_t>(buf * N + 32), xb);
-          float ks_next = 1.f;
-          if constexpr (kFp8) {
-            if (kt + 1 < g.kt_end) ks_next = key_scale(kt + 1);
+          float acc = part[0];
+          if constexpr (kFp8) acc *= kscale;
+          if (tok < g.ntok && col_ok) {
+            const float val = (s >= rs_s[tok] && s < re_s[tok]) ? acc : -INFINITY;
+            p.logits[static_cast<int64_t>(g.row0 + tok) * p.ld + s] = val;
           }
-          consume(xa, 0, kt, ks_cur);
-          tmem_wait_ld(xb);
-          tc_fence_before_sync();
-          mbar_arrive(&acce[buf]);
-          ++tcount;
-          const bool more = kt + 1 < g.kt_end;
-          if (more) {
-            const int nbuf = tcount & 1;
-            const uint32_t nphase = static_cast<uint32_t>(tcount >> 1) & 1u;
-            ok = __all_sync(0xffffffffu,
-                            mbar_wait_bounded(&accf[nbuf], nphase, abort_flag) ? 1 : 0);
-            if (ok) {
-              tc_fence_after_sync();
-              tmem_ld32_async(tmem_base + col0 + static_cast<uint32_t>(nbuf * N), xa);
-            }
-          }
-          consume(xb, 1, kt, ks_cur);
-          if (more && ok) tmem_wait_ld(xa);
-          ks_cur = ks_next;
-        }
-      } else {
-        for (int kt = g.kt_begin; ok && kt < g.kt_end; ++kt) {
-          const int buf = tcount & 1;
-          const uint32_t aphase = static_cast<uint32_t>(tcount >> 1) & 1u;
-          // Warp-uniform outcome: tcgen05.ld below needs every lane.
-          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&accf[buf], aphase, abort_flag) ? 1 : 0);
-          if (!ok) break;
-          tc_fence_after_sync();
-          tmem_ld32_async(tmem_base + col0 + static_cast<uint32_t>(buf * N), xa);
-          float kscale = 1.f;
-          if constexpr (kFp8) kscale = key_scale(kt);
-          tmem_wait_ld(xa);
-          tc_fence_before_sync();
-          mbar_arrive(&acce[buf]);
-          ++tcount;
-          consume(xa, 0, kt, kscale);
         }
       }
     }
