@@ -63,10 +63,15 @@ struct ScoreCfg {
   static constexpr int MISC_BARS = (MISC_BTE + BT * 4 + 7) / 8 * 8;
   static constexpr int MISC_SLOT = MISC_BARS + 24 * 8;
   static constexpr int MISC_BYTES = (MISC_SLOT + 16 + 127) / 128 * 128;
-  static constexpr int SMEM_LIMIT = 232448;
-  static constexpr int NST_FIT = (SMEM_LIMIT - 1024 - MISC_BYTES - 2 * Q_BYTES) / STAGE_BYTES;
+  // Prefill: one persistent CTA per SM with two q buffers.  Paged decode: one
+  // CTA per work item, two resident per SM (one streams while the other starts
+  // up), a single q buffer each.
+  static constexpr int QBUF = kPaged ? 1 : 2;
+  static constexpr int CTAS_PER_SM = (kPaged && Q_BYTES <= 32768 && THREADS <= 320) ? 2 : 1;
+  static constexpr int SMEM_LIMIT = CTAS_PER_SM == 2 ? (233472 / 2 - 1024) : 232448;
+  static constexpr int NST_FIT = (SMEM_LIMIT - 1024 - MISC_BYTES - QBUF * Q_BYTES) / STAGE_BYTES;
   static constexpr int NST = NST_FIT > 8 ? 8 : NST_FIT;
-  static constexpr int SMEM = 1024 + 2 * Q_BYTES + NST * STAGE_BYTES + MISC_BYTES;
+  static constexpr int SMEM = 1024 + QBUF * Q_BYTES + NST * STAGE_BYTES + MISC_BYTES;
   static constexpr uint32_t TMEM_COLS = 2u * N;
   static constexpr uint32_t IDESC = mma_idesc(kFp8 ? 0u : 1u, TILE, N);
 
@@ -168,14 +173,15 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, float (&v)[COLS])
 }
 
 template <int H, int N, int D, bool kFp8, bool kPaged>
-__global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
+__global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS,
+                                  ScoreCfg<H, N, D, kFp8, kPaged>::CTAS_PER_SM)
     score_kernel(const __grid_constant__ ScoreParams p) {
   using C = ScoreCfg<H, N, D, kFp8, kPaged>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* q_s = smem;                         // 2 x Q_BYTES
-  uint8_t* k_s = smem + 2 * C::Q_BYTES;        // NST x STAGE_BYTES
+  uint8_t* q_s = smem;                         // QBUF x Q_BYTES
+  uint8_t* k_s = smem + C::QBUF * C::Q_BYTES;  // NST x STAGE_BYTES
   uint8_t* misc = k_s + C::NST * C::STAGE_BYTES;
   float* w_s = reinterpret_cast<float*>(misc + C::MISC_W);
   int* rs_s = reinterpret_cast<int*>(misc + C::MISC_RS);
@@ -271,8 +277,9 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
         __syncwarp();
       }
       if (lane == 0) {
-        const int qb = ngroups & 1;
-        if (!mbar_wait_bounded(&qempty[qb], ((ngroups >> 1) & 1u) ^ 1u, abort_flag)) {
+        const int qb = ngroups % C::QBUF;
+        if (!mbar_wait_bounded(&qempty[qb], (static_cast<uint32_t>(ngroups / C::QBUF) & 1u) ^ 1u,
+                               abort_flag)) {
           ok = false;
         } else {
           mbar_arrive_expect_tx(&qfull[qb], C::Q_BYTES);
@@ -321,8 +328,8 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
       for (int i = first; i < kiter; ++i)
         mbar_wait_bounded(&full[i % C::NST], static_cast<uint32_t>(i / C::NST) & 1u, nullptr,
                           100000000ull);
-      for (int j = qissued > 2 ? qissued - 2 : 0; j < qissued; ++j)
-        mbar_wait_bounded(&qfull[j & 1], static_cast<uint32_t>(j >> 1) & 1u, nullptr,
+      for (int j = qissued > C::QBUF ? qissued - C::QBUF : 0; j < qissued; ++j)
+        mbar_wait_bounded(&qfull[j % C::QBUF], static_cast<uint32_t>(j / C::QBUF) & 1u, nullptr,
                           100000000ull);
     }
   } else if (warp == 1) {
@@ -335,8 +342,9 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
       const ScoreGroup g = score_group<C::TOK, kPaged>(p, slot, lane);
       if (g.kt_end <= g.kt_begin) continue;
       if (lane == 0) {
-        const int qb = ngroups & 1;
-        ok = mbar_wait_bounded(&qfull[qb], static_cast<uint32_t>(ngroups >> 1) & 1u, abort_flag);
+        const int qb = ngroups % C::QBUF;
+        ok = mbar_wait_bounded(&qfull[qb], static_cast<uint32_t>(ngroups / C::QBUF) & 1u,
+                               abort_flag);
         const uint32_t q_addr = smem_u32(q_s + qb * C::Q_BYTES);
         for (int kt = g.kt_begin; ok && kt < g.kt_end; ++kt) {
           const int stage = kiter % C::NST;
