@@ -48,12 +48,18 @@ struct ScoreCfg {
   static constexpr int EPI_WG = (N / MINCOLS) < 4 ? (N / MINCOLS) : 4;
   static constexpr int EPI_COLS = N / EPI_WG;       // accumulator columns per epilogue thread
   static constexpr int EPI_TOK = EPI_COLS / H;
+  // Paged decode has few columns: up to four warpgroups form EPI_SETS
+  // independent epilogue sets that take alternate tiles (tile i goes to set
+  // i % EPI_SETS), with NBUF TMEM accumulators in flight.
+  static constexpr int EPI_SETS = (kPaged && EPI_WG < 4) ? 4 / EPI_WG : 1;
+  static constexpr int NBUF = 2 * EPI_SETS;
+  static constexpr int EPI_THREADS = 128 * EPI_WG * EPI_SETS;
   static constexpr int NPART = H < 8 ? H : 8;       // partial sums of the head reduction
-  static constexpr int THREADS = 64 + 128 * EPI_WG;
+  static constexpr int THREADS = 64 + EPI_THREADS;
   static constexpr int Q_BYTES = ATOMS * N * 128;
   static constexpr int STAGE_BYTES = ATOMS * TILE * 128;
   // misc: w_s[N] | rs_s[TOK] | re_s[TOK] | paged block-table slices for the
-  // producer and the epilogue (BT entries each) | 24 barriers | tmem slot + abort
+  // producer and the epilogue (BT entries each) | 36 barriers | tmem slot + abort
   static constexpr int BT = kPaged ? 256 : 0;  // >= chunk keys / smallest block (2048 / 8)
   static constexpr int MISC_W = 0;
   static constexpr int MISC_RS = N * 4;
@@ -61,7 +67,7 @@ struct ScoreCfg {
   static constexpr int MISC_BTP = MISC_RE + TOK * 4;
   static constexpr int MISC_BTE = MISC_BTP + BT * 4;
   static constexpr int MISC_BARS = (MISC_BTE + BT * 4 + 7) / 8 * 8;
-  static constexpr int MISC_SLOT = MISC_BARS + 24 * 8;
+  static constexpr int MISC_SLOT = MISC_BARS + 36 * 8;
   static constexpr int MISC_BYTES = (MISC_SLOT + 16 + 127) / 128 * 128;
   // Prefill: one persistent CTA per SM with two q buffers.  Paged decode: one
   // CTA per work item, two resident per SM (one streams while the other starts
@@ -72,7 +78,7 @@ struct ScoreCfg {
   static constexpr int NST_FIT = (SMEM_LIMIT - 1024 - MISC_BYTES - QBUF * Q_BYTES) / STAGE_BYTES;
   static constexpr int NST = NST_FIT > 8 ? 8 : NST_FIT;
   static constexpr int SMEM = 1024 + QBUF * Q_BYTES + NST * STAGE_BYTES + MISC_BYTES;
-  static constexpr uint32_t TMEM_COLS = 2u * N;
+  static constexpr uint32_t TMEM_COLS = static_cast<uint32_t>(NBUF * N);
   static constexpr uint32_t IDESC = mma_idesc(kFp8 ? 0u : 1u, TILE, N);
 
   static_assert(ROW_BYTES % 128 == 0, "a key row must be a whole number of swizzle atoms");
@@ -191,8 +197,8 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS,
   uint64_t* empty = bars + 8;    // [8]
   uint64_t* qfull = bars + 16;   // [2]
   uint64_t* qempty = bars + 18;  // [2]
-  uint64_t* accf = bars + 20;    // [2]
-  uint64_t* acce = bars + 22;    // [2]
+  uint64_t* accf = bars + 20;    // [8]
+  uint64_t* acce = bars + 28;    // [8]
   int* bt_p = reinterpret_cast<int*>(misc + C::MISC_BTP);  // producer's block-table slice
   int* bt_e = reinterpret_cast<int*>(misc + C::MISC_BTE);  // epilogue's block-table slice
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + C::MISC_SLOT);
@@ -231,8 +237,10 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS,
     for (int i = 0; i < 2; ++i) {
       mbar_init(&qfull[i], 1);
       mbar_init(&qempty[i], 1);
+    }
+    for (int i = 0; i < C::NBUF; ++i) {
       mbar_init(&accf[i], 1);
-      mbar_init(&acce[i], 128 * C::EPI_WG);
+      mbar_init(&acce[i], 128 * C::EPI_WG);  // one epilogue set
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -349,8 +357,8 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS,
         for (int kt = g.kt_begin; ok && kt < g.kt_end; ++kt) {
           const int stage = kiter % C::NST;
           const uint32_t phase = static_cast<uint32_t>(kiter / C::NST) & 1u;
-          const int buf = tcount & 1;
-          const uint32_t aphase = static_cast<uint32_t>(tcount >> 1) & 1u;
+          const int buf = tcount % C::NBUF;
+          const uint32_t aphase = static_cast<uint32_t>(tcount / C::NBUF) & 1u;
           if (!mbar_wait_bounded(&acce[buf], aphase ^ 1u, abort_flag) ||
               !mbar_wait_bounded(&full[stage], phase, abort_flag)) {
             ok = false;
@@ -383,18 +391,19 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS,
       if (tcount > 0) {
         // The last commit covers every MMA issued before it.
         const int last = tcount - 1;
-        mbar_wait_bounded(&accf[last & 1], static_cast<uint32_t>(last >> 1) & 1u, nullptr,
-                          100000000ull);
+        mbar_wait_bounded(&accf[last % C::NBUF], static_cast<uint32_t>(last / C::NBUF) & 1u,
+                          nullptr, 100000000ull);
       }
     }
   } else {
     // ------------------------------------------------------------- epilogue
     const int ew = warp - 2;
-    const int wg = ew >> 2;        // column group of this warpgroup
+    const int set = ew / (4 * C::EPI_WG);  // tiles i with i % EPI_SETS == set
+    const int wg = (ew >> 2) % C::EPI_WG;  // column group of this warpgroup
     const int quarter = warp & 3;  // the TMEM lane quarter this warp may access
     const int key_in_tile = quarter * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-    const int etid = threadIdx.x - 64;  // 0 .. 128*EPI_WG-1
+    const int etid = threadIdx.x - 64;  // 0 .. EPI_THREADS-1
     int tcount = 0;
     bool ok = true;
     // No early exit from this loop: every epilogue warp must reach the same
@@ -407,8 +416,8 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS,
       if (g.kt_end <= g.kt_begin) continue;
       // Stage this group's weights and row ranges (every epilogue thread has
       // finished the previous group when the named barrier opens).
-      asm volatile("bar.sync 1, %0;" ::"r"(128 * C::EPI_WG) : "memory");
-      for (int i = etid; i < N; i += 128 * C::EPI_WG) {
+      asm volatile("bar.sync 1, %0;" ::"r"(C::EPI_THREADS) : "memory");
+      for (int i = etid; i < N; i += C::EPI_THREADS) {
         const int tok = i / H, h = i % H;
         float wv = 0.f;
         if (tok < g.ntok) {
@@ -425,7 +434,7 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS,
         const int nblk = (g.L + bs - 1) / bs;
         const int lb0 = g.kt_begin * (C::TILE / bs);
         const int cnt = (g.kt_end - g.kt_begin) * (C::TILE / bs);
-        for (int i = etid; i < cnt; i += 128 * C::EPI_WG) {
+        for (int i = etid; i < cnt; i += C::EPI_THREADS) {
           int lb = lb0 + i;
           if (lb > nblk - 1) lb = nblk - 1;
           int pb = p.block_table[static_cast<int64_t>(g.b) * p.max_blocks + lb];
@@ -433,7 +442,7 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS,
           bt_e[i] = pb;
         }
       }
-      for (int i = etid; i < C::TOK; i += 128 * C::EPI_WG) {
+      for (int i = etid; i < C::TOK; i += C::EPI_THREADS) {
         int lo = 0, hi = 0;
         if (i < g.ntok) {
           if constexpr (kPaged) {
@@ -448,7 +457,7 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS,
         rs_s[i] = lo;
         re_s[i] = hi;
       }
-      asm volatile("bar.sync 1, %0;" ::"r"(128 * C::EPI_WG) : "memory");
+      asm volatile("bar.sync 1, %0;" ::"r"(C::EPI_THREADS) : "memory");
 
       // fp8: this thread's key scale, loaded one tile ahead of its use.
       auto key_scale = [&](int kt) -> float {
@@ -464,11 +473,20 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS,
           return s < p.S ? p.k_scale[s] : 0.f;
         }
       };
+      // This set's first tile of the group (tiles alternate between sets);
+      // tcount keeps counting every tile of the CTA.
+      const int skip = ((set - tcount) % C::EPI_SETS + C::EPI_SETS) % C::EPI_SETS;
+      const int kt0 = g.kt_begin + skip;
+      const int ntile = g.kt_end - g.kt_begin;
       float ks_next = 1.f;
-      if constexpr (kFp8) ks_next = key_scale(g.kt_begin);
-      for (int kt = g.kt_begin; ok && kt < g.kt_end; ++kt) {
-        const int buf = tcount & 1;
-        const uint32_t aphase = static_cast<uint32_t>(tcount >> 1) & 1u;
+      if constexpr (kFp8) {
+        if (kt0 < g.kt_end) ks_next = key_scale(kt0);
+      }
+      int tc = tcount + skip;
+      tcount += ntile;
+      for (int kt = kt0; ok && kt < g.kt_end; kt += C::EPI_SETS, tc += C::EPI_SETS) {
+        const int buf = tc % C::NBUF;
+        const uint32_t aphase = static_cast<uint32_t>(tc / C::NBUF) & 1u;
         // Warp-uniform outcome: tcgen05.ld below needs every lane.
         ok = __all_sync(0xffffffffu, mbar_wait_bounded(&accf[buf], aphase, abort_flag) ? 1 : 0);
         if (!ok) break;
@@ -478,12 +496,11 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS,
             tmem_base + lane_addr + static_cast<uint32_t>(buf * N + wg * C::EPI_COLS), v);
         tc_fence_before_sync();
         mbar_arrive(&acce[buf]);
-        ++tcount;
 
         const int s = kt * C::TILE + key_in_tile;
         const float kscale = ks_next;
         if constexpr (kFp8) {
-          if (kt + 1 < g.kt_end) ks_next = key_scale(kt + 1);
+          if (kt + C::EPI_SETS < g.kt_end) ks_next = key_scale(kt + C::EPI_SETS);
         }
         const bool col_ok = s < p.S;
 #pragma unroll
