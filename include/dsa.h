@@ -140,6 +140,7 @@ dsa_status_t dsa_indexer_topk(const void* q, const float* q_scale, const void* k
  * Index logits of paged decode (the paged indexer K cache of
  * KimiK3DSAIndexer: KimiK3IndexerCache / DeepseekV32IndexerCache).
  *
+ *   B            requests, 0 <= B <= 2048 (DSA_ERR_UNSUPPORTED above)
  *   q            [B*next_n, H, D]; query row r = b*next_n + j is token j of request b
  *   q_scale      NULL or [B*next_n, H] fp32
  *   weights      [B*next_n, H] fp32

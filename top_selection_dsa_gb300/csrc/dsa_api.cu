@@ -206,6 +206,7 @@ dsa_status_t check_paged_args(const void* q, const float* q_scale, const float* 
   dsa_status_t st = check_elems(dtype, s.H, s.D, k_scale);
   if (st != DSA_OK) return st;
   if (!score_paged_supported(dtype == DSA_E4M3, s.H, s.D, s.next_n)) return DSA_ERR_UNSUPPORTED;
+  if (s.B > kMaxPagedRequests) return DSA_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(s.max_blocks) * s.block_size >= (int64_t(1) << 30) ||
       static_cast<int64_t>(s.B) * s.next_n * s.H >= (int64_t(1) << 31))
     return DSA_ERR_UNSUPPORTED;

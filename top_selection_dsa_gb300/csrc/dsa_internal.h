@@ -33,6 +33,10 @@ struct ScoreParams {
   uint32_t* err;    // device error word
 };
 
+// Largest batch of paged-decode requests one call takes (the scoring kernel
+// keeps a per-request prefix sum of its work list in shared memory).
+constexpr int kMaxPagedRequests = 2048;
+
 struct TopkParams {
   const float* logits;  // [R, ld]
   int64_t ld;

@@ -61,20 +61,20 @@ struct ScoreCfg {
   // misc: w_s[N] | rs_s[TOK] | re_s[TOK] | paged block-table slices for the
   // producer and the epilogue (BT entries each) | 36 barriers | tmem slot + abort
   static constexpr int BT = kPaged ? 256 : 0;  // >= chunk keys / smallest block (2048 / 8)
+  static constexpr int PFX = kPaged ? kMaxPagedRequests + 1 : 0;  // work-list prefix sums
   static constexpr int MISC_W = 0;
   static constexpr int MISC_RS = N * 4;
   static constexpr int MISC_RE = MISC_RS + TOK * 4;
   static constexpr int MISC_BTP = MISC_RE + TOK * 4;
   static constexpr int MISC_BTE = MISC_BTP + BT * 4;
-  static constexpr int MISC_BARS = (MISC_BTE + BT * 4 + 7) / 8 * 8;
+  static constexpr int MISC_PFX = MISC_BTE + BT * 4;
+  static constexpr int MISC_BARS = (MISC_PFX + PFX * 4 + 7) / 8 * 8;
   static constexpr int MISC_SLOT = MISC_BARS + 36 * 8;
   static constexpr int MISC_BYTES = (MISC_SLOT + 16 + 127) / 128 * 128;
-  // Prefill: one persistent CTA per SM with two q buffers.  Paged decode: one
-  // CTA per work item, two resident per SM (one streams while the other starts
-  // up), a single q buffer each.
-  static constexpr int QBUF = kPaged ? 1 : 2;
-  static constexpr int CTAS_PER_SM = (kPaged && Q_BYTES <= 32768 && THREADS <= 320) ? 2 : 1;
-  static constexpr int SMEM_LIMIT = CTAS_PER_SM == 2 ? (233472 / 2 - 1024) : 232448;
+  // One persistent CTA per SM with two q buffers (the next group's q tile
+  // loads while the current group runs).
+  static constexpr int QBUF = 2;
+  static constexpr int SMEM_LIMIT = 232448;
   static constexpr int NST_FIT = (SMEM_LIMIT - 1024 - MISC_BYTES - QBUF * Q_BYTES) / STAGE_BYTES;
   static constexpr int NST = NST_FIT > 8 ? 8 : NST_FIT;
   static constexpr int SMEM = 1024 + QBUF * Q_BYTES + NST * STAGE_BYTES + MISC_BYTES;
@@ -101,19 +101,26 @@ struct ScoreGroup {
   bool bad_len;  // paged: context length was out of range
 };
 
-// Work item `slot`.  Must be called by all 32 lanes of a warp.
+// Work item `slot`.  Must be called by all 32 lanes of a warp.  Paged decode:
+// slot indexes the CTA's compacted list of non-empty (request, chunk) items,
+// pfx[b] being the number of items of requests before b.
 template <int TOK, bool kPaged>
-__device__ __forceinline__ ScoreGroup score_group(const ScoreParams& p, int slot, int lane) {
+__device__ __forceinline__ ScoreGroup score_group(const ScoreParams& p, int slot, int lane,
+                                                  const int* pfx) {
   ScoreGroup g;
   g.bad_len = false;
   if constexpr (kPaged) {
     const int B = p.R / p.next_n;
-    const int c = slot / B;
-    g.b = slot % B;
+    int lo_b = 0, hi_b = B;  // largest b with pfx[b] <= slot
+    while (hi_b - lo_b > 1) {
+      const int mid = (lo_b + hi_b) >> 1;
+      if (pfx[mid] <= slot) lo_b = mid; else hi_b = mid;
+    }
+    g.b = lo_b;
+    const int c = slot - pfx[lo_b];
     const int Lraw = p.context_lens[g.b];
     const int cap = p.max_blocks * p.block_size;
     g.L = Lraw < 0 ? 0 : (Lraw > cap ? cap : Lraw);
-    g.bad_len = (c == 0) && (Lraw < 0 || Lraw > cap);
     const int lo = c * p.chunk_keys;
     const int hi = min(g.L, lo + p.chunk_keys);
     g.row0 = g.b * p.next_n;
@@ -179,8 +186,7 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, float (&v)[COLS])
 }
 
 template <int H, int N, int D, bool kFp8, bool kPaged>
-__global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS,
-                                  ScoreCfg<H, N, D, kFp8, kPaged>::CTAS_PER_SM)
+__global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
     score_kernel(const __grid_constant__ ScoreParams p) {
   using C = ScoreCfg<H, N, D, kFp8, kPaged>;
   extern __shared__ uint8_t smem_raw[];
@@ -208,25 +214,43 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS,
   const int lane = threadIdx.x & 31;
   const int P = gridDim.x;
   const int cta = blockIdx.x;
+  int* pfx = reinterpret_cast<int*>(misc + C::MISC_PFX);
+  if constexpr (kPaged) {
+    // The work list: every non-empty chunk of every request, request-major.
+    // Each CTA derives it from the context lengths (no global state).
+    if (warp == 0) {
+      const int B = p.R / p.next_n;
+      const int cap = p.max_blocks * p.block_size;
+      int carry = 0;
+      if (lane == 0) pfx[0] = 0;
+      for (int base = 0; base < B; base += 32) {
+        const int b = base + lane;
+        int cnt = 0;
+        if (b < B) {
+          const int Lraw = p.context_lens[b];
+          if ((Lraw < 0 || Lraw > cap) && cta == 0) record_error(p.err, kErrBadIndex);
+          const int L = Lraw < 0 ? 0 : (Lraw > cap ? cap : Lraw);
+          cnt = (L + p.chunk_keys - 1) / p.chunk_keys;
+        }
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        if (b < B) pfx[b + 1] = carry + incl;
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+      }
+    }
+    __syncthreads();
+  }
   int nslots;
   if constexpr (kPaged) {
-    nslots = (p.R / p.next_n) * p.chunks_per_req;
+    nslots = pfx[p.R / p.next_n];
   } else {
     nslots = (p.R + C::TOK - 1) / C::TOK;
   }
   const int rounds = (nslots + P - 1) / P;
-  if constexpr (kPaged) {
-    // Paged decode launches one CTA per work item: a CTA whose chunk lies past
-    // its request's context leaves before touching barriers or TMEM.
-    if (rounds == 1) {
-      const int slot = snake_slot(0, P, cta);
-      const ScoreGroup g0 = score_group<C::TOK, kPaged>(p, slot, lane);
-      if (slot >= nslots || g0.kt_end <= g0.kt_begin) {
-        if (threadIdx.x == 0 && slot < nslots && g0.bad_len) record_error(p.err, kErrBadIndex);
-        return;
-      }
-    }
-  }
 
   // -------------------------------------------------------------------- setup
   if (threadIdx.x == 0) {
@@ -262,7 +286,7 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS,
     for (int r = 0; r < rounds && ok; ++r) {
       const int slot = snake_slot(r, P, cta);
       if (slot >= nslots) continue;
-      const ScoreGroup g = score_group<C::TOK, kPaged>(p, slot, lane);
+      const ScoreGroup g = score_group<C::TOK, kPaged>(p, slot, lane, pfx);
       if (g.kt_end <= g.kt_begin) continue;
       if constexpr (kPaged) {
         // The group's physical block ids, read once with coalesced loads
@@ -347,7 +371,7 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS,
     for (int r = 0; r < rounds && ok; ++r) {
       const int slot = snake_slot(r, P, cta);
       if (slot >= nslots) continue;
-      const ScoreGroup g = score_group<C::TOK, kPaged>(p, slot, lane);
+      const ScoreGroup g = score_group<C::TOK, kPaged>(p, slot, lane, pfx);
       if (g.kt_end <= g.kt_begin) continue;
       if (lane == 0) {
         const int qb = ngroups % C::QBUF;
@@ -411,8 +435,7 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS,
     for (int r = 0; r < rounds; ++r) {
       const int slot = snake_slot(r, P, cta);
       if (slot >= nslots) continue;
-      const ScoreGroup g = score_group<C::TOK, kPaged>(p, slot, lane);
-      if (etid == 0 && g.bad_len) record_error(p.err, kErrBadIndex);
+      const ScoreGroup g = score_group<C::TOK, kPaged>(p, slot, lane, pfx);
       if (g.kt_end <= g.kt_begin) continue;
       // Stage this group's weights and row ranges (every epilogue thread has
       // finished the previous group when the named barrier opens).
@@ -563,8 +586,8 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS,
 
 int device_sm_count();
 
-// Prefill runs persistent CTAs (one per SM); paged decode runs one CTA per
-// work item, most of which exit at once, and lets the hardware balance them.
+// Persistent CTAs: one per SM, at most one per work item (paged decode: the
+// number of (request, chunk) slots bounds the non-empty items).
 template <int H, int N, int D, bool kFp8, bool kPaged>
 cudaError_t launch_score_instance(const ScoreParams& p, int work_items, cudaStream_t st) {
   using C = ScoreCfg<H, N, D, kFp8, kPaged>;
@@ -572,12 +595,9 @@ cudaError_t launch_score_instance(const ScoreParams& p, int work_items, cudaStre
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   if (work_items <= 0) return cudaSuccess;
-  int grid = work_items;
-  if constexpr (!kPaged) {
-    const int sms = device_sm_count();
-    if (sms <= 0) return cudaErrorInvalidDevice;
-    grid = work_items < sms ? work_items : sms;
-  }
+  const int sms = device_sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const int grid = work_items < sms ? work_items : sms;
   kern<<<grid, C::THREADS, C::SMEM, st>>>(p);
   return cudaGetLastError();
 }
