@@ -282,24 +282,34 @@ def run_ours(args):
         ks = cuda(p.k_scale) if p.k_scale is not None else None
         rows_per_step = p.T
         ld = (p.S + 3) // 4 * 4
-        logits = torch.empty((p.T, ld), dtype=torch.float32, device=device)
+        # One workspace as the composed call lays it out: logits, then (few
+        # long rows only) the split top-k scratch.
+        ws = torch.empty(api.workspace_bytes(api.DSA_OP_INDEXER_TOPK, p.T, p.S, p.topk),
+                         dtype=torch.uint8, device=device)
+        lg_bytes = (p.T * ld * 4 + 255) // 256 * 256
+        logits = ws[:p.T * ld * 4].view(torch.float32).view(p.T, ld)
+        ws_topk = ws[lg_bytes:]
         out = torch.empty((p.T, p.topk), dtype=torch.int32, device=device)
 
         def score():
             api.indexer_logits(q, k, w, rs, re_, k_scale=ks, logits=logits)
 
         def select():
-            api.topk(logits, rs, re_, p.topk, S=p.S, out=out)
+            api.topk(logits, rs, re_, p.topk, S=p.S, out=out, workspace=ws_topk)
 
         def fused(o):
-            return api.indexer_topk(q, k, w, rs, re_, p.topk, k_scale=ks, out=o, workspace=logits)
+            return api.indexer_topk(q, k, w, rs, re_, p.topk, k_scale=ks, out=o, workspace=ws)
     else:
         q, w, kc = elems(p.q), cuda(p.w), elems(p.k_cache)
         bt, cl = cuda(p.block_table), cuda(p.context_lens)
         ks = cuda(p.k_scale.reshape(-1)) if p.k_scale is not None else None
         rows_per_step = p.R
         ld = p.max_ctx()
-        logits = torch.empty((p.R, ld), dtype=torch.float32, device=device)
+        ws = torch.empty(api.workspace_bytes(api.DSA_OP_INDEXER_TOPK_PAGED, p.R, ld, p.topk),
+                         dtype=torch.uint8, device=device)
+        lg_bytes = (p.R * ld * 4 + 255) // 256 * 256
+        logits = ws[:p.R * ld * 4].view(torch.float32).view(p.R, ld)
+        ws_topk = ws[lg_bytes:]
         out = torch.empty((p.R, p.topk), dtype=torch.int32, device=device)
         rs_np, re_np = (np.zeros(p.R, np.int32),
                         np.array([max(int(p.context_lens[r // p.next_n]) - p.next_n
@@ -311,11 +321,11 @@ def run_ours(args):
                                      logits=logits)
 
         def select():
-            api.topk(logits, rs, re_, p.topk, out=out)
+            api.topk(logits, rs, re_, p.topk, out=out, workspace=ws_topk)
 
         def fused(o):
             return api.indexer_topk_paged(q, w, kc, bt, cl, p.topk, next_n=p.next_n,
-                                          k_scale=ks, out=o, workspace=logits)
+                                          k_scale=ks, out=o, workspace=ws)
 
     # The fused entry point is the same two kernels: check bit-identity once.
     score()

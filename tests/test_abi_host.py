@@ -53,8 +53,13 @@ def test_workspace_bytes(api):
     assert wb(api.DSA_OP_INDEXER_LOGITS, 10, 10, 4) == 0
     assert wb(api.DSA_OP_TOPK, 10, 10, 4) == 0
     assert wb(api.DSA_OP_INDEXER_TOPK, 4096, 4096, 2048) == 4096 * 4096 * 4
-    assert wb(api.DSA_OP_INDEXER_TOPK, 3, 5, 1) == 3 * 8 * 4          # rows padded to 16 B
-    assert wb(api.DSA_OP_INDEXER_TOPK_PAGED, 128, 131072, 2048) == 128 * 131072 * 4
+    assert wb(api.DSA_OP_INDEXER_TOPK, 3, 5, 1) == 256        # rows padded to 16 B, total to 256
+    # few long rows: per-row first-digit histograms (2048 words) follow the logits
+    assert wb(api.DSA_OP_TOPK, 128, 131072, 2048) == 128 * 2048 * 4
+    assert wb(api.DSA_OP_TOPK, 4096, 131072, 2048) == 0       # many rows: no scratch
+    assert wb(api.DSA_OP_TOPK, 128, 16384, 2048) == 0         # short rows: no scratch
+    assert wb(api.DSA_OP_INDEXER_TOPK_PAGED, 128, 131072, 2048) == \
+        128 * 131072 * 4 + 128 * 2048 * 4
     assert wb(api.DSA_OP_INDEXER_TOPK, 0, 100, 1) == 0
     bad = ctypes.c_size_t(-1).value
     assert wb(api.DSA_OP_INDEXER_TOPK, -1, 5, 1) == bad
@@ -96,6 +101,11 @@ def test_indexer_logits_validation(api):
 def test_topk_validation(api):
     E = api.DSA_ERR_INVALID_ARG
     f = api.lib.dsa_topk
+    need = api.lib.dsa_workspace_bytes(api.DSA_OP_TOPK, 4, 100000, 8)
+    assert need > 0
+    assert f(A, 100000, A, A, 4, 100000, 8, A, NUL, 0, NUL) == E       # split path needs scratch
+    assert f(A, 100000, A, A, 4, 100000, 8, A, A, need - 1, NUL) == E
+    assert f(A, 100000, A, A, 4, 100000, 8, A, MIS, need, NUL) == E
     assert f(NUL, 8, A, A, 4, 8, 2, A, NUL, 0, NUL) == E
     assert f(A, 8, A, A, 4, 8, 0, A, NUL, 0, NUL) == E       # k < 1
     assert f(A, 4, A, A, 4, 8, 2, A, NUL, 0, NUL) == E       # ld < S

@@ -149,7 +149,7 @@ def indexer_logits(q, k, weights, row_starts, row_ends, *, q_scale=None, k_scale
     return logits
 
 
-def topk(logits, row_starts, row_ends, k, *, S=None, out=None):
+def topk(logits, row_starts, row_ends, k, *, S=None, out=None, workspace=None):
     """Masked top-k [T, k] int32 of fp32 logits [T, ld] over columns [0, S)."""
     T, ld = logits.shape
     S = ld if S is None else S
@@ -160,8 +160,10 @@ def topk(logits, row_starts, row_ends, k, *, S=None, out=None):
     if out is None:
         out = torch.empty((T, k), dtype=torch.int32, device=dev)
     _need(out, "out", (torch.int32,), dev)
+    nbytes = workspace_bytes(DSA_OP_TOPK, T, S, k)
+    ws = _workspace(nbytes, dev, workspace)
     st = lib.dsa_topk(_ptr(logits), ld, _ptr(row_starts), _ptr(row_ends), T, S, k, _ptr(out),
-                      None, 0, _stream(dev))
+                      _ptr(ws) if nbytes else None, nbytes, _stream(dev))
     _check(st, "dsa_topk")
     return out
 

@@ -115,6 +115,19 @@ bool encode_map(CUtensorMap* map, const void* base, dsa_dtype_t dtype, int D, in
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
+// Workspace of the composed calls: the fp32 logits [rows, round_up(cols, 4)],
+// padded to 256 bytes, then (split top-k path only) the per-row histograms.
+size_t logits_scratch_bytes(int64_t rows, int64_t cols) {
+  return static_cast<size_t>(round_up(
+      rows * round_up(cols > 0 ? cols : 1, 4) * static_cast<int64_t>(sizeof(float)), 256));
+}
+
+uint32_t* split_scratch(void* workspace, int64_t rows, int64_t cols) {
+  if (!topk_split_rows(rows, cols)) return nullptr;
+  return reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) +
+                                     logits_scratch_bytes(rows, cols));
+}
+
 // ---------------------------------------------------------------- validation
 
 dsa_status_t check_elems(dsa_dtype_t dtype, int H, int D, const void* k_scale) {
@@ -170,7 +183,7 @@ dsa_status_t run_logits(const void* q, const float* q_scale, const void* k, cons
 
 dsa_status_t run_topk(const float* logits, int64_t ld, const int32_t* row_starts,
                       const int32_t* row_ends, const int32_t* context_lens, int next_n, int R,
-                      int S, int k, int32_t* out, cudaStream_t st) {
+                      int S, int k, int32_t* out, cudaStream_t st, uint32_t* hist0 = nullptr) {
   if (R == 0) return DSA_OK;
   TopkParams p = {};
   p.logits = logits;
@@ -184,6 +197,7 @@ dsa_status_t run_topk(const float* logits, int64_t ld, const int32_t* row_starts
   p.k = k;
   p.bitmap_words = topk_bitmap_words(S);
   p.out = out;
+  p.hist0 = hist0;
   return from_cuda(launch_topk(p, st));
 }
 
@@ -315,15 +329,17 @@ dsa_status_t dsa_indexer_logits(const void* q, const float* q_scale, const void*
 dsa_status_t dsa_topk(const float* logits, int64_t ld, const int32_t* row_starts,
                       const int32_t* row_ends, int T, int S, int k, int32_t* out, void* workspace,
                       size_t ws_bytes, dsa_stream_t stream) {
-  (void)workspace;
-  (void)ws_bytes;
   if (!logits || !row_starts || !row_ends || !out) return DSA_ERR_INVALID_ARG;
   if (T < 0 || S < 0 || k < 1 || ld < S || ld < 1) return DSA_ERR_INVALID_ARG;
   if (!aligned(logits, 4) || !aligned(out, 4) || !aligned(row_starts, 4) ||
       !aligned(row_ends, 4))
     return DSA_ERR_INVALID_ARG;
   if (!topk_supported(S)) return DSA_ERR_UNSUPPORTED;
-  return run_topk(logits, ld, row_starts, row_ends, nullptr, 1, T, S, k, out, as_stream(stream));
+  const size_t need = dsa_workspace_bytes(DSA_OP_TOPK, T, S, k);
+  if (need > 0 && (!workspace || ws_bytes < need || !aligned(workspace, 256)))
+    return DSA_ERR_INVALID_ARG;
+  return run_topk(logits, ld, row_starts, row_ends, nullptr, 1, T, S, k, out, as_stream(stream),
+                  need > 0 ? static_cast<uint32_t*>(workspace) : nullptr);
 }
 
 dsa_status_t dsa_indexer_topk(const void* q, const float* q_scale, const void* k,
@@ -345,7 +361,8 @@ dsa_status_t dsa_indexer_topk(const void* q, const float* q_scale, const void* k
   st = run_logits(q, q_scale, k, k_scale, dtype, weights, row_starts, row_ends, T, S, H, D, lg, ld,
                   as_stream(stream));
   if (st != DSA_OK) return st;
-  return run_topk(lg, ld, row_starts, row_ends, nullptr, 1, T, S, topk, out, as_stream(stream));
+  return run_topk(lg, ld, row_starts, row_ends, nullptr, 1, T, S, topk, out, as_stream(stream),
+                  split_scratch(workspace, T, S));
 }
 
 dsa_status_t dsa_indexer_logits_paged(const void* q, const float* q_scale, const float* weights,
@@ -388,21 +405,23 @@ dsa_status_t dsa_indexer_topk_paged(const void* q, const float* q_scale, const f
                         lg, ld, as_stream(stream));
   if (st != DSA_OK) return st;
   return run_topk(lg, ld, nullptr, nullptr, context_lens, next_n, static_cast<int>(R),
-                  static_cast<int>(max_ctx), topk, out, as_stream(stream));
+                  static_cast<int>(max_ctx), topk, out, as_stream(stream),
+                  split_scratch(workspace, R, max_ctx));
 }
 
 size_t dsa_workspace_bytes(dsa_op_t op, int64_t rows, int64_t cols, int k) {
   if (rows < 0 || cols < 0 || k < 0) return static_cast<size_t>(-1);
   switch (op) {
     case DSA_OP_INDEXER_LOGITS:
-    case DSA_OP_TOPK:
     case DSA_OP_INDEXER_LOGITS_PAGED:
       return 0;
+    case DSA_OP_TOPK:
+      return topk_split_rows(rows, cols) ? static_cast<size_t>(rows) * kTopkSplitBytesPerRow : 0;
     case DSA_OP_INDEXER_TOPK:
     case DSA_OP_INDEXER_TOPK_PAGED:
       if (rows == 0) return 0;
-      return static_cast<size_t>(rows) * static_cast<size_t>(round_up(cols > 0 ? cols : 1, 4)) *
-             sizeof(float);
+      return logits_scratch_bytes(rows, cols) +
+             (topk_split_rows(rows, cols) ? static_cast<size_t>(rows) * kTopkSplitBytesPerRow : 0);
     default:
       return static_cast<size_t>(-1);
   }

@@ -407,8 +407,7 @@ __global__ void __launch_bounds__(THREADS, 65536 / (THREADS * 64)) topk_reg_kern
 
 // --------------------------------------------------------------- streaming
 
-constexpr int kStreamThreads = 256;
-
+template <int kStreamThreads>
 __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const TopkParams p) {
   extern __shared__ uint32_t sm[];
   uint32_t* hist = sm;                   // kHistBins
@@ -426,7 +425,22 @@ __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const TopkP
   const float* src = p.logits + static_cast<int64_t>(row) * p.ld + lo;
   int32_t* dst = p.out + static_cast<int64_t>(row) * p.k;
 
-  // Pass 0: histogram of the top 11 key bits, 16-byte loads from memory.
+  // Pass 0: histogram of the top 11 key bits, 16-byte loads from memory (or,
+  // on the split path, the histogram the segment CTAs already built).
+  if (p.hist0) {
+    const uint32_t* h0 = p.hist0 + static_cast<int64_t>(row) * kHistBins;
+    uint32_t nv = 0;
+    for (int i = tid; i < kHistBins; i += kStreamThreads) {
+      const uint32_t v = h0[i];
+      hist[i] = v;
+      nv += v;
+    }
+    if (tid == 0) valid_count = 0u;
+    __syncthreads();
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) nv += __shfl_xor_sync(0xffffffffu, nv, o);
+    if (lane == 0 && nv) atomicAdd(&valid_count, nv);
+  } else {
   for (int i = tid; i < kHistBins; i += kStreamThreads) hist[i] = 0u;
   if (tid == 0) valid_count = 0u;
   __syncthreads();
@@ -455,6 +469,7 @@ __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const TopkP
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) nv += __shfl_xor_sync(0xffffffffu, nv, o);
     if (lane == 0 && nv) atomicAdd(&valid_count, nv);
+  }
   }
   __syncthreads();
   const uint32_t nvalid = valid_count;
@@ -537,6 +552,37 @@ __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const TopkP
   for (int i = nsel + tid; i < p.k; i += kStreamThreads) dst[i] = -1;
 }
 
+// Split path, step 1: CTA (segment, row) histograms the top 11 key bits of
+// keys [seg*4096, seg*4096 + 4096) of the row's range into the row's global
+// histogram (valid keys only).
+constexpr int kSegKeys = 4096;
+constexpr int kSegThreads = 256;
+
+__global__ void __launch_bounds__(kSegThreads) topk_hist_kernel(const TopkParams p) {
+  __shared__ uint32_t hist[kHistBins];
+  const int row = blockIdx.y;
+  const int tid = threadIdx.x;
+  int lo, hi;
+  row_range(p, row, &lo, &hi);
+  const int s0 = static_cast<int>(blockIdx.x) * kSegKeys;
+  const int cnt = min(hi - lo - s0, kSegKeys);
+  if (cnt <= 0) return;
+  for (int i = tid; i < kHistBins; i += kSegThreads) hist[i] = 0u;
+  __syncthreads();
+  const float* src = p.logits + static_cast<int64_t>(row) * p.ld + lo + s0;
+#pragma unroll 4
+  for (int i = tid; i < cnt; i += kSegThreads) {
+    const uint32_t kk = order_key(src[i]);
+    if (kk != 0u) atomicAdd(&hist[kk >> 21], 1u);
+  }
+  __syncthreads();
+  uint32_t* g = p.hist0 + static_cast<int64_t>(row) * kHistBins;
+  for (int i = tid; i < kHistBins; i += kSegThreads) {
+    const uint32_t v = hist[i];
+    if (v) atomicAdd(&g[i], v);
+  }
+}
+
 template <int THREADS, int ITEMS, int CL>
 cudaError_t launch_reg(const TopkParams& p, cudaStream_t s) {
   auto kern = topk_reg_kernel<THREADS, ITEMS, CL>;
@@ -573,26 +619,45 @@ bool topk_supported(int max_row) {
 // Longest row (in keys) the register-resident kernel takes.
 constexpr int kTopkRegMaxRow = 1024 * 32 * 8;
 
+bool topk_split_rows(int64_t rows, int64_t max_row) {
+  return max_row > 16384 && rows <= 512;
+}
+
+template <int THREADS>
+cudaError_t launch_stream(const TopkParams& p, cudaStream_t s) {
+  const size_t smem =
+      sizeof(uint32_t) * (static_cast<size_t>(kHistBins) + 2 * static_cast<size_t>(p.bitmap_words));
+  if (smem > 232448) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(topk_stream_kernel<THREADS>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  topk_stream_kernel<THREADS><<<p.R, THREADS, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t s) {
   if (p.R <= 0) return cudaSuccess;
   const int S = p.S;
+  if (p.hist0) {
+    // Few long rows: histograms from many CTAs per row, then one CTA per row.
+    cudaError_t e = cudaMemsetAsync(p.hist0, 0, static_cast<size_t>(p.R) * kTopkSplitBytesPerRow, s);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((S + kSegKeys - 1) / kSegKeys, static_cast<unsigned>(p.R));
+    topk_hist_kernel<<<grid, kSegThreads, 0, s>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_stream<1024>(p, s);
+  }
   // Short rows: keys in registers, one CTA per row, several rows per SM.
   if (S <= 4096) return launch_reg<128, 32, 1>(p, s);
   if (S <= 8192) return launch_reg<256, 32, 1>(p, s);
   if (S <= 16384) return launch_reg<512, 32, 1>(p, s);
-  // Very long rows (decode): a cluster of register-resident CTAs per row.
+  // Very long rows without split scratch: a cluster of register-resident CTAs per row.
   if (S > 65536 && S <= 131072) return launch_reg<1024, 32, 4>(p, s);
   if (S > 131072 && S <= kTopkRegMaxRow) return launch_reg<1024, 32, 8>(p, s);
   // Otherwise: 256-thread CTAs that stream the row (8 rows in flight per SM).
-  const size_t smem =
-      sizeof(uint32_t) * (static_cast<size_t>(kHistBins) + 2 * static_cast<size_t>(p.bitmap_words));
-  if (smem > 232448) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(topk_stream_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  topk_stream_kernel<<<p.R, kStreamThreads, smem, s>>>(p);
-  return cudaGetLastError();
+  return launch_stream<256>(p, s);
 }
 
 }  // namespace dsa
