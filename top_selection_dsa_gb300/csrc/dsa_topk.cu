@@ -407,6 +407,25 @@ __global__ void __launch_bounds__(THREADS, 65536 / (THREADS * 64)) topk_reg_kern
 
 // --------------------------------------------------------------- streaming
 
+// Visit src[0..n) with THREADS threads, element i = base + u*THREADS for
+// u < U: U independent read-only loads are issued before any is used, so
+// that each thread keeps U requests in flight.  fn(i, x) sees every element
+// once; lanes of a warp see consecutive elements for each u.
+template <int THREADS, int U, class Fn>
+__device__ __forceinline__ void stream_row(const float* __restrict__ src, int n, Fn&& fn) {
+  for (int base = static_cast<int>(threadIdx.x); base < n; base += THREADS * U) {
+    float x[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * THREADS;
+      x[u] = i < n ? __ldg(src + i) : -INFINITY;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) fn(base + u * THREADS, x[u]);
+  }
+}
+
+
 template <int kStreamThreads>
 __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const TopkParams p) {
   extern __shared__ uint32_t sm[];
@@ -418,7 +437,7 @@ __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const TopkP
   __shared__ uint32_t valid_count;
 
   const int row = blockIdx.x;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31;
   int lo, hi;
   row_range(p, row, &lo, &hi);
   const int n = hi - lo;
@@ -458,12 +477,20 @@ __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const TopkP
     };
     for (int i = tid; i < head; i += kStreamThreads) add(src[i]);
     const float4* src4 = reinterpret_cast<const float4*>(src + head);
-    for (int i = tid; i < body; i += kStreamThreads) {
-      const float4 v = __ldg(src4 + i);
-      add(v.x);
-      add(v.y);
-      add(v.z);
-      add(v.w);
+    for (int i0 = tid; i0 < body; i0 += 4 * kStreamThreads) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * kStreamThreads;
+        v[u] = i < body ? __ldg(src4 + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        add(v[u].x);
+        add(v[u].y);
+        add(v[u].z);
+        add(v[u].w);
+      }
     }
     for (int i = head + 4 * body + tid; i < n; i += kStreamThreads) add(src[i]);
 #pragma unroll
@@ -485,11 +512,11 @@ __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const TopkP
         const int pshift = d == 1 ? 21 : 10;
         for (int i = tid; i < nbins; i += kStreamThreads) hist[i] = 0u;
         __syncthreads();
-        for (int i = tid; i < n; i += kStreamThreads) {
-          const uint32_t kk = order_key(src[i]);
+        stream_row<kStreamThreads, 8>(src, n, [&](int, float x) {
+          const uint32_t kk = order_key(x);
           if ((kk >> pshift) == prefix)
             atomicAdd(&hist[(kk >> shift) & static_cast<uint32_t>(nbins - 1)], 1u);
-        }
+        });
         __syncthreads();
       }
       uint32_t b, above;
@@ -511,16 +538,16 @@ __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const TopkP
     for (int i = tid; i < n; i += kStreamThreads) dst[i] = lo + i;
   } else {
     const int nwords = (n + 31) >> 5;
-    for (int w = warp; w < nwords; w += kStreamThreads / 32) {
-      const int i = (w << 5) + lane;
-      const uint32_t kk = i < n ? order_key(src[i]) : 0u;
+    // Every warp-load covers one 32-column word (n rounded up to whole words).
+    stream_row<kStreamThreads, 8>(src, nwords << 5, [&](int i, float x) {
+      const uint32_t kk = i < n ? order_key(x) : 0u;
       const uint32_t g = __ballot_sync(0xffffffffu, kk > tau);
       const uint32_t e = __ballot_sync(0xffffffffu, need_eq > 0u && kk == tau);
       if (lane == 0) {
-        gt_bits[w] = g;
-        eq_bits[w] = e;
+        gt_bits[i >> 5] = g;
+        eq_bits[i >> 5] = e;
       }
-    }
+    });
     __syncthreads();
     const int per = (nwords + kStreamThreads - 1) / kStreamThreads;
     const int w0 = min(tid * per, nwords), w1 = min(w0 + per, nwords);
@@ -570,11 +597,10 @@ __global__ void __launch_bounds__(kSegThreads) topk_hist_kernel(const TopkParams
   for (int i = tid; i < kHistBins; i += kSegThreads) hist[i] = 0u;
   __syncthreads();
   const float* src = p.logits + static_cast<int64_t>(row) * p.ld + lo + s0;
-#pragma unroll 4
-  for (int i = tid; i < cnt; i += kSegThreads) {
-    const uint32_t kk = order_key(src[i]);
+  stream_row<kSegThreads, 16>(src, cnt, [&](int, float x) {
+    const uint32_t kk = order_key(x);
     if (kk != 0u) atomicAdd(&hist[kk >> 21], 1u);
-  }
+  });
   __syncthreads();
   uint32_t* g = p.hist0 + static_cast<int64_t>(row) * kHistBins;
   for (int i = tid; i < kHistBins; i += kSegThreads) {
