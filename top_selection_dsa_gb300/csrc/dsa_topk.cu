@@ -407,18 +407,22 @@ __global__ void __launch_bounds__(THREADS, 65536 / (THREADS * 64)) topk_reg_kern
 
 // --------------------------------------------------------------- streaming
 
-// Visit src[0..n) with THREADS threads, element i = base + u*THREADS for
+// Visit slots i in [0, n_iter) with THREADS threads, i = base + u*THREADS for
 // u < U: U independent read-only loads are issued before any is used, so
-// that each thread keeps U requests in flight.  fn(i, x) sees every element
-// once; lanes of a warp see consecutive elements for each u.
+// that each thread keeps U requests in flight.  Only src[0..n_load) is read;
+// x = -inf for every other slot.  fn(i, x) is called for every slot of a
+// batch, also for i >= n_iter, so that warp-collective code inside fn runs on
+// full warps; fn must not touch memory indexed by such an i.  Lanes of a warp
+// see consecutive i for each u.
 template <int THREADS, int U, class Fn>
-__device__ __forceinline__ void stream_row(const float* __restrict__ src, int n, Fn&& fn) {
-  for (int base = static_cast<int>(threadIdx.x); base < n; base += THREADS * U) {
+__device__ __forceinline__ void stream_row(const float* __restrict__ src, int n_iter, int n_load,
+                                           Fn&& fn) {
+  for (int base = static_cast<int>(threadIdx.x); base < n_iter; base += THREADS * U) {
     float x[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int i = base + u * THREADS;
-      x[u] = i < n ? __ldg(src + i) : -INFINITY;
+      x[u] = i < n_load ? __ldg(src + i) : -INFINITY;
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) fn(base + u * THREADS, x[u]);
@@ -512,7 +516,7 @@ __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const TopkP
         const int pshift = d == 1 ? 21 : 10;
         for (int i = tid; i < nbins; i += kStreamThreads) hist[i] = 0u;
         __syncthreads();
-        stream_row<kStreamThreads, 8>(src, n, [&](int, float x) {
+        stream_row<kStreamThreads, 8>(src, n, n, [&](int, float x) {
           const uint32_t kk = order_key(x);
           if ((kk >> pshift) == prefix)
             atomicAdd(&hist[(kk >> shift) & static_cast<uint32_t>(nbins - 1)], 1u);
@@ -539,11 +543,11 @@ __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const TopkP
   } else {
     const int nwords = (n + 31) >> 5;
     // Every warp-load covers one 32-column word (n rounded up to whole words).
-    stream_row<kStreamThreads, 8>(src, nwords << 5, [&](int i, float x) {
+    stream_row<kStreamThreads, 8>(src, nwords << 5, n, [&](int i, float x) {
       const uint32_t kk = i < n ? order_key(x) : 0u;
       const uint32_t g = __ballot_sync(0xffffffffu, kk > tau);
       const uint32_t e = __ballot_sync(0xffffffffu, need_eq > 0u && kk == tau);
-      if (lane == 0) {
+      if (lane == 0 && (i >> 5) < nwords) {
         gt_bits[i >> 5] = g;
         eq_bits[i >> 5] = e;
       }
@@ -597,7 +601,7 @@ __global__ void __launch_bounds__(kSegThreads) topk_hist_kernel(const TopkParams
   for (int i = tid; i < kHistBins; i += kSegThreads) hist[i] = 0u;
   __syncthreads();
   const float* src = p.logits + static_cast<int64_t>(row) * p.ld + lo + s0;
-  stream_row<kSegThreads, 16>(src, cnt, [&](int, float x) {
+  stream_row<kSegThreads, 16>(src, cnt, cnt, [&](int, float x) {
     const uint32_t kk = order_key(x);
     if (kk != 0u) atomicAdd(&hist[kk >> 21], 1u);
   });
