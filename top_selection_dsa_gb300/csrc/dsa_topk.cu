@@ -222,9 +222,9 @@ __global__ void __launch_bounds__(THREADS, 65536 / (THREADS * 64)) topk_reg_kern
   const float* src = p.logits + static_cast<int64_t>(row) * p.ld + lo + seg0;
   int32_t* dst = p.out + static_cast<int64_t>(row) * p.k;
 
+  // hist[1] is cleared at the end of pass 0, before its first use.
   for (int i = tid; i < kHistSlots; i += THREADS) {
     hist[0][i] = 0u;
-    hist[1][i] = 0u;
     if (CL > 1) merged[0][i] = 0u;
   }
   if (tid == 0) {
@@ -250,12 +250,15 @@ __global__ void __launch_bounds__(THREADS, 65536 / (THREADS * 64)) topk_reg_kern
   if constexpr (CL > 1) cluster_barrier(); else __syncthreads();
   if (lane == 0 && nv) atomicAdd(&valid_count, nv);
 
-  // Pass 0 histogram of the top 11 bits (invalid keys are left out).
+  // Pass 0 histogram of the top 11 bits (invalid keys are left out).  A row
+  // of at most k columns takes every valid key: only the count is needed.
+  if (n > p.k) {
 #pragma unroll
-  for (int u = 0; u < ITEMS; ++u) {
-    if (u * THREADS < mine_n) {
-      const uint32_t kk = key[u];
-      if (kk != 0u) atomicAdd(&hist[0][hpad(static_cast<int>(kk >> 21))], 1u);
+    for (int u = 0; u < ITEMS; ++u) {
+      if (u * THREADS < mine_n) {
+        const uint32_t kk = key[u];
+        if (kk != 0u) atomicAdd(&hist[0][hpad(static_cast<int>(kk >> 21))], 1u);
+      }
     }
   }
 
@@ -432,13 +435,19 @@ __device__ __forceinline__ void stream_row(const float* __restrict__ src, int n_
 
 template <int kStreamThreads>
 __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const TopkParams p) {
+  // Loads in flight per thread in the streaming passes.
+  constexpr int U = kStreamThreads >= 1024 ? 16 : 8;
+  // Keys of the threshold bin gathered after pass 0 (when they fit).
+  constexpr int kCand = kStreamThreads >= 1024 ? 8192 : 2048;
   extern __shared__ uint32_t sm[];
   uint32_t* hist = sm;                   // kHistBins
-  uint32_t* gt_bits = sm + kHistBins;    // ceil(S/32) words
+  uint32_t* cand = sm + kHistBins;       // kCand keys
+  uint32_t* gt_bits = cand + kCand;      // ceil(S/32) words
   uint32_t* eq_bits = gt_bits + p.bitmap_words;
   __shared__ uint2 warp_sums[kStreamThreads / 32];
   __shared__ uint32_t sel[4];
   __shared__ uint32_t valid_count;
+  __shared__ uint32_t ncand;
 
   const int row = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31;
@@ -472,10 +481,12 @@ __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const TopkP
     const uintptr_t addr = reinterpret_cast<uintptr_t>(src);
     const int head = min(static_cast<int>(((16u - (addr & 15u)) & 15u) >> 2), n);
     const int body = (n - head) >> 2;
+    // A row of at most k columns takes every valid key: only the count is needed.
+    const bool need_hist = n > p.k;
     auto add = [&](float x) {
       const uint32_t kk = order_key(x);
       if (kk != 0u) {
-        atomicAdd(&hist[kk >> 21], 1u);
+        if (need_hist) atomicAdd(&hist[kk >> 21], 1u);
         ++nv;
       }
     };
@@ -508,6 +519,7 @@ __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const TopkP
 
   uint32_t prefix = 0u, rem = static_cast<uint32_t>(p.k), tau = 0u, need_eq = 0u;
   if (nvalid > static_cast<uint32_t>(p.k)) {
+    bool gathered = false;  // the keys still in play sit in cand[0..ncand)
 #pragma unroll 1
     for (int d = 0; d < 3; ++d) {
       const int nbins = d == 2 ? 1024 : 2048;
@@ -516,11 +528,20 @@ __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const TopkP
         const int pshift = d == 1 ? 21 : 10;
         for (int i = tid; i < nbins; i += kStreamThreads) hist[i] = 0u;
         __syncthreads();
-        stream_row<kStreamThreads, 8>(src, n, n, [&](int, float x) {
-          const uint32_t kk = order_key(x);
-          if ((kk >> pshift) == prefix)
-            atomicAdd(&hist[(kk >> shift) & static_cast<uint32_t>(nbins - 1)], 1u);
-        });
+        if (gathered) {
+          const int nc = min(static_cast<int>(ncand), kCand);
+          for (int i = tid; i < nc; i += kStreamThreads) {
+            const uint32_t kk = cand[i];
+            if ((kk >> pshift) == prefix)
+              atomicAdd(&hist[(kk >> shift) & static_cast<uint32_t>(nbins - 1)], 1u);
+          }
+        } else {
+          stream_row<kStreamThreads, U>(src, n, n, [&](int, float x) {
+            const uint32_t kk = order_key(x);
+            if ((kk >> pshift) == prefix)
+              atomicAdd(&hist[(kk >> shift) & static_cast<uint32_t>(nbins - 1)], 1u);
+          });
+        }
         __syncthreads();
       }
       uint32_t b, above;
@@ -535,6 +556,27 @@ __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const TopkP
         need_eq = d == 2 ? rem : 0u;
         break;
       }
+      if (d == 0 && cnt <= static_cast<uint32_t>(kCand)) {
+        // One pass gathers the keys of the threshold bin; the later passes
+        // read them from shared memory instead of the row.
+        if (tid == 0) ncand = 0u;
+        __syncthreads();
+        // Warp-collective body: iterate over whole warps (loads stay < n).
+        stream_row<kStreamThreads, U>(src, (n + 31) & ~31, n, [&](int, float x) {
+          const uint32_t kk = order_key(x);
+          const bool hit = (kk >> 21) == prefix;
+          const uint32_t m = __ballot_sync(0xffffffffu, hit);
+          if (m) {
+            uint32_t slot = 0u;
+            if (lane == 0) slot = atomicAdd(&ncand, static_cast<uint32_t>(__popc(m)));
+            slot = __shfl_sync(0xffffffffu, slot, 0);
+            const uint32_t idx = slot + __popc(m & ((1u << lane) - 1u));
+            if (hit && idx < static_cast<uint32_t>(kCand)) cand[idx] = kk;
+          }
+        });
+        __syncthreads();
+        gathered = true;
+      }
     }
   }
 
@@ -543,7 +585,7 @@ __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const TopkP
   } else {
     const int nwords = (n + 31) >> 5;
     // Every warp-load covers one 32-column word (n rounded up to whole words).
-    stream_row<kStreamThreads, 8>(src, nwords << 5, n, [&](int i, float x) {
+    stream_row<kStreamThreads, U>(src, nwords << 5, n, [&](int i, float x) {
       const uint32_t kk = i < n ? order_key(x) : 0u;
       const uint32_t g = __ballot_sync(0xffffffffu, kk > tau);
       const uint32_t e = __ballot_sync(0xffffffffu, need_eq > 0u && kk == tau);
@@ -641,8 +683,8 @@ cudaError_t launch_reg(const TopkParams& p, cudaStream_t s) {
 int topk_bitmap_words(int max_row) { return (max_row + 31) / 32; }
 
 bool topk_supported(int max_row) {
-  const size_t stream_smem = sizeof(uint32_t) *
-      (static_cast<size_t>(kHistBins) + 2 * static_cast<size_t>(topk_bitmap_words(max_row)));
+  const size_t stream_smem = sizeof(uint32_t) * (static_cast<size_t>(kHistBins) + 8192 +
+                                                 2 * static_cast<size_t>(topk_bitmap_words(max_row)));
   return max_row >= 0 && stream_smem <= 232448;
 }
 
@@ -655,8 +697,9 @@ bool topk_split_rows(int64_t rows, int64_t max_row) {
 
 template <int THREADS>
 cudaError_t launch_stream(const TopkParams& p, cudaStream_t s) {
-  const size_t smem =
-      sizeof(uint32_t) * (static_cast<size_t>(kHistBins) + 2 * static_cast<size_t>(p.bitmap_words));
+  const size_t cand = THREADS >= 1024 ? 8192 : 2048;
+  const size_t smem = sizeof(uint32_t) * (static_cast<size_t>(kHistBins) + cand +
+                                          2 * static_cast<size_t>(p.bitmap_words));
   if (smem > 232448) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(topk_stream_kernel<THREADS>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
