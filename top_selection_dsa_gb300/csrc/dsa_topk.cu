@@ -434,9 +434,10 @@ __device__ __forceinline__ void stream_row(const float* __restrict__ src, int n_
 
 
 template <int kStreamThreads>
-__global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const TopkParams p) {
+__global__ void __launch_bounds__(kStreamThreads, kStreamThreads >= 1024 ? 1 : 8)
+    topk_stream_kernel(const TopkParams p) {
   // Loads in flight per thread in the streaming passes.
-  constexpr int U = kStreamThreads >= 1024 ? 16 : 8;
+  constexpr int U = kStreamThreads >= 1024 ? 16 : 4;
   // Keys of the threshold bin gathered after pass 0 (when they fit).
   constexpr int kCand = kStreamThreads >= 1024 ? 8192 : 2048;
   extern __shared__ uint32_t sm[];
