@@ -122,6 +122,11 @@ size_t logits_scratch_bytes(int64_t rows, int64_t cols) {
       rows * round_up(cols > 0 ? cols : 1, 4) * static_cast<int64_t>(sizeof(float)), 256));
 }
 
+size_t split_scratch_bytes(int64_t rows, int64_t cols) {
+  return static_cast<size_t>(rows) * static_cast<size_t>(topk_split_words(cols)) *
+         sizeof(uint32_t);
+}
+
 uint32_t* split_scratch(void* workspace, int64_t rows, int64_t cols) {
   if (!topk_split_rows(rows, cols)) return nullptr;
   return reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) +
@@ -183,7 +188,7 @@ dsa_status_t run_logits(const void* q, const float* q_scale, const void* k, cons
 
 dsa_status_t run_topk(const float* logits, int64_t ld, const int32_t* row_starts,
                       const int32_t* row_ends, const int32_t* context_lens, int next_n, int R,
-                      int S, int k, int32_t* out, cudaStream_t st, uint32_t* hist0 = nullptr) {
+                      int S, int k, int32_t* out, cudaStream_t st, uint32_t* split = nullptr) {
   if (R == 0) return DSA_OK;
   TopkParams p = {};
   p.logits = logits;
@@ -197,7 +202,8 @@ dsa_status_t run_topk(const float* logits, int64_t ld, const int32_t* row_starts
   p.k = k;
   p.bitmap_words = topk_bitmap_words(S);
   p.out = out;
-  p.hist0 = hist0;
+  p.split = split;
+  p.split_words = split ? topk_split_words(S) : 0;
   return from_cuda(launch_topk(p, st));
 }
 
@@ -416,12 +422,12 @@ size_t dsa_workspace_bytes(dsa_op_t op, int64_t rows, int64_t cols, int k) {
     case DSA_OP_INDEXER_LOGITS_PAGED:
       return 0;
     case DSA_OP_TOPK:
-      return topk_split_rows(rows, cols) ? static_cast<size_t>(rows) * kTopkSplitBytesPerRow : 0;
+      return topk_split_rows(rows, cols) ? split_scratch_bytes(rows, cols) : 0;
     case DSA_OP_INDEXER_TOPK:
     case DSA_OP_INDEXER_TOPK_PAGED:
       if (rows == 0) return 0;
       return logits_scratch_bytes(rows, cols) +
-             (topk_split_rows(rows, cols) ? static_cast<size_t>(rows) * kTopkSplitBytesPerRow : 0);
+             (topk_split_rows(rows, cols) ? split_scratch_bytes(rows, cols) : 0);
     default:
       return static_cast<size_t>(-1);
   }

@@ -49,7 +49,8 @@ struct TopkParams {
   int k;
   int bitmap_words;  // ceil(S / 32): shared-memory selection bitmaps per row
   int32_t* out;      // [R, k]
-  uint32_t* hist0;   // null, or [R, 2048] scratch for the split path (see topk_split_rows)
+  uint32_t* split;   // null, or [R, split_words] scratch of the split path (topk_split_rows)
+  int split_words;   // words of split scratch per row (topk_split_words(S))
 };
 
 // Launchers (return the launch error, if any).  Shapes were validated by the
@@ -69,11 +70,13 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t s);
 int topk_bitmap_words(int max_row);
 // Whether rows of up to max_row columns fit the top-k kernels.
 bool topk_supported(int max_row);
-// Few long rows take the split path: many CTAs per row build the first-digit
-// histograms in global scratch (R * 2048 words), then one CTA per row selects.
-// Depends on the shape only, so the workspace size is known on the host.
+// Few long rows take the split path: every phase runs on many CTAs per row
+// (one per 4096-key segment), exchanging per-row histograms, candidate keys,
+// the threshold and per-segment counts through global scratch of
+// topk_split_words(max_row) words per row.  Depends on the shape only, so the
+// workspace size is known on the host.
 bool topk_split_rows(int64_t rows, int64_t max_row);
-constexpr size_t kTopkSplitBytesPerRow = 2048 * sizeof(uint32_t);
+int topk_split_words(int64_t max_row);
 cudaError_t launch_fill(float* dst, int64_t rows, int64_t cols, int64_t ld, float value,
                         cudaStream_t s);
 cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint64_t timeout_ns, cudaStream_t s);

@@ -458,22 +458,8 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamThreads >= 1024 ? 1 : 8
   const float* src = p.logits + static_cast<int64_t>(row) * p.ld + lo;
   int32_t* dst = p.out + static_cast<int64_t>(row) * p.k;
 
-  // Pass 0: histogram of the top 11 key bits, 16-byte loads from memory (or,
-  // on the split path, the histogram the segment CTAs already built).
-  if (p.hist0) {
-    const uint32_t* h0 = p.hist0 + static_cast<int64_t>(row) * kHistBins;
-    uint32_t nv = 0;
-    for (int i = tid; i < kHistBins; i += kStreamThreads) {
-      const uint32_t v = h0[i];
-      hist[i] = v;
-      nv += v;
-    }
-    if (tid == 0) valid_count = 0u;
-    __syncthreads();
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) nv += __shfl_xor_sync(0xffffffffu, nv, o);
-    if (lane == 0 && nv) atomicAdd(&valid_count, nv);
-  } else {
+  // Pass 0: histogram of the top 11 key bits, 16-byte loads from memory.
+  {
   for (int i = tid; i < kHistBins; i += kStreamThreads) hist[i] = 0u;
   if (tid == 0) valid_count = 0u;
   __syncthreads();
@@ -626,11 +612,45 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamThreads >= 1024 ? 1 : 8
   for (int i = nsel + tid; i < p.k; i += kStreamThreads) dst[i] = -1;
 }
 
-// Split path, step 1: CTA (segment, row) histograms the top 11 key bits of
-// keys [seg*4096, seg*4096 + 4096) of the row's range into the row's global
-// histogram (valid keys only).
+// ----------------------------------------------------------- split path
+//
+// Few long rows (decode): every phase runs on a grid of (4096-key segment,
+// row) CTAs, or one CTA per row for the small refine step, and the phases
+// talk through per-row scratch:
+//   hist[2048]      first-digit (top 11 bits) histogram of the row's valid keys
+//   state[8]        mode, tau, need_eq, nvalid, ncand
+//   cand[kSplitCand] keys of the threshold bin
+//   segcnt[2*segs]  per-segment (key > tau, key == tau) counts
+// Steps: hist -> gather (each CTA finds the threshold bin from the row
+// histogram and appends its keys in that bin) -> refine (one CTA per row:
+// exact tau / need_eq from the gathered keys, or from streaming passes when
+// the bin is too large) -> count -> write (each segment places its selected
+// columns after those of the earlier segments, in column order).
 constexpr int kSegKeys = 4096;
 constexpr int kSegThreads = 256;
+constexpr int kSegItems = kSegKeys / kSegThreads;  // 16
+constexpr int kSplitCand = 4096;
+constexpr int kStHist = 0, kStState = kHistBins, kStCand = kHistBins + 8,
+              kStSeg = kHistBins + 8 + kSplitCand;
+enum : uint32_t { kModeSelect = 1u, kModeIota = 2u };
+
+__device__ __forceinline__ uint32_t* split_row(const TopkParams& p, int row) {
+  return p.split + static_cast<int64_t>(row) * p.split_words;
+}
+
+// The row's first-digit histogram into shared memory; returns nvalid and,
+// when nvalid > k, the threshold bin b1, the count above it and its size.
+template <int THREADS>
+__device__ __forceinline__ uint32_t split_decide(const uint32_t* g, int k, uint32_t* hist,
+                                                 uint2* warp_sums, uint32_t* sel, uint32_t* b1,
+                                                 uint32_t* above, uint32_t* cnt) {
+  for (int i = threadIdx.x; i < kHistBins; i += THREADS) hist[i] = g[i];
+  __syncthreads();
+  const uint32_t nvalid = find_bin<THREADS>(hist, kHistBins, static_cast<uint32_t>(k), warp_sums,
+                                            sel, b1, above);
+  *cnt = nvalid > static_cast<uint32_t>(k) ? hist[*b1] : 0u;
+  return nvalid;
+}
 
 __global__ void __launch_bounds__(kSegThreads) topk_hist_kernel(const TopkParams p) {
   __shared__ uint32_t hist[kHistBins];
@@ -644,15 +664,234 @@ __global__ void __launch_bounds__(kSegThreads) topk_hist_kernel(const TopkParams
   for (int i = tid; i < kHistBins; i += kSegThreads) hist[i] = 0u;
   __syncthreads();
   const float* src = p.logits + static_cast<int64_t>(row) * p.ld + lo + s0;
-  stream_row<kSegThreads, 16>(src, cnt, cnt, [&](int, float x) {
+  stream_row<kSegThreads, kSegItems>(src, cnt, cnt, [&](int, float x) {
     const uint32_t kk = order_key(x);
     if (kk != 0u) atomicAdd(&hist[kk >> 21], 1u);
   });
   __syncthreads();
-  uint32_t* g = p.hist0 + static_cast<int64_t>(row) * kHistBins;
+  uint32_t* g = split_row(p, row) + kStHist;
   for (int i = tid; i < kHistBins; i += kSegThreads) {
     const uint32_t v = hist[i];
     if (v) atomicAdd(&g[i], v);
+  }
+}
+
+__global__ void __launch_bounds__(kSegThreads) topk_gather_kernel(const TopkParams p) {
+  __shared__ uint32_t hist[kHistBins];
+  __shared__ uint2 warp_sums[kSegThreads / 32];
+  __shared__ uint32_t sel[2];
+  const int row = blockIdx.y;
+  const int lane = threadIdx.x & 31;
+  int lo, hi;
+  row_range(p, row, &lo, &hi);
+  const int s0 = static_cast<int>(blockIdx.x) * kSegKeys;
+  const int cnt = min(hi - lo - s0, kSegKeys);
+  if (cnt <= 0) return;
+  uint32_t* w = split_row(p, row);
+  uint32_t b1, above, bcnt;
+  const uint32_t nvalid =
+      split_decide<kSegThreads>(w + kStHist, p.k, hist, warp_sums, sel, &b1, &above, &bcnt);
+  if (nvalid <= static_cast<uint32_t>(p.k)) return;                 // take every valid key
+  if (static_cast<uint32_t>(p.k) - above == bcnt) return;           // the whole bin is taken
+  if (bcnt > static_cast<uint32_t>(kSplitCand)) return;             // refine streams instead
+  const float* src = p.logits + static_cast<int64_t>(row) * p.ld + lo + s0;
+  uint32_t* ncand = w + kStState + 4;
+  uint32_t* cand = w + kStCand;
+  // Warp-collective body: iterate over whole warps (loads stay < cnt).
+  stream_row<kSegThreads, kSegItems>(src, (cnt + 31) & ~31, cnt, [&](int, float x) {
+    const uint32_t kk = order_key(x);
+    const bool hit = (kk >> 21) == b1;
+    const uint32_t m = __ballot_sync(0xffffffffu, hit);
+    if (m) {
+      uint32_t slot = 0u;
+      if (lane == 0) slot = atomicAdd(ncand, static_cast<uint32_t>(__popc(m)));
+      slot = __shfl_sync(0xffffffffu, slot, 0);
+      const uint32_t idx = slot + __popc(m & ((1u << lane) - 1u));
+      if (hit && idx < static_cast<uint32_t>(kSplitCand)) cand[idx] = kk;
+    }
+  });
+}
+
+constexpr int kRefineThreads = 1024;
+
+__global__ void __launch_bounds__(kRefineThreads) topk_refine_kernel(const TopkParams p) {
+  __shared__ uint32_t hist[kHistBins];
+  __shared__ uint32_t cand[kSplitCand];
+  __shared__ uint2 warp_sums[kRefineThreads / 32];
+  __shared__ uint32_t sel[2];
+  const int row = blockIdx.x;
+  const int tid = threadIdx.x;
+  int lo, hi;
+  row_range(p, row, &lo, &hi);
+  const int n = hi - lo;
+  uint32_t* w = split_row(p, row);
+  uint32_t b1, above, bcnt;
+  const uint32_t nvalid =
+      split_decide<kRefineThreads>(w + kStHist, p.k, hist, warp_sums, sel, &b1, &above, &bcnt);
+  uint32_t tau = 0u, need_eq = 0u;
+  if (nvalid > static_cast<uint32_t>(p.k)) {
+    uint32_t rem = static_cast<uint32_t>(p.k) - above;
+    uint32_t prefix = b1;
+    if (rem == bcnt) {
+      tau = (prefix << 21) - 1u;
+    } else {
+      const bool gathered = bcnt <= static_cast<uint32_t>(kSplitCand);
+      const int nc = gathered ? min(static_cast<int>(w[kStState + 4]), kSplitCand) : 0;
+      for (int i = tid; i < nc; i += kRefineThreads) cand[i] = w[kStCand + i];
+      const float* src = p.logits + static_cast<int64_t>(row) * p.ld + lo;
+#pragma unroll 1
+      for (int d = 1; d < 3; ++d) {
+        const int nbins = d == 2 ? 1024 : 2048;
+        const int shift = d == 1 ? 10 : 0;
+        const int pshift = d == 1 ? 21 : 10;
+        __syncthreads();
+        for (int i = tid; i < nbins; i += kRefineThreads) hist[i] = 0u;
+        __syncthreads();
+        if (gathered) {
+          for (int i = tid; i < nc; i += kRefineThreads) {
+            const uint32_t kk = cand[i];
+            if ((kk >> pshift) == prefix)
+              atomicAdd(&hist[(kk >> shift) & static_cast<uint32_t>(nbins - 1)], 1u);
+          }
+        } else {
+          stream_row<kRefineThreads, 16>(src, n, n, [&](int, float x) {
+            const uint32_t kk = order_key(x);
+            if ((kk >> pshift) == prefix)
+              atomicAdd(&hist[(kk >> shift) & static_cast<uint32_t>(nbins - 1)], 1u);
+          });
+        }
+        __syncthreads();
+        uint32_t b, ab;
+        find_bin<kRefineThreads>(hist, nbins, rem, warp_sums, sel, &b, &ab);
+        const uint32_t c = hist[b];
+        rem -= ab;
+        prefix = (prefix << (d == 1 ? 11 : 10)) | b;
+        if (rem == c || d == 2) {
+          tau = d == 2 ? prefix : (prefix << 10) - 1u;
+          need_eq = d == 2 ? rem : 0u;
+          break;
+        }
+      }
+    }
+  }
+  if (tid == 0) {
+    w[kStState + 0] = (nvalid <= static_cast<uint32_t>(p.k) && nvalid == static_cast<uint32_t>(n))
+                          ? kModeIota
+                          : kModeSelect;
+    w[kStState + 1] = tau;
+    w[kStState + 2] = need_eq;
+    w[kStState + 3] = nvalid;
+  }
+}
+
+__global__ void __launch_bounds__(kSegThreads) topk_count_kernel(const TopkParams p) {
+  __shared__ uint2 warp_sums[kSegThreads / 32];
+  const int row = blockIdx.y;
+  const int tid = threadIdx.x;
+  int lo, hi;
+  row_range(p, row, &lo, &hi);
+  const int s0 = static_cast<int>(blockIdx.x) * kSegKeys;
+  const int cnt = min(hi - lo - s0, kSegKeys);
+  if (cnt <= 0) return;
+  uint32_t* w = split_row(p, row);
+  if (w[kStState + 0] == kModeIota) return;
+  const uint32_t tau = w[kStState + 1], need_eq = w[kStState + 2];
+  const float* src = p.logits + static_cast<int64_t>(row) * p.ld + lo + s0;
+  uint2 c = make_uint2(0u, 0u);
+  stream_row<kSegThreads, kSegItems>(src, cnt, cnt, [&](int, float x) {
+    const uint32_t kk = order_key(x);
+    c.x += kk > tau ? 1u : 0u;
+    c.y += (need_eq > 0u && kk == tau) ? 1u : 0u;
+  });
+  uint2 total;
+  block_scan2<kSegThreads>(c, warp_sums, &total);
+  if (tid == 0) {
+    w[kStSeg + 2 * blockIdx.x] = total.x;
+    w[kStSeg + 2 * blockIdx.x + 1] = total.y;
+  }
+}
+
+__global__ void __launch_bounds__(kSegThreads) topk_write_kernel(const TopkParams p) {
+  constexpr int NW = kSegThreads / 32;
+  constexpr int WORDS = kSegKeys / 32;
+  __shared__ uint32_t gt_bits[WORDS];
+  __shared__ uint32_t eq_bits[WORDS];
+  __shared__ uint2 warp_sums[NW];
+  __shared__ uint2 seg_base;
+  const int row = blockIdx.y;
+  const int seg = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int lo, hi;
+  row_range(p, row, &lo, &hi);
+  const uint32_t* w = split_row(p, row);
+  const uint32_t mode = w[kStState + 0];
+  const uint32_t tau = w[kStState + 1], need_eq = w[kStState + 2], nvalid = w[kStState + 3];
+  int32_t* dst = p.out + static_cast<int64_t>(row) * p.k;
+  if (seg == 0) {
+    const int nsel = nvalid < static_cast<uint32_t>(p.k) ? static_cast<int>(nvalid) : p.k;
+    for (int i = nsel + tid; i < p.k; i += kSegThreads) dst[i] = -1;
+  }
+  const int s0 = seg * kSegKeys;
+  const int cnt = min(hi - lo - s0, kSegKeys);
+  if (cnt <= 0) return;
+  if (mode == kModeIota) {
+    for (int i = tid; i < cnt; i += kSegThreads) dst[s0 + i] = lo + s0 + i;
+    return;
+  }
+  if (warp == 0) {
+    // Selected columns of the earlier segments come first.
+    uint2 acc = make_uint2(0u, 0u);
+    for (int i = lane; i < seg; i += 32) {
+      acc.x += w[kStSeg + 2 * i];
+      acc.y += w[kStSeg + 2 * i + 1];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      acc.x += __shfl_xor_sync(0xffffffffu, acc.x, o);
+      acc.y += __shfl_xor_sync(0xffffffffu, acc.y, o);
+    }
+    if (lane == 0) seg_base = acc;
+  }
+  const float* src = p.logits + static_cast<int64_t>(row) * p.ld + lo + s0;
+  uint32_t key[kSegItems];
+#pragma unroll
+  for (int u = 0; u < kSegItems; ++u) {
+    const int e = u * kSegThreads + tid;
+    key[u] = e < cnt ? order_key(__ldg(src + e)) : 0u;
+  }
+  // Word u*NW + warp holds segment columns (u*NW + warp)*32 + lane.
+#pragma unroll
+  for (int u = 0; u < kSegItems; ++u) {
+    const uint32_t g = __ballot_sync(0xffffffffu, key[u] > tau);
+    const uint32_t e = __ballot_sync(0xffffffffu, need_eq > 0u && key[u] == tau);
+    if (lane == 0) {
+      gt_bits[u * NW + warp] = g;
+      eq_bits[u * NW + warp] = e;
+    }
+  }
+  __syncthreads();
+  uint2 mine = make_uint2(0u, 0u);
+  if (tid < WORDS) mine = make_uint2(__popc(gt_bits[tid]), __popc(eq_bits[tid]));
+  uint2 total;
+  const uint2 before = block_scan2<kSegThreads>(mine, warp_sums, &total);
+  if (tid < WORDS) {
+    gt_bits[tid] = seg_base.x + before.x;  // word prefixes replace the words
+    eq_bits[tid] = seg_base.y + before.y;
+  }
+  __syncthreads();
+  const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+  for (int u = 0; u < kSegItems; ++u) {
+    const int wd = u * NW + warp;
+    const bool g = key[u] > tau;
+    const bool e = need_eq > 0u && key[u] == tau;
+    const uint32_t gm = __ballot_sync(0xffffffffu, g);
+    const uint32_t em = __ballot_sync(0xffffffffu, e);
+    const uint32_t gb = gt_bits[wd] + __popc(gm & lt);
+    const uint32_t eb = eq_bits[wd] + __popc(em & lt);
+    const int col = lo + s0 + u * kSegThreads + tid;
+    if (g) dst[gb + min(eb, need_eq)] = col;
+    else if (e && eb < need_eq) dst[gb + eb] = col;
   }
 }
 
@@ -696,6 +935,12 @@ bool topk_split_rows(int64_t rows, int64_t max_row) {
   return max_row > 16384 && rows <= 512;
 }
 
+int topk_split_words(int64_t max_row) {
+  const int64_t segs = (max_row + kSegKeys - 1) / kSegKeys;
+  const int64_t words = kStSeg + 2 * segs;
+  return static_cast<int>((words + 63) / 64 * 64);  // rows stay 256-byte aligned
+}
+
 template <int THREADS>
 cudaError_t launch_stream(const TopkParams& p, cudaStream_t s) {
   const size_t cand = THREADS >= 1024 ? 8192 : 2048;
@@ -713,15 +958,18 @@ cudaError_t launch_stream(const TopkParams& p, cudaStream_t s) {
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t s) {
   if (p.R <= 0) return cudaSuccess;
   const int S = p.S;
-  if (p.hist0) {
-    // Few long rows: histograms from many CTAs per row, then one CTA per row.
-    cudaError_t e = cudaMemsetAsync(p.hist0, 0, static_cast<size_t>(p.R) * kTopkSplitBytesPerRow, s);
+  if (p.split) {
+    // Few long rows: every phase on (segment, row) grids, see the split path.
+    cudaError_t e = cudaMemsetAsync(
+        p.split, 0, static_cast<size_t>(p.R) * p.split_words * sizeof(uint32_t), s);
     if (e != cudaSuccess) return e;
     const dim3 grid((S + kSegKeys - 1) / kSegKeys, static_cast<unsigned>(p.R));
     topk_hist_kernel<<<grid, kSegThreads, 0, s>>>(p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    return launch_stream<1024>(p, s);
+    topk_gather_kernel<<<grid, kSegThreads, 0, s>>>(p);
+    topk_refine_kernel<<<p.R, kRefineThreads, 0, s>>>(p);
+    topk_count_kernel<<<grid, kSegThreads, 0, s>>>(p);
+    topk_write_kernel<<<grid, kSegThreads, 0, s>>>(p);
+    return cudaGetLastError();
   }
   // Short rows: keys in registers, one CTA per row, several rows per SM.
   if (S <= 4096) return launch_reg<128, 32, 1>(p, s);
