@@ -54,12 +54,17 @@ def test_workspace_bytes(api):
     assert wb(api.DSA_OP_TOPK, 10, 10, 4) == 0
     assert wb(api.DSA_OP_INDEXER_TOPK, 4096, 4096, 2048) == 4096 * 4096 * 4
     assert wb(api.DSA_OP_INDEXER_TOPK, 3, 5, 1) == 256        # rows padded to 16 B, total to 256
-    # few long rows: per-row first-digit histograms (2048 words) follow the logits
-    assert wb(api.DSA_OP_TOPK, 128, 131072, 2048) == 128 * 2048 * 4
+    # few long rows: per-row scratch of the split top-k (2048-bin histogram,
+    # 8 state words, 4096 candidate keys, 2 counts per 4096-key segment),
+    # rounded up to 64 words; it follows the logits in the composed calls
+    def split(rows, S):
+        words = 2048 + 8 + 4096 + 2 * (-(-S // 4096))
+        return rows * (-(-words // 64) * 64) * 4
+    assert wb(api.DSA_OP_TOPK, 128, 131072, 2048) == split(128, 131072)
     assert wb(api.DSA_OP_TOPK, 4096, 131072, 2048) == 0       # many rows: no scratch
     assert wb(api.DSA_OP_TOPK, 128, 16384, 2048) == 0         # short rows: no scratch
     assert wb(api.DSA_OP_INDEXER_TOPK_PAGED, 128, 131072, 2048) == \
-        128 * 131072 * 4 + 128 * 2048 * 4
+        128 * 131072 * 4 + split(128, 131072)
     assert wb(api.DSA_OP_INDEXER_TOPK, 0, 100, 1) == 0
     bad = ctypes.c_size_t(-1).value
     assert wb(api.DSA_OP_INDEXER_TOPK, -1, 5, 1) == bad
