@@ -619,7 +619,7 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamThreads >= 1024 ? 1 : 8
 // talk through per-row scratch:
 //   hist[2048]      first-digit (top 11 bits) histogram of the row's valid keys
 //   state[8]        mode, tau, need_eq, nvalid, ncand
-//   cand[kSplitCand] keys of the threshold bin
+//   cand[kSplitCand] keys of the threshold bin (16384)
 //   segcnt[2*segs]  per-segment (key > tau, key == tau) counts
 // Steps: hist -> gather (each CTA finds the threshold bin from the row
 // histogram and appends its keys in that bin) -> refine (one CTA per row:
@@ -629,7 +629,7 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamThreads >= 1024 ? 1 : 8
 constexpr int kSegKeys = 4096;
 constexpr int kSegThreads = 256;
 constexpr int kSegItems = kSegKeys / kSegThreads;  // 16
-constexpr int kSplitCand = 4096;
+constexpr int kSplitCand = 16384;
 constexpr int kStHist = 0, kStState = kHistBins, kStCand = kHistBins + 8,
               kStSeg = kHistBins + 8 + kSplitCand;
 enum : uint32_t { kModeSelect = 1u, kModeIota = 2u };
@@ -716,7 +716,7 @@ constexpr int kRefineThreads = 1024;
 
 __global__ void __launch_bounds__(kRefineThreads) topk_refine_kernel(const TopkParams p) {
   __shared__ uint32_t hist[kHistBins];
-  __shared__ uint32_t cand[kSplitCand];
+  extern __shared__ uint32_t cand[];  // kSplitCand keys (dynamic shared memory)
   __shared__ uint2 warp_sums[kRefineThreads / 32];
   __shared__ uint32_t sel[2];
   const int row = blockIdx.x;
@@ -966,7 +966,11 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t s) {
     const dim3 grid((S + kSegKeys - 1) / kSegKeys, static_cast<unsigned>(p.R));
     topk_hist_kernel<<<grid, kSegThreads, 0, s>>>(p);
     topk_gather_kernel<<<grid, kSegThreads, 0, s>>>(p);
-    topk_refine_kernel<<<p.R, kRefineThreads, 0, s>>>(p);
+    const int refine_smem = kSplitCand * static_cast<int>(sizeof(uint32_t));
+    e = cudaFuncSetAttribute(topk_refine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             refine_smem);
+    if (e != cudaSuccess) return e;
+    topk_refine_kernel<<<p.R, kRefineThreads, refine_smem, s>>>(p);
     topk_count_kernel<<<grid, kSegThreads, 0, s>>>(p);
     topk_write_kernel<<<grid, kSegThreads, 0, s>>>(p);
     return cudaGetLastError();
