@@ -55,10 +55,10 @@ def test_workspace_bytes(api):
     assert wb(api.DSA_OP_INDEXER_TOPK, 4096, 4096, 2048) == 4096 * 4096 * 4
     assert wb(api.DSA_OP_INDEXER_TOPK, 3, 5, 1) == 256        # rows padded to 16 B, total to 256
     # few long rows: per-row scratch of the split top-k (2048-bin histogram,
-    # 8 state words, 16384 candidate keys, 2 counts per 4096-key segment),
+    # 16 state words, 16384 candidate keys, 2 counts per 16384-key segment),
     # rounded up to 64 words; it follows the logits in the composed calls
     def split(rows, S):
-        words = 2048 + 8 + 16384 + 2 * (-(-S // 4096))
+        words = 2048 + 16 + 16384 + 2 * (-(-S // 16384))
         return rows * (-(-words // 64) * 64) * 4
     assert wb(api.DSA_OP_TOPK, 128, 131072, 2048) == split(128, 131072)
     assert wb(api.DSA_OP_TOPK, 4096, 131072, 2048) == 0       # many rows: no scratch

@@ -614,53 +614,72 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamThreads >= 1024 ? 1 : 8
 
 // ----------------------------------------------------------- split path
 //
-// Few long rows (decode): every phase runs on a grid of (4096-key segment,
-// row) CTAs, or one CTA per row for the small refine step, and the phases
-// talk through per-row scratch:
-//   hist[2048]      first-digit (top 11 bits) histogram of the row's valid keys
-//   state[8]        mode, tau, need_eq, nvalid, ncand
-//   cand[kSplitCand] keys of the threshold bin (16384)
-//   segcnt[2*segs]  per-segment (key > tau, key == tau) counts
-// Steps: hist -> gather (each CTA finds the threshold bin from the row
-// histogram and appends its keys in that bin) -> refine (one CTA per row:
-// exact tau / need_eq from the gathered keys, or from streaming passes when
-// the bin is too large) -> count -> write (each segment places its selected
-// columns after those of the earlier segments, in column order).
-constexpr int kSegKeys = 4096;
-constexpr int kSegThreads = 256;
+// Few long rows (decode): every phase runs on a grid of (16384-key segment,
+// row) CTAs, and the phases talk through per-row scratch:
+//   hist[2048]        first-digit (top 11 bits) histogram of the row's valid keys
+//   state[16]         mode, tau, need_eq, nvalid, b1, rem, done counters, ncand
+//   cand[kSplitCand]  keys of the threshold bin
+//   segcnt[2*segs]    per-segment (key > tau, key == tau) counts
+// Steps (one launch each, after zeroing the scratch):
+//   hist    segments add their histograms; the last segment CTA of a row to
+//           finish (a completion counter after a fence; nobody waits) finds
+//           the threshold bin and the row's mode;
+//   gather  segments append the keys of the threshold bin; the last one of a
+//           row refines them to the exact tau / need_eq (or, when the bin
+//           holds more than kSplitCand keys, streams the row);
+//   count   per-segment counts of keys > tau and == tau;
+//   write   each segment places its selected columns after those of the
+//           earlier segments, in column order; segment 0 writes the -1 tail.
+constexpr int kSegKeys = 16384;
+constexpr int kSegThreads = 1024;
 constexpr int kSegItems = kSegKeys / kSegThreads;  // 16
 constexpr int kSplitCand = 16384;
-constexpr int kStHist = 0, kStState = kHistBins, kStCand = kHistBins + 8,
-              kStSeg = kHistBins + 8 + kSplitCand;
-enum : uint32_t { kModeSelect = 1u, kModeIota = 2u };
+constexpr int kStateWords = 16;
+constexpr int kStHist = 0, kStState = kHistBins, kStCand = kHistBins + kStateWords,
+              kStSeg = kHistBins + kStateWords + kSplitCand;
+// state words
+constexpr int kSMode = 0, kSTau = 1, kSNeed = 2, kSValid = 3, kSB1 = 4, kSRem = 5,
+              kSDoneHist = 6, kSDoneGather = 7, kSNcand = 8;
+enum : uint32_t { kModeSelect = 1u, kModeIota = 2u, kModeGather = 3u, kModeStream = 4u };
 
 __device__ __forceinline__ uint32_t* split_row(const TopkParams& p, int row) {
   return p.split + static_cast<int64_t>(row) * p.split_words;
 }
 
-// The row's first-digit histogram into shared memory; returns nvalid and,
-// when nvalid > k, the threshold bin b1, the count above it and its size.
-template <int THREADS>
-__device__ __forceinline__ uint32_t split_decide(const uint32_t* g, int k, uint32_t* hist,
-                                                 uint2* warp_sums, uint32_t* sel, uint32_t* b1,
-                                                 uint32_t* above, uint32_t* cnt) {
-  for (int i = threadIdx.x; i < kHistBins; i += THREADS) hist[i] = g[i];
+// True in every thread of the CTA that is the last of `total` CTAs to pass
+// here for this counter: each CTA fences its earlier global writes, then
+// counts itself in.  No CTA ever waits for another.
+__device__ __forceinline__ bool last_to_arrive(uint32_t* counter, uint32_t total,
+                                               uint32_t* flag_smem) {
+  __threadfence();
   __syncthreads();
-  const uint32_t nvalid = find_bin<THREADS>(hist, kHistBins, static_cast<uint32_t>(k), warp_sums,
-                                            sel, b1, above);
-  *cnt = nvalid > static_cast<uint32_t>(k) ? hist[*b1] : 0u;
-  return nvalid;
+  if (threadIdx.x == 0) *flag_smem = (atomicAdd(counter, 1u) == total - 1u) ? 1u : 0u;
+  __syncthreads();
+  const bool last = *flag_smem != 0u;
+  if (last) __threadfence();
+  return last;
 }
 
 __global__ void __launch_bounds__(kSegThreads) topk_hist_kernel(const TopkParams p) {
   __shared__ uint32_t hist[kHistBins];
+  __shared__ uint2 warp_sums[kSegThreads / 32];
+  __shared__ uint32_t sel[2];
+  __shared__ uint32_t flag;
   const int row = blockIdx.y;
   const int tid = threadIdx.x;
   int lo, hi;
   row_range(p, row, &lo, &hi);
+  const int n = hi - lo;
   const int s0 = static_cast<int>(blockIdx.x) * kSegKeys;
-  const int cnt = min(hi - lo - s0, kSegKeys);
-  if (cnt <= 0) return;
+  const int cnt = min(n - s0, kSegKeys);
+  uint32_t* w = split_row(p, row);
+  if (cnt <= 0) {
+    if (blockIdx.x == 0 && tid == 0) {  // empty row: nothing to select
+      w[kStState + kSMode] = kModeIota;
+      w[kStState + kSValid] = 0u;
+    }
+    return;
+  }
   for (int i = tid; i < kHistBins; i += kSegThreads) hist[i] = 0u;
   __syncthreads();
   const float* src = p.logits + static_cast<int64_t>(row) * p.ld + lo + s0;
@@ -669,10 +688,38 @@ __global__ void __launch_bounds__(kSegThreads) topk_hist_kernel(const TopkParams
     if (kk != 0u) atomicAdd(&hist[kk >> 21], 1u);
   });
   __syncthreads();
-  uint32_t* g = split_row(p, row) + kStHist;
+  uint32_t* g = w + kStHist;
   for (int i = tid; i < kHistBins; i += kSegThreads) {
     const uint32_t v = hist[i];
     if (v) atomicAdd(&g[i], v);
+  }
+  const uint32_t nseg = static_cast<uint32_t>((n + kSegKeys - 1) / kSegKeys);
+  if (!last_to_arrive(&w[kStState + kSDoneHist], nseg, &flag)) return;
+  // The row's histogram is complete: find the threshold bin once.
+  for (int i = tid; i < kHistBins; i += kSegThreads) hist[i] = __ldcg(&g[i]);
+  __syncthreads();
+  uint32_t b1, above;
+  const uint32_t nvalid =
+      find_bin<kSegThreads>(hist, kHistBins, static_cast<uint32_t>(p.k), warp_sums, sel, &b1, &above);
+  if (tid == 0) {
+    w[kStState + kSValid] = nvalid;
+    if (nvalid <= static_cast<uint32_t>(p.k)) {
+      w[kStState + kSMode] = nvalid == static_cast<uint32_t>(n) ? kModeIota : kModeSelect;
+      w[kStState + kSTau] = 0u;
+      w[kStState + kSNeed] = 0u;
+    } else {
+      const uint32_t rem = static_cast<uint32_t>(p.k) - above;
+      const uint32_t bcnt = hist[b1];
+      w[kStState + kSB1] = b1;
+      w[kStState + kSRem] = rem;
+      if (rem == bcnt) {  // the whole bin is taken
+        w[kStState + kSMode] = kModeSelect;
+        w[kStState + kSTau] = (b1 << 21) - 1u;
+        w[kStState + kSNeed] = 0u;
+      } else {
+        w[kStState + kSMode] = bcnt <= static_cast<uint32_t>(kSplitCand) ? kModeGather : kModeStream;
+      }
+    }
   }
 }
 
@@ -680,107 +727,84 @@ __global__ void __launch_bounds__(kSegThreads) topk_gather_kernel(const TopkPara
   __shared__ uint32_t hist[kHistBins];
   __shared__ uint2 warp_sums[kSegThreads / 32];
   __shared__ uint32_t sel[2];
+  __shared__ uint32_t flag;
   const int row = blockIdx.y;
-  const int lane = threadIdx.x & 31;
-  int lo, hi;
-  row_range(p, row, &lo, &hi);
-  const int s0 = static_cast<int>(blockIdx.x) * kSegKeys;
-  const int cnt = min(hi - lo - s0, kSegKeys);
-  if (cnt <= 0) return;
-  uint32_t* w = split_row(p, row);
-  uint32_t b1, above, bcnt;
-  const uint32_t nvalid =
-      split_decide<kSegThreads>(w + kStHist, p.k, hist, warp_sums, sel, &b1, &above, &bcnt);
-  if (nvalid <= static_cast<uint32_t>(p.k)) return;                 // take every valid key
-  if (static_cast<uint32_t>(p.k) - above == bcnt) return;           // the whole bin is taken
-  if (bcnt > static_cast<uint32_t>(kSplitCand)) return;             // refine streams instead
-  const float* src = p.logits + static_cast<int64_t>(row) * p.ld + lo + s0;
-  uint32_t* ncand = w + kStState + 4;
-  uint32_t* cand = w + kStCand;
-  // Warp-collective body: iterate over whole warps (loads stay < cnt).
-  stream_row<kSegThreads, kSegItems>(src, (cnt + 31) & ~31, cnt, [&](int, float x) {
-    const uint32_t kk = order_key(x);
-    const bool hit = (kk >> 21) == b1;
-    const uint32_t m = __ballot_sync(0xffffffffu, hit);
-    if (m) {
-      uint32_t slot = 0u;
-      if (lane == 0) slot = atomicAdd(ncand, static_cast<uint32_t>(__popc(m)));
-      slot = __shfl_sync(0xffffffffu, slot, 0);
-      const uint32_t idx = slot + __popc(m & ((1u << lane) - 1u));
-      if (hit && idx < static_cast<uint32_t>(kSplitCand)) cand[idx] = kk;
-    }
-  });
-}
-
-constexpr int kRefineThreads = 1024;
-
-__global__ void __launch_bounds__(kRefineThreads) topk_refine_kernel(const TopkParams p) {
-  __shared__ uint32_t hist[kHistBins];
-  extern __shared__ uint32_t cand[];  // kSplitCand keys (dynamic shared memory)
-  __shared__ uint2 warp_sums[kRefineThreads / 32];
-  __shared__ uint32_t sel[2];
-  const int row = blockIdx.x;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
   int lo, hi;
   row_range(p, row, &lo, &hi);
   const int n = hi - lo;
+  const int s0 = static_cast<int>(blockIdx.x) * kSegKeys;
+  const int cnt = min(n - s0, kSegKeys);
+  if (cnt <= 0) return;
   uint32_t* w = split_row(p, row);
-  uint32_t b1, above, bcnt;
-  const uint32_t nvalid =
-      split_decide<kRefineThreads>(w + kStHist, p.k, hist, warp_sums, sel, &b1, &above, &bcnt);
-  uint32_t tau = 0u, need_eq = 0u;
-  if (nvalid > static_cast<uint32_t>(p.k)) {
-    uint32_t rem = static_cast<uint32_t>(p.k) - above;
-    uint32_t prefix = b1;
-    if (rem == bcnt) {
-      tau = (prefix << 21) - 1u;
-    } else {
-      const bool gathered = bcnt <= static_cast<uint32_t>(kSplitCand);
-      const int nc = gathered ? min(static_cast<int>(w[kStState + 4]), kSplitCand) : 0;
-      for (int i = tid; i < nc; i += kRefineThreads) cand[i] = w[kStCand + i];
-      const float* src = p.logits + static_cast<int64_t>(row) * p.ld + lo;
-#pragma unroll 1
-      for (int d = 1; d < 3; ++d) {
-        const int nbins = d == 2 ? 1024 : 2048;
-        const int shift = d == 1 ? 10 : 0;
-        const int pshift = d == 1 ? 21 : 10;
-        __syncthreads();
-        for (int i = tid; i < nbins; i += kRefineThreads) hist[i] = 0u;
-        __syncthreads();
-        if (gathered) {
-          for (int i = tid; i < nc; i += kRefineThreads) {
-            const uint32_t kk = cand[i];
-            if ((kk >> pshift) == prefix)
-              atomicAdd(&hist[(kk >> shift) & static_cast<uint32_t>(nbins - 1)], 1u);
-          }
-        } else {
-          stream_row<kRefineThreads, 16>(src, n, n, [&](int, float x) {
-            const uint32_t kk = order_key(x);
-            if ((kk >> pshift) == prefix)
-              atomicAdd(&hist[(kk >> shift) & static_cast<uint32_t>(nbins - 1)], 1u);
-          });
-        }
-        __syncthreads();
-        uint32_t b, ab;
-        find_bin<kRefineThreads>(hist, nbins, rem, warp_sums, sel, &b, &ab);
-        const uint32_t c = hist[b];
-        rem -= ab;
-        prefix = (prefix << (d == 1 ? 11 : 10)) | b;
-        if (rem == c || d == 2) {
-          tau = d == 2 ? prefix : (prefix << 10) - 1u;
-          need_eq = d == 2 ? rem : 0u;
-          break;
-        }
+  const uint32_t mode = w[kStState + kSMode];
+  if (mode != kModeGather && mode != kModeStream) return;
+  const uint32_t b1 = w[kStState + kSB1];
+  uint32_t* cand = w + kStCand;
+  if (mode == kModeGather) {
+    const float* src = p.logits + static_cast<int64_t>(row) * p.ld + lo + s0;
+    // Warp-collective body: iterate over whole warps (loads stay < cnt).
+    stream_row<kSegThreads, kSegItems>(src, (cnt + 31) & ~31, cnt, [&](int, float x) {
+      const uint32_t kk = order_key(x);
+      const bool hit = (kk >> 21) == b1;
+      const uint32_t m = __ballot_sync(0xffffffffu, hit);
+      if (m) {
+        uint32_t slot = 0u;
+        if (lane == 0) slot = atomicAdd(&w[kStState + kSNcand], static_cast<uint32_t>(__popc(m)));
+        slot = __shfl_sync(0xffffffffu, slot, 0);
+        const uint32_t idx = slot + __popc(m & ((1u << lane) - 1u));
+        if (hit && idx < static_cast<uint32_t>(kSplitCand)) cand[idx] = kk;
       }
+    });
+  }
+  const uint32_t nseg = static_cast<uint32_t>((n + kSegKeys - 1) / kSegKeys);
+  if (!last_to_arrive(&w[kStState + kSDoneGather], nseg, &flag)) return;
+  // Last gather CTA of the row: exact tau / need_eq from the candidates (or
+  // from streaming passes over the row when the bin was too large).
+  extern __shared__ uint32_t cand_s[];  // kSplitCand keys
+  const bool gathered = mode == kModeGather;
+  const int nc = gathered ? min(static_cast<int>(__ldcg(&w[kStState + kSNcand])), kSplitCand) : 0;
+  for (int i = tid; i < nc; i += kSegThreads) cand_s[i] = __ldcg(&cand[i]);
+  const float* row_src = p.logits + static_cast<int64_t>(row) * p.ld + lo;
+  uint32_t rem = w[kStState + kSRem];
+  uint32_t prefix = b1, tau = 0u, need_eq = 0u;
+#pragma unroll 1
+  for (int d = 1; d < 3; ++d) {
+    const int nbins = d == 2 ? 1024 : 2048;
+    const int shift = d == 1 ? 10 : 0;
+    const int pshift = d == 1 ? 21 : 10;
+    __syncthreads();
+    for (int i = tid; i < nbins; i += kSegThreads) hist[i] = 0u;
+    __syncthreads();
+    if (gathered) {
+      for (int i = tid; i < nc; i += kSegThreads) {
+        const uint32_t kk = cand_s[i];
+        if ((kk >> pshift) == prefix)
+          atomicAdd(&hist[(kk >> shift) & static_cast<uint32_t>(nbins - 1)], 1u);
+      }
+    } else {
+      stream_row<kSegThreads, 16>(row_src, n, n, [&](int, float x) {
+        const uint32_t kk = order_key(x);
+        if ((kk >> pshift) == prefix)
+          atomicAdd(&hist[(kk >> shift) & static_cast<uint32_t>(nbins - 1)], 1u);
+      });
+    }
+    __syncthreads();
+    uint32_t b, ab;
+    find_bin<kSegThreads>(hist, nbins, rem, warp_sums, sel, &b, &ab);
+    const uint32_t c = hist[b];
+    rem -= ab;
+    prefix = (prefix << (d == 1 ? 11 : 10)) | b;
+    if (rem == c || d == 2) {
+      tau = d == 2 ? prefix : (prefix << 10) - 1u;
+      need_eq = d == 2 ? rem : 0u;
+      break;
     }
   }
   if (tid == 0) {
-    w[kStState + 0] = (nvalid <= static_cast<uint32_t>(p.k) && nvalid == static_cast<uint32_t>(n))
-                          ? kModeIota
-                          : kModeSelect;
-    w[kStState + 1] = tau;
-    w[kStState + 2] = need_eq;
-    w[kStState + 3] = nvalid;
+    w[kStState + kSTau] = tau;
+    w[kStState + kSNeed] = need_eq;
+    w[kStState + kSMode] = kModeSelect;
   }
 }
 
@@ -794,8 +818,8 @@ __global__ void __launch_bounds__(kSegThreads) topk_count_kernel(const TopkParam
   const int cnt = min(hi - lo - s0, kSegKeys);
   if (cnt <= 0) return;
   uint32_t* w = split_row(p, row);
-  if (w[kStState + 0] == kModeIota) return;
-  const uint32_t tau = w[kStState + 1], need_eq = w[kStState + 2];
+  if (w[kStState + kSMode] == kModeIota) return;
+  const uint32_t tau = w[kStState + kSTau], need_eq = w[kStState + kSNeed];
   const float* src = p.logits + static_cast<int64_t>(row) * p.ld + lo + s0;
   uint2 c = make_uint2(0u, 0u);
   stream_row<kSegThreads, kSegItems>(src, cnt, cnt, [&](int, float x) {
@@ -813,7 +837,7 @@ __global__ void __launch_bounds__(kSegThreads) topk_count_kernel(const TopkParam
 
 __global__ void __launch_bounds__(kSegThreads) topk_write_kernel(const TopkParams p) {
   constexpr int NW = kSegThreads / 32;
-  constexpr int WORDS = kSegKeys / 32;
+  constexpr int WORDS = kSegKeys / 32;  // 512
   __shared__ uint32_t gt_bits[WORDS];
   __shared__ uint32_t eq_bits[WORDS];
   __shared__ uint2 warp_sums[NW];
@@ -824,8 +848,9 @@ __global__ void __launch_bounds__(kSegThreads) topk_write_kernel(const TopkParam
   int lo, hi;
   row_range(p, row, &lo, &hi);
   const uint32_t* w = split_row(p, row);
-  const uint32_t mode = w[kStState + 0];
-  const uint32_t tau = w[kStState + 1], need_eq = w[kStState + 2], nvalid = w[kStState + 3];
+  const uint32_t mode = w[kStState + kSMode];
+  const uint32_t tau = w[kStState + kSTau], need_eq = w[kStState + kSNeed];
+  const uint32_t nvalid = w[kStState + kSValid];
   int32_t* dst = p.out + static_cast<int64_t>(row) * p.k;
   if (seg == 0) {
     const int nsel = nvalid < static_cast<uint32_t>(p.k) ? static_cast<int>(nvalid) : p.k;
@@ -963,14 +988,13 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t s) {
     cudaError_t e = cudaMemsetAsync(
         p.split, 0, static_cast<size_t>(p.R) * p.split_words * sizeof(uint32_t), s);
     if (e != cudaSuccess) return e;
+    const int gather_smem = kSplitCand * static_cast<int>(sizeof(uint32_t));
+    e = cudaFuncSetAttribute(topk_gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             gather_smem);
+    if (e != cudaSuccess) return e;
     const dim3 grid((S + kSegKeys - 1) / kSegKeys, static_cast<unsigned>(p.R));
     topk_hist_kernel<<<grid, kSegThreads, 0, s>>>(p);
-    topk_gather_kernel<<<grid, kSegThreads, 0, s>>>(p);
-    const int refine_smem = kSplitCand * static_cast<int>(sizeof(uint32_t));
-    e = cudaFuncSetAttribute(topk_refine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             refine_smem);
-    if (e != cudaSuccess) return e;
-    topk_refine_kernel<<<p.R, kRefineThreads, refine_smem, s>>>(p);
+    topk_gather_kernel<<<grid, kSegThreads, gather_smem, s>>>(p);
     topk_count_kernel<<<grid, kSegThreads, 0, s>>>(p);
     topk_write_kernel<<<grid, kSegThreads, 0, s>>>(p);
     return cudaGetLastError();
