@@ -36,11 +36,13 @@ namespace {
 constexpr int kHistBins = 2048;
 
 __device__ __forceinline__ uint32_t order_key(float x) {
-  uint32_t u = __float_as_uint(x);
-  if (u == 0x80000000u) u = 0u;                        // -0.0 -> +0.0
-  const uint32_t key = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  const bool invalid = (x != x) || (u == 0xFF800000u);  // NaN or -inf
-  return invalid ? 0u : key;
+  // fmaxf returns the other operand for a NaN (NaN -> -inf); adding +0.0
+  // turns -0.0 into +0.0 (round to nearest).
+  const float y = fmaxf(x, -INFINITY) + 0.0f;
+  const uint32_t u = __float_as_uint(y);
+  // Negative: all bits flipped; positive: the sign bit set.
+  const uint32_t key = u ^ (static_cast<uint32_t>(static_cast<int32_t>(u) >> 31) | 0x80000000u);
+  return key > 0x007FFFFFu ? key : 0u;  // -inf (0x007FFFFF) -> 0
 }
 
 // ---------------------------------------------------------------- clusters
@@ -164,11 +166,12 @@ __device__ __forceinline__ void row_range(const TopkParams& p, int row, int* lo,
 __device__ __forceinline__ int hpad(int bin) { return bin + (bin >> 5); }
 constexpr int kHistSlots = kHistBins + kHistBins / 32;
 
-// find_bin over a padded histogram (see find_bin).  Three barriers.
+// find_bin over a padded histogram (see find_bin), also returning the
+// count of the selected bin.  Three barriers.
 template <int THREADS>
-__device__ __forceinline__ void find_bin_padded(const uint32_t* hist, int nbins, uint32_t r,
-                                                uint2* warp_sums, uint32_t* sel, uint32_t* bin,
-                                                uint32_t* above, uint32_t* count) {
+__device__ __forceinline__ uint32_t find_bin_padded(const uint32_t* hist, int nbins, uint32_t r,
+                                                    uint2* warp_sums, uint32_t* sel, uint32_t* bin,
+                                                    uint32_t* above, uint32_t* count) {
   const int per = nbins / THREADS;  // consecutive bins per thread, highest first
   const int top = nbins - 1 - static_cast<int>(threadIdx.x) * per;
   uint32_t local = 0;
@@ -192,6 +195,7 @@ __device__ __forceinline__ void find_bin_padded(const uint32_t* hist, int nbins,
   *bin = sel[0];
   *above = sel[1];
   *count = sel[2];
+  return total.x;
 }
 
 template <int THREADS, int ITEMS, int CL>
@@ -408,6 +412,183 @@ __global__ void __launch_bounds__(THREADS, 65536 / (THREADS * 64)) topk_reg_kern
     for (int i = nsel + tid; i < p.k; i += THREADS) dst[i] = -1;
 }
 
+// ------------------------------------------------------------- short rows
+
+// One CTA per row of up to THREADS*ITEMS keys, held in registers.  Warp w
+// owns columns [w*32*ITEMS, (w+1)*32*ITEMS) of the row, item u of lane l
+// being column w*32*ITEMS + u*32 + l: every load is warp-contiguous, and a
+// warp meets its columns in order, so each selected column's output position
+// is a running per-warp count plus the selected columns of earlier warps.
+template <int THREADS, int ITEMS, int MINB>
+__global__ void __launch_bounds__(THREADS, MINB) topk_row_kernel(const TopkParams p) {
+  constexpr int NW = THREADS / 32;
+  constexpr int WSPAN = 32 * ITEMS;
+  __shared__ __align__(16) uint32_t hist[2][kHistSlots];
+  __shared__ uint2 warp_sums[NW];
+  __shared__ uint2 warp_cnt[NW];
+  __shared__ uint32_t sel[4];
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int row = blockIdx.x;
+  int lo, hi;
+  row_range(p, row, &lo, &hi);
+  const int n = hi - lo;
+  const float* src = p.logits + static_cast<int64_t>(row) * p.ld + lo;
+  int32_t* dst = p.out + static_cast<int64_t>(row) * p.k;
+  const int wbase = warp * WSPAN;
+  // Items of this warp holding at least one column of the row (warp-uniform).
+  const int nit = min(max((n - wbase + 31) >> 5, 0), ITEMS);
+
+  float x[ITEMS];
+#pragma unroll
+  for (int u = 0; u < ITEMS; ++u) {
+    const int c = wbase + u * 32 + lane;
+    x[u] = c < n ? __ldg(src + c) : -INFINITY;
+  }
+
+  uint32_t tau = 0u, need_eq = 0u;  // take every key > tau, then the first need_eq == tau
+  int nsel;
+  uint32_t key[ITEMS];
+  if (n <= p.k) {
+    // Every valid key is taken: tau = 0.  All of them valid: lo, lo+1, ...
+    // (x > -inf is false for -inf and NaN alone.)
+    uint32_t nv = 0u;
+#pragma unroll
+    for (int u = 0; u < ITEMS; ++u) nv += x[u] > -INFINITY ? 1u : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) nv += __shfl_xor_sync(0xffffffffu, nv, o);
+    if (lane == 0) warp_cnt[warp].x = nv;
+    __syncthreads();
+    uint32_t all = 0u;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) all += warp_cnt[w].x;
+    if (all == static_cast<uint32_t>(n)) {
+      for (int i = tid; i < p.k; i += THREADS) dst[i] = i < n ? lo + i : -1;
+      return;
+    }
+    nsel = static_cast<int>(all);
+#pragma unroll
+    for (int u = 0; u < ITEMS; ++u) key[u] = order_key(x[u]);
+    __syncthreads();  // warp_cnt is rewritten below
+  } else {
+#pragma unroll
+    for (int u = 0; u < ITEMS; ++u) key[u] = order_key(x[u]);
+    for (int i = tid; i < kHistSlots / 4; i += THREADS) {
+      reinterpret_cast<uint4*>(hist[0])[i] = make_uint4(0u, 0u, 0u, 0u);
+      reinterpret_cast<uint4*>(hist[1])[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    __syncthreads();
+    // Digit 1: the top 11 key bits (invalid keys are left out).
+#pragma unroll
+    for (int u = 0; u < ITEMS; ++u) {
+      if (u < nit) {
+        const uint32_t kk = key[u];
+        if (kk != 0u) atomicAdd(&hist[0][hpad(static_cast<int>(kk >> 21))], 1u);
+      }
+    }
+    __syncthreads();
+    uint32_t b, above, cnt;
+    const uint32_t nvalid =
+        find_bin_padded<THREADS>(hist[0], kHistBins, static_cast<uint32_t>(p.k), warp_sums, sel,
+                                 &b, &above, &cnt);
+    if (nvalid <= static_cast<uint32_t>(p.k)) {
+      nsel = static_cast<int>(nvalid);  // every valid key is taken
+    } else {
+      nsel = p.k;
+      uint32_t rem = static_cast<uint32_t>(p.k) - above;
+      uint32_t prefix = b;
+      if (rem == cnt) {
+        tau = (prefix << 21) - 1u;  // the whole bin is taken
+      } else {
+        // Digit 2: bits 20..10 of the keys in bin `prefix`; hist[0] is
+        // cleared meanwhile for digit 3.
+#pragma unroll
+        for (int u = 0; u < ITEMS; ++u) {
+          if (u < nit) {
+            const uint32_t kk = key[u];
+            if ((kk >> 21) == prefix)
+              atomicAdd(&hist[1][hpad(static_cast<int>((kk >> 10) & 2047u))], 1u);
+          }
+        }
+        for (int i = tid; i < kHistSlots / 4; i += THREADS)
+          reinterpret_cast<uint4*>(hist[0])[i] = make_uint4(0u, 0u, 0u, 0u);
+        __syncthreads();
+        find_bin_padded<THREADS>(hist[1], kHistBins, rem, warp_sums, sel, &b, &above, &cnt);
+        rem -= above;
+        prefix = (prefix << 11) | b;
+        if (rem == cnt) {
+          tau = (prefix << 10) - 1u;
+        } else {
+          // Digit 3: bits 9..0 of the keys with the 22-bit prefix.
+#pragma unroll
+          for (int u = 0; u < ITEMS; ++u) {
+            if (u < nit) {
+              const uint32_t kk = key[u];
+              if ((kk >> 10) == prefix) atomicAdd(&hist[0][hpad(static_cast<int>(kk & 1023u))], 1u);
+            }
+          }
+          __syncthreads();
+          find_bin_padded<THREADS>(hist[0], 1024, rem, warp_sums, sel, &b, &above, &cnt);
+          tau = (prefix << 10) | b;
+          need_eq = rem - above;
+        }
+      }
+    }
+  }
+
+  // Per-warp counts of keys > tau (and == tau), then the ordered writes.
+  uint32_t cg = 0u, ce = 0u;
+#pragma unroll
+  for (int u = 0; u < ITEMS; ++u) cg += key[u] > tau ? 1u : 0u;
+  if (need_eq != 0u) {
+#pragma unroll
+    for (int u = 0; u < ITEMS; ++u) ce += key[u] == tau ? 1u : 0u;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    cg += __shfl_xor_sync(0xffffffffu, cg, o);
+    ce += __shfl_xor_sync(0xffffffffu, ce, o);
+  }
+  if (lane == 0) warp_cnt[warp] = make_uint2(cg, ce);
+  __syncthreads();
+  uint32_t grun = 0u, erun = 0u;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    if (w < warp) {
+      grun += warp_cnt[w].x;
+      erun += warp_cnt[w].y;
+    }
+  }
+  const uint32_t lt = (1u << lane) - 1u;
+  if (need_eq == 0u) {
+#pragma unroll
+    for (int u = 0; u < ITEMS; ++u) {
+      if (u < nit) {
+        const bool g = key[u] > tau;
+        const uint32_t m = __ballot_sync(0xffffffffu, g);
+        if (g) dst[grun + __popc(m & lt)] = lo + wbase + u * 32 + lane;
+        grun += __popc(m);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int u = 0; u < ITEMS; ++u) {
+      if (u < nit) {
+        const bool g = key[u] > tau, e = key[u] == tau;
+        const uint32_t mg = __ballot_sync(0xffffffffu, g);
+        const uint32_t me = __ballot_sync(0xffffffffu, e);
+        const uint32_t gb = grun + __popc(mg & lt), eb = erun + __popc(me & lt);
+        const int col = lo + wbase + u * 32 + lane;
+        if (g) dst[gb + min(eb, need_eq)] = col;
+        else if (e && eb < need_eq) dst[gb + eb] = col;
+        grun += __popc(mg);
+        erun += __popc(me);
+      }
+    }
+  }
+  for (int i = nsel + tid; i < p.k; i += THREADS) dst[i] = -1;
+}
+
 // --------------------------------------------------------------- streaming
 
 // Visit slots i in [0, n_iter) with THREADS threads, i = base + u*THREADS for
@@ -617,30 +798,42 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamThreads >= 1024 ? 1 : 8
 // Few long rows (decode): every phase runs on a grid of (16384-key segment,
 // row) CTAs, and the phases talk through per-row scratch:
 //   hist[2048]        first-digit (top 11 bits) histogram of the row's valid keys
-//   state[16]         mode, tau, need_eq, nvalid, b1, rem, done counters, ncand
-//   cand[kSplitCand]  keys of the threshold bin
-//   segcnt[2*segs]    per-segment (key > tau, key == tau) counts
-// Steps (one launch each, after zeroing the scratch):
+//   state[16]         mode, tau, need_eq, nvalid, b1, rem, completion counters, ncand
+//   cand[kSplitCand]  keys of the threshold bin b1: their low 21 bits, and the
+//                     segment they came from in the bits above
+//   seg[3*kSplitSegs] per segment: keys above the first threshold, then the
+//                     numbers of selected keys > tau and == tau in earlier segments
+// Only hist and state are zeroed before the first phase.  Phases (one launch
+// each):
 //   hist    segments add their histograms; the last segment CTA of a row to
-//           finish (a completion counter after a fence; nobody waits) finds
-//           the threshold bin and the row's mode;
-//   gather  segments append the keys of the threshold bin; the last one of a
-//           row refines them to the exact tau / need_eq (or, when the bin
-//           holds more than kSplitCand keys, streams the row);
-//   count   per-segment counts of keys > tau and == tau;
-//   write   each segment places its selected columns after those of the
-//           earlier segments, in column order; segment 0 writes the -1 tail.
+//           finish (a completion counter after a fence; nobody waits) picks
+//           the threshold bin b1 and the row's mode;
+//   gather  segments count their keys above bin b1 and append the keys of
+//           bin b1; the last one of a row refines them to the exact tau and
+//           need_eq (streaming the row when the bin holds more than
+//           kSplitCand keys) and turns the per-segment counts into the output
+//           offsets of every segment;
+//   write   each segment places its selected columns at its offsets, in
+//           column order; segment 0 writes the -1 tail.
 constexpr int kSegKeys = 16384;
 constexpr int kSegThreads = 1024;
 constexpr int kSegItems = kSegKeys / kSegThreads;  // 16
 constexpr int kSplitCand = 16384;
+constexpr int kSplitSegs = 64;  // rows of up to 64 * 16384 keys
 constexpr int kStateWords = 16;
 constexpr int kStHist = 0, kStState = kHistBins, kStCand = kHistBins + kStateWords,
-              kStSeg = kHistBins + kStateWords + kSplitCand;
+              kStSeg = kHistBins + kStateWords + kSplitCand,
+              kStBase = kStSeg + kSplitSegs,  // (gt, eq) offset pairs
+              kStWords = kStBase + 2 * kSplitSegs;
+constexpr int kStZeroWords = kHistBins + kStateWords;  // zeroed before the first phase
 // state words
 constexpr int kSMode = 0, kSTau = 1, kSNeed = 2, kSValid = 3, kSB1 = 4, kSRem = 5,
               kSDoneHist = 6, kSDoneGather = 7, kSNcand = 8;
+// Rows after the first phase: every valid key taken in place (iota); the
+// exact tau known (select); the keys of bin b1 to be gathered and refined
+// (gather), or, too many of them, the row to be streamed (stream).
 enum : uint32_t { kModeSelect = 1u, kModeIota = 2u, kModeGather = 3u, kModeStream = 4u };
+constexpr uint32_t kLow21 = (1u << 21) - 1u;
 
 __device__ __forceinline__ uint32_t* split_row(const TopkParams& p, int row) {
   return p.split + static_cast<int64_t>(row) * p.split_words;
@@ -660,21 +853,21 @@ __device__ __forceinline__ bool last_to_arrive(uint32_t* counter, uint32_t total
   return last;
 }
 
-__global__ void __launch_bounds__(kSegThreads) topk_hist_kernel(const TopkParams p) {
+__global__ void __launch_bounds__(kSegThreads, 2) topk_hist_kernel(const TopkParams p) {
   __shared__ uint32_t hist[kHistBins];
   __shared__ uint2 warp_sums[kSegThreads / 32];
   __shared__ uint32_t sel[2];
   __shared__ uint32_t flag;
-  const int row = blockIdx.y;
+  const int row = blockIdx.x;
   const int tid = threadIdx.x;
   int lo, hi;
   row_range(p, row, &lo, &hi);
   const int n = hi - lo;
-  const int s0 = static_cast<int>(blockIdx.x) * kSegKeys;
+  const int s0 = static_cast<int>(blockIdx.y) * kSegKeys;
   const int cnt = min(n - s0, kSegKeys);
   uint32_t* w = split_row(p, row);
   if (cnt <= 0) {
-    if (blockIdx.x == 0 && tid == 0) {  // empty row: nothing to select
+    if (blockIdx.y == 0 && tid == 0) {  // empty row: nothing to select
       w[kStState + kSMode] = kModeIota;
       w[kStState + kSValid] = 0u;
     }
@@ -704,6 +897,7 @@ __global__ void __launch_bounds__(kSegThreads) topk_hist_kernel(const TopkParams
   if (tid == 0) {
     w[kStState + kSValid] = nvalid;
     if (nvalid <= static_cast<uint32_t>(p.k)) {
+      // Every valid key is taken: tau = 0 (invalid keys are 0).
       w[kStState + kSMode] = nvalid == static_cast<uint32_t>(n) ? kModeIota : kModeSelect;
       w[kStState + kSTau] = 0u;
       w[kStState + kSNeed] = 0u;
@@ -723,51 +917,16 @@ __global__ void __launch_bounds__(kSegThreads) topk_hist_kernel(const TopkParams
   }
 }
 
-__global__ void __launch_bounds__(kSegThreads) topk_gather_kernel(const TopkParams p) {
-  __shared__ uint32_t hist[kHistBins];
-  __shared__ uint2 warp_sums[kSegThreads / 32];
-  __shared__ uint32_t sel[2];
-  __shared__ uint32_t flag;
-  const int row = blockIdx.y;
-  const int tid = threadIdx.x, lane = tid & 31;
-  int lo, hi;
-  row_range(p, row, &lo, &hi);
-  const int n = hi - lo;
-  const int s0 = static_cast<int>(blockIdx.x) * kSegKeys;
-  const int cnt = min(n - s0, kSegKeys);
-  if (cnt <= 0) return;
-  uint32_t* w = split_row(p, row);
-  const uint32_t mode = w[kStState + kSMode];
-  if (mode != kModeGather && mode != kModeStream) return;
-  const uint32_t b1 = w[kStState + kSB1];
-  uint32_t* cand = w + kStCand;
-  if (mode == kModeGather) {
-    const float* src = p.logits + static_cast<int64_t>(row) * p.ld + lo + s0;
-    // Warp-collective body: iterate over whole warps (loads stay < cnt).
-    stream_row<kSegThreads, kSegItems>(src, (cnt + 31) & ~31, cnt, [&](int, float x) {
-      const uint32_t kk = order_key(x);
-      const bool hit = (kk >> 21) == b1;
-      const uint32_t m = __ballot_sync(0xffffffffu, hit);
-      if (m) {
-        uint32_t slot = 0u;
-        if (lane == 0) slot = atomicAdd(&w[kStState + kSNcand], static_cast<uint32_t>(__popc(m)));
-        slot = __shfl_sync(0xffffffffu, slot, 0);
-        const uint32_t idx = slot + __popc(m & ((1u << lane) - 1u));
-        if (hit && idx < static_cast<uint32_t>(kSplitCand)) cand[idx] = kk;
-      }
-    });
-  }
-  const uint32_t nseg = static_cast<uint32_t>((n + kSegKeys - 1) / kSegKeys);
-  if (!last_to_arrive(&w[kStState + kSDoneGather], nseg, &flag)) return;
-  // Last gather CTA of the row: exact tau / need_eq from the candidates (or
-  // from streaming passes over the row when the bin was too large).
-  extern __shared__ uint32_t cand_s[];  // kSplitCand keys
-  const bool gathered = mode == kModeGather;
-  const int nc = gathered ? min(static_cast<int>(__ldcg(&w[kStState + kSNcand])), kSplitCand) : 0;
-  for (int i = tid; i < nc; i += kSegThreads) cand_s[i] = __ldcg(&cand[i]);
-  const float* row_src = p.logits + static_cast<int64_t>(row) * p.ld + lo;
-  uint32_t rem = w[kStState + kSRem];
-  uint32_t prefix = b1, tau = 0u, need_eq = 0u;
+// Digits two and three of the radix select inside bin b1, over the keys
+// key_at(i) for i < n (a key outside bin b1 is skipped).  rem is the rank
+// still wanted inside bin b1.  Returns tau; *need_eq = keys == tau to take.
+// Contains barriers: every thread must call it.
+template <class KeyAt>
+__device__ __forceinline__ uint32_t refine_in_bin(uint32_t b1, uint32_t rem, uint32_t* hist,
+                                                  uint2* warp_sums, uint32_t* sel,
+                                                  uint32_t* need_eq, KeyAt&& visit) {
+  const int tid = threadIdx.x;
+  uint32_t prefix = b1;
 #pragma unroll 1
   for (int d = 1; d < 3; ++d) {
     const int nbins = d == 2 ? 1024 : 2048;
@@ -776,119 +935,213 @@ __global__ void __launch_bounds__(kSegThreads) topk_gather_kernel(const TopkPara
     __syncthreads();
     for (int i = tid; i < nbins; i += kSegThreads) hist[i] = 0u;
     __syncthreads();
-    if (gathered) {
-      for (int i = tid; i < nc; i += kSegThreads) {
-        const uint32_t kk = cand_s[i];
-        if ((kk >> pshift) == prefix)
-          atomicAdd(&hist[(kk >> shift) & static_cast<uint32_t>(nbins - 1)], 1u);
-      }
-    } else {
-      stream_row<kSegThreads, 16>(row_src, n, n, [&](int, float x) {
-        const uint32_t kk = order_key(x);
-        if ((kk >> pshift) == prefix)
-          atomicAdd(&hist[(kk >> shift) & static_cast<uint32_t>(nbins - 1)], 1u);
-      });
-    }
+    visit([&](uint32_t kk) {
+      if ((kk >> pshift) == prefix)
+        atomicAdd(&hist[(kk >> shift) & static_cast<uint32_t>(nbins - 1)], 1u);
+    });
     __syncthreads();
     uint32_t b, ab;
     find_bin<kSegThreads>(hist, nbins, rem, warp_sums, sel, &b, &ab);
     const uint32_t c = hist[b];
     rem -= ab;
     prefix = (prefix << (d == 1 ? 11 : 10)) | b;
-    if (rem == c || d == 2) {
-      tau = d == 2 ? prefix : (prefix << 10) - 1u;
-      need_eq = d == 2 ? rem : 0u;
-      break;
+    if (d == 1 && rem == c) {  // the whole sub-bin is taken
+      *need_eq = 0u;
+      return (prefix << 10) - 1u;
     }
   }
-  if (tid == 0) {
-    w[kStState + kSTau] = tau;
-    w[kStState + kSNeed] = need_eq;
-    w[kStState + kSMode] = kModeSelect;
-  }
+  *need_eq = rem;
+  return prefix;
 }
 
-__global__ void __launch_bounds__(kSegThreads) topk_count_kernel(const TopkParams p) {
-  __shared__ uint2 warp_sums[kSegThreads / 32];
-  const int row = blockIdx.y;
-  const int tid = threadIdx.x;
+__global__ void __launch_bounds__(kSegThreads, 2) topk_gather_kernel(const TopkParams p) {
+  constexpr int NW = kSegThreads / 32;
+  __shared__ uint32_t hist[kHistBins];
+  __shared__ uint2 warp_sums[NW];
+  __shared__ uint32_t sel[2];
+  __shared__ uint32_t flag;
+  __shared__ uint32_t cta_hits, cta_base;
+  __shared__ uint32_t seg_gt[kSplitSegs], seg_eq[kSplitSegs];
+  extern __shared__ uint32_t cand_s[];  // kSplitCand keys: staging, then the refine's copy
+  const int row = blockIdx.x;
+  const int seg = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int lo, hi;
   row_range(p, row, &lo, &hi);
-  const int s0 = static_cast<int>(blockIdx.x) * kSegKeys;
-  const int cnt = min(hi - lo - s0, kSegKeys);
+  const int n = hi - lo;
+  const int s0 = seg * kSegKeys;
+  const int cnt = min(n - s0, kSegKeys);
   if (cnt <= 0) return;
   uint32_t* w = split_row(p, row);
-  if (w[kStState + kSMode] == kModeIota) return;
-  const uint32_t tau = w[kStState + kSTau], need_eq = w[kStState + kSNeed];
   const float* src = p.logits + static_cast<int64_t>(row) * p.ld + lo + s0;
-  uint2 c = make_uint2(0u, 0u);
-  stream_row<kSegThreads, kSegItems>(src, cnt, cnt, [&](int, float x) {
-    const uint32_t kk = order_key(x);
-    c.x += kk > tau ? 1u : 0u;
-    c.y += (need_eq > 0u && kk == tau) ? 1u : 0u;
-  });
-  uint2 total;
-  block_scan2<kSegThreads>(c, warp_sums, &total);
+  float x[kSegItems];
+#pragma unroll
+  for (int u = 0; u < kSegItems; ++u) {
+    const int e = u * kSegThreads + tid;
+    x[u] = e < cnt ? __ldg(src + e) : -INFINITY;
+  }
+  const uint32_t mode = w[kStState + kSMode];
+  if (mode == kModeIota) return;
+  const uint32_t b1 = w[kStState + kSB1];
+  // Keys above `thr` are taken whatever the refinement finds; keys of bin
+  // `want` (none unless gathering) are the candidates.
+  const uint32_t thr = mode == kModeSelect ? w[kStState + kSTau] : ((b1 + 1u) << 21) - 1u;
+  const uint32_t want = mode == kModeGather ? b1 : 0xFFFFFFFFu;
+  if (tid == 0) cta_hits = 0u;
+  __syncthreads();
+  // This segment's candidates are staged in shared memory (any order), then
+  // copied to one slot range of the row's candidate list.
+  const uint32_t lt = (1u << lane) - 1u;
+  uint32_t above = 0u;
+#pragma unroll
+  for (int u = 0; u < kSegItems; ++u) {
+    const uint32_t kk = order_key(x[u]);
+    above += kk > thr ? 1u : 0u;
+    const bool hit = (kk >> 21) == want;
+    const uint32_t m = __ballot_sync(0xffffffffu, hit);
+    if (m) {
+      uint32_t slot = 0u;
+      if (lane == 0) slot = atomicAdd(&cta_hits, static_cast<uint32_t>(__popc(m)));
+      slot = __shfl_sync(0xffffffffu, slot, 0) + __popc(m & lt);
+      if (hit) cand_s[slot] = (static_cast<uint32_t>(seg) << 21) | (kk & kLow21);
+    }
+  }
+  // Keys above the threshold in this segment (block reduction).
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) above += __shfl_xor_sync(0xffffffffu, above, o);
+  if (lane == 0) warp_sums[warp] = make_uint2(above, 0u);
+  __syncthreads();
   if (tid == 0) {
-    w[kStSeg + 2 * blockIdx.x] = total.x;
-    w[kStSeg + 2 * blockIdx.x + 1] = total.y;
+    uint32_t a = 0u;
+    for (int i = 0; i < NW; ++i) a += warp_sums[i].x;
+    w[kStSeg + seg] = a;
+    cta_base = cta_hits ? atomicAdd(&w[kStState + kSNcand], cta_hits) : 0u;
+  }
+  __syncthreads();
+  {
+    const uint32_t nh = cta_hits, base = cta_base;
+    uint32_t* cand = w + kStCand;
+    for (uint32_t i = tid; i < nh; i += kSegThreads)
+      if (base + i < static_cast<uint32_t>(kSplitCand)) cand[base + i] = cand_s[i];
+  }
+  const uint32_t nseg = static_cast<uint32_t>((n + kSegKeys - 1) / kSegKeys);
+  if (!last_to_arrive(&w[kStState + kSDoneGather], nseg, &flag)) return;
+
+  // Last gather CTA of the row: the exact tau / need_eq, then the offsets of
+  // every segment's selected columns.
+  for (int i = tid; i < kSplitSegs; i += kSegThreads) {
+    seg_gt[i] = 0u;
+    seg_eq[i] = 0u;
+  }
+  uint32_t tau = thr, need_eq = 0u;
+  if (mode == kModeGather) {
+    const int nc = min(static_cast<int>(__ldcg(&w[kStState + kSNcand])), kSplitCand);
+    const uint32_t* cand = w + kStCand;
+    for (int i = tid; i < nc; i += kSegThreads) cand_s[i] = __ldcg(&cand[i]);
+    const uint32_t hi_bits = b1 << 21;
+    tau = refine_in_bin(b1, w[kStState + kSRem], hist, warp_sums, sel, &need_eq, [&](auto&& fn) {
+      for (int i = tid; i < nc; i += kSegThreads) fn(hi_bits | (cand_s[i] & kLow21));
+    });
+    for (int i = tid; i < nc; i += kSegThreads) {
+      const uint32_t c = cand_s[i];
+      const uint32_t kk = hi_bits | (c & kLow21);
+      if (kk > tau) atomicAdd(&seg_gt[c >> 21], 1u);
+      else if (kk == tau && need_eq) atomicAdd(&seg_eq[c >> 21], 1u);
+    }
+  } else if (mode == kModeStream) {
+    const float* row_src = p.logits + static_cast<int64_t>(row) * p.ld + lo;
+    tau = refine_in_bin(b1, w[kStState + kSRem], hist, warp_sums, sel, &need_eq, [&](auto&& fn) {
+      stream_row<kSegThreads, kSegItems>(row_src, n, n, [&](int, float x) { fn(order_key(x)); });
+    });
+    stream_row<kSegThreads, kSegItems>(row_src, n, n, [&](int i, float x) {
+      const uint32_t kk = order_key(x);
+      if ((kk >> 21) == b1) {
+        if (kk > tau) atomicAdd(&seg_gt[i / kSegKeys], 1u);
+        else if (kk == tau && need_eq) atomicAdd(&seg_eq[i / kSegKeys], 1u);
+      }
+    });
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // Exclusive prefix sums over the (at most 64) segments, two per lane.
+    uint32_t g[2], e[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int s = h * 32 + lane;
+      g[h] = s < static_cast<int>(nseg) ? __ldcg(&w[kStSeg + s]) + seg_gt[s] : 0u;
+      e[h] = s < static_cast<int>(nseg) ? seg_eq[s] : 0u;
+    }
+    uint32_t carry_g = 0u, carry_e = 0u;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t ig = g[h], ie = e[h];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t a = __shfl_up_sync(0xffffffffu, ig, o);
+        const uint32_t b = __shfl_up_sync(0xffffffffu, ie, o);
+        if (lane >= o) {
+          ig += a;
+          ie += b;
+        }
+      }
+      const int s = h * 32 + lane;
+      if (s < static_cast<int>(nseg)) {
+        w[kStBase + 2 * s] = carry_g + ig - g[h];
+        w[kStBase + 2 * s + 1] = carry_e + ie - e[h];
+      }
+      carry_g += __shfl_sync(0xffffffffu, ig, 31);
+      carry_e += __shfl_sync(0xffffffffu, ie, 31);
+    }
+    if (lane == 0) {
+      w[kStState + kSTau] = tau;
+      w[kStState + kSNeed] = need_eq;
+      w[kStState + kSMode] = kModeSelect;
+    }
   }
 }
 
-__global__ void __launch_bounds__(kSegThreads) topk_write_kernel(const TopkParams p) {
+__global__ void __launch_bounds__(kSegThreads, 2) topk_write_kernel(const TopkParams p) {
   constexpr int NW = kSegThreads / 32;
   constexpr int WORDS = kSegKeys / 32;  // 512
-  __shared__ uint32_t gt_bits[WORDS];
-  __shared__ uint32_t eq_bits[WORDS];
+  // Word u*NW + warp covers segment columns (u*NW + warp)*32 + lane: the
+  // ballots of (key > tau) and (key == tau), then the number of selected
+  // columns before the word (this segment's offsets included).
+  __shared__ uint32_t gt_bits[WORDS], eq_bits[WORDS];
+  __shared__ uint32_t gt_pre[WORDS], eq_pre[WORDS];
   __shared__ uint2 warp_sums[NW];
-  __shared__ uint2 seg_base;
-  const int row = blockIdx.y;
-  const int seg = blockIdx.x;
+  const int row = blockIdx.x;
+  const int seg = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int lo, hi;
   row_range(p, row, &lo, &hi);
   const uint32_t* w = split_row(p, row);
-  const uint32_t mode = w[kStState + kSMode];
-  const uint32_t tau = w[kStState + kSTau], need_eq = w[kStState + kSNeed];
-  const uint32_t nvalid = w[kStState + kSValid];
   int32_t* dst = p.out + static_cast<int64_t>(row) * p.k;
   if (seg == 0) {
+    const uint32_t nvalid = w[kStState + kSValid];
     const int nsel = nvalid < static_cast<uint32_t>(p.k) ? static_cast<int>(nvalid) : p.k;
     for (int i = nsel + tid; i < p.k; i += kSegThreads) dst[i] = -1;
   }
   const int s0 = seg * kSegKeys;
   const int cnt = min(hi - lo - s0, kSegKeys);
   if (cnt <= 0) return;
+  const float* src = p.logits + static_cast<int64_t>(row) * p.ld + lo + s0;
+  float x[kSegItems];
+#pragma unroll
+  for (int u = 0; u < kSegItems; ++u) {
+    const int e = u * kSegThreads + tid;
+    x[u] = e < cnt ? __ldg(src + e) : -INFINITY;
+  }
+  const uint32_t mode = w[kStState + kSMode];
   if (mode == kModeIota) {
     for (int i = tid; i < cnt; i += kSegThreads) dst[s0 + i] = lo + s0 + i;
     return;
   }
-  if (warp == 0) {
-    // Selected columns of the earlier segments come first.
-    uint2 acc = make_uint2(0u, 0u);
-    for (int i = lane; i < seg; i += 32) {
-      acc.x += w[kStSeg + 2 * i];
-      acc.y += w[kStSeg + 2 * i + 1];
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      acc.x += __shfl_xor_sync(0xffffffffu, acc.x, o);
-      acc.y += __shfl_xor_sync(0xffffffffu, acc.y, o);
-    }
-    if (lane == 0) seg_base = acc;
-  }
-  const float* src = p.logits + static_cast<int64_t>(row) * p.ld + lo + s0;
-  uint32_t key[kSegItems];
+  const uint32_t tau = w[kStState + kSTau], need_eq = w[kStState + kSNeed];
 #pragma unroll
   for (int u = 0; u < kSegItems; ++u) {
-    const int e = u * kSegThreads + tid;
-    key[u] = e < cnt ? order_key(__ldg(src + e)) : 0u;
-  }
-  // Word u*NW + warp holds segment columns (u*NW + warp)*32 + lane.
-#pragma unroll
-  for (int u = 0; u < kSegItems; ++u) {
-    const uint32_t g = __ballot_sync(0xffffffffu, key[u] > tau);
-    const uint32_t e = __ballot_sync(0xffffffffu, need_eq > 0u && key[u] == tau);
+    const uint32_t kk = order_key(x[u]);
+    const uint32_t g = __ballot_sync(0xffffffffu, kk > tau);
+    const uint32_t e = need_eq ? __ballot_sync(0xffffffffu, kk == tau) : 0u;
     if (lane == 0) {
       gt_bits[u * NW + warp] = g;
       eq_bits[u * NW + warp] = e;
@@ -900,24 +1153,28 @@ __global__ void __launch_bounds__(kSegThreads) topk_write_kernel(const TopkParam
   uint2 total;
   const uint2 before = block_scan2<kSegThreads>(mine, warp_sums, &total);
   if (tid < WORDS) {
-    gt_bits[tid] = seg_base.x + before.x;  // word prefixes replace the words
-    eq_bits[tid] = seg_base.y + before.y;
+    gt_pre[tid] = w[kStBase + 2 * seg] + before.x;
+    eq_pre[tid] = w[kStBase + 2 * seg + 1] + before.y;
   }
   __syncthreads();
-  const uint32_t lt = (1u << lane) - 1u;
-#pragma unroll
+  const uint32_t bit = 1u << lane, lt = bit - 1u;
+#pragma unroll 4
   for (int u = 0; u < kSegItems; ++u) {
     const int wd = u * NW + warp;
-    const bool g = key[u] > tau;
-    const bool e = need_eq > 0u && key[u] == tau;
-    const uint32_t gm = __ballot_sync(0xffffffffu, g);
-    const uint32_t em = __ballot_sync(0xffffffffu, e);
-    const uint32_t gb = gt_bits[wd] + __popc(gm & lt);
-    const uint32_t eb = eq_bits[wd] + __popc(em & lt);
+    const uint32_t gm = gt_bits[wd], em = eq_bits[wd];
+    if ((gm | em) == 0u) continue;  // nothing selected in these 32 columns
+    const uint32_t gb = gt_pre[wd] + __popc(gm & lt);
+    const uint32_t eb = eq_pre[wd] + __popc(em & lt);
     const int col = lo + s0 + u * kSegThreads + tid;
-    if (g) dst[gb + min(eb, need_eq)] = col;
-    else if (e && eb < need_eq) dst[gb + eb] = col;
+    if (gm & bit) dst[gb + min(eb, need_eq)] = col;
+    else if ((em & bit) && eb < need_eq) dst[gb + eb] = col;
   }
+}
+
+template <int THREADS, int ITEMS, int MINB>
+cudaError_t launch_row(const TopkParams& p, cudaStream_t s) {
+  topk_row_kernel<THREADS, ITEMS, MINB><<<p.R, THREADS, 0, s>>>(p);
+  return cudaGetLastError();
 }
 
 template <int THREADS, int ITEMS, int CL>
@@ -957,13 +1214,12 @@ bool topk_supported(int max_row) {
 constexpr int kTopkRegMaxRow = 1024 * 32 * 8;
 
 bool topk_split_rows(int64_t rows, int64_t max_row) {
-  return max_row > 16384 && rows <= 512;
+  return max_row > kSegKeys && max_row <= static_cast<int64_t>(kSplitSegs) * kSegKeys &&
+         rows <= 512;
 }
 
-int topk_split_words(int64_t max_row) {
-  const int64_t segs = (max_row + kSegKeys - 1) / kSegKeys;
-  const int64_t words = kStSeg + 2 * segs;
-  return static_cast<int>((words + 63) / 64 * 64);  // rows stay 256-byte aligned
+int topk_split_words(int64_t) {
+  return (kStWords + 63) / 64 * 64;  // rows stay 256-byte aligned
 }
 
 template <int THREADS>
@@ -985,24 +1241,27 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t s) {
   const int S = p.S;
   if (p.split) {
     // Few long rows: every phase on (segment, row) grids, see the split path.
-    cudaError_t e = cudaMemsetAsync(
-        p.split, 0, static_cast<size_t>(p.R) * p.split_words * sizeof(uint32_t), s);
+    // Only each row's histogram and state words start at zero.
+    cudaError_t e = cudaMemset2DAsync(p.split, static_cast<size_t>(p.split_words) * sizeof(uint32_t),
+                                      0, kStZeroWords * sizeof(uint32_t),
+                                      static_cast<size_t>(p.R), s);
     if (e != cudaSuccess) return e;
     const int gather_smem = kSplitCand * static_cast<int>(sizeof(uint32_t));
     e = cudaFuncSetAttribute(topk_gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              gather_smem);
     if (e != cudaSuccess) return e;
-    const dim3 grid((S + kSegKeys - 1) / kSegKeys, static_cast<unsigned>(p.R));
+    // Rows vary fastest: every row's first segment is scheduled before any
+    // second one, and the empty tail segments of short rows come last.
+    const dim3 grid(static_cast<unsigned>(p.R), (S + kSegKeys - 1) / kSegKeys);
     topk_hist_kernel<<<grid, kSegThreads, 0, s>>>(p);
     topk_gather_kernel<<<grid, kSegThreads, gather_smem, s>>>(p);
-    topk_count_kernel<<<grid, kSegThreads, 0, s>>>(p);
     topk_write_kernel<<<grid, kSegThreads, 0, s>>>(p);
     return cudaGetLastError();
   }
   // Short rows: keys in registers, one CTA per row, several rows per SM.
-  if (S <= 4096) return launch_reg<128, 32, 1>(p, s);
-  if (S <= 8192) return launch_reg<256, 32, 1>(p, s);
-  if (S <= 16384) return launch_reg<512, 32, 1>(p, s);
+  if (S <= 4096) return launch_row<256, 16, 6>(p, s);
+  if (S <= 8192) return launch_row<512, 16, 3>(p, s);
+  if (S <= 16384) return launch_row<1024, 16, 1>(p, s);
   // Very long rows without split scratch: a cluster of register-resident CTAs per row.
   if (S > 65536 && S <= 131072) return launch_reg<1024, 32, 4>(p, s);
   if (S > 131072 && S <= kTopkRegMaxRow) return launch_reg<1024, 32, 8>(p, s);
