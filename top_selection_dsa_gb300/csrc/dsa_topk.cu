@@ -8,23 +8,24 @@
 // selected, and the selected columns are written in ascending column order.
 //
 // Every logit becomes an order-preserving 32-bit key (larger float -> larger
-// key; -0.0 folded onto +0.0; -inf and NaN -> 0, which no valid score maps
-// to).  The exact k-th largest key tau is found by a radix select over the key
-// bits (11 + 11 + 10), after which every key > tau and the first need_eq keys
-// == tau (in column order) are taken.  The output order comes from warp-ballot
-// bitmaps of (key > tau) and (key == tau) and one prefix count over their
-// words, so selected columns are written in ascending order directly.
+// key; -0.0 folded onto +0.0; -inf and NaN below every valid score).  The
+// exact k-th largest key tau is found by a radix select over the key bits
+// (11 + 11 + 10), after which every key > tau and the first need_eq keys ==
+// tau (in column order) are taken, in ascending column order.
 //
-// Two kernels:
-//   topk_reg_kernel<THREADS, ITEMS, CL>  a row of up to CL*THREADS*ITEMS keys
-//       is read once from memory into registers (ITEMS per thread, striped so
-//       that each warp's loads are contiguous); the radix passes and the
-//       ordered writes work on registers.  CL > 1 spreads a row over a
-//       thread-block cluster whose CTAs merge their histograms and counts
-//       through distributed shared memory (few, very long rows).
-//   topk_stream_kernel  256 threads per row, several rows per SM: the first
-//       pass streams the row with 16-byte loads, later passes re-read it
-//       (from L2).
+// Kernels (dispatch in launch_topk):
+//   topk_rows_kernel   one 256-thread CTA per row, rows of up to 262144
+//       columns in 4096-key chunks.  A one-chunk row lives in registers:
+//       radix passes over registers, then ballots and per-warp counts place
+//       every selected column.  A longer row is read twice (histogram, then a
+//       pass that marks the keys above the threshold bin in a shared-memory
+//       bitmap and gathers the threshold bin's keys); the exact threshold
+//       comes from the gathered keys, and a scan of the bitmap writes the
+//       columns out.
+//   split path         few long rows (decode): every phase on a grid of
+//       (16384-key segment, row) CTAs that talk through per-row scratch.
+//   topk_stream_kernel rows longer than the others take: 256 threads per
+//       row stream the row with 16-byte loads for each pass.
 // A row whose columns are all valid and that has at most k of them is
 // written directly as lo, lo+1, ..., hi-1.
 #include "dsa_common.cuh"
@@ -43,39 +44,6 @@ __device__ __forceinline__ uint32_t order_key(float x) {
   // Negative: all bits flipped; positive: the sign bit set.
   const uint32_t key = u ^ (static_cast<uint32_t>(static_cast<int32_t>(u) >> 31) | 0x80000000u);
   return key > 0x007FFFFFu ? key : 0u;  // -inf (0x007FFFFF) -> 0
-}
-
-// ---------------------------------------------------------------- clusters
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// Every thread of every CTA of the cluster arrives and waits (release/acquire
-// ordering of shared memory across the cluster).
-__device__ __forceinline__ void cluster_barrier() {
-  asm volatile(
-      "barrier.cluster.arrive.release.aligned;\n\t"
-      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Address of `p` (this CTA's shared memory) in the shared memory of CTA `rank`.
-__device__ __forceinline__ uint32_t cluster_map(const void* p, uint32_t rank) {
-  uint32_t out;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(smem_u32(p)), "r"(rank));
-  return out;
-}
-
-__device__ __forceinline__ void cluster_add(uint32_t addr, uint32_t v) {
-  asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_load(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
 }
 
 // ------------------------------------------------------------- block scans
@@ -159,31 +127,61 @@ __device__ __forceinline__ void row_range(const TopkParams& p, int row, int* lo,
   }
 }
 
-// ------------------------------------------------------ register-resident
-
-// Histogram slots are padded by one word every 32 bins, so that a thread
-// reading a run of consecutive bins never shares a bank with its neighbours.
-__device__ __forceinline__ int hpad(int bin) { return bin + (bin >> 5); }
-constexpr int kHistSlots = kHistBins + kHistBins / 32;
-
-// find_bin over a padded histogram (see find_bin), also returning the
-// count of the selected bin.  Three barriers.
-template <int THREADS>
-__device__ __forceinline__ uint32_t find_bin_padded(const uint32_t* hist, int nbins, uint32_t r,
-                                                    uint2* warp_sums, uint32_t* sel, uint32_t* bin,
-                                                    uint32_t* above, uint32_t* count) {
-  const int per = nbins / THREADS;  // consecutive bins per thread, highest first
-  const int top = nbins - 1 - static_cast<int>(threadIdx.x) * per;
-  uint32_t local = 0;
-  for (int i = 0; i < per; ++i) local += hist[hpad(top - i)];
-  uint2 total;
-  const uint32_t excl = block_scan2<THREADS>(make_uint2(local, 0u), warp_sums, &total).x;
+// Over hist[0..NBINS) (unpadded, 16-byte aligned), the bin b holding the r-th
+// largest element, as find_bin; also that bin's count, and the sum of all bins
+// is returned.  Thread t sums the PER bins [NBINS-(t+1)*PER, NBINS-t*PER)
+// (lower threads hold higher bins); a warp scan and one exchange of warp
+// totals give each thread its exclusive prefix.  Two barriers; wsum holds
+// THREADS/32 words.
+template <int THREADS, int NBINS>
+__device__ __forceinline__ uint32_t find_bin_fast(const uint32_t* hist, uint32_t r, uint32_t* wsum,
+                                                  uint32_t* sel, uint32_t* bin, uint32_t* above,
+                                                  uint32_t* count) {
+  constexpr int PER = NBINS / THREADS;
+  constexpr int NW = THREADS / 32;
+  static_assert(PER >= 1 && NBINS % THREADS == 0, "bins per thread");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int first = NBINS - (tid + 1) * PER;
+  uint32_t v[PER];
+  if constexpr (PER % 4 == 0) {
+#pragma unroll
+    for (int j = 0; j < PER / 4; ++j) {
+      const uint4 q = reinterpret_cast<const uint4*>(hist + first)[j];
+      v[4 * j] = q.x;
+      v[4 * j + 1] = q.y;
+      v[4 * j + 2] = q.z;
+      v[4 * j + 3] = q.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < PER; ++j) v[j] = hist[first + j];
+  }
+  uint32_t local = 0u;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) local += v[j];
+  uint32_t incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  uint32_t before = 0u, total = 0u;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    const uint32_t t = wsum[w];
+    if (w < warp) before += t;
+    total += t;
+  }
+  const uint32_t excl = before + incl - local;
   if (excl < r && r <= excl + local) {
+    // One thread: walk its run again, highest bin first.
     uint32_t acc = excl;
-    for (int i = 0; i < per; ++i) {
-      const uint32_t h = hist[hpad(top - i)];
+    for (int j = PER - 1; j >= 0; --j) {
+      const uint32_t h = hist[first + j];
       if (acc + h >= r) {
-        sel[0] = static_cast<uint32_t>(top - i);
+        sel[0] = static_cast<uint32_t>(first + j);
         sel[1] = acc;
         sel[2] = h;
         break;
@@ -195,238 +193,95 @@ __device__ __forceinline__ uint32_t find_bin_padded(const uint32_t* hist, int nb
   *bin = sel[0];
   *above = sel[1];
   *count = sel[2];
-  return total.x;
+  return total;
 }
 
-template <int THREADS, int ITEMS, int CL>
-__global__ void __launch_bounds__(THREADS, 65536 / (THREADS * 64)) topk_reg_kernel(const TopkParams p) {
-  constexpr int NW = THREADS / 32;
-  constexpr int SEG = THREADS * ITEMS;  // keys per CTA
-  constexpr int WORDS = SEG / 32;
-  static_assert(kHistBins % THREADS == 0 || THREADS <= kHistBins, "bins per thread");
-  __shared__ uint32_t hist[2][kHistSlots];   // double buffer: one pass fills, the next is cleared
-  // Cluster merge targets (read on the leader), double-buffered like hist.
-  __shared__ uint32_t merged[CL > 1 ? 2 : 1][CL > 1 ? kHistSlots : 1];
-  __shared__ uint32_t gt_bits[WORDS];
-  __shared__ uint32_t eq_bits[WORDS];
-  __shared__ uint2 warp_sums[NW];
-  __shared__ uint32_t sel[4];
-  __shared__ uint32_t valid_count;
-  __shared__ uint2 cta_total;
-  __shared__ uint2 cta_base;
+// ------------------------------------------------------------ bitmap rows
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint32_t rank = CL > 1 ? cluster_rank() : 0u;
-  const int row = CL > 1 ? static_cast<int>(blockIdx.x) / CL : static_cast<int>(blockIdx.x);
-  int lo, hi;
-  row_range(p, row, &lo, &hi);
-  const int n = hi - lo;
-  const int seg0 = static_cast<int>(rank) * SEG;
-  const int mine_n = min(max(n - seg0, 0), SEG);  // keys of this CTA's segment
-  const float* src = p.logits + static_cast<int64_t>(row) * p.ld + lo + seg0;
-  int32_t* dst = p.out + static_cast<int64_t>(row) * p.k;
+// One CTA of THREADS threads per row, the row taken in chunks of THREADS*16
+// keys.  In chunk q, lane l of warp w holds the columns
+// q*CH + w*512 + g*128 + j*32 + l (g, j = 0..3): every load is a
+// warp-contiguous 128-byte line, and the ballot of the 32 lanes for (g, j)
+// is exactly the selection-bitmap word of those columns.  A row of one chunk
+// stays in registers; longer rows are read again for every pass (from L2).
+//
+//   pass 1   histogram of the top 11 key bits -> the bin b1 holding rank k;
+//   pass 2   keys above bin b1 are selected (bitmap words written by
+//            ballot); the keys of bin b1 are gathered with their columns;
+//   refine   bits 20..10, then 9..0, of the gathered keys -> tau and the
+//            number need_eq of keys == tau to take; the selected candidates
+//            are added to the bitmap (keys == tau to a second bitmap);
+//   emit     a scan over the bitmap words gives each word its output offset
+//            (keys == tau are taken in column order up to need_eq), and each
+//            word's set bits are written out in order.
+// When bin b1 holds more keys than the candidate list, digits 2 and 3 are
+// found by two more passes over the row and one pass marks the bitmaps.
+//
+// Keys map -inf, NaN and the padding slots to one value, kNoKey (0x007FFFFF,
+// the key of -inf), below every valid key (>= 0x00800000); in the first
+// digit they all land in bin 3, which is left out.
+constexpr uint32_t kNoKey = 0x007FFFFFu;
+constexpr int kChunkMax = 64;  // chunks per row: rows of up to 64 * 4096 keys
 
-  // hist[1] is cleared at the end of pass 0, before its first use.
-  for (int i = tid; i < kHistSlots; i += THREADS) {
-    hist[0][i] = 0u;
-    if (CL > 1) merged[0][i] = 0u;
-  }
-  if (tid == 0) {
-    valid_count = 0u;
-    sel[3] = 0u;
-  }
+__device__ __forceinline__ uint32_t chunk_key(float x) {
+  const float y = fmaxf(x, -INFINITY) + 0.0f;  // NaN -> -inf, -0 -> +0
+  const uint32_t u = __float_as_uint(y);
+  return u ^ (static_cast<uint32_t>(static_cast<int32_t>(u) >> 31) | 0x80000000u);
+}
 
-  // One read of the segment: element u*THREADS + tid; slots past the row end
-  // are skipped a whole item at a time.
-  uint32_t key[ITEMS];
+// Keys of chunk q for this thread: key[4g + j].
+template <int THREADS>
+__device__ __forceinline__ void load_chunk(const float* src, int n, int q, int warp, int lane,
+                                           uint32_t (&key)[16]) {
+  constexpr int CH = THREADS * 16;
+  const int c0 = q * CH + warp * 512 + lane;
+  if ((q + 1) * CH <= n) {
 #pragma unroll
-  for (int u = 0; u < ITEMS; ++u) {
-    const int e = u * THREADS + tid;
-    key[u] = 0u;
-    if (u * THREADS < mine_n && e < mine_n) key[u] = order_key(src[e]);
-  }
-  uint32_t nv = 0;
-#pragma unroll
-  for (int u = 0; u < ITEMS; ++u) nv += key[u] != 0u ? 1u : 0u;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) nv += __shfl_xor_sync(0xffffffffu, nv, o);
-  // Histograms cleared (in every CTA of the cluster, before any merge).
-  if constexpr (CL > 1) cluster_barrier(); else __syncthreads();
-  if (lane == 0 && nv) atomicAdd(&valid_count, nv);
-
-  // Pass 0 histogram of the top 11 bits (invalid keys are left out).  A row
-  // of at most k columns takes every valid key: only the count is needed.
-  if (n > p.k) {
-#pragma unroll
-    for (int u = 0; u < ITEMS; ++u) {
-      if (u * THREADS < mine_n) {
-        const uint32_t kk = key[u];
-        if (kk != 0u) atomicAdd(&hist[0][hpad(static_cast<int>(kk >> 21))], 1u);
-      }
-    }
-  }
-
-  uint32_t prefix = 0u, rem = static_cast<uint32_t>(p.k);
-  uint32_t tau = 0u, need_eq = 0u;  // take every key > tau, then the first need_eq == tau
-  uint32_t nvalid = 0u;
-#pragma unroll 1
-  for (int d = 0; d < 3; ++d) {
-    uint32_t* hcur = hist[d & 1];
-    const int nbins = d == 2 ? 1024 : 2048;
-    if (d > 0) {
-      const int shift = d == 1 ? 10 : 0;
-      const int pshift = d == 1 ? 21 : 10;
-#pragma unroll
-      for (int u = 0; u < ITEMS; ++u) {
-        if (u * THREADS < mine_n) {
-          // prefix >= 4 here (the smallest valid key is 0x00800000), so an
-          // invalid key (0) never matches.
-          const uint32_t kk = key[u];
-          if ((kk >> pshift) == prefix)
-            atomicAdd(&hcur[hpad(static_cast<int>((kk >> shift) & static_cast<uint32_t>(nbins - 1)))], 1u);
-        }
-      }
-    }
-    __syncthreads();
-    if constexpr (CL > 1) {
-      // Merge into the leader's histogram, then every CTA takes a copy.  The
-      // leader zeroes the other merge buffer for the next pass meanwhile; the
-      // second barrier orders that before anyone adds into it.
-      const uint32_t leader = cluster_map(merged[d & 1], 0);
-      for (int i = tid; i < kHistSlots; i += THREADS) {
-        const uint32_t v = hcur[i];
-        if (v) cluster_add(leader + 4u * i, v);
-      }
-      if (d == 0 && tid == 0 && valid_count) cluster_add(cluster_map(&sel[3], 0), valid_count);
-      cluster_barrier();
-      for (int i = tid; i < kHistSlots; i += THREADS) hcur[i] = cluster_load(leader + 4u * i);
-      if (d == 0 && tid == 0) valid_count = cluster_load(cluster_map(&sel[3], 0));
-      if (rank == 0)
-        for (int i = tid; i < kHistSlots; i += THREADS) merged[(d + 1) & 1][i] = 0u;
-      cluster_barrier();
-    }
-    if (d == 0) {
-      nvalid = valid_count;
-      if (nvalid <= static_cast<uint32_t>(p.k)) break;  // every valid key is taken
-    }
-    uint32_t b, above, cnt;
-    find_bin_padded<THREADS>(hcur, nbins, rem, warp_sums, sel, &b, &above, &cnt);
-    rem -= above;
-    prefix = d == 0 ? b : ((prefix << (d == 1 ? 11 : 10)) | b);
-    if (rem == cnt || d == 2) {
-      // Either the whole bin is taken (every key whose top bits are >= prefix)
-      // or the key is complete.
-      const int used = d == 0 ? 11 : (d == 1 ? 22 : 32);
-      if (d == 2) {
-        tau = prefix;
-        need_eq = rem;
-      } else {
-        tau = (prefix << (32 - used)) - 1u;
-        need_eq = 0u;
-      }
-      break;
-    }
-    // Clear the other buffer for the next pass (it held pass d-1).
-    uint32_t* hnext = hist[(d + 1) & 1];
-    for (int i = tid; i < kHistSlots; i += THREADS) hnext[i] = 0u;
-    __syncthreads();
-  }
-
-  const int nsel = nvalid < static_cast<uint32_t>(p.k) ? static_cast<int>(nvalid) : p.k;
-  if (nvalid <= static_cast<uint32_t>(p.k) && nvalid == static_cast<uint32_t>(n)) {
-    // Every column of the row is valid and taken: indices lo .. hi-1, in order.
-    for (int i = tid; i < mine_n; i += THREADS) dst[seg0 + i] = lo + seg0 + i;
+    for (int i = 0; i < 16; ++i) key[i] = chunk_key(__ldg(src + c0 + i * 32));
   } else {
-    // Ballot words: word u*NW + warp holds columns seg0 + (u*NW + warp)*32 + lane.
 #pragma unroll
-    for (int u = 0; u < ITEMS; ++u) {
-      if (u * THREADS < mine_n) {
-        const uint32_t g = __ballot_sync(0xffffffffu, key[u] > tau);
-        const uint32_t e = __ballot_sync(0xffffffffu, need_eq > 0u && key[u] == tau);
-        if (lane == 0) {
-          gt_bits[u * NW + warp] = g;
-          eq_bits[u * NW + warp] = e;
-        }
-      }
-    }
-    __syncthreads();
-    // Prefix counts over the words, in column order (each thread a run of words).
-    const int nwords = (mine_n + 31) >> 5;
-    const int per = (nwords + THREADS - 1) / THREADS;
-    const int w0 = min(tid * per, nwords), w1 = min(w0 + per, nwords);
-    uint2 mine = make_uint2(0u, 0u);
-    for (int w = w0; w < w1; ++w) {
-      mine.x += __popc(gt_bits[w]);
-      mine.y += __popc(eq_bits[w]);
-    }
-    uint2 total;
-    const uint2 before = block_scan2<THREADS>(mine, warp_sums, &total);
-    uint2 base = make_uint2(0u, 0u);
-    if constexpr (CL > 1) {
-      // Counts of the lower-ranked CTAs of the cluster come first.
-      if (tid == 0) cta_total = total;
-      cluster_barrier();
-      if (tid == 0) {
-        uint2 acc = make_uint2(0u, 0u);
-        for (uint32_t r = 0; r < rank; ++r) {
-          const uint32_t a = cluster_map(&cta_total, r);
-          acc.x += cluster_load(a);
-          acc.y += cluster_load(a + 4u);
-        }
-        cta_base = acc;
-      }
-      __syncthreads();
-      base = cta_base;
-      cluster_barrier();  // no CTA leaves while another may still read its shared memory
-    }
-    // Word prefixes (gt count, eq count) replace the ballot words in place.
-    uint32_t gp = base.x + before.x, ep = base.y + before.y;
-    for (int w = w0; w < w1; ++w) {
-      const uint32_t g = gt_bits[w], e = eq_bits[w];
-      gt_bits[w] = gp;
-      eq_bits[w] = ep;
-      gp += __popc(g);
-      ep += __popc(e);
-    }
-    __syncthreads();
-    // Every lane writes its own column: position = selected columns before it.
-    const uint32_t lt = (1u << lane) - 1u;
-#pragma unroll
-    for (int u = 0; u < ITEMS; ++u) {
-      if (u * THREADS < mine_n) {
-        const int w = u * NW + warp;
-        const uint32_t kk = key[u];
-        const bool g = kk > tau;
-        const bool e = need_eq > 0u && kk == tau;
-        const uint32_t gm = __ballot_sync(0xffffffffu, g);
-        const uint32_t em = __ballot_sync(0xffffffffu, e);
-        const uint32_t gb = gt_bits[w] + __popc(gm & lt);
-        const uint32_t eb = eq_bits[w] + __popc(em & lt);
-        const int col = lo + seg0 + u * THREADS + tid;
-        if (g) dst[gb + min(eb, need_eq)] = col;
-        else if (e && eb < need_eq) dst[gb + eb] = col;
-      }
+    for (int i = 0; i < 16; ++i) {
+      const int c = c0 + i * 32;
+      key[i] = c < n ? chunk_key(__ldg(src + c)) : kNoKey;
     }
   }
-  if (rank == 0)
-    for (int i = nsel + tid; i < p.k; i += THREADS) dst[i] = -1;
 }
 
-// ------------------------------------------------------------- short rows
+// Groups of this warp in chunk q that hold a column of the row (warp-uniform).
+template <int THREADS>
+__device__ __forceinline__ int chunk_groups(int n, int q, int warp) {
+  const int first = q * THREADS * 16 + warp * 512;
+  return min(max((n - first + 127) >> 7, 0), 4);
+}
 
-// One CTA per row of up to THREADS*ITEMS keys, held in registers.  Warp w
-// owns columns [w*32*ITEMS, (w+1)*32*ITEMS) of the row, item u of lane l
-// being column w*32*ITEMS + u*32 + l: every load is warp-contiguous, and a
-// warp meets its columns in order, so each selected column's output position
-// is a running per-warp count plus the selected columns of earlier warps.
-template <int THREADS, int ITEMS, int MINB>
-__global__ void __launch_bounds__(THREADS, MINB) topk_row_kernel(const TopkParams p) {
+// Bitmap word of (chunk q, warp, item i = 4g + j).
+template <int THREADS>
+__device__ __forceinline__ int chunk_word(int q, int warp, int i) {
+  return q * (THREADS / 2) + warp * 16 + i;
+}
+
+// Shared-memory words the kernel needs for rows of up to max_row columns and
+// a candidate list of `cand` keys.
+template <int THREADS>
+__host__ __device__ constexpr int bitmap_row_words(int max_row) {
+  return (max_row + THREADS * 16 - 1) / (THREADS * 16) * (THREADS / 2);
+}
+
+template <int THREADS, int MINB>
+__global__ void __launch_bounds__(THREADS, MINB) topk_rows_kernel(const TopkParams p, int cand_cap,
+                                                                    int words) {
   constexpr int NW = THREADS / 32;
-  constexpr int WSPAN = 32 * ITEMS;
-  __shared__ __align__(16) uint32_t hist[2][kHistSlots];
+  constexpr int CH = THREADS * 16;
+  extern __shared__ __align__(16) uint32_t smem[];
+  uint32_t* hist = smem;                        // kHistBins
+  uint32_t* cand_key = hist + kHistBins;        // cand_cap: low 21 key bits (or a 2nd histogram)
+  uint32_t* cand_col = cand_key + cand_cap;     // cand_cap: columns
+  uint32_t* sel_bits = cand_col + cand_cap;     // words
+  uint32_t* eq_bits = sel_bits + words;         // words
+  __shared__ __align__(16) uint32_t wsum[NW];
   __shared__ uint2 warp_sums[NW];
-  __shared__ uint2 warp_cnt[NW];
   __shared__ uint32_t sel[4];
+  __shared__ uint32_t ncand;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int row = blockIdx.x;
@@ -435,158 +290,309 @@ __global__ void __launch_bounds__(THREADS, MINB) topk_row_kernel(const TopkParam
   const int n = hi - lo;
   const float* src = p.logits + static_cast<int64_t>(row) * p.ld + lo;
   int32_t* dst = p.out + static_cast<int64_t>(row) * p.k;
-  const int wbase = warp * WSPAN;
-  // Items of this warp holding at least one column of the row (warp-uniform).
-  const int nit = min(max((n - wbase + 31) >> 5, 0), ITEMS);
+  const int nch = (n + CH - 1) / CH;
+  const uint32_t lt = (1u << lane) - 1u;
 
-  float x[ITEMS];
-#pragma unroll
-  for (int u = 0; u < ITEMS; ++u) {
-    const int c = wbase + u * 32 + lane;
-    x[u] = c < n ? __ldg(src + c) : -INFINITY;
-  }
-
-  uint32_t tau = 0u, need_eq = 0u;  // take every key > tau, then the first need_eq == tau
-  int nsel;
-  uint32_t key[ITEMS];
   if (n <= p.k) {
-    // Every valid key is taken: tau = 0.  All of them valid: lo, lo+1, ...
-    // (x > -inf is false for -inf and NaN alone.)
+    // Every valid key is taken; all of them valid (x > -inf is false for
+    // -inf and NaN alone): lo, lo+1, ...
     uint32_t nv = 0u;
-#pragma unroll
-    for (int u = 0; u < ITEMS; ++u) nv += x[u] > -INFINITY ? 1u : 0u;
+    for (int c = tid; c < n; c += THREADS * 2) {
+      nv += __ldg(src + c) > -INFINITY ? 1u : 0u;
+      if (c + THREADS < n) nv += __ldg(src + c + THREADS) > -INFINITY ? 1u : 0u;
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) nv += __shfl_xor_sync(0xffffffffu, nv, o);
-    if (lane == 0) warp_cnt[warp].x = nv;
+    if (lane == 0) wsum[warp] = nv;
     __syncthreads();
     uint32_t all = 0u;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) all += warp_cnt[w].x;
+    for (int w = 0; w < NW; ++w) all += wsum[w];
     if (all == static_cast<uint32_t>(n)) {
       for (int i = tid; i < p.k; i += THREADS) dst[i] = i < n ? lo + i : -1;
       return;
     }
-    nsel = static_cast<int>(all);
+  }
+
+  uint32_t key[16];
+  if (nch == 1) load_chunk<THREADS>(src, n, 0, warp, lane, key);
+
+  uint32_t tau = kNoKey, need_eq = 0u;  // keys > tau, then need_eq keys == tau
+  int nsel;
+  bool marked = false;                  // bitmaps already complete (gather path)
+  if (n <= p.k) {
+    uint32_t all = 0u;
 #pragma unroll
-    for (int u = 0; u < ITEMS; ++u) key[u] = order_key(x[u]);
-    __syncthreads();  // warp_cnt is rewritten below
+    for (int w = 0; w < NW; ++w) all += wsum[w];
+    nsel = static_cast<int>(all);  // every valid key
   } else {
+    for (int i = tid; i < kHistBins / 4; i += THREADS)
+      reinterpret_cast<uint4*>(hist)[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (tid == 0) ncand = 0u;
+    __syncthreads();
+    // Pass 1: the top 11 key bits (bin 3 collects the invalid slots).
+    for (int q = 0; q < nch; ++q) {
+      if (nch > 1) load_chunk<THREADS>(src, n, q, warp, lane, key);
+      const int ng = chunk_groups<THREADS>(n, q, warp);
 #pragma unroll
-    for (int u = 0; u < ITEMS; ++u) key[u] = order_key(x[u]);
-    for (int i = tid; i < kHistSlots / 4; i += THREADS) {
-      reinterpret_cast<uint4*>(hist[0])[i] = make_uint4(0u, 0u, 0u, 0u);
-      reinterpret_cast<uint4*>(hist[1])[i] = make_uint4(0u, 0u, 0u, 0u);
+      for (int i = 0; i < 16; ++i)
+        if (i / 4 < ng) atomicAdd(&hist[key[i] >> 21], 1u);
     }
     __syncthreads();
-    // Digit 1: the top 11 key bits (invalid keys are left out).
-#pragma unroll
-    for (int u = 0; u < ITEMS; ++u) {
-      if (u < nit) {
-        const uint32_t kk = key[u];
-        if (kk != 0u) atomicAdd(&hist[0][hpad(static_cast<int>(kk >> 21))], 1u);
-      }
-    }
-    __syncthreads();
-    uint32_t b, above, cnt;
+    // Read before the barriers of find_bin_fast, hence before any clear.
+    // Bin 3 lies below every valid bin, so rank k of a row with more than k
+    // valid keys is found above it.
+    const uint32_t invalid = hist[3];
+    uint32_t b1, above, c1;
     const uint32_t nvalid =
-        find_bin_padded<THREADS>(hist[0], kHistBins, static_cast<uint32_t>(p.k), warp_sums, sel,
-                                 &b, &above, &cnt);
+        find_bin_fast<THREADS, kHistBins>(hist, static_cast<uint32_t>(p.k), wsum, sel, &b1,
+                                          &above, &c1) - invalid;
     if (nvalid <= static_cast<uint32_t>(p.k)) {
-      nsel = static_cast<int>(nvalid);  // every valid key is taken
+      nsel = static_cast<int>(nvalid);  // every valid key
     } else {
       nsel = p.k;
       uint32_t rem = static_cast<uint32_t>(p.k) - above;
-      uint32_t prefix = b;
-      if (rem == cnt) {
-        tau = (prefix << 21) - 1u;  // the whole bin is taken
-      } else {
-        // Digit 2: bits 20..10 of the keys in bin `prefix`; hist[0] is
-        // cleared meanwhile for digit 3.
+      if (rem == c1) {
+        tau = (b1 << 21) - 1u;  // the whole bin is taken
+      } else if (nch > 2 && c1 <= static_cast<uint32_t>(cand_cap)) {
+        // Pass 2: keys above bin b1 are selected straight into the bitmap;
+        // the keys of bin b1 are gathered with their columns.
+        const uint32_t thr = ((b1 + 1u) << 21) - 1u;
+        for (int q = 0; q < nch; ++q) {
+          load_chunk<THREADS>(src, n, q, warp, lane, key);
+          const int ng = chunk_groups<THREADS>(n, q, warp);
 #pragma unroll
-        for (int u = 0; u < ITEMS; ++u) {
-          if (u < nit) {
-            const uint32_t kk = key[u];
-            if ((kk >> 21) == prefix)
-              atomicAdd(&hist[1][hpad(static_cast<int>((kk >> 10) & 2047u))], 1u);
+          for (int i = 0; i < 16; ++i) {
+            if (i / 4 >= ng) continue;  // words of later groups lie past the row
+            const uint32_t kk = key[i];
+            const uint32_t g = __ballot_sync(0xffffffffu, kk > thr);
+            if (lane == 0) {
+              sel_bits[chunk_word<THREADS>(q, warp, i)] = g;
+              eq_bits[chunk_word<THREADS>(q, warp, i)] = 0u;
+            }
+            const bool hit = (kk >> 21) == b1;
+            const uint32_t m = __ballot_sync(0xffffffffu, hit);
+            if (m) {
+              uint32_t slot = 0u;
+              if (lane == 0) slot = atomicAdd(&ncand, static_cast<uint32_t>(__popc(m)));
+              slot = __shfl_sync(0xffffffffu, slot, 0) + __popc(m & lt);
+              if (hit) {
+                cand_key[slot] = kk & 0x1FFFFFu;
+                cand_col[slot] = static_cast<uint32_t>(q * CH + warp * 512 + i * 32 + lane);
+              }
+            }
           }
         }
-        for (int i = tid; i < kHistSlots / 4; i += THREADS)
-          reinterpret_cast<uint4*>(hist[0])[i] = make_uint4(0u, 0u, 0u, 0u);
         __syncthreads();
-        find_bin_padded<THREADS>(hist[1], kHistBins, rem, warp_sums, sel, &b, &above, &cnt);
-        rem -= above;
-        prefix = (prefix << 11) | b;
-        if (rem == cnt) {
+        // Refine over the c1 gathered keys: bits 20..10, then 9..0.
+        const int nc = static_cast<int>(c1);
+        for (int i = tid; i < kHistBins / 4; i += THREADS)
+          reinterpret_cast<uint4*>(hist)[i] = make_uint4(0u, 0u, 0u, 0u);
+        __syncthreads();
+        for (int i = tid; i < nc; i += THREADS) atomicAdd(&hist[cand_key[i] >> 10], 1u);
+        __syncthreads();
+        uint32_t b2, a2, c2;
+        find_bin_fast<THREADS, kHistBins>(hist, rem, wsum, sel, &b2, &a2, &c2);
+        rem -= a2;
+        uint32_t low;  // low 21 bits of tau
+        if (rem == c2) {
+          low = (b2 << 10) - 1u;  // b2 > 0 here, since rem < c1
+        } else {
+          for (int i = tid; i < 1024 / 4; i += THREADS)
+            reinterpret_cast<uint4*>(hist)[i] = make_uint4(0u, 0u, 0u, 0u);
+          __syncthreads();
+          for (int i = tid; i < nc; i += THREADS) {
+            const uint32_t ck = cand_key[i];
+            if ((ck >> 10) == b2) atomicAdd(&hist[ck & 1023u], 1u);
+          }
+          __syncthreads();
+          uint32_t b3, a3, c3;
+          find_bin_fast<THREADS, 1024>(hist, rem, wsum, sel, &b3, &a3, &c3);
+          low = (b2 << 10) | b3;
+          need_eq = rem - a3;
+        }
+        tau = (b1 << 21) | low;
+        for (int i = tid; i < nc; i += THREADS) {
+          const uint32_t kk = (b1 << 21) | cand_key[i];
+          const uint32_t col = cand_col[i];
+          if (kk > tau) atomicOr(&sel_bits[col >> 5], 1u << (col & 31u));
+          else if (kk == tau && need_eq) atomicOr(&eq_bits[col >> 5], 1u << (col & 31u));
+        }
+        marked = true;
+      } else {
+        // Digits 2 and 3 from the keys (registers, or the row again).  The
+        // second histogram lives in the candidate space (>= 2048 words).
+        uint32_t* h2 = cand_key;
+        for (int i = tid; i < kHistBins / 4; i += THREADS)
+          reinterpret_cast<uint4*>(h2)[i] = make_uint4(0u, 0u, 0u, 0u);
+        for (int q = 0; q < nch; ++q) {
+          if (nch > 1) load_chunk<THREADS>(src, n, q, warp, lane, key);
+          const int ng = chunk_groups<THREADS>(n, q, warp);
+          __syncthreads();  // h2 cleared (first chunk)
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const uint32_t kk = key[i];
+            if (i / 4 < ng && (kk >> 21) == b1) atomicAdd(&h2[(kk >> 10) & 2047u], 1u);
+          }
+        }
+        // hist is free again: cleared for digit 3 meanwhile.
+        for (int i = tid; i < 1024 / 4; i += THREADS)
+          reinterpret_cast<uint4*>(hist)[i] = make_uint4(0u, 0u, 0u, 0u);
+        __syncthreads();
+        uint32_t b2, a2, c2;
+        find_bin_fast<THREADS, kHistBins>(h2, rem, wsum, sel, &b2, &a2, &c2);
+        rem -= a2;
+        const uint32_t prefix = (b1 << 11) | b2;
+        if (rem == c2) {
           tau = (prefix << 10) - 1u;
         } else {
-          // Digit 3: bits 9..0 of the keys with the 22-bit prefix.
+          for (int q = 0; q < nch; ++q) {
+            if (nch > 1) load_chunk<THREADS>(src, n, q, warp, lane, key);
+            const int ng = chunk_groups<THREADS>(n, q, warp);
 #pragma unroll
-          for (int u = 0; u < ITEMS; ++u) {
-            if (u < nit) {
-              const uint32_t kk = key[u];
-              if ((kk >> 10) == prefix) atomicAdd(&hist[0][hpad(static_cast<int>(kk & 1023u))], 1u);
+            for (int i = 0; i < 16; ++i) {
+              const uint32_t kk = key[i];
+              if (i / 4 < ng && (kk >> 10) == prefix) atomicAdd(&hist[kk & 1023u], 1u);
             }
           }
           __syncthreads();
-          find_bin_padded<THREADS>(hist[0], 1024, rem, warp_sums, sel, &b, &above, &cnt);
-          tau = (prefix << 10) | b;
-          need_eq = rem - above;
+          uint32_t b3, a3, c3;
+          find_bin_fast<THREADS, 1024>(hist, rem, wsum, sel, &b3, &a3, &c3);
+          tau = (prefix << 10) | b3;
+          need_eq = rem - a3;
         }
       }
     }
   }
 
-  // Per-warp counts of keys > tau (and == tau), then the ordered writes.
-  uint32_t cg = 0u, ce = 0u;
+  if (nch == 1) {
+    // One chunk, in registers: warp w owns columns [w*512, (w+1)*512) in
+    // item order; per-warp counts give each warp its output offset.
+    const int ng = chunk_groups<THREADS>(n, 0, warp);
+    uint32_t cg = 0u, ce = 0u;
 #pragma unroll
-  for (int u = 0; u < ITEMS; ++u) cg += key[u] > tau ? 1u : 0u;
-  if (need_eq != 0u) {
+    for (int i = 0; i < 16; ++i) cg += key[i] > tau ? 1u : 0u;
+    if (need_eq) {
 #pragma unroll
-    for (int u = 0; u < ITEMS; ++u) ce += key[u] == tau ? 1u : 0u;
+      for (int i = 0; i < 16; ++i) ce += key[i] == tau ? 1u : 0u;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      cg += __shfl_xor_sync(0xffffffffu, cg, o);
+      ce += __shfl_xor_sync(0xffffffffu, ce, o);
+    }
+    __syncthreads();  // every reader of warp_sums / wsum is done
+    if (lane == 0) warp_sums[warp] = make_uint2(cg, ce);
+    __syncthreads();
+    uint32_t grun = 0u, erun = 0u;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      if (w < warp) {
+        grun += warp_sums[w].x;
+        erun += warp_sums[w].y;
+      }
+    }
+    const int col0 = lo + warp * 512 + lane;
+    if (need_eq == 0u) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        if (i / 4 < ng) {
+          const bool g = key[i] > tau;
+          const uint32_t m = __ballot_sync(0xffffffffu, g);
+          if (g) dst[grun + __popc(m & lt)] = col0 + i * 32;
+          grun += __popc(m);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        if (i / 4 < ng) {
+          const bool g = key[i] > tau, e = key[i] == tau;
+          const uint32_t mg = __ballot_sync(0xffffffffu, g);
+          const uint32_t me = __ballot_sync(0xffffffffu, e);
+          const uint32_t gb = grun + __popc(mg & lt), eb = erun + __popc(me & lt);
+          if (g) dst[gb + min(eb, need_eq)] = col0 + i * 32;
+          else if (e && eb < need_eq) dst[gb + eb] = col0 + i * 32;
+          grun += __popc(mg);
+          erun += __popc(me);
+        }
+      }
+    }
+    for (int i = nsel + tid; i < p.k; i += THREADS) dst[i] = -1;
+    return;
   }
+
+  // Several chunks: bitmaps (unless the gather path filled them), then the
+  // emit.  Words of groups past the row are never read.
+  if (!marked) {
+    for (int q = 0; q < nch; ++q) {
+      load_chunk<THREADS>(src, n, q, warp, lane, key);
+      const int ng = chunk_groups<THREADS>(n, q, warp);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    cg += __shfl_xor_sync(0xffffffffu, cg, o);
-    ce += __shfl_xor_sync(0xffffffffu, ce, o);
+      for (int i = 0; i < 16; ++i) {
+        if (i / 4 < ng) {
+          const uint32_t g = __ballot_sync(0xffffffffu, key[i] > tau);
+          const uint32_t e = need_eq ? __ballot_sync(0xffffffffu, key[i] == tau) : 0u;
+          if (lane == 0) {
+            sel_bits[chunk_word<THREADS>(q, warp, i)] = g;
+            eq_bits[chunk_word<THREADS>(q, warp, i)] = e;
+          }
+        }
+      }
+    }
   }
-  if (lane == 0) warp_cnt[warp] = make_uint2(cg, ce);
   __syncthreads();
-  uint32_t grun = 0u, erun = 0u;
-#pragma unroll
-  for (int w = 0; w < NW; ++w) {
-    if (w < warp) {
-      grun += warp_cnt[w].x;
-      erun += warp_cnt[w].y;
+  // Thread t walks the words [t*per, (t+1)*per) of the row.  The columns go
+  // through shared memory (the candidate space is dead by now) when k fits,
+  // so that the global stores are coalesced.
+  uint32_t* stage = cand_key;
+  const bool staged = p.k <= 2 * cand_cap;
+  {
+    const int nwords = (n + 31) >> 5;
+    const int per = (nwords + THREADS - 1) / THREADS;
+    const int w0 = min(tid * per, nwords), w1 = min(w0 + per, nwords);
+    uint2 mine = make_uint2(0u, 0u);
+    for (int w = w0; w < w1; ++w) {
+      mine.x += __popc(sel_bits[w]);
+      mine.y += __popc(eq_bits[w]);
+    }
+    uint2 total;
+    uint2 before = block_scan2<THREADS>(mine, warp_sums, &total);
+    for (int w = w0; w < w1; ++w) {
+      const uint32_t s = sel_bits[w];
+      uint32_t e = eq_bits[w];
+      const uint32_t ecount = __popc(e);
+      if (e) {
+        // Keys == tau are taken in column order until need_eq of them.
+        const uint32_t room = need_eq > before.y ? need_eq - before.y : 0u;
+        uint32_t keep = 0u;
+        for (uint32_t t = 0; t < room && e; ++t) {
+          const uint32_t b = e & (0u - e);
+          keep |= b;
+          e ^= b;
+        }
+        e = keep;
+      }
+      uint32_t f = s | e;
+      uint32_t pos = before.x + min(before.y, need_eq);
+      while (f) {
+        const int b = __ffs(static_cast<int>(f)) - 1;
+        const int col = lo + w * 32 + b;
+        if (staged) stage[pos] = static_cast<uint32_t>(col);
+        else dst[pos] = col;
+        ++pos;
+        f &= f - 1u;
+      }
+      before.x += __popc(s);
+      before.y += ecount;
     }
   }
-  const uint32_t lt = (1u << lane) - 1u;
-  if (need_eq == 0u) {
-#pragma unroll
-    for (int u = 0; u < ITEMS; ++u) {
-      if (u < nit) {
-        const bool g = key[u] > tau;
-        const uint32_t m = __ballot_sync(0xffffffffu, g);
-        if (g) dst[grun + __popc(m & lt)] = lo + wbase + u * 32 + lane;
-        grun += __popc(m);
-      }
-    }
+  if (staged) {
+    __syncthreads();
+    for (int i = tid; i < p.k; i += THREADS) dst[i] = i < nsel ? static_cast<int>(stage[i]) : -1;
   } else {
-#pragma unroll
-    for (int u = 0; u < ITEMS; ++u) {
-      if (u < nit) {
-        const bool g = key[u] > tau, e = key[u] == tau;
-        const uint32_t mg = __ballot_sync(0xffffffffu, g);
-        const uint32_t me = __ballot_sync(0xffffffffu, e);
-        const uint32_t gb = grun + __popc(mg & lt), eb = erun + __popc(me & lt);
-        const int col = lo + wbase + u * 32 + lane;
-        if (g) dst[gb + min(eb, need_eq)] = col;
-        else if (e && eb < need_eq) dst[gb + eb] = col;
-        grun += __popc(mg);
-        erun += __popc(me);
-      }
-    }
+    for (int i = nsel + tid; i < p.k; i += THREADS) dst[i] = -1;
   }
-  for (int i = nsel + tid; i < p.k; i += THREADS) dst[i] = -1;
 }
 
 // --------------------------------------------------------------- streaming
@@ -1171,35 +1177,6 @@ __global__ void __launch_bounds__(kSegThreads, 2) topk_write_kernel(const TopkPa
   }
 }
 
-template <int THREADS, int ITEMS, int MINB>
-cudaError_t launch_row(const TopkParams& p, cudaStream_t s) {
-  topk_row_kernel<THREADS, ITEMS, MINB><<<p.R, THREADS, 0, s>>>(p);
-  return cudaGetLastError();
-}
-
-template <int THREADS, int ITEMS, int CL>
-cudaError_t launch_reg(const TopkParams& p, cudaStream_t s) {
-  auto kern = topk_reg_kernel<THREADS, ITEMS, CL>;
-  if constexpr (CL == 1) {
-    kern<<<p.R, THREADS, 0, s>>>(p);
-    return cudaGetLastError();
-  } else {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(p.R) * CL);
-    cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CL;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, p);
-  }
-}
-
 }  // namespace
 
 int topk_bitmap_words(int max_row) { return (max_row + 31) / 32; }
@@ -1209,9 +1186,6 @@ bool topk_supported(int max_row) {
                                                  2 * static_cast<size_t>(topk_bitmap_words(max_row)));
   return max_row >= 0 && stream_smem <= 232448;
 }
-
-// Longest row (in keys) the register-resident kernel takes.
-constexpr int kTopkRegMaxRow = 1024 * 32 * 8;
 
 bool topk_split_rows(int64_t rows, int64_t max_row) {
   return max_row > kSegKeys && max_row <= static_cast<int64_t>(kSplitSegs) * kSegKeys &&
@@ -1258,13 +1232,17 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t s) {
     topk_write_kernel<<<grid, kSegThreads, 0, s>>>(p);
     return cudaGetLastError();
   }
-  // Short rows: keys in registers, one CTA per row, several rows per SM.
-  if (S <= 4096) return launch_row<256, 16, 6>(p, s);
-  if (S <= 8192) return launch_row<512, 16, 3>(p, s);
-  if (S <= 16384) return launch_row<1024, 16, 1>(p, s);
-  // Very long rows without split scratch: a cluster of register-resident CTAs per row.
-  if (S > 65536 && S <= 131072) return launch_reg<1024, 32, 4>(p, s);
-  if (S > 131072 && S <= kTopkRegMaxRow) return launch_reg<1024, 32, 8>(p, s);
+  // One 256-thread CTA per row, the row in 4096-key chunks.
+  if (S <= kChunkMax * 4096) {
+    const int cand = S <= 8192 ? 2048 : 4096;
+    const int words = bitmap_row_words<256>(S);
+    const int smem = (kHistBins + 2 * cand + 2 * words) * static_cast<int>(sizeof(uint32_t));
+    cudaError_t e = cudaFuncSetAttribute(topk_rows_kernel<256, 5>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    topk_rows_kernel<256, 5><<<p.R, 256, smem, s>>>(p, cand, words);
+    return cudaGetLastError();
+  }
   // Otherwise: 256-thread CTAs that stream the row (8 rows in flight per SM).
   return launch_stream<256>(p, s);
 }
