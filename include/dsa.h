@@ -119,7 +119,7 @@ dsa_status_t dsa_indexer_logits(const void* q, const float* q_scale, const void*
  *   workspace  dsa_workspace_bytes(DSA_OP_TOPK, T, S, k) bytes, 256-byte aligned.
  *              That is 0 (workspace may be NULL) except for few long rows
  *              (T <= 512 and S > 16384), where many CTAs per row share
- *              per-row scratch there (about 73 KiB per row).
+ *              per-row scratch there (about 75 KiB per row).
  */
 dsa_status_t dsa_topk(const float* logits, int64_t ld, const int32_t* row_starts,
                       const int32_t* row_ends, int T, int S, int k, int32_t* out,
@@ -226,7 +226,7 @@ dsa_status_t dsa_indexer_topk_noalloc(const void* q, const float* q_scale, const
  * Scratch bytes an operation needs.  rows/cols are T/S for the prefill ops and
  * B*next_n / max_blocks*block_size for the paged ones; k is index_topk.  The
  * composed calls need the fp32 logits (rows * round_up(cols, 4) floats, padded
- * to 256 bytes) plus, for few long rows, the top-k scratch (about 73 KiB per
+ * to 256 bytes) plus, for few long rows, the top-k scratch (about 75 KiB per
  * row).
  * Returns 0 for operations that need none, and (size_t)-1 for bad arguments.
  */

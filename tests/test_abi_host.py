@@ -55,11 +55,11 @@ def test_workspace_bytes(api):
     assert wb(api.DSA_OP_INDEXER_TOPK, 4096, 4096, 2048) == 4096 * 4096 * 4
     assert wb(api.DSA_OP_INDEXER_TOPK, 3, 5, 1) == 256        # rows padded to 16 B, total to 256
     # few long rows: per-row scratch of the split top-k (2048-bin histogram,
-    # 16 state words, 16384 candidate keys, 3 words for each of up to 64
-    # 16384-key segments), rounded up to 64 words; it follows the logits in
-    # the composed calls
+    # 16 state words, 3 words for each of up to 256 4096-key units, 16384
+    # candidate keys), rounded up to 64 words; it follows the logits in the
+    # composed calls
     def split(rows, S):
-        words = 2048 + 16 + 16384 + 3 * 64
+        words = 2048 + 16 + 3 * 256 + 16384
         return rows * (-(-words // 64) * 64) * 4
     assert wb(api.DSA_OP_TOPK, 128, 131072, 2048) == split(128, 131072)
     assert wb(api.DSA_OP_TOPK, 4096, 131072, 2048) == 0       # many rows: no scratch

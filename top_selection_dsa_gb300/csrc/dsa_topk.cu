@@ -801,43 +801,41 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamThreads >= 1024 ? 1 : 8
 
 // ----------------------------------------------------------- split path
 //
-// Few long rows (decode): every phase runs on a grid of (16384-key segment,
-// row) CTAs, and the phases talk through per-row scratch:
-//   hist[2048]        first-digit (top 11 bits) histogram of the row's valid keys
-//   state[16]         mode, tau, need_eq, nvalid, b1, rem, completion counters, ncand
-//   cand[kSplitCand]  keys of the threshold bin b1: their low 21 bits, and the
-//                     segment they came from in the bits above
-//   seg[3*kSplitSegs] per segment: keys above the first threshold, then the
-//                     numbers of selected keys > tau and == tau in earlier segments
+// Few long rows (decode): every phase runs on a grid of (row, 4096-key unit)
+// CTAs of 256 threads, each holding its unit in registers in the chunk
+// layout of topk_rows_kernel.  The phases talk through per-row scratch:
+//   hist[2048]          first-digit histogram of the row's valid keys
+//   state[16]           mode, tau, need_eq, nvalid, b1, rem, completion
+//                       counters, ncand
+//   above[kSplitUnits]  per unit: keys above the threshold (bin b1, or tau)
+//   base[2*kSplitUnits] per unit: selected keys > tau and == tau before it
+//   cand[kSplitCand]    keys of bin b1: low 21 key bits, the unit above them
 // Only hist and state are zeroed before the first phase.  Phases (one launch
-// each):
-//   hist    segments add their histograms; the last segment CTA of a row to
-//           finish (a completion counter after a fence; nobody waits) picks
-//           the threshold bin b1 and the row's mode;
-//   gather  segments count their keys above bin b1 and append the keys of
-//           bin b1; the last one of a row refines them to the exact tau and
-//           need_eq (streaming the row when the bin holds more than
-//           kSplitCand keys) and turns the per-segment counts into the output
-//           offsets of every segment;
-//   write   each segment places its selected columns at its offsets, in
-//           column order; segment 0 writes the -1 tail.
-constexpr int kSegKeys = 16384;
-constexpr int kSegThreads = 1024;
-constexpr int kSegItems = kSegKeys / kSegThreads;  // 16
+// each, no CTA ever waits for another):
+//   hist    units add their histograms; the last unit CTA of a row to finish
+//           (a completion counter after a fence) finds bin b1 and the row's
+//           mode;
+//   gather  units count their keys above bin b1 and append the keys of bin
+//           b1; the last one of a row refines those to tau and need_eq
+//           (streaming the row when bin b1 holds more than kSplitCand keys)
+//           and turns the per-unit counts into every unit's output offsets;
+//   write   each unit places its selected columns at its offsets, in column
+//           order; unit 0 writes the -1 tail.
+constexpr int kUnitThreads = 256;
+constexpr int kUnitKeys = kUnitThreads * 16;  // 4096
+constexpr int kSplitUnits = 256;              // rows of up to 256 * 4096 keys
 constexpr int kSplitCand = 16384;
-constexpr int kSplitSegs = 64;  // rows of up to 64 * 16384 keys
 constexpr int kStateWords = 16;
-constexpr int kStHist = 0, kStState = kHistBins, kStCand = kHistBins + kStateWords,
-              kStSeg = kHistBins + kStateWords + kSplitCand,
-              kStBase = kStSeg + kSplitSegs,  // (gt, eq) offset pairs
-              kStWords = kStBase + 2 * kSplitSegs;
+constexpr int kStHist = 0, kStState = kHistBins, kStAbove = kStState + kStateWords,
+              kStBase = kStAbove + kSplitUnits, kStCand = kStBase + 2 * kSplitUnits,
+              kStWords = kStCand + kSplitCand;
 constexpr int kStZeroWords = kHistBins + kStateWords;  // zeroed before the first phase
 // state words
 constexpr int kSMode = 0, kSTau = 1, kSNeed = 2, kSValid = 3, kSB1 = 4, kSRem = 5,
               kSDoneHist = 6, kSDoneGather = 7, kSNcand = 8;
-// Rows after the first phase: every valid key taken in place (iota); the
-// exact tau known (select); the keys of bin b1 to be gathered and refined
-// (gather), or, too many of them, the row to be streamed (stream).
+// Rows after the first phase: every valid key taken in place (iota); tau
+// known (select); the keys of bin b1 to be gathered and refined (gather), or,
+// too many of them, the row to be streamed (stream).
 enum : uint32_t { kModeSelect = 1u, kModeIota = 2u, kModeGather = 3u, kModeStream = 4u };
 constexpr uint32_t kLow21 = (1u << 21) - 1u;
 
@@ -859,133 +857,108 @@ __device__ __forceinline__ bool last_to_arrive(uint32_t* counter, uint32_t total
   return last;
 }
 
-__global__ void __launch_bounds__(kSegThreads, 2) topk_hist_kernel(const TopkParams p) {
-  __shared__ uint32_t hist[kHistBins];
-  __shared__ uint2 warp_sums[kSegThreads / 32];
-  __shared__ uint32_t sel[2];
+// Programmatic dependent launch: the next kernel of the stream may start
+// once every CTA of this one has run launch_dependents; it runs
+// grid_dependency_wait (which returns once this grid has completed and its
+// writes are visible) before reading anything this grid writes.  Both are
+// no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(kUnitThreads, 5) topk_unit_hist_kernel(const TopkParams p) {
+  constexpr int NW = kUnitThreads / 32;
+  __shared__ __align__(16) uint32_t hist[kHistBins];
+  __shared__ __align__(16) uint32_t wsum[NW];
+  __shared__ uint32_t sel[4];
   __shared__ uint32_t flag;
-  const int row = blockIdx.x;
-  const int tid = threadIdx.x;
+  const int row = blockIdx.x, unit = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  launch_dependents();
   int lo, hi;
   row_range(p, row, &lo, &hi);
   const int n = hi - lo;
-  const int s0 = static_cast<int>(blockIdx.y) * kSegKeys;
-  const int cnt = min(n - s0, kSegKeys);
+  const int c0 = unit * kUnitKeys;
+  const int cnt = min(n - c0, kUnitKeys);
   uint32_t* w = split_row(p, row);
   if (cnt <= 0) {
-    if (blockIdx.y == 0 && tid == 0) {  // empty row: nothing to select
+    if (unit == 0 && tid == 0) {  // empty row: nothing to select
       w[kStState + kSMode] = kModeIota;
       w[kStState + kSValid] = 0u;
     }
     return;
   }
-  for (int i = tid; i < kHistBins; i += kSegThreads) hist[i] = 0u;
+  uint32_t key[16];
+  load_chunk<kUnitThreads>(p.logits + static_cast<int64_t>(row) * p.ld + lo + c0, cnt, 0, warp,
+                           lane, key);
+  for (int i = tid; i < kHistBins / 4; i += kUnitThreads)
+    reinterpret_cast<uint4*>(hist)[i] = make_uint4(0u, 0u, 0u, 0u);
   __syncthreads();
-  const float* src = p.logits + static_cast<int64_t>(row) * p.ld + lo + s0;
-  stream_row<kSegThreads, kSegItems>(src, cnt, cnt, [&](int, float x) {
-    const uint32_t kk = order_key(x);
-    if (kk != 0u) atomicAdd(&hist[kk >> 21], 1u);
-  });
+  const int ng = chunk_groups<kUnitThreads>(cnt, 0, warp);
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    if (i / 4 < ng) atomicAdd(&hist[key[i] >> 21], 1u);
   __syncthreads();
   uint32_t* g = w + kStHist;
-  for (int i = tid; i < kHistBins; i += kSegThreads) {
+  // Bin 3 holds the invalid slots (kNoKey) alone: it is left out.
+  for (int i = tid; i < kHistBins; i += kUnitThreads) {
     const uint32_t v = hist[i];
-    if (v) atomicAdd(&g[i], v);
+    if (v && i != 3) atomicAdd(&g[i], v);
   }
-  const uint32_t nseg = static_cast<uint32_t>((n + kSegKeys - 1) / kSegKeys);
-  if (!last_to_arrive(&w[kStState + kSDoneHist], nseg, &flag)) return;
+  const uint32_t nunits = static_cast<uint32_t>((n + kUnitKeys - 1) / kUnitKeys);
+  if (!last_to_arrive(&w[kStState + kSDoneHist], nunits, &flag)) return;
   // The row's histogram is complete: find the threshold bin once.
-  for (int i = tid; i < kHistBins; i += kSegThreads) hist[i] = __ldcg(&g[i]);
+  for (int i = tid; i < kHistBins; i += kUnitThreads) hist[i] = __ldcg(&g[i]);
   __syncthreads();
-  uint32_t b1, above;
-  const uint32_t nvalid =
-      find_bin<kSegThreads>(hist, kHistBins, static_cast<uint32_t>(p.k), warp_sums, sel, &b1, &above);
+  uint32_t b1, above, c1;
+  const uint32_t nvalid = find_bin_fast<kUnitThreads, kHistBins>(
+      hist, static_cast<uint32_t>(p.k), wsum, sel, &b1, &above, &c1);
   if (tid == 0) {
     w[kStState + kSValid] = nvalid;
     if (nvalid <= static_cast<uint32_t>(p.k)) {
-      // Every valid key is taken: tau = 0 (invalid keys are 0).
+      // Every valid key is taken: tau = kNoKey.
       w[kStState + kSMode] = nvalid == static_cast<uint32_t>(n) ? kModeIota : kModeSelect;
-      w[kStState + kSTau] = 0u;
-      w[kStState + kSNeed] = 0u;
+      w[kStState + kSTau] = kNoKey;
     } else {
       const uint32_t rem = static_cast<uint32_t>(p.k) - above;
-      const uint32_t bcnt = hist[b1];
       w[kStState + kSB1] = b1;
       w[kStState + kSRem] = rem;
-      if (rem == bcnt) {  // the whole bin is taken
+      if (rem == c1) {  // the whole bin is taken
         w[kStState + kSMode] = kModeSelect;
         w[kStState + kSTau] = (b1 << 21) - 1u;
-        w[kStState + kSNeed] = 0u;
       } else {
-        w[kStState + kSMode] = bcnt <= static_cast<uint32_t>(kSplitCand) ? kModeGather : kModeStream;
+        w[kStState + kSMode] = c1 <= static_cast<uint32_t>(kSplitCand) ? kModeGather : kModeStream;
       }
     }
   }
 }
 
-// Digits two and three of the radix select inside bin b1, over the keys
-// key_at(i) for i < n (a key outside bin b1 is skipped).  rem is the rank
-// still wanted inside bin b1.  Returns tau; *need_eq = keys == tau to take.
-// Contains barriers: every thread must call it.
-template <class KeyAt>
-__device__ __forceinline__ uint32_t refine_in_bin(uint32_t b1, uint32_t rem, uint32_t* hist,
-                                                  uint2* warp_sums, uint32_t* sel,
-                                                  uint32_t* need_eq, KeyAt&& visit) {
-  const int tid = threadIdx.x;
-  uint32_t prefix = b1;
-#pragma unroll 1
-  for (int d = 1; d < 3; ++d) {
-    const int nbins = d == 2 ? 1024 : 2048;
-    const int shift = d == 1 ? 10 : 0;
-    const int pshift = d == 1 ? 21 : 10;
-    __syncthreads();
-    for (int i = tid; i < nbins; i += kSegThreads) hist[i] = 0u;
-    __syncthreads();
-    visit([&](uint32_t kk) {
-      if ((kk >> pshift) == prefix)
-        atomicAdd(&hist[(kk >> shift) & static_cast<uint32_t>(nbins - 1)], 1u);
-    });
-    __syncthreads();
-    uint32_t b, ab;
-    find_bin<kSegThreads>(hist, nbins, rem, warp_sums, sel, &b, &ab);
-    const uint32_t c = hist[b];
-    rem -= ab;
-    prefix = (prefix << (d == 1 ? 11 : 10)) | b;
-    if (d == 1 && rem == c) {  // the whole sub-bin is taken
-      *need_eq = 0u;
-      return (prefix << 10) - 1u;
-    }
-  }
-  *need_eq = rem;
-  return prefix;
-}
-
-__global__ void __launch_bounds__(kSegThreads, 2) topk_gather_kernel(const TopkParams p) {
-  constexpr int NW = kSegThreads / 32;
-  __shared__ uint32_t hist[kHistBins];
+__global__ void __launch_bounds__(kUnitThreads, 4) topk_unit_gather_kernel(const TopkParams p) {
+  constexpr int NW = kUnitThreads / 32;
+  __shared__ __align__(16) uint32_t hist[kHistBins];
+  __shared__ __align__(16) uint32_t wsum[NW];
   __shared__ uint2 warp_sums[NW];
-  __shared__ uint32_t sel[2];
-  __shared__ uint32_t flag;
-  __shared__ uint32_t cta_hits, cta_base;
-  __shared__ uint32_t seg_gt[kSplitSegs], seg_eq[kSplitSegs];
-  extern __shared__ uint32_t cand_s[];  // kSplitCand keys: staging, then the refine's copy
-  const int row = blockIdx.x;
-  const int seg = blockIdx.y;
+  __shared__ uint32_t sel[4];
+  __shared__ uint32_t flag, cta_hits, cta_base;
+  __shared__ uint32_t stage[kUnitKeys];  // this unit's candidates
+  __shared__ uint32_t unit_gt[kSplitUnits], unit_eq[kSplitUnits];
+  const int row = blockIdx.x, unit = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int lo, hi;
   row_range(p, row, &lo, &hi);
   const int n = hi - lo;
-  const int s0 = seg * kSegKeys;
-  const int cnt = min(n - s0, kSegKeys);
+  const int c0 = unit * kUnitKeys;
+  const int cnt = min(n - c0, kUnitKeys);
+  launch_dependents();
   if (cnt <= 0) return;
   uint32_t* w = split_row(p, row);
-  const float* src = p.logits + static_cast<int64_t>(row) * p.ld + lo + s0;
-  float x[kSegItems];
-#pragma unroll
-  for (int u = 0; u < kSegItems; ++u) {
-    const int e = u * kSegThreads + tid;
-    x[u] = e < cnt ? __ldg(src + e) : -INFINITY;
-  }
+  const float* row_src = p.logits + static_cast<int64_t>(row) * p.ld + lo;
+  uint32_t key[16];
+  load_chunk<kUnitThreads>(row_src + c0, cnt, 0, warp, lane, key);
+  grid_dependency_wait();  // the histogram phase is complete
   const uint32_t mode = w[kStState + kSMode];
   if (mode == kModeIota) return;
   const uint32_t b1 = w[kStState + kSB1];
@@ -995,185 +968,226 @@ __global__ void __launch_bounds__(kSegThreads, 2) topk_gather_kernel(const TopkP
   const uint32_t want = mode == kModeGather ? b1 : 0xFFFFFFFFu;
   if (tid == 0) cta_hits = 0u;
   __syncthreads();
-  // This segment's candidates are staged in shared memory (any order), then
-  // copied to one slot range of the row's candidate list.
+  const int ng = chunk_groups<kUnitThreads>(cnt, 0, warp);
   const uint32_t lt = (1u << lane) - 1u;
-  uint32_t above = 0u;
+  uint32_t nab = 0u;
 #pragma unroll
-  for (int u = 0; u < kSegItems; ++u) {
-    const uint32_t kk = order_key(x[u]);
-    above += kk > thr ? 1u : 0u;
+  for (int i = 0; i < 16; ++i) {
+    if (i / 4 >= ng) continue;
+    const uint32_t kk = key[i];
+    nab += kk > thr ? 1u : 0u;  // kNoKey is never above thr (>= kNoKey)
     const bool hit = (kk >> 21) == want;
     const uint32_t m = __ballot_sync(0xffffffffu, hit);
     if (m) {
       uint32_t slot = 0u;
       if (lane == 0) slot = atomicAdd(&cta_hits, static_cast<uint32_t>(__popc(m)));
       slot = __shfl_sync(0xffffffffu, slot, 0) + __popc(m & lt);
-      if (hit) cand_s[slot] = (static_cast<uint32_t>(seg) << 21) | (kk & kLow21);
+      if (hit) stage[slot] = (static_cast<uint32_t>(unit) << 21) | (kk & kLow21);
     }
   }
-  // Keys above the threshold in this segment (block reduction).
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) above += __shfl_xor_sync(0xffffffffu, above, o);
-  if (lane == 0) warp_sums[warp] = make_uint2(above, 0u);
+  for (int o = 16; o > 0; o >>= 1) nab += __shfl_xor_sync(0xffffffffu, nab, o);
+  if (lane == 0) wsum[warp] = nab;
   __syncthreads();
   if (tid == 0) {
     uint32_t a = 0u;
-    for (int i = 0; i < NW; ++i) a += warp_sums[i].x;
-    w[kStSeg + seg] = a;
+#pragma unroll
+    for (int i = 0; i < NW; ++i) a += wsum[i];
+    w[kStAbove + unit] = a;
     cta_base = cta_hits ? atomicAdd(&w[kStState + kSNcand], cta_hits) : 0u;
   }
   __syncthreads();
   {
     const uint32_t nh = cta_hits, base = cta_base;
     uint32_t* cand = w + kStCand;
-    for (uint32_t i = tid; i < nh; i += kSegThreads)
-      if (base + i < static_cast<uint32_t>(kSplitCand)) cand[base + i] = cand_s[i];
+    for (uint32_t i = tid; i < nh; i += kUnitThreads)
+      if (base + i < static_cast<uint32_t>(kSplitCand)) cand[base + i] = stage[i];
   }
-  const uint32_t nseg = static_cast<uint32_t>((n + kSegKeys - 1) / kSegKeys);
-  if (!last_to_arrive(&w[kStState + kSDoneGather], nseg, &flag)) return;
+  const uint32_t nunits = static_cast<uint32_t>((n + kUnitKeys - 1) / kUnitKeys);
+  if (!last_to_arrive(&w[kStState + kSDoneGather], nunits, &flag)) return;
 
-  // Last gather CTA of the row: the exact tau / need_eq, then the offsets of
-  // every segment's selected columns.
-  for (int i = tid; i < kSplitSegs; i += kSegThreads) {
-    seg_gt[i] = 0u;
-    seg_eq[i] = 0u;
+  // Last gather CTA of the row: tau / need_eq, then the offsets of every
+  // unit's selected columns.
+  for (int i = tid; i < kSplitUnits; i += kUnitThreads) {
+    unit_gt[i] = 0u;
+    unit_eq[i] = 0u;
   }
   uint32_t tau = thr, need_eq = 0u;
-  if (mode == kModeGather) {
-    const int nc = min(static_cast<int>(__ldcg(&w[kStState + kSNcand])), kSplitCand);
+  if (mode == kModeGather || mode == kModeStream) {
+    const bool gathered = mode == kModeGather;
     const uint32_t* cand = w + kStCand;
-    for (int i = tid; i < nc; i += kSegThreads) cand_s[i] = __ldcg(&cand[i]);
-    const uint32_t hi_bits = b1 << 21;
-    tau = refine_in_bin(b1, w[kStState + kSRem], hist, warp_sums, sel, &need_eq, [&](auto&& fn) {
-      for (int i = tid; i < nc; i += kSegThreads) fn(hi_bits | (cand_s[i] & kLow21));
-    });
-    for (int i = tid; i < nc; i += kSegThreads) {
-      const uint32_t c = cand_s[i];
-      const uint32_t kk = hi_bits | (c & kLow21);
-      if (kk > tau) atomicAdd(&seg_gt[c >> 21], 1u);
-      else if (kk == tau && need_eq) atomicAdd(&seg_eq[c >> 21], 1u);
-    }
-  } else if (mode == kModeStream) {
-    const float* row_src = p.logits + static_cast<int64_t>(row) * p.ld + lo;
-    tau = refine_in_bin(b1, w[kStState + kSRem], hist, warp_sums, sel, &need_eq, [&](auto&& fn) {
-      stream_row<kSegThreads, kSegItems>(row_src, n, n, [&](int, float x) { fn(order_key(x)); });
-    });
-    stream_row<kSegThreads, kSegItems>(row_src, n, n, [&](int i, float x) {
-      const uint32_t kk = order_key(x);
-      if ((kk >> 21) == b1) {
-        if (kk > tau) atomicAdd(&seg_gt[i / kSegKeys], 1u);
-        else if (kk == tau && need_eq) atomicAdd(&seg_eq[i / kSegKeys], 1u);
+    const int nc = gathered ? min(static_cast<int>(__ldcg(&w[kStState + kSNcand])), kSplitCand) : 0;
+    const int nq = (n + kUnitKeys - 1) / kUnitKeys;
+    uint32_t rem = w[kStState + kSRem];
+    // Calls fn(low 21 bits, unit) for every key of bin b1.  Gathered keys
+    // pass through shared memory (`stage`) kUnitKeys at a time, loaded once
+    // when they all fit.
+    const bool resident = nc <= kUnitKeys;
+    auto stage_from = [&](int base) {
+      const int m = min(nc - base, kUnitKeys);
+      __syncthreads();  // earlier readers of stage are done
+      uint32_t v[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int i = tid + j * kUnitThreads;
+        v[j] = i < m ? __ldcg(&cand[base + i]) : 0u;
       }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int i = tid + j * kUnitThreads;
+        if (i < m) stage[i] = v[j];
+      }
+      __syncthreads();
+    };
+    if (gathered && resident) stage_from(0);
+    auto for_each_in_bin = [&](auto&& fn) {
+      if (gathered) {
+        for (int base = 0; base < nc; base += kUnitKeys) {
+          if (!resident) stage_from(base);
+          const int m = min(nc - base, kUnitKeys);
+          for (int i = tid; i < m; i += kUnitThreads) {
+            const uint32_t c = stage[i];
+            fn(c & kLow21, c >> 21);
+          }
+        }
+      } else {
+        for (int q = 0; q < nq; ++q) {
+          load_chunk<kUnitThreads>(row_src, n, q, warp, lane, key);
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if ((key[i] >> 21) == b1) fn(key[i] & kLow21, static_cast<uint32_t>(q));
+        }
+      }
+    };
+    __syncthreads();
+    for (int i = tid; i < kHistBins / 4; i += kUnitThreads)
+      reinterpret_cast<uint4*>(hist)[i] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    for_each_in_bin([&](uint32_t low, uint32_t) { atomicAdd(&hist[low >> 10], 1u); });
+    __syncthreads();
+    uint32_t b2, a2, c2;
+    find_bin_fast<kUnitThreads, kHistBins>(hist, rem, wsum, sel, &b2, &a2, &c2);
+    rem -= a2;
+    uint32_t low;
+    if (rem == c2) {
+      low = (b2 << 10) - 1u;  // b2 > 0 here, since rem < c1
+    } else {
+      for (int i = tid; i < 1024 / 4; i += kUnitThreads)
+        reinterpret_cast<uint4*>(hist)[i] = make_uint4(0u, 0u, 0u, 0u);
+      __syncthreads();
+      for_each_in_bin([&](uint32_t lw, uint32_t) {
+        if ((lw >> 10) == b2) atomicAdd(&hist[lw & 1023u], 1u);
+      });
+      __syncthreads();
+      uint32_t b3, a3, c3;
+      find_bin_fast<kUnitThreads, 1024>(hist, rem, wsum, sel, &b3, &a3, &c3);
+      low = (b2 << 10) | b3;
+      need_eq = rem - a3;
+    }
+    tau = (b1 << 21) | low;
+    for_each_in_bin([&](uint32_t lw, uint32_t u) {
+      const uint32_t kk = (b1 << 21) | lw;
+      if (kk > tau) atomicAdd(&unit_gt[u], 1u);
+      else if (kk == tau && need_eq) atomicAdd(&unit_eq[u], 1u);
     });
   }
   __syncthreads();
-  if (warp == 0) {
-    // Exclusive prefix sums over the (at most 64) segments, two per lane.
-    uint32_t g[2], e[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int s = h * 32 + lane;
-      g[h] = s < static_cast<int>(nseg) ? __ldcg(&w[kStSeg + s]) + seg_gt[s] : 0u;
-      e[h] = s < static_cast<int>(nseg) ? seg_eq[s] : 0u;
-    }
-    uint32_t carry_g = 0u, carry_e = 0u;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      uint32_t ig = g[h], ie = e[h];
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t a = __shfl_up_sync(0xffffffffu, ig, o);
-        const uint32_t b = __shfl_up_sync(0xffffffffu, ie, o);
-        if (lane >= o) {
-          ig += a;
-          ie += b;
-        }
-      }
-      const int s = h * 32 + lane;
-      if (s < static_cast<int>(nseg)) {
-        w[kStBase + 2 * s] = carry_g + ig - g[h];
-        w[kStBase + 2 * s + 1] = carry_e + ie - e[h];
-      }
-      carry_g += __shfl_sync(0xffffffffu, ig, 31);
-      carry_e += __shfl_sync(0xffffffffu, ie, 31);
-    }
-    if (lane == 0) {
-      w[kStState + kSTau] = tau;
-      w[kStState + kSNeed] = need_eq;
-      w[kStState + kSMode] = kModeSelect;
-    }
+  // Exclusive prefix over the units (at most kSplitUnits = kUnitThreads).
+  uint2 mine = make_uint2(0u, 0u);
+  if (tid < static_cast<int>(nunits))
+    mine = make_uint2(__ldcg(&w[kStAbove + tid]) + unit_gt[tid], unit_eq[tid]);
+  uint2 total;
+  const uint2 before = block_scan2<kUnitThreads>(mine, warp_sums, &total);
+  if (tid < static_cast<int>(nunits)) {
+    w[kStBase + 2 * tid] = before.x;
+    w[kStBase + 2 * tid + 1] = before.y;
+  }
+  if (tid == 0) {
+    w[kStState + kSTau] = tau;
+    w[kStState + kSNeed] = need_eq;
+    w[kStState + kSMode] = kModeSelect;
   }
 }
 
-__global__ void __launch_bounds__(kSegThreads, 2) topk_write_kernel(const TopkParams p) {
-  constexpr int NW = kSegThreads / 32;
-  constexpr int WORDS = kSegKeys / 32;  // 512
-  // Word u*NW + warp covers segment columns (u*NW + warp)*32 + lane: the
-  // ballots of (key > tau) and (key == tau), then the number of selected
-  // columns before the word (this segment's offsets included).
-  __shared__ uint32_t gt_bits[WORDS], eq_bits[WORDS];
-  __shared__ uint32_t gt_pre[WORDS], eq_pre[WORDS];
-  __shared__ uint2 warp_sums[NW];
-  const int row = blockIdx.x;
-  const int seg = blockIdx.y;
+__global__ void __launch_bounds__(kUnitThreads, 5) topk_unit_write_kernel(const TopkParams p) {
+  constexpr int NW = kUnitThreads / 32;
+  __shared__ uint2 warp_cnt[NW];
+  const int row = blockIdx.x, unit = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int lo, hi;
   row_range(p, row, &lo, &hi);
+  const int n = hi - lo;
   const uint32_t* w = split_row(p, row);
   int32_t* dst = p.out + static_cast<int64_t>(row) * p.k;
-  if (seg == 0) {
+  const int c0 = unit * kUnitKeys;
+  const int cnt = min(n - c0, kUnitKeys);
+  uint32_t key[16];
+  if (cnt > 0)
+    load_chunk<kUnitThreads>(p.logits + static_cast<int64_t>(row) * p.ld + lo + c0, cnt, 0, warp,
+                             lane, key);
+  grid_dependency_wait();  // the gather phase is complete
+  if (unit == 0) {
     const uint32_t nvalid = w[kStState + kSValid];
     const int nsel = nvalid < static_cast<uint32_t>(p.k) ? static_cast<int>(nvalid) : p.k;
-    for (int i = nsel + tid; i < p.k; i += kSegThreads) dst[i] = -1;
+    for (int i = nsel + tid; i < p.k; i += kUnitThreads) dst[i] = -1;
   }
-  const int s0 = seg * kSegKeys;
-  const int cnt = min(hi - lo - s0, kSegKeys);
   if (cnt <= 0) return;
-  const float* src = p.logits + static_cast<int64_t>(row) * p.ld + lo + s0;
-  float x[kSegItems];
-#pragma unroll
-  for (int u = 0; u < kSegItems; ++u) {
-    const int e = u * kSegThreads + tid;
-    x[u] = e < cnt ? __ldg(src + e) : -INFINITY;
-  }
   const uint32_t mode = w[kStState + kSMode];
   if (mode == kModeIota) {
-    for (int i = tid; i < cnt; i += kSegThreads) dst[s0 + i] = lo + s0 + i;
+    for (int i = tid; i < cnt; i += kUnitThreads) dst[c0 + i] = lo + c0 + i;
     return;
   }
   const uint32_t tau = w[kStState + kSTau], need_eq = w[kStState + kSNeed];
+  const int ng = chunk_groups<kUnitThreads>(cnt, 0, warp);
+  uint32_t cg = 0u, ce = 0u;
 #pragma unroll
-  for (int u = 0; u < kSegItems; ++u) {
-    const uint32_t kk = order_key(x[u]);
-    const uint32_t g = __ballot_sync(0xffffffffu, kk > tau);
-    const uint32_t e = need_eq ? __ballot_sync(0xffffffffu, kk == tau) : 0u;
-    if (lane == 0) {
-      gt_bits[u * NW + warp] = g;
-      eq_bits[u * NW + warp] = e;
+  for (int i = 0; i < 16; ++i) cg += key[i] > tau ? 1u : 0u;
+  if (need_eq) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) ce += key[i] == tau ? 1u : 0u;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    cg += __shfl_xor_sync(0xffffffffu, cg, o);
+    ce += __shfl_xor_sync(0xffffffffu, ce, o);
+  }
+  if (lane == 0) warp_cnt[warp] = make_uint2(cg, ce);
+  __syncthreads();
+  // Selected columns of earlier units, then of earlier warps, come first.
+  uint32_t grun = w[kStBase + 2 * unit], erun = w[kStBase + 2 * unit + 1];
+#pragma unroll
+  for (int i = 0; i < NW; ++i) {
+    if (i < warp) {
+      grun += warp_cnt[i].x;
+      erun += warp_cnt[i].y;
     }
   }
-  __syncthreads();
-  uint2 mine = make_uint2(0u, 0u);
-  if (tid < WORDS) mine = make_uint2(__popc(gt_bits[tid]), __popc(eq_bits[tid]));
-  uint2 total;
-  const uint2 before = block_scan2<kSegThreads>(mine, warp_sums, &total);
-  if (tid < WORDS) {
-    gt_pre[tid] = w[kStBase + 2 * seg] + before.x;
-    eq_pre[tid] = w[kStBase + 2 * seg + 1] + before.y;
-  }
-  __syncthreads();
-  const uint32_t bit = 1u << lane, lt = bit - 1u;
-#pragma unroll 4
-  for (int u = 0; u < kSegItems; ++u) {
-    const int wd = u * NW + warp;
-    const uint32_t gm = gt_bits[wd], em = eq_bits[wd];
-    if ((gm | em) == 0u) continue;  // nothing selected in these 32 columns
-    const uint32_t gb = gt_pre[wd] + __popc(gm & lt);
-    const uint32_t eb = eq_pre[wd] + __popc(em & lt);
-    const int col = lo + s0 + u * kSegThreads + tid;
-    if (gm & bit) dst[gb + min(eb, need_eq)] = col;
-    else if ((em & bit) && eb < need_eq) dst[gb + eb] = col;
+  const uint32_t lt = (1u << lane) - 1u;
+  const int col0 = lo + c0 + warp * 512 + lane;
+  if (need_eq == 0u) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i / 4 < ng) {
+        const bool g = key[i] > tau;
+        const uint32_t m = __ballot_sync(0xffffffffu, g);
+        if (g) dst[grun + __popc(m & lt)] = col0 + i * 32;
+        grun += __popc(m);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i / 4 < ng) {
+        const bool g = key[i] > tau, e = key[i] == tau;
+        const uint32_t mg = __ballot_sync(0xffffffffu, g);
+        const uint32_t me = __ballot_sync(0xffffffffu, e);
+        const uint32_t gb = grun + __popc(mg & lt), eb = erun + __popc(me & lt);
+        if (g) dst[gb + min(eb, need_eq)] = col0 + i * 32;
+        else if (e && eb < need_eq) dst[gb + eb] = col0 + i * 32;
+        grun += __popc(mg);
+        erun += __popc(me);
+      }
+    }
   }
 }
 
@@ -1188,7 +1202,7 @@ bool topk_supported(int max_row) {
 }
 
 bool topk_split_rows(int64_t rows, int64_t max_row) {
-  return max_row > kSegKeys && max_row <= static_cast<int64_t>(kSplitSegs) * kSegKeys &&
+  return max_row > 16384 && max_row <= static_cast<int64_t>(kSplitUnits) * kUnitKeys &&
          rows <= 512;
 }
 
@@ -1214,23 +1228,33 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t s) {
   if (p.R <= 0) return cudaSuccess;
   const int S = p.S;
   if (p.split) {
-    // Few long rows: every phase on (segment, row) grids, see the split path.
+    // Few long rows: every phase on (row, unit) grids, see the split path.
     // Only each row's histogram and state words start at zero.
     cudaError_t e = cudaMemset2DAsync(p.split, static_cast<size_t>(p.split_words) * sizeof(uint32_t),
                                       0, kStZeroWords * sizeof(uint32_t),
                                       static_cast<size_t>(p.R), s);
     if (e != cudaSuccess) return e;
-    const int gather_smem = kSplitCand * static_cast<int>(sizeof(uint32_t));
-    e = cudaFuncSetAttribute(topk_gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             gather_smem);
+    // Rows vary fastest: every row's first unit is scheduled before any
+    // second one, and the empty tail units of short rows come last.
+    const dim3 grid(static_cast<unsigned>(p.R), (S + kUnitKeys - 1) / kUnitKeys);
+    topk_unit_hist_kernel<<<grid, kUnitThreads, 0, s>>>(p);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    // Rows vary fastest: every row's first segment is scheduled before any
-    // second one, and the empty tail segments of short rows come last.
-    const dim3 grid(static_cast<unsigned>(p.R), (S + kSegKeys - 1) / kSegKeys);
-    topk_hist_kernel<<<grid, kSegThreads, 0, s>>>(p);
-    topk_gather_kernel<<<grid, kSegThreads, gather_smem, s>>>(p);
-    topk_write_kernel<<<grid, kSegThreads, 0, s>>>(p);
-    return cudaGetLastError();
+    // The later phases start early (their loads overlap the previous
+    // phase's tail) and wait for it in hardware before reading its results.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kUnitThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, topk_unit_gather_kernel, p);
+    if (e != cudaSuccess) return e;
+    return cudaLaunchKernelEx(&cfg, topk_unit_write_kernel, p);
   }
   // One 256-thread CTA per row, the row in 4096-key chunks.
   if (S <= kChunkMax * 4096) {
