@@ -481,6 +481,29 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
         re_s[i] = hi;
       }
       asm volatile("bar.sync 1, %0;" ::"r"(C::EPI_THREADS) : "memory");
+      // This thread's row ranges, kept in registers for the whole group.
+      int rlo[C::EPI_TOK], rhi[C::EPI_TOK];
+#pragma unroll
+      for (int j = 0; j < C::EPI_TOK; ++j) {
+        rlo[j] = rs_s[wg * C::EPI_TOK + j];
+        rhi[j] = re_s[wg * C::EPI_TOK + j];
+      }
+      // e4m3, H >= 16: this thread's EPI_COLS weights live in registers for
+      // the whole group, and the accumulator is read 8 columns at a time, so
+      // that the epilogue leaves shared-memory bandwidth to the MMA operand
+      // reads (an e4m3 tile takes half the MMA time of a bf16 one).
+      constexpr bool kRegW = kFp8 && H >= 16 && C::NPART == 8;
+      float wr[kRegW ? C::EPI_COLS : 1];
+      if constexpr (kRegW) {
+#pragma unroll
+        for (int i = 0; i < C::EPI_COLS / 4; ++i) {
+          const float4 w4 = reinterpret_cast<const float4*>(w_s + wg * C::EPI_COLS)[i];
+          wr[4 * i] = w4.x;
+          wr[4 * i + 1] = w4.y;
+          wr[4 * i + 2] = w4.z;
+          wr[4 * i + 3] = w4.w;
+        }
+      }
 
       // fp8: this thread's key scale, loaded one tile ahead of its use.
       auto key_scale = [&](int kt) -> float {
@@ -514,18 +537,64 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
         ok = __all_sync(0xffffffffu, mbar_wait_bounded(&accf[buf], aphase, abort_flag) ? 1 : 0);
         if (!ok) break;
         tc_fence_after_sync();
-        float v[C::EPI_COLS];
-        tmem_load_cols<C::EPI_COLS>(
-            tmem_base + lane_addr + static_cast<uint32_t>(buf * N + wg * C::EPI_COLS), v);
-        tc_fence_before_sync();
-        mbar_arrive(&acce[buf]);
-
+        const uint32_t tcol =
+            tmem_base + lane_addr + static_cast<uint32_t>(buf * N + wg * C::EPI_COLS);
         const int s = kt * C::TILE + key_in_tile;
         const float kscale = ks_next;
         if constexpr (kFp8) {
           if (kt + C::EPI_SETS < g.kt_end) ks_next = key_scale(kt + C::EPI_SETS);
         }
         const bool col_ok = s < p.S;
+        if constexpr (kRegW) {
+#pragma unroll
+          for (int j = 0; j < C::EPI_TOK; ++j) {
+            const int tok = wg * C::EPI_TOK + j;
+            // Heads in pairs: one packed FMA per pair, partial h % 8 taking its
+            // heads in ascending order (the same sums as the path below).
+            float2 part2[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) part2[i] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int c = 0; c < H / 8; ++c) {
+              float v[8];
+              tmem_load8(tcol + static_cast<uint32_t>(j * H + c * 8), v);
+              if (j == C::EPI_TOK - 1 && c == H / 8 - 1) {
+                // Every column of this tile is in registers: release it.
+                tc_fence_before_sync();
+                mbar_arrive(&acce[buf]);
+              }
+#pragma unroll
+              for (int hh = 0; hh < 8; hh += 2) {
+                const int h = c * 8 + hh;
+                const float2 y2 = make_float2(relu_term(h, v[hh]), relu_term(h + 1, v[hh + 1]));
+                const float2 w2 = make_float2(wr[j * H + h], wr[j * H + h + 1]);
+                part2[(h % 8) / 2] = __ffma2_rn(w2, y2, part2[(h % 8) / 2]);
+              }
+            }
+            float part[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              part[2 * i] = part2[i].x;
+              part[2 * i + 1] = part2[i].y;
+            }
+#pragma unroll
+            for (int w = 4; w > 0; w >>= 1) {
+#pragma unroll
+              for (int i = 0; i < w; ++i) part[i] = part[i] + part[i + w];
+            }
+            float acc = part[0];
+            if constexpr (kFp8) acc *= kscale;
+            if (tok < g.ntok && col_ok) {
+              const float val = (s >= rlo[j] && s < rhi[j]) ? acc : -INFINITY;
+              p.logits[static_cast<int64_t>(g.row0 + tok) * p.ld + s] = val;
+            }
+          }
+          continue;
+        }
+        float v[C::EPI_COLS];
+        tmem_load_cols<C::EPI_COLS>(tcol, v);
+        tc_fence_before_sync();
+        mbar_arrive(&acce[buf]);
 #pragma unroll
         for (int j = 0; j < C::EPI_TOK; ++j) {
           const int tok = wg * C::EPI_TOK + j;
@@ -535,15 +604,22 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
           for (int i = 0; i < C::NPART; ++i) part[i] = 0.f;
           if constexpr (C::NPART == 8) {
             // Heads in pairs: one packed FMA per pair, same partials and order.
+            // Weights come four at a time (one 16-byte shared load), which
+            // halves the epilogue's share of the shared-memory bandwidth the
+            // MMAs read their operands through.
             float2 part2[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) part2[i] = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int h = 0; h < H; h += 2) {
-              const float2 w2 = *reinterpret_cast<const float2*>(wt + h);
-              const float2 y2 = make_float2(relu_term(h, v[j * H + h]),
-                                            relu_term(h + 1, v[j * H + h + 1]));
-              part2[(h % 8) / 2] = __ffma2_rn(w2, y2, part2[(h % 8) / 2]);
+            for (int h = 0; h < H; h += 4) {
+              const float4 w4 = *reinterpret_cast<const float4*>(wt + h);
+              const float2 y2a = make_float2(relu_term(h, v[j * H + h]),
+                                             relu_term(h + 1, v[j * H + h + 1]));
+              const float2 y2b = make_float2(relu_term(h + 2, v[j * H + h + 2]),
+                                             relu_term(h + 3, v[j * H + h + 3]));
+              part2[(h % 8) / 2] = __ffma2_rn(make_float2(w4.x, w4.y), y2a, part2[(h % 8) / 2]);
+              part2[(h % 8) / 2 + 1] =
+                  __ffma2_rn(make_float2(w4.z, w4.w), y2b, part2[(h % 8) / 2 + 1]);
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -563,7 +639,7 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
           float acc = part[0];
           if constexpr (kFp8) acc *= kscale;
           if (tok < g.ntok && col_ok) {
-            const float val = (s >= rs_s[tok] && s < re_s[tok]) ? acc : -INFINITY;
+            const float val = (s >= rlo[j] && s < rhi[j]) ? acc : -INFINITY;
             p.logits[static_cast<int64_t>(g.row0 + tok) * p.ld + s] = val;
           }
         }
