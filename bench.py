@@ -78,6 +78,17 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def launches_per_step(p):
+    """This library's kernel launches in one step: the scoring kernel, then one
+    top-k kernel, or three (histogram, gather, write) when the top-k takes its
+    split path -- at most 512 rows, some row longer than 16384 columns and
+    none longer than 1048576 (the rule of topk_split_rows in dsa_topk.cu)."""
+    rows = p.T if hasattr(p, "row_starts") else p.R
+    cols = p.S if hasattr(p, "row_starts") else p.max_ctx()
+    split = rows <= 512 and 16384 < cols <= 256 * 4096
+    return 1 + (3 if split else 1)
+
+
 def kernel_sha():
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
@@ -469,7 +480,7 @@ def run_ours(args):
                     "topk_gbs": topk_bytes / (t_ms / 1e3) / 1e9,
                     "topk_hbm_frac": topk_bytes / (t_ms / 1e3) / 1e9 / peaks["hbm_gbs"]},
         "roofline": roof,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": launches_per_step(p) * args.steps,
         "wall_s_timed_region": wall,
     }
     if e2e is not None:
