@@ -42,6 +42,12 @@
  *    from a later call, or from dsa_get_last_device_error().
  *  - No C++ exception crosses this boundary.  All entry points are safe to
  *    call from several host threads at once.
+ *  - CUDA graphs: once an entry point has run on a device (its first call
+ *    looks up per-device state), its calls can be captured into a CUDA graph.
+ *    A capture fixes the shapes (rows, key capacity, k) and the pointers;
+ *    row ranges, context lengths, block tables and the inputs themselves are
+ *    read when the graph runs, so one graph serves every step of a decode
+ *    loop.  dsa_get_last_device_error synchronises and is not capturable.
  */
 #ifndef DSA_H_
 #define DSA_H_

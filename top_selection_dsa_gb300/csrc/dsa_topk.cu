@@ -196,6 +196,18 @@ __device__ __forceinline__ uint32_t find_bin_fast(const uint32_t* hist, uint32_t
   return total;
 }
 
+// Programmatic dependent launch: the next kernel of the stream may start
+// once every CTA of this one has run launch_dependents; it runs
+// grid_dependency_wait (which returns once this grid has completed and its
+// writes are visible) before reading anything this grid writes.  Both are
+// no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------------------ bitmap rows
 
 // One CTA of THREADS threads per row, the row taken in chunks of THREADS*16
@@ -292,6 +304,9 @@ __global__ void __launch_bounds__(THREADS, MINB) topk_rows_kernel(const TopkPara
   int32_t* dst = p.out + static_cast<int64_t>(row) * p.k;
   const int nch = (n + CH - 1) / CH;
   const uint32_t lt = (1u << lane) - 1u;
+  // Launched as a programmatic dependent of the kernel that wrote the logits
+  // (when there is one): everything above overlaps its tail.
+  grid_dependency_wait();
 
   if (n <= p.k) {
     // Every valid key is taken; all of them valid (x > -inf is false for
@@ -857,18 +872,6 @@ __device__ __forceinline__ bool last_to_arrive(uint32_t* counter, uint32_t total
   return last;
 }
 
-// Programmatic dependent launch: the next kernel of the stream may start
-// once every CTA of this one has run launch_dependents; it runs
-// grid_dependency_wait (which returns once this grid has completed and its
-// writes are visible) before reading anything this grid writes.  Both are
-// no-ops for a kernel launched without the attribute.
-__device__ __forceinline__ void launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void grid_dependency_wait() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
 __global__ void __launch_bounds__(kUnitThreads, 5) topk_unit_hist_kernel(const TopkParams p) {
   constexpr int NW = kUnitThreads / 32;
   __shared__ __align__(16) uint32_t hist[kHistBins];
@@ -1264,8 +1267,17 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(topk_rows_kernel<256, 5>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    topk_rows_kernel<256, 5><<<p.R, 256, smem, s>>>(p, cand, words);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.R));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, topk_rows_kernel<256, 5>, p, cand, words);
   }
   // Otherwise: 256-thread CTAs that stream the row (8 rows in flight per SM).
   return launch_stream<256>(p, s);
