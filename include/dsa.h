@@ -229,6 +229,28 @@ dsa_status_t dsa_indexer_topk_noalloc(const void* q, const float* q_scale, const
                                       int topk, int32_t* out, dsa_stream_t stream);
 
 /*
+ * Reorders top-k rows in place into descending order of score: the order of
+ * torch.topk, which torch_dsa_topk (vime PR #502, third review comment)
+ * returns, where every other entry point here writes ascending column order.
+ * Equal scores keep the lower column first (-0.0 equals +0.0), -inf and NaN
+ * scores (which no top-k entry point selects) come after the others, and the
+ * -1 padding stays at the tail.  The pages fix no order for a consumer; this
+ * is the optional score-sorted output.
+ *
+ *   logits  [T, ld] fp32, the scores the indices refer to.  After
+ *           dsa_indexer_topk or dsa_indexer_topk_paged they are still at the
+ *           start of that call's workspace, with ld = round_up(S, 4) or
+ *           round_up(max_blocks * block_size, 4), until it is reused.
+ *   topk    [T, k] int32, read and rewritten.  An entry outside [0, ld) other
+ *           than -1 is treated as padding (written back as -1, its column is
+ *           never read) and reported by dsa_get_last_device_error as
+ *           DSA_ERR_INVALID_ARG.
+ *   k       1 .. 8192 (larger k: DSA_ERR_UNSUPPORTED)
+ */
+dsa_status_t dsa_topk_sort_by_score(const float* logits, int64_t ld, int32_t* topk, int T, int k,
+                                    dsa_stream_t stream);
+
+/*
  * Scratch bytes an operation needs.  rows/cols are T/S for the prefill ops and
  * B*next_n / max_blocks*block_size for the paged ones; k is index_topk.  The
  * composed calls need the fp32 logits (rows * round_up(cols, 4) floats, padded
@@ -245,7 +267,8 @@ const char* dsa_status_string(dsa_status_t status);
  * Synchronises the current device, then reports and clears the sticky
  * device-side error word of the current device: DSA_ERR_TIMEOUT when a
  * kernel's bounded wait gave up since the last call, DSA_ERR_INVALID_ARG when
- * a paged call met a block id or context length out of range, DSA_ERR_CUDA
+ * a paged call met a block id or context length out of range (or
+ * dsa_topk_sort_by_score an index outside its row), DSA_ERR_CUDA
  * when the synchronisation itself failed, else DSA_OK.
  */
 dsa_status_t dsa_get_last_device_error(void);

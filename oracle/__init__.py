@@ -17,6 +17,7 @@ Functions:
     paged_row_ranges()   the row ranges of paged decode
     topk(...)            masked per-row top-k of given fp32 logits
                          (torch_dsa_topk, vime PR #502, third review comment)
+    sort_by_score(...)   a top-k index buffer in descending score order
     bf16_to_f64 / e4m3_to_f64   element decoders
 """
 from __future__ import annotations
@@ -205,4 +206,28 @@ def topk(logits_f32, row_starts, row_ends, k, *, S=None, nthreads=0) -> np.ndarr
                                  _ptr(out), nthreads)
     if rc != 0:
         raise ValueError("oracle topk: bad arguments")
+    return out
+
+
+def sort_by_score(logits_f32, topk_idx) -> np.ndarray:
+    """Rows of a top-k index buffer [T, k] in descending order of their score.
+
+    torch_dsa_topk (vime PR #502, third review comment) takes torch.topk,
+    whose indices come in descending order of value; the library's canonical
+    output is ascending column order instead, and this puts a row back into
+    score order.  Reading where the page is silent: equal scores keep
+    ascending column order (-0.0 equals +0.0), -inf and NaN scores (which
+    no top-k selects) count as equal and lowest, and the -1 padding stays at
+    the tail.  Plain numpy: one stable two-key sort per row.
+    """
+    lg = np.asarray(logits_f32, dtype=np.float32)
+    idx = np.asarray(topk_idx, dtype=np.int32)
+    out = np.full_like(idx, -1)
+    for t in range(idx.shape[0]):
+        cols = idx[t][idx[t] >= 0]
+        v = lg[t, cols].astype(np.float64)
+        v = np.where(np.isnan(v) | (v == -np.inf), -np.inf, v)
+        v = np.where(v == 0.0, 0.0, v)                 # -0.0 -> +0.0
+        order = np.lexsort((cols, -v))                  # score descending, then column ascending
+        out[t, :cols.size] = cols[order]
     return out

@@ -164,3 +164,16 @@ def test_binding_refuses_cpu_tensors(api):
     r = torch.zeros(4, dtype=torch.int32)
     with pytest.raises(ValueError):
         api.indexer_logits(q, k, w, r, r)
+
+
+def test_topk_sort_by_score_validation(api):
+    E, U = api.DSA_ERR_INVALID_ARG, api.DSA_ERR_UNSUPPORTED
+    f = api.lib.dsa_topk_sort_by_score
+    assert f(NUL, 8, A, 4, 2, NUL) == E
+    assert f(A, 8, NUL, 4, 2, NUL) == E
+    assert f(A, 8, A, -1, 2, NUL) == E
+    assert f(A, 8, A, 4, 0, NUL) == E
+    assert f(A, 0, A, 4, 2, NUL) == E
+    assert f(ctypes.c_void_p(0x10002), 8, A, 4, 2, NUL) == E     # logits not 4-byte aligned
+    assert f(A, 8, A, 4, 8193, NUL) == U                         # k above the sort's limit
+    assert f(A, 8, A, 0, 2, NUL) == api.DSA_OK                   # nothing to do, nothing launched

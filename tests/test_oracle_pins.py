@@ -396,3 +396,45 @@ def test_topk_closed_forms():
     assert oracle.topk(const, rs, re, 5)[0].tolist() == [10, 11, 12, 13, 14]
     assert oracle.topk(inc, rs, re, 80)[0].tolist() == list(range(10, 90))
     assert oracle.topk(inc, rs, re, 83)[0].tolist() == list(range(10, 90)) + [-1] * 3
+
+
+# ------------------------------------------------------------ score order
+
+def test_sort_by_score_hand_example():
+    # torch.topk's order (vime PR #502, torch_dsa_topk): descending value;
+    # equal values keep the lower column first, -0.0 equals +0.0, and the -1
+    # padding stays at the tail.
+    lg = np.array([[1.0, 3.0, 2.0, 3.0, -0.0, 0.0]], np.float32)
+    assert oracle.sort_by_score(lg, np.array([[0, 1, 2, 3, 4, 5]], np.int32)).tolist() == \
+        [[1, 3, 2, 0, 4, 5]]
+    assert oracle.sort_by_score(lg, np.array([[5, 4, 2, -1, -1]], np.int32)).tolist() == \
+        [[2, 4, 5, -1, -1]]
+    # -inf and NaN (never selected by a top-k) are equal and lowest.
+    lg2 = np.array([[np.nan, -np.inf, 1.0, np.nan, 2.0]], np.float32)
+    assert oracle.sort_by_score(lg2, np.array([[0, 1, 2, 3, 4]], np.int32)).tolist() == \
+        [[4, 2, 0, 1, 3]]
+
+
+def test_sort_by_score_values_match_torch_topk():
+    # The sorted scores are exactly torch.topk's (sorted=True) values; the
+    # order among equal scores is checked by the invariant below.
+    rng = np.random.default_rng(5)
+    for _ in range(20):
+        S, k = int(rng.integers(5, 300)), int(rng.integers(1, 40))
+        lg = rng.standard_normal((3, S)).astype(np.float32)
+        lg[:, rng.integers(0, S, size=S // 4)] = np.round(lg[:, :S // 4], 1)  # ties
+        rs = np.zeros(3, np.int32)
+        re_ = np.full(3, S, np.int32)
+        top = oracle.topk(lg, rs, re_, k)
+        srt = oracle.sort_by_score(lg, top)
+        for t in range(3):
+            n = int((srt[t] >= 0).sum())
+            want = torch.topk(torch.from_numpy(lg[t]), n).values.numpy()
+            assert np.array_equal(lg[t, srt[t, :n]], want)
+            # the same set of columns, padding at the tail
+            assert sorted(srt[t, :n].tolist()) == sorted(top[t][top[t] >= 0].tolist())
+            assert (srt[t, n:] == -1).all()
+            # equal scores in ascending column order
+            v, c = lg[t, srt[t, :n]], srt[t, :n]
+            assert all(v[i] > v[i + 1] or (v[i] == v[i + 1] and c[i] < c[i + 1])
+                       for i in range(n - 1))

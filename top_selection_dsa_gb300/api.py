@@ -28,6 +28,7 @@ EXPORTS = (
     "dsa_indexer_logits", "dsa_topk", "dsa_indexer_topk", "dsa_indexer_logits_paged",
     "dsa_indexer_topk_paged", "dsa_workspace_bytes", "dsa_status_string",
     "dsa_get_last_device_error", "dsa_selftest_wait_timeout", "dsa_indexer_topk_noalloc",
+    "dsa_topk_sort_by_score",
 )
 
 
@@ -58,9 +59,11 @@ def _load():
     lib.dsa_status_string.restype = ctypes.c_char_p
     lib.dsa_get_last_device_error.argtypes = []
     lib.dsa_selftest_wait_timeout.argtypes = [U64, P]
+    lib.dsa_topk_sort_by_score.argtypes = [P, I64, P, I, I, P]
     for name in ("dsa_indexer_logits", "dsa_topk", "dsa_indexer_topk",
                  "dsa_indexer_logits_paged", "dsa_indexer_topk_paged",
-                 "dsa_get_last_device_error", "dsa_selftest_wait_timeout"):
+                 "dsa_get_last_device_error", "dsa_selftest_wait_timeout",
+                 "dsa_topk_sort_by_score"):
         getattr(lib, name).restype = I
     return lib
 
@@ -239,6 +242,23 @@ def indexer_topk_paged(q, weights, k_cache, block_table, context_lens, topk_k, *
                                     _ptr(out), _ptr(ws), nbytes, _stream(dev))
     _check(st, "dsa_indexer_topk_paged")
     return out
+
+
+def topk_sort_by_score(logits, topk_idx):
+    """Rows of a top-k index buffer [T, k] reordered in place into descending
+    score order (ties to the lower column, -1 padding at the tail)."""
+    dev = topk_idx.device
+    _need(logits, "logits", (torch.float32,), dev)
+    _need(topk_idx, "topk_idx", (torch.int32,), dev)
+    if logits.dim() != 2 or topk_idx.dim() != 2 or logits.shape[0] != topk_idx.shape[0]:
+        raise ValueError("logits [T, ld] and topk_idx [T, k] expected")
+    if logits.stride(1) != 1 or not topk_idx.is_contiguous():
+        raise ValueError("row-major logits and a contiguous topk_idx expected")
+    T, k = topk_idx.shape
+    st = lib.dsa_topk_sort_by_score(_ptr(logits), logits.stride(0), _ptr(topk_idx), T, k,
+                                    _stream(dev))
+    _check(st, "dsa_topk_sort_by_score")
+    return topk_idx
 
 
 def last_device_error() -> int:

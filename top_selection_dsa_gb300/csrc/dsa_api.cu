@@ -415,6 +415,15 @@ dsa_status_t dsa_indexer_topk_paged(const void* q, const float* q_scale, const f
                   split_scratch(workspace, R, max_ctx));
 }
 
+dsa_status_t dsa_topk_sort_by_score(const float* logits, int64_t ld, int32_t* topk, int T, int k,
+                                    dsa_stream_t stream) {
+  if (!logits || !topk || T < 0 || k < 1 || ld < 1) return DSA_ERR_INVALID_ARG;
+  if (!aligned(logits, 4) || !aligned(topk, 4)) return DSA_ERR_INVALID_ARG;
+  if (k > kTopkSortMax) return DSA_ERR_UNSUPPORTED;
+  if (T == 0) return DSA_OK;
+  return from_cuda(launch_topk_sort(logits, ld, topk, T, k, error_word(), as_stream(stream)));
+}
+
 size_t dsa_workspace_bytes(dsa_op_t op, int64_t rows, int64_t cols, int k) {
   if (rows < 0 || cols < 0 || k < 0) return static_cast<size_t>(-1);
   switch (op) {

@@ -79,6 +79,11 @@ bool topk_split_rows(int64_t rows, int64_t max_row);
 int topk_split_words(int64_t max_row);
 cudaError_t launch_fill(float* dst, int64_t rows, int64_t cols, int64_t ld, float value,
                         cudaStream_t s);
+// Rows of k top-k indices reordered by descending score in place (k <=
+// kTopkSortMax); indices outside [0, ld) are treated as padding and recorded.
+constexpr int kTopkSortMax = 8192;
+cudaError_t launch_topk_sort(const float* logits, int64_t ld, int32_t* topk, int T, int k,
+                             uint32_t* err, cudaStream_t s);
 cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint64_t timeout_ns, cudaStream_t s);
 
 }  // namespace dsa

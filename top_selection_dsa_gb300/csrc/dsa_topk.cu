@@ -1194,6 +1194,61 @@ __global__ void __launch_bounds__(kUnitThreads, 5) topk_unit_write_kernel(const 
   }
 }
 
+// ------------------------------------------------------------- score order
+//
+// torch_dsa_topk takes torch.topk, whose indices come in descending order of
+// score; the canonical output here is ascending column order.  This pass
+// puts each row back into score order: one CTA per row sorts 64-bit
+// composites (score key << 32 | ~column) descending with a bitonic network in
+// shared memory, so that equal scores keep the lower column first and the
+// -1 padding (composite 0) stays at the tail.
+constexpr int kSortThreads = 256;
+
+__global__ void __launch_bounds__(kSortThreads) topk_sort_kernel(const float* __restrict__ logits,
+                                                                 int64_t ld, int32_t* topk, int k,
+                                                                 int n, uint32_t* err) {
+  extern __shared__ __align__(16) unsigned long long sk[];  // n = k rounded up to a power of two
+  const int row = blockIdx.x, tid = threadIdx.x;
+  int32_t* r = topk + static_cast<int64_t>(row) * k;
+  const float* lg = logits + static_cast<int64_t>(row) * ld;
+  bool bad = false;
+  for (int i = tid; i < n; i += kSortThreads) {
+    unsigned long long v = 0ull;
+    if (i < k) {
+      const int c = r[i];
+      if (c >= 0 && c < ld) {
+        // Invalid scores (-inf, NaN) get key 0: after every valid one.
+        const uint32_t key = order_key(__ldg(lg + c));
+        v = (static_cast<unsigned long long>(key) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(c));
+      } else if (c >= 0) {
+        bad = true;  // past the row: treated as padding, never read
+      }
+    }
+    sk[i] = v;
+  }
+  if (bad) record_error(err, kErrBadIndex);
+  __syncthreads();
+  for (int size = 2; size <= n; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = tid; i < n / 2; i += kSortThreads) {
+        const int a = 2 * i - (i & (stride - 1));
+        const int b = a + stride;
+        const bool desc = (a & size) == 0;
+        const unsigned long long x = sk[a], y = sk[b];
+        if ((x < y) == desc) {
+          sk[a] = y;
+          sk[b] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = tid; i < k; i += kSortThreads) {
+    const unsigned long long v = sk[i];
+    r[i] = v ? static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(v)) : -1;
+  }
+}
+
 }  // namespace
 
 int topk_bitmap_words(int max_row) { return (max_row + 31) / 32; }
@@ -1281,6 +1336,19 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t s) {
   }
   // Otherwise: 256-thread CTAs that stream the row (8 rows in flight per SM).
   return launch_stream<256>(p, s);
+}
+
+cudaError_t launch_topk_sort(const float* logits, int64_t ld, int32_t* topk, int T, int k,
+                             uint32_t* err, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  int n = 1;
+  while (n < k) n <<= 1;
+  const int smem = n * static_cast<int>(sizeof(unsigned long long));
+  cudaError_t e = cudaFuncSetAttribute(topk_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       smem);
+  if (e != cudaSuccess) return e;
+  topk_sort_kernel<<<T, kSortThreads, smem, s>>>(logits, ld, topk, k, n, err);
+  return cudaGetLastError();
 }
 
 }  // namespace dsa
