@@ -56,6 +56,10 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="prefill_causal",
                     choices=("prefill_causal", "prefill_thd", "prefill_fp8", "paged_decode",
                              "tiny_causal"))
+    ap.add_argument("--prologue", action="store_true",
+                    help="time the steps before the indexer (query quantisation + weight "
+                         "fold, key LayerNorm + e4m3 paged insert) at the e4m3 workload's "
+                         "sizes instead of the hot path; one JSON line per step")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true",
@@ -495,10 +499,75 @@ def run_ours(args):
     return 0
 
 
+def run_prologue(args):
+    """The two steps before the indexer, each timed alone with CUDA events on
+    inputs in HBM (L2 flushed before every step), against the measured HBM
+    copy bandwidth: bytes = every input read once + every output written."""
+    import torch
+    from top_selection_dsa_gb300 import api
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    T, H, D = (args.tokens or 32768), 64, 128
+    g = torch.Generator(device=device)
+    g.manual_seed(0)
+    q = (torch.randn((T, H, D), device=device, generator=g) / D ** 0.5).to(torch.bfloat16)
+    w = torch.randn((T, H), device=device, generator=g) / 8
+    q8 = torch.empty((T, H, D), dtype=torch.uint8, device=device)
+    wo = torch.empty((T, H), dtype=torch.float32, device=device)
+    k = (torch.randn((T, D), device=device, generator=g) * 0.5).to(torch.bfloat16)
+    gamma = torch.ones(D, device=device)
+    beta = torch.zeros(D, device=device)
+    bs = 64
+    nb = (T + bs - 1) // bs
+    slots = torch.randperm(nb * bs, device=device, generator=g)[:T].to(torch.int64)
+    cache = torch.empty((nb, bs, D), dtype=torch.uint8, device=device)
+    scale = torch.empty(nb * bs, dtype=torch.float32, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    ws = float(D ** -0.5 * H ** -0.5)
+    ops = {
+        "q_quant_fold_weights": (lambda: api.q_quant_fold_weights(q, w, ws, H, q_fp8=q8,
+                                                                  weights_out=wo),
+                                 T * H * (D * 2 + 4 + D + 4)),
+        "k_norm_quant_insert": (lambda: api.k_norm_quant_insert(k, gamma, beta, 1e-6, slots,
+                                                                cache, scale),
+                                T * (D * 2 + 8 + D + 4) + 2 * D * 4),
+    }
+    peaks, src = measured_peaks()
+    stream = torch.cuda.current_stream(device)
+    for name, (fn, nbytes) in ops.items():
+        for _ in range(args.warmup):
+            flush.zero_()
+            fn()
+        times = []
+        for _ in range(args.steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+        ms = statistics.median(times)
+        gbs = nbytes / (ms / 1e3) / 1e9
+        print(json.dumps({"metric": f"{name} GB/s vs HBM (before the indexer)", "value": gbs,
+                          "unit": "GB/s", "ms_per_step": ms, "steps": args.steps,
+                          "warmup": args.warmup, "higher_is_better": True,
+                          "config": {"tokens": T, "H": H, "D": D, "bytes_per_step": nbytes,
+                                     "l2": "flushed before every step"},
+                          "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                                       "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                                       "peak_source": f"{src} hbm copy"}}))
+    if api.last_device_error() != api.DSA_OK:
+        raise RuntimeError("device error word set")
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.prologue:
+        return run_prologue(args)
     return run_ours(args)
 
 

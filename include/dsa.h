@@ -251,6 +251,52 @@ dsa_status_t dsa_topk_sort_by_score(const float* logits, int64_t ld, int32_t* to
                                     dsa_stream_t stream);
 
 /*
+ * The query side of the e4m3 path, before dsa_indexer_logits / _topk /
+ * _topk_paged: indexer_q_quant_fold_weights of KimiK3DSAIndexer.score (vLLM
+ * API docs, "vllm.models.kimi_k3.nvidia.dsa").  Every (t, h) row of D query
+ * elements becomes e4m3 codes with one UE8M0 scale s (the smallest power of
+ * two with max|q[t,h,:]| <= 448 s; 1 for an all-zero row), codes = q / s
+ * rounded to nearest even; the scale is folded into the weight,
+ * weights_out[t,h] = fl32(fl32(weights[t,h] * weight_scale) * s), so the
+ * scoring calls take q_scale = NULL.  Heads H .. padded_heads-1 get zero codes
+ * and zero weights (the page pads to 32 or 64 index heads).
+ *
+ *   q            [T, H, D] bf16, 16-byte aligned
+ *   weights      [T, H] fp32
+ *   weight_scale the page's index_softmax_scale * indexer_weight_scale
+ *   q_fp8        [T, padded_heads, D] e4m3 output, 8-byte aligned
+ *   weights_out  [T, padded_heads] fp32 output
+ *   D = 128, H <= padded_heads <= 64 (else DSA_ERR_UNSUPPORTED)
+ */
+dsa_status_t dsa_q_quant_fold_weights(const void* q, const float* weights, float weight_scale,
+                                      int T, int H, int D, int padded_heads, void* q_fp8,
+                                      float* weights_out, dsa_stream_t stream);
+
+/*
+ * The key side: indexer_k_norm_quant_insert of KimiK3DSAIndexer._fused_k_insert
+ * with KimiK3DSAIndexerKNorm (same page).  Every new key row goes through the
+ * bias-full LayerNorm in fp32 -- (k - mean) / sqrt(var + eps) * ln_weight +
+ * ln_bias, population variance -- is cast back to bf16, and is written to
+ * row slot_mapping[t] of the paged cache (block slot / block_size, row
+ * slot % block_size): as bf16 (DSA_BF16), or as e4m3 codes with one UE8M0
+ * scale per row like the query side (DSA_E4M3, scale to k_scale[slot]).
+ *
+ *   k            [T, D] bf16 new keys, 16-byte aligned
+ *   ln_weight, ln_bias  [D] fp32, 16-byte aligned
+ *   slot_mapping [T] int64: a slot below 0 marks a padding token (skipped);
+ *                a slot >= num_blocks * block_size is skipped and reported
+ *                by dsa_get_last_device_error as DSA_ERR_INVALID_ARG
+ *   k_cache      [num_blocks, block_size, D] of cache_dtype, the layout
+ *                dsa_indexer_logits_paged reads
+ *   k_scale      [num_blocks * block_size] fp32 for DSA_E4M3, NULL for bf16
+ *   D = 128 (else DSA_ERR_UNSUPPORTED)
+ */
+dsa_status_t dsa_k_norm_quant_insert(const void* k, const float* ln_weight, const float* ln_bias,
+                                     float eps, const int64_t* slot_mapping, int T, int D,
+                                     dsa_dtype_t cache_dtype, void* k_cache, float* k_scale,
+                                     int num_blocks, int block_size, dsa_stream_t stream);
+
+/*
  * Scratch bytes an operation needs.  rows/cols are T/S for the prefill ops and
  * B*next_n / max_blocks*block_size for the paged ones; k is index_topk.  The
  * composed calls need the fp32 logits (rows * round_up(cols, 4) floats, padded
@@ -268,7 +314,8 @@ const char* dsa_status_string(dsa_status_t status);
  * device-side error word of the current device: DSA_ERR_TIMEOUT when a
  * kernel's bounded wait gave up since the last call, DSA_ERR_INVALID_ARG when
  * a paged call met a block id or context length out of range (or
- * dsa_topk_sort_by_score an index outside its row), DSA_ERR_CUDA
+ * dsa_topk_sort_by_score an index outside its row, or
+ * dsa_k_norm_quant_insert a slot past the cache), DSA_ERR_CUDA
  * when the synchronisation itself failed, else DSA_OK.
  */
 dsa_status_t dsa_get_last_device_error(void);

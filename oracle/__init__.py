@@ -18,6 +18,9 @@ Functions:
     topk(...)            masked per-row top-k of given fp32 logits
                          (torch_dsa_topk, vime PR #502, third review comment)
     sort_by_score(...)   a top-k index buffer in descending score order
+    f64_to_e4m3()        E4M3 encoder (nearest, ties to even, saturating)
+    q_quant_fold(...)    query quantisation + weight fold (before the indexer)
+    k_norm_insert(...)   key LayerNorm + quantisation + paged insert
     bf16_to_f64 / e4m3_to_f64   element decoders
 """
 from __future__ import annotations
@@ -77,6 +80,13 @@ def _load():
         lib.dsa_oracle_logits_paged.restype = i32
         lib.dsa_oracle_topk.argtypes = [P, i64, P, P, i64, i64, i32, P, i32]
         lib.dsa_oracle_topk.restype = i32
+        lib.dsa_oracle_f64_to_e4m3.argtypes = [ctypes.c_double]
+        lib.dsa_oracle_f64_to_e4m3.restype = ctypes.c_uint8
+        lib.dsa_oracle_q_quant_fold.argtypes = [P, P, ctypes.c_float, i32, i32, i32, i32, P, P]
+        lib.dsa_oracle_q_quant_fold.restype = i32
+        lib.dsa_oracle_k_norm_insert.argtypes = [P, P, P, ctypes.c_float, P, i32, i32, i32, i64,
+                                                 P, P]
+        lib.dsa_oracle_k_norm_insert.restype = i32
         lib.dsa_oracle_max_threads.argtypes = []
         lib.dsa_oracle_max_threads.restype = i32
         _lib = lib
@@ -231,3 +241,42 @@ def sort_by_score(logits_f32, topk_idx) -> np.ndarray:
         order = np.lexsort((cols, -v))                  # score descending, then column ascending
         out[t, :cols.size] = cols[order]
     return out
+
+
+def f64_to_e4m3(values) -> np.ndarray:
+    """E4M3 codes of the given values (uint8): the nearest code, ties to even."""
+    lib = _load()
+    v = np.asarray(values, dtype=np.float64).ravel()
+    return np.array([lib.dsa_oracle_f64_to_e4m3(float(x)) for x in v], dtype=np.uint8)
+
+
+def q_quant_fold(q_bf16_bits, weights, weight_scale, padded_heads):
+    """q [T,H,D] bf16 bits -> (e4m3 codes [T,Hp,D], folded weights [T,Hp])."""
+    q = np.ascontiguousarray(q_bf16_bits).view(np.uint16)
+    T, H, D = q.shape
+    w = _c(weights, np.float32)
+    q8 = np.empty((T, padded_heads, D), np.uint8)
+    wo = np.empty((T, padded_heads), np.float32)
+    rc = _load().dsa_oracle_q_quant_fold(_ptr(q), _ptr(w), float(weight_scale), T, H, D,
+                                         padded_heads, _ptr(q8), _ptr(wo))
+    if rc != 0:
+        raise ValueError("oracle q_quant_fold: bad arguments")
+    return q8, wo
+
+
+def k_norm_insert(k_bf16_bits, ln_weight, ln_bias, eps, slots, cache, scale=None):
+    """LayerNorm + cast to bf16 (+ e4m3 quantisation when scale is given) of
+    k [T,D] bf16 bits into cache [num_blocks, block_size, D] (uint16 bf16
+    bits, or uint8 e4m3 codes with scale [num_blocks*block_size]), in place."""
+    k = np.ascontiguousarray(k_bf16_bits).view(np.uint16)
+    T, D = k.shape
+    g, b = _c(ln_weight, np.float32), _c(ln_bias, np.float32)
+    sl = _c(slots, np.int64)
+    assert cache.flags.c_contiguous and (scale is None or scale.flags.c_contiguous)
+    dtype = 0 if scale is None else 1
+    capacity = cache.shape[0] * cache.shape[1]
+    rc = _load().dsa_oracle_k_norm_insert(_ptr(k), _ptr(g), _ptr(b), float(eps), _ptr(sl), T, D,
+                                          dtype, capacity, _ptr(cache), _ptr(scale))
+    if rc != 0:
+        raise ValueError("oracle k_norm_insert: bad arguments")
+    return cache, scale

@@ -373,3 +373,158 @@ int dsa_oracle_max_threads(void)
     return 1;
 #endif
 }
+
+/* ------------------------------------------------------------- prologue
+ *
+ * The two steps just before the indexer on [vLLM-dsa]:
+ *   - KimiK3DSAIndexer.score: indexer_q_quant_fold_weights(index_q,
+ *     index_weights, weight_scale, padded_index_num_heads) -- the query rows
+ *     quantised to e4m3 with one UE8M0 scale each, the scale and weight_scale
+ *     folded into the head weights, heads padded with zeros;
+ *   - KimiK3DSAIndexer._fused_k_insert + KimiK3DSAIndexerKNorm:
+ *     indexer_k_norm_quant_insert -- F.layer_norm(x.float(), (D,), weight,
+ *     bias, eps).type_as(x) (fp32 LayerNorm, cast back to bf16), then the
+ *     row quantised like the query and written to its slot of the paged
+ *     cache.
+ * The pages show only the calls.  Readings: the UE8M0 scale of a row is the
+ * smallest power of two s with max|x| <= 448 s (s = 1 for an all-zero row);
+ * codes are x / s rounded to the nearest E4M3 value, ties to the even code,
+ * saturating at 448; the folded weight is fl32(fl32(w * weight_scale) * s);
+ * a negative slot is a padding token; the LayerNorm uses the population
+ * variance.  The LayerNorm itself is computed here in double precision and
+ * rounded once to bf16 (the pages fix fp32; results agree to within one bf16
+ * step, which the tests allow). */
+
+/* Nearest E4M3 code to v per [OCP-FP8]: the positive codes 0x00..0x7E are
+ * decoded and searched for the closest value; an exact tie goes to the even
+ * code (mantissa LSB 0); magnitudes above 448 saturate to 0x7E.  The sign
+ * bit follows v's sign bit (so -0.0 -> 0x80).  v must not be NaN. */
+uint8_t dsa_oracle_f64_to_e4m3(double v)
+{
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs(v);
+    int best = 0;
+    double best_d = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {
+        double d = fabs(dsa_oracle_e4m3_to_f64((uint8_t)c) - a);
+        if (d < best_d || (d == best_d && (c & 1) == 0)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return (uint8_t)(sign | best);
+}
+
+/* Exponent e of the UE8M0 scale 2^e: smallest integer with amax <= 448 * 2^e. */
+static int ue8m0_exp(double amax)
+{
+    if (!(amax > 0.0))
+        return 0;
+    int e = -160;
+    while (amax > 448.0 * ldexp(1.0, e))
+        ++e;
+    return e;
+}
+
+/* v rounded once to bf16 (the upper half of a binary32): of the two bf16
+ * values around |v|, the nearer one, ties to the even one; v's sign kept. */
+static uint16_t f64_to_bf16_rne(double v)
+{
+    double a = fabs(v);
+    float fa = (float)a;
+    uint32_t u;
+    memcpy(&u, &fa, sizeof u);
+    uint32_t lo = u & 0xFFFF0000u;          /* a bf16 value at or near a */
+    float flo;
+    memcpy(&flo, &lo, sizeof flo);
+    if ((double)flo > a)                    /* fa was rounded up onto a bf16 value */
+        lo -= 0x10000u;
+    uint32_t hi = lo + 0x10000u;
+    float f_lo, f_hi;
+    memcpy(&f_lo, &lo, sizeof f_lo);
+    memcpy(&f_hi, &hi, sizeof f_hi);
+    double dl = a - (double)f_lo, dh = (double)f_hi - a;
+    uint32_t r = dl < dh ? lo : (dh < dl ? hi : (((lo >> 16) & 1u) ? hi : lo));
+    return (uint16_t)((r >> 16) | (signbit(v) ? 0x8000u : 0u));
+}
+
+/* q [T,H,D] bf16 -> q8 [T,Hp,D] e4m3 codes and w_out [T,Hp] fp32. */
+int dsa_oracle_q_quant_fold(const uint16_t* q, const float* w, float weight_scale, int T, int H,
+                            int D, int Hp, uint8_t* q8, float* w_out)
+{
+    if (!q || !w || !q8 || !w_out || T < 0 || H < 1 || Hp < H || D < 1)
+        return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int h = 0; h < Hp; ++h) {
+            uint8_t* dst = q8 + (t * Hp + h) * D;
+            if (h >= H) {
+                memset(dst, 0, (size_t)D);
+                w_out[t * Hp + h] = 0.0f;
+                continue;
+            }
+            const uint16_t* src = q + (t * H + h) * D;
+            double amax = 0.0;
+            for (int d = 0; d < D; ++d) {
+                double x = fabs(dsa_oracle_bf16_to_f64(src[d]));
+                if (x > amax)
+                    amax = x;
+            }
+            int e = ue8m0_exp(amax);
+            for (int d = 0; d < D; ++d)
+                dst[d] = dsa_oracle_f64_to_e4m3(ldexp(dsa_oracle_bf16_to_f64(src[d]), -e));
+            float wf = w[t * H + h] * weight_scale;          /* fl32(w * weight_scale) */
+            w_out[t * Hp + h] = (float)((double)wf * ldexp(1.0, e));
+        }
+    }
+    return 0;
+}
+
+/* k [T,D] bf16 -> LayerNorm -> bf16 -> the cache row at slots[t].
+ * dtype 0: cache holds bf16 (uint16) rows; 1: e4m3 codes + scale[slot]. */
+int dsa_oracle_k_norm_insert(const uint16_t* k, const float* gamma, const float* beta, float eps,
+                             const int64_t* slots, int T, int D, int dtype, int64_t capacity,
+                             void* cache, float* scale)
+{
+    if (!k || !gamma || !beta || !slots || !cache || T < 0 || D < 1 || (dtype == 1 && !scale))
+        return -1;
+    double* y = (double*)malloc(sizeof(double) * (size_t)D);
+    if (!y)
+        return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        int64_t slot = slots[t];
+        if (slot < 0 || slot >= capacity)
+            continue;
+        const uint16_t* src = k + t * D;
+        double mean = 0.0, var = 0.0;
+        for (int d = 0; d < D; ++d)
+            mean += dsa_oracle_bf16_to_f64(src[d]);
+        mean /= D;
+        for (int d = 0; d < D; ++d) {
+            double c = dsa_oracle_bf16_to_f64(src[d]) - mean;
+            var += c * c;
+        }
+        var /= D;
+        double rstd = 1.0 / sqrt(var + (double)eps);
+        for (int d = 0; d < D; ++d) {
+            double v = (dsa_oracle_bf16_to_f64(src[d]) - mean) * rstd * gamma[d] + beta[d];
+            y[d] = dsa_oracle_bf16_to_f64(f64_to_bf16_rne(v));   /* .type_as(x) */
+        }
+        if (dtype == 0) {
+            uint16_t* dst = (uint16_t*)cache + slot * D;
+            for (int d = 0; d < D; ++d)
+                dst[d] = f64_to_bf16_rne(y[d]);
+        } else {
+            uint8_t* dst = (uint8_t*)cache + slot * D;
+            double amax = 0.0;
+            for (int d = 0; d < D; ++d)
+                if (fabs(y[d]) > amax)
+                    amax = fabs(y[d]);
+            int e = ue8m0_exp(amax);
+            for (int d = 0; d < D; ++d)
+                dst[d] = dsa_oracle_f64_to_e4m3(ldexp(y[d], -e));
+            scale[slot] = (float)ldexp(1.0, e);
+        }
+    }
+    free(y);
+    return 0;
+}

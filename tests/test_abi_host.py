@@ -177,3 +177,21 @@ def test_topk_sort_by_score_validation(api):
     assert f(ctypes.c_void_p(0x10002), 8, A, 4, 2, NUL) == E     # logits not 4-byte aligned
     assert f(A, 8, A, 4, 8193, NUL) == U                         # k above the sort's limit
     assert f(A, 8, A, 0, 2, NUL) == api.DSA_OK                   # nothing to do, nothing launched
+
+
+def test_prologue_validation(api):
+    E, U = api.DSA_ERR_INVALID_ARG, api.DSA_ERR_UNSUPPORTED
+    f = api.lib.dsa_q_quant_fold_weights
+    assert f(NUL, A, 1.0, 4, 64, 128, 64, A, A, NUL) == E
+    assert f(A, A, 1.0, 4, 64, 128, 32, A, A, NUL) == E          # padded_heads < H
+    assert f(MIS, A, 1.0, 4, 64, 128, 64, A, A, NUL) == E        # q not 16-byte aligned
+    assert f(A, A, 1.0, 4, 64, 64, 64, A, A, NUL) == U           # D != 128
+    assert f(A, A, 1.0, 4, 16, 128, 128, A, A, NUL) == U         # more than 64 heads
+    g = api.lib.dsa_k_norm_quant_insert
+    B16, E8 = api.DSA_BF16, api.DSA_E4M3
+    assert g(NUL, A, A, 1e-6, A, 4, 128, B16, A, NUL, 8, 64, NUL) == E
+    assert g(A, A, A, 1e-6, A, 4, 128, E8, A, NUL, 8, 64, NUL) == E    # e4m3 needs scales
+    assert g(A, A, A, 1e-6, A, 4, 128, B16, A, A, 8, 64, NUL) == E     # bf16 takes none
+    assert g(A, A, A, -1.0, A, 4, 128, B16, A, NUL, 8, 64, NUL) == E   # eps < 0
+    assert g(A, A, A, 1e-6, A, 4, 128, B16, A, NUL, 0, 64, NUL) == E   # no blocks
+    assert g(A, A, A, 1e-6, A, 4, 64, B16, A, NUL, 8, 64, NUL) == U    # D != 128

@@ -438,3 +438,95 @@ def test_sort_by_score_values_match_torch_topk():
             v, c = lg[t, srt[t, :n]], srt[t, :n]
             assert all(v[i] > v[i + 1] or (v[i] == v[i + 1] and c[i] < c[i + 1])
                        for i in range(n - 1))
+
+
+# -------------------------------------------------- prologue (q quant, K insert)
+
+def test_e4m3_encoder_round_trip_and_ties():
+    # Every finite code decodes and encodes back to itself ([OCP-FP8]).
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
+    vals = oracle.e4m3_to_f64(codes)
+    assert np.array_equal(oracle.f64_to_e4m3(vals), codes)
+    # Midpoints between neighbouring positive codes go to the even code.
+    pos = np.arange(0, 0x7E, dtype=np.uint8)
+    a, b = oracle.e4m3_to_f64(pos), oracle.e4m3_to_f64(pos + 1)
+    mids = oracle.f64_to_e4m3((a + b) / 2)
+    assert np.array_equal(mids, np.where(pos % 2 == 0, pos, pos + 1))
+    # Saturation and signed zero.
+    assert oracle.f64_to_e4m3([448.0, 460.0, 1e6, -1e6, -0.0]).tolist() == [0x7E, 0x7E, 0x7E, 0xFE, 0x80]
+
+
+def test_e4m3_encoder_matches_torch_cast():
+    rng = np.random.default_rng(3)
+    v = (rng.standard_normal(4000) * rng.choice([1e-3, 0.05, 1.0, 60.0], 4000)).clip(-440, 440)
+    got = oracle.f64_to_e4m3(v)
+    ref = torch.from_numpy(v.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(got, ref)
+
+
+def test_q_quant_fold_closed_forms():
+    D = 128
+    rows = np.zeros((1, 5, D), np.float32)
+    rows[0, 0, 0] = 448.0                     # amax = 448: scale 1
+    rows[0, 1, 3] = -452.0                    # just above (exact in bf16): scale 2
+    rows[0, 2, :] = 0.0                       # all zero: scale 1, codes 0
+    rows[0, 3, :] = np.linspace(-1, 1, D)     # amax 1: scale 2^-8 (1 <= 448 * 2^-8 = 1.75)
+    rows[0, 4, 7] = 2.0 ** -20                # tiny: scale 2^-28 (2^-20 <= 448 * 2^-28)
+    q = bf16(rows)
+    w = np.array([[1.0, -2.0, 3.0, 0.5, 4.0]], np.float32)
+    q8, wo = oracle.q_quant_fold(q, w, 0.25, padded_heads=8)
+    scales = np.array([1.0, 2.0, 1.0, 2.0 ** -8, 2.0 ** -28])
+    assert np.array_equal(wo[0, :5], (w[0] * np.float32(0.25)).astype(np.float32) * scales.astype(np.float32))
+    assert (wo[0, 5:] == 0).all() and (q8[0, 5:] == 0).all()            # padded heads
+    assert q8[0, 0, 0] == 0x7E and q8[0, 1, 3] == oracle.f64_to_e4m3([-226.0])[0] == 0xF6
+    assert (q8[0, 2] == 0).all()
+    deq = oracle.e4m3_to_f64(q8[0, 3]) * 2.0 ** -8
+    src = oracle.bf16_to_f64(q[0, 3])
+    assert np.all(np.abs(deq - src) <= np.maximum(np.abs(src) * 2.0 ** -4, 2.0 ** -18))
+    assert oracle.e4m3_to_f64(q8[0, 4, 7:8])[0] * 2.0 ** -28 == 2.0 ** -20
+
+
+def test_q_quant_fold_matches_torch_quantisation():
+    # The input generator quantises with torch's own e4m3 cast and the same
+    # UE8M0 rule: an independent implementation of the same definition.
+    rng = np.random.default_rng(1)
+    src = wl.bf16_bits_to_f32(bf16(rng.standard_normal((6, 4, 128)) * 0.1))
+    q8_ref, s_ref = wl.quantize_e4m3_blocks(src.reshape(24, 128))
+    q8, wo = oracle.q_quant_fold(bf16(src), np.ones((6, 4), np.float32), 1.0, padded_heads=4)
+    assert np.array_equal(q8.reshape(24, 128), q8_ref)
+    assert np.array_equal(wo.reshape(24), s_ref)
+
+
+def test_k_norm_insert_layer_norm_and_slots():
+    rng = np.random.default_rng(2)
+    T, D = 6, 128
+    k = rng.standard_normal((T, D)) * 0.3
+    k[1] = 0.7                                                 # constant row: output is the bias
+    kb = bf16(k)
+    g = (1 + 0.1 * rng.standard_normal(D)).astype(np.float32)
+    b = (0.05 * rng.standard_normal(D)).astype(np.float32)
+    slots = np.array([5, 0, -1, 11, 3, 9], np.int64)           # -1: a padding token
+    cache = np.full((3, 4, D), 0x7FC0, np.uint16)              # sentinel bf16 NaN
+    oracle.k_norm_insert(kb, g, b, 1e-6, slots, cache)
+    flat = cache.reshape(12, D)
+    ref = torch.nn.functional.layer_norm(torch.from_numpy(wl.bf16_bits_to_f32(kb)).double(), (D,),
+                                         torch.from_numpy(g).double(), torch.from_numpy(b).double(),
+                                         1e-6).numpy()
+    for t, s in enumerate(slots):
+        if s < 0:
+            continue
+        got = oracle.bf16_to_f64(flat[s])
+        assert np.all(np.abs(got - ref[t]) <= np.abs(ref[t]) * 2.0 ** -8 + 1e-30)
+    assert np.array_equal(oracle.bf16_to_f64(flat[0]), oracle.bf16_to_f64(bf16(b)))   # constant row
+    untouched = [i for i in range(12) if i not in set(slots.tolist())]
+    assert (flat[untouched] == 0x7FC0).all()
+    # e4m3 cache: the bf16 row quantised with its UE8M0 scale
+    c8 = np.zeros((3, 4, D), np.uint8)
+    sc = np.zeros(12, np.float32)
+    oracle.k_norm_insert(kb, g, b, 1e-6, slots, c8, sc)
+    for t, s in enumerate(slots):
+        if s < 0:
+            continue
+        row = oracle.bf16_to_f64(flat[s])
+        q8, wo = oracle.q_quant_fold(flat[s][None, None, :], np.ones((1, 1), np.float32), 1.0, 1)
+        assert np.array_equal(c8.reshape(12, D)[s], q8[0, 0]) and sc[s] == wo[0, 0]

@@ -28,7 +28,7 @@ EXPORTS = (
     "dsa_indexer_logits", "dsa_topk", "dsa_indexer_topk", "dsa_indexer_logits_paged",
     "dsa_indexer_topk_paged", "dsa_workspace_bytes", "dsa_status_string",
     "dsa_get_last_device_error", "dsa_selftest_wait_timeout", "dsa_indexer_topk_noalloc",
-    "dsa_topk_sort_by_score",
+    "dsa_topk_sort_by_score", "dsa_q_quant_fold_weights", "dsa_k_norm_quant_insert",
 )
 
 
@@ -60,10 +60,14 @@ def _load():
     lib.dsa_get_last_device_error.argtypes = []
     lib.dsa_selftest_wait_timeout.argtypes = [U64, P]
     lib.dsa_topk_sort_by_score.argtypes = [P, I64, P, I, I, P]
+    F = ctypes.c_float
+    lib.dsa_q_quant_fold_weights.argtypes = [P, P, F, I, I, I, I, P, P, P]
+    lib.dsa_k_norm_quant_insert.argtypes = [P, P, P, F, P, I, I, I, P, P, I, I, P]
     for name in ("dsa_indexer_logits", "dsa_topk", "dsa_indexer_topk",
                  "dsa_indexer_logits_paged", "dsa_indexer_topk_paged",
                  "dsa_get_last_device_error", "dsa_selftest_wait_timeout",
-                 "dsa_topk_sort_by_score"):
+                 "dsa_topk_sort_by_score", "dsa_q_quant_fold_weights",
+                 "dsa_k_norm_quant_insert"):
         getattr(lib, name).restype = I
     return lib
 
@@ -259,6 +263,48 @@ def topk_sort_by_score(logits, topk_idx):
                                     _stream(dev))
     _check(st, "dsa_topk_sort_by_score")
     return topk_idx
+
+
+def q_quant_fold_weights(q, weights, weight_scale, padded_heads=None, *, q_fp8=None,
+                         weights_out=None):
+    """bf16 q [T,H,128] -> (e4m3 q [T,Hp,128], fp32 weights [T,Hp]) with each
+    row's UE8M0 scale and weight_scale folded into the weights."""
+    dev = q.device
+    _need(q, "q", (torch.bfloat16,), dev)
+    _need(weights, "weights", (torch.float32,), dev)
+    T, H, D = q.shape
+    Hp = H if padded_heads is None else int(padded_heads)
+    if q_fp8 is None:
+        q_fp8 = torch.empty((T, Hp, D), dtype=torch.float8_e4m3fn, device=dev)
+    if weights_out is None:
+        weights_out = torch.empty((T, Hp), dtype=torch.float32, device=dev)
+    _need(q_fp8, "q_fp8", (torch.float8_e4m3fn, torch.uint8), dev)
+    _need(weights_out, "weights_out", (torch.float32,), dev)
+    st = lib.dsa_q_quant_fold_weights(_ptr(q), _ptr(weights), float(weight_scale), T, H, D, Hp,
+                                      _ptr(q_fp8), _ptr(weights_out), _stream(dev))
+    _check(st, "dsa_q_quant_fold_weights")
+    return q_fp8, weights_out
+
+
+def k_norm_quant_insert(k, ln_weight, ln_bias, eps, slot_mapping, k_cache, k_scale=None):
+    """LayerNorm the new keys k [T,128] (bf16) and write them to their slots of
+    the paged cache k_cache [num_blocks, block_size, 128]: bf16, or e4m3 codes
+    with k_scale [num_blocks*block_size] for an e4m3 cache.  In place."""
+    dev = k.device
+    _need(k, "k", (torch.bfloat16,), dev)
+    _need(ln_weight, "ln_weight", (torch.float32,), dev)
+    _need(ln_bias, "ln_bias", (torch.float32,), dev)
+    _need(slot_mapping, "slot_mapping", (torch.int64,), dev)
+    _need(k_cache, "k_cache", (torch.bfloat16, torch.float8_e4m3fn, torch.uint8), dev)
+    _need(k_scale, "k_scale", (torch.float32,), dev)
+    T, D = k.shape
+    num_blocks, block_size = k_cache.shape[0], k_cache.shape[1]
+    dt = DSA_BF16 if k_cache.dtype == torch.bfloat16 else DSA_E4M3
+    st = lib.dsa_k_norm_quant_insert(_ptr(k), _ptr(ln_weight), _ptr(ln_bias), float(eps),
+                                     _ptr(slot_mapping), T, D, dt, _ptr(k_cache), _ptr(k_scale),
+                                     num_blocks, block_size, _stream(dev))
+    _check(st, "dsa_k_norm_quant_insert")
+    return k_cache, k_scale
 
 
 def last_device_error() -> int:

@@ -424,6 +424,37 @@ dsa_status_t dsa_topk_sort_by_score(const float* logits, int64_t ld, int32_t* to
   return from_cuda(launch_topk_sort(logits, ld, topk, T, k, error_word(), as_stream(stream)));
 }
 
+dsa_status_t dsa_q_quant_fold_weights(const void* q, const float* weights, float weight_scale,
+                                      int T, int H, int D, int padded_heads, void* q_fp8,
+                                      float* weights_out, dsa_stream_t stream) {
+  if (!q || !weights || !q_fp8 || !weights_out || T < 0 || H < 1 || padded_heads < H)
+    return DSA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(q_fp8, 8) || !aligned(weights, 4) || !aligned(weights_out, 4))
+    return DSA_ERR_INVALID_ARG;
+  if (D != 128 || padded_heads > 64) return DSA_ERR_UNSUPPORTED;
+  return from_cuda(launch_q_quant_fold(q, weights, weight_scale, T, H, padded_heads, q_fp8,
+                                       weights_out, as_stream(stream)));
+}
+
+dsa_status_t dsa_k_norm_quant_insert(const void* k, const float* ln_weight, const float* ln_bias,
+                                     float eps, const int64_t* slot_mapping, int T, int D,
+                                     dsa_dtype_t cache_dtype, void* k_cache, float* k_scale,
+                                     int num_blocks, int block_size, dsa_stream_t stream) {
+  if (!k || !ln_weight || !ln_bias || !slot_mapping || !k_cache || T < 0 || num_blocks < 1 ||
+      block_size < 1 || !(eps >= 0.f))
+    return DSA_ERR_INVALID_ARG;
+  if (cache_dtype != DSA_BF16 && cache_dtype != DSA_E4M3) return DSA_ERR_INVALID_ARG;
+  const bool fp8 = cache_dtype == DSA_E4M3;
+  if (fp8 != (k_scale != nullptr)) return DSA_ERR_INVALID_ARG;  // scales exactly for e4m3
+  if (!aligned(k, 16) || !aligned(k_cache, 16) || !aligned(ln_weight, 16) || !aligned(ln_bias, 16) ||
+      !aligned(slot_mapping, 8) || (k_scale && !aligned(k_scale, 4)))
+    return DSA_ERR_INVALID_ARG;
+  if (D != 128) return DSA_ERR_UNSUPPORTED;
+  const int64_t capacity = static_cast<int64_t>(num_blocks) * block_size;
+  return from_cuda(launch_k_norm_insert(k, ln_weight, ln_bias, eps, slot_mapping, T, fp8, capacity,
+                                        k_cache, k_scale, error_word(), as_stream(stream)));
+}
+
 size_t dsa_workspace_bytes(dsa_op_t op, int64_t rows, int64_t cols, int k) {
   if (rows < 0 || cols < 0 || k < 0) return static_cast<size_t>(-1);
   switch (op) {

@@ -85,5 +85,13 @@ constexpr int kTopkSortMax = 8192;
 cudaError_t launch_topk_sort(const float* logits, int64_t ld, int32_t* topk, int T, int k,
                              uint32_t* err, cudaStream_t s);
 cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint64_t timeout_ns, cudaStream_t s);
+// SM count of the current device (queried once per device).
+int device_sm_count();
+// The steps before the indexer (dsa_prologue.cu); D = 128.
+cudaError_t launch_q_quant_fold(const void* q, const float* w, float weight_scale, int T, int H,
+                                int Hp, void* q8, float* w_out, cudaStream_t s);
+cudaError_t launch_k_norm_insert(const void* k, const float* gamma, const float* beta, float eps,
+                                 const int64_t* slots, int T, bool fp8, int64_t capacity,
+                                 void* cache, float* cache_scale, uint32_t* err, cudaStream_t s);
 
 }  // namespace dsa
