@@ -251,6 +251,27 @@ dsa_status_t dsa_topk_sort_by_score(const float* logits, int64_t ld, int32_t* to
                                     dsa_stream_t stream);
 
 /*
+ * Merge of per-rank top-k candidates into the global top-k (decode context
+ * parallelism: KimiK3DSAIndexer.__init__ on the vLLM page, where each rank
+ * scores its interleaved share of the key cache, takes a local top-k, and the
+ * op merges the ranks' local top-k into the global top-k).  Per row, of the C
+ * candidates (score, global column) -- typically W ranks x k, gathered by
+ * one exchange -- the k best by score are kept (ties to the lower column,
+ * -0.0 equal to +0.0, -inf and NaN never), and written in ascending column
+ * order with -1 padding: exactly dsa_topk's output on the whole row, because
+ * every column of the global top-k is in its rank's local top-k.
+ *
+ *   cand_scores [T, C] fp32
+ *   cand_cols   [T, C] int32 global columns; a negative column is an empty slot.
+ *               Columns must be distinct within a row (ranks own disjoint
+ *               positions).
+ *   out         [T, k] int32
+ *   C, k <= 16384 (else DSA_ERR_UNSUPPORTED)
+ */
+dsa_status_t dsa_topk_merge(const float* cand_scores, const int32_t* cand_cols, int T, int C,
+                            int k, int32_t* out, dsa_stream_t stream);
+
+/*
  * The query side of the e4m3 path, before dsa_indexer_logits / _topk /
  * _topk_paged: indexer_q_quant_fold_weights of KimiK3DSAIndexer.score (vLLM
  * API docs, "vllm.models.kimi_k3.nvidia.dsa").  Every (t, h) row of D query

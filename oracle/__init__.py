@@ -18,6 +18,7 @@ Functions:
     topk(...)            masked per-row top-k of given fp32 logits
                          (torch_dsa_topk, vime PR #502, third review comment)
     sort_by_score(...)   a top-k index buffer in descending score order
+    topk_merge(...)      per-rank (score, column) candidates -> the global top-k
     f64_to_e4m3()        E4M3 encoder (nearest, ties to even, saturating)
     q_quant_fold(...)    query quantisation + weight fold (before the indexer)
     k_norm_insert(...)   key LayerNorm + quantisation + paged insert
@@ -280,3 +281,21 @@ def k_norm_insert(k_bf16_bits, ln_weight, ln_bias, eps, slots, cache, scale=None
     if rc != 0:
         raise ValueError("oracle k_norm_insert: bad arguments")
     return cache, scale
+
+
+def topk_merge(cand_scores, cand_cols, k) -> np.ndarray:
+    """The k best of each row's (score, column) candidates [T, C]: valid ones
+    (column >= 0, score neither -inf nor NaN) ordered by score descending, ties
+    to the lower column (-0.0 equals +0.0); written in ascending column order,
+    -1 padding.  The definition of the global top-k applied to the union of
+    the ranks' candidates (decode context parallelism, vLLM page)."""
+    sc = np.asarray(cand_scores, dtype=np.float32)
+    cc = np.asarray(cand_cols, dtype=np.int64)
+    out = np.full((sc.shape[0], k), -1, np.int32)
+    for t in range(sc.shape[0]):
+        v = sc[t].astype(np.float64)
+        ok = (cc[t] >= 0) & ~np.isnan(v) & (v != -np.inf)
+        cols, vals = cc[t][ok], np.where(v[ok] == 0.0, 0.0, v[ok])
+        take = cols[np.lexsort((cols, -vals))][:k]
+        out[t, :take.size] = np.sort(take)
+    return out

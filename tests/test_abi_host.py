@@ -195,3 +195,14 @@ def test_prologue_validation(api):
     assert g(A, A, A, -1.0, A, 4, 128, B16, A, NUL, 8, 64, NUL) == E   # eps < 0
     assert g(A, A, A, 1e-6, A, 4, 128, B16, A, NUL, 0, 64, NUL) == E   # no blocks
     assert g(A, A, A, 1e-6, A, 4, 64, B16, A, NUL, 8, 64, NUL) == U    # D != 128
+
+
+def test_topk_merge_validation(api):
+    E, U = api.DSA_ERR_INVALID_ARG, api.DSA_ERR_UNSUPPORTED
+    f = api.lib.dsa_topk_merge
+    assert f(NUL, A, 4, 16, 8, A, NUL) == E
+    assert f(A, A, 4, 0, 8, A, NUL) == E
+    assert f(A, A, 4, 16, 0, A, NUL) == E
+    assert f(A, A, -1, 16, 8, A, NUL) == E
+    assert f(A, A, 4, 16385, 8, A, NUL) == U
+    assert f(A, A, 4, 16, 16385, A, NUL) == U

@@ -530,3 +530,41 @@ def test_k_norm_insert_layer_norm_and_slots():
         row = oracle.bf16_to_f64(flat[s])
         q8, wo = oracle.q_quant_fold(flat[s][None, None, :], np.ones((1, 1), np.float32), 1.0, 1)
         assert np.array_equal(c8.reshape(12, D)[s], q8[0, 0]) and sc[s] == wo[0, 0]
+
+
+# ----------------------------------------------------------- rank merge
+
+def test_topk_merge_hand_example_and_whole_row():
+    sc = np.array([[0.5, 2.0, 2.0, -np.inf, 1.0, 0.0, -0.0, np.nan]], np.float32)
+    cc = np.array([[10, 7, 3, 4, -1, 2, 1, 9]], np.int32)     # -1: an empty slot
+    # 2.0 at columns 3 and 7 (3 first), then 0.5 (10), then 0.0 / -0.0 (1 before 2)
+    assert oracle.topk_merge(sc, cc, 4).tolist() == [[1, 3, 7, 10]]
+    assert oracle.topk_merge(sc, cc, 8).tolist() == [[1, 2, 3, 7, 10, -1, -1, -1]]
+    # All columns of a row as one candidate set: the masked top-k itself.
+    rng = np.random.default_rng(8)
+    lg = np.round(rng.standard_normal((4, 90)), 1).astype(np.float32)
+    cols = np.tile(np.arange(90, dtype=np.int32), (4, 1))
+    assert np.array_equal(oracle.topk_merge(lg, cols, 17),
+                          oracle.topk(lg, np.zeros(4, np.int32), np.full(4, 90, np.int32), 17))
+
+
+def test_topk_merge_of_interleaved_local_topk_is_the_global_topk():
+    # Every column of the global top-k is in its own rank's local top-k, so
+    # merging the local top-ks reproduces the global one, ties included.
+    from top_selection_dsa_gb300 import dcp
+    rng = np.random.default_rng(4)
+    for world, inter in ((2, 1), (3, 4), (4, 64)):
+        S, T, k = 700, 5, 40
+        lg = np.round(rng.standard_normal((T, S)), 1).astype(np.float32)
+        L = rng.integers(1, S + 1, T).astype(np.int32)
+        cand_s, cand_c = [], []
+        for r in range(world):
+            pos = dcp.owned_positions(S, r, world, inter).numpy()
+            loc = lg[:, pos]
+            ln = np.array([dcp.local_len(int(x), r, world, inter) for x in L], np.int32)
+            top = oracle.topk(loc, np.zeros(T, np.int32), ln, k)
+            g = np.where(top >= 0, pos[np.maximum(top, 0)], -1)
+            cand_s.append(np.where(top >= 0, np.take_along_axis(loc, np.maximum(top, 0), 1), -np.inf))
+            cand_c.append(g)
+        merged = oracle.topk_merge(np.concatenate(cand_s, 1), np.concatenate(cand_c, 1), k)
+        assert np.array_equal(merged, oracle.topk(lg, np.zeros(T, np.int32), L, k))

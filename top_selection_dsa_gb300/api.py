@@ -29,6 +29,7 @@ EXPORTS = (
     "dsa_indexer_topk_paged", "dsa_workspace_bytes", "dsa_status_string",
     "dsa_get_last_device_error", "dsa_selftest_wait_timeout", "dsa_indexer_topk_noalloc",
     "dsa_topk_sort_by_score", "dsa_q_quant_fold_weights", "dsa_k_norm_quant_insert",
+    "dsa_topk_merge",
 )
 
 
@@ -63,11 +64,12 @@ def _load():
     F = ctypes.c_float
     lib.dsa_q_quant_fold_weights.argtypes = [P, P, F, I, I, I, I, P, P, P]
     lib.dsa_k_norm_quant_insert.argtypes = [P, P, P, F, P, I, I, I, P, P, I, I, P]
+    lib.dsa_topk_merge.argtypes = [P, P, I, I, I, P, P]
     for name in ("dsa_indexer_logits", "dsa_topk", "dsa_indexer_topk",
                  "dsa_indexer_logits_paged", "dsa_indexer_topk_paged",
                  "dsa_get_last_device_error", "dsa_selftest_wait_timeout",
                  "dsa_topk_sort_by_score", "dsa_q_quant_fold_weights",
-                 "dsa_k_norm_quant_insert"):
+                 "dsa_k_norm_quant_insert", "dsa_topk_merge"):
         getattr(lib, name).restype = I
     return lib
 
@@ -263,6 +265,24 @@ def topk_sort_by_score(logits, topk_idx):
                                     _stream(dev))
     _check(st, "dsa_topk_sort_by_score")
     return topk_idx
+
+
+def topk_merge(cand_scores, cand_cols, k, *, out=None):
+    """[T, C] (score, global column) candidates -> the [T, k] global top-k,
+    ascending columns, -1 padding (negative columns are empty slots)."""
+    dev = cand_scores.device
+    _need(cand_scores, "cand_scores", (torch.float32,), dev)
+    _need(cand_cols, "cand_cols", (torch.int32,), dev)
+    T, C = cand_scores.shape
+    if tuple(cand_cols.shape) != (T, C):
+        raise ValueError("cand_scores and cand_cols must have the same [T, C] shape")
+    if out is None:
+        out = torch.empty((T, k), dtype=torch.int32, device=dev)
+    _need(out, "out", (torch.int32,), dev)
+    st = lib.dsa_topk_merge(_ptr(cand_scores), _ptr(cand_cols), T, C, int(k), _ptr(out),
+                            _stream(dev))
+    _check(st, "dsa_topk_merge")
+    return out
 
 
 def q_quant_fold_weights(q, weights, weight_scale, padded_heads=None, *, q_fp8=None,

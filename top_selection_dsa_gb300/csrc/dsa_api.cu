@@ -424,6 +424,15 @@ dsa_status_t dsa_topk_sort_by_score(const float* logits, int64_t ld, int32_t* to
   return from_cuda(launch_topk_sort(logits, ld, topk, T, k, error_word(), as_stream(stream)));
 }
 
+dsa_status_t dsa_topk_merge(const float* cand_scores, const int32_t* cand_cols, int T, int C,
+                            int k, int32_t* out, dsa_stream_t stream) {
+  if (!cand_scores || !cand_cols || !out || T < 0 || C < 1 || k < 1) return DSA_ERR_INVALID_ARG;
+  if (!aligned(cand_scores, 4) || !aligned(cand_cols, 4) || !aligned(out, 4))
+    return DSA_ERR_INVALID_ARG;
+  if (C > kTopkMergeMax || k > kTopkMergeMax) return DSA_ERR_UNSUPPORTED;
+  return from_cuda(launch_topk_merge(cand_scores, cand_cols, T, C, k, out, as_stream(stream)));
+}
+
 dsa_status_t dsa_q_quant_fold_weights(const void* q, const float* weights, float weight_scale,
                                       int T, int H, int D, int padded_heads, void* q_fp8,
                                       float* weights_out, dsa_stream_t stream) {

@@ -82,6 +82,11 @@ cudaError_t launch_fill(float* dst, int64_t rows, int64_t cols, int64_t ld, floa
 // Rows of k top-k indices reordered by descending score in place (k <=
 // kTopkSortMax); indices outside [0, ld) are treated as padding and recorded.
 constexpr int kTopkSortMax = 8192;
+// Merge of C (score, global column) candidates per row into the k best,
+// ascending columns, -1 padding (C, k <= kTopkMergeMax).
+constexpr int kTopkMergeMax = 16384;
+cudaError_t launch_topk_merge(const float* scores, const int32_t* cols, int T, int C, int k,
+                              int32_t* out, cudaStream_t s);
 cudaError_t launch_topk_sort(const float* logits, int64_t ld, int32_t* topk, int T, int k,
                              uint32_t* err, cudaStream_t s);
 cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint64_t timeout_ns, cudaStream_t s);

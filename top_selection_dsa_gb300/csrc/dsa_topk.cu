@@ -1249,6 +1249,78 @@ __global__ void __launch_bounds__(kSortThreads) topk_sort_kernel(const float* __
   }
 }
 
+// ------------------------------------------------------------ rank merge
+//
+// Decode context parallelism (KimiK3DSAIndexer.__init__ on the vLLM page:
+// each rank scores its interleaved share of the key cache, takes a local
+// top-k, and the op merges the ranks' local top-k into the global one): the
+// merge of C candidates per row (score, global column; column < 0 = empty)
+// into the k best by (score descending, column ascending), written in
+// ascending column order with -1 padding.  One CTA per row: a bitonic sort of
+// composites (key << 32 | ~column) puts the winners first, a second one puts
+// their columns in ascending order.
+constexpr int kMergeThreads = 512;
+
+template <class K>
+__device__ __forceinline__ void bitonic_desc(K* a, int n) {
+  for (int size = 2; size <= n; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < n / 2; i += blockDim.x) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const bool desc = (lo & size) == 0;
+        const K x = a[lo], y = a[hi];
+        if ((x < y) == desc) {
+          a[lo] = y;
+          a[hi] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(
+    const float* __restrict__ scores, const int32_t* __restrict__ cols, int C, int n, int k,
+    int m, int32_t* __restrict__ out) {
+  extern __shared__ __align__(16) unsigned long long mk[];  // n composites
+  const int row = blockIdx.x;
+  const float* sr = scores + static_cast<int64_t>(row) * C;
+  const int32_t* cr = cols + static_cast<int64_t>(row) * C;
+  __shared__ uint32_t nvalid;
+  if (threadIdx.x == 0) nvalid = 0u;
+  __syncthreads();
+  uint32_t mine = 0u;
+  for (int i = threadIdx.x; i < n; i += kMergeThreads) {
+    unsigned long long v = 0ull;
+    if (i < C) {
+      const int c = __ldg(cr + i);
+      const uint32_t key = c >= 0 ? order_key(__ldg(sr + i)) : 0u;  // -inf / NaN: never taken
+      if (key != 0u) {
+        v = (static_cast<unsigned long long>(key) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(c));
+        ++mine;
+      }
+    }
+    mk[i] = v;
+  }
+  if (mine) atomicAdd(&nvalid, mine);
+  __syncthreads();
+  bitonic_desc(mk, n);
+  // The winners' columns (the first min(k, valid) composites), ascending.
+  const int take = min(k, static_cast<int>(nvalid));
+  uint32_t* col = reinterpret_cast<uint32_t*>(mk + n);  // m words after the composites
+  for (int i = threadIdx.x; i < m; i += kMergeThreads)
+    col[i] = i < take ? 0xFFFFFFFFu - static_cast<uint32_t>(mk[i]) : 0xFFFFFFFFu;
+  __syncthreads();
+  // Descending sort of the complements = ascending columns; padding (~0 -> 0) last.
+  for (int i = threadIdx.x; i < m; i += kMergeThreads) col[i] = ~col[i];
+  __syncthreads();
+  bitonic_desc(col, m);
+  int32_t* dst = out + static_cast<int64_t>(row) * k;
+  for (int i = threadIdx.x; i < k; i += kMergeThreads)
+    dst[i] = i < take ? static_cast<int32_t>(~col[i]) : -1;
+}
+
 }  // namespace
 
 int topk_bitmap_words(int max_row) { return (max_row + 31) / 32; }
@@ -1348,6 +1420,22 @@ cudaError_t launch_topk_sort(const float* logits, int64_t ld, int32_t* topk, int
                                        smem);
   if (e != cudaSuccess) return e;
   topk_sort_kernel<<<T, kSortThreads, smem, s>>>(logits, ld, topk, k, n, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk_merge(const float* scores, const int32_t* cols, int T, int C, int k,
+                              int32_t* out, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  int n = 1;
+  while (n < C) n <<= 1;
+  int m = 1;
+  while (m < k) m <<= 1;
+  const int smem = n * static_cast<int>(sizeof(unsigned long long)) +
+                   m * static_cast<int>(sizeof(uint32_t));
+  cudaError_t e = cudaFuncSetAttribute(topk_merge_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  topk_merge_kernel<<<T, kMergeThreads, smem, s>>>(scores, cols, C, n, k, m, out);
   return cudaGetLastError();
 }
 
