@@ -259,6 +259,20 @@ __device__ __forceinline__ void load_chunk(const float* src, int n, int q, int w
   }
 }
 
+// The raw values of chunk q for this thread (-inf past the row): loads only,
+// so that they can be issued a chunk ahead of their use.
+template <int THREADS>
+__device__ __forceinline__ void load_chunk_raw(const float* src, int n, int q, int warp, int lane,
+                                               float (&x)[16]) {
+  constexpr int CH = THREADS * 16;
+  const int c0 = q * CH + warp * 512 + lane;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int c = c0 + i * 32;
+    x[i] = c < n ? __ldg(src + c) : -INFINITY;
+  }
+}
+
 // Groups of this warp in chunk q that hold a column of the row (warp-uniform).
 template <int THREADS>
 __device__ __forceinline__ int chunk_groups(int n, int q, int warp) {
@@ -345,13 +359,27 @@ __global__ void __launch_bounds__(THREADS, MINB) topk_rows_kernel(const TopkPara
       reinterpret_cast<uint4*>(hist)[i] = make_uint4(0u, 0u, 0u, 0u);
     if (tid == 0) ncand = 0u;
     __syncthreads();
-    // Pass 1: the top 11 key bits (bin 3 collects the invalid slots).
-    for (int q = 0; q < nch; ++q) {
-      if (nch > 1) load_chunk<THREADS>(src, n, q, warp, lane, key);
-      const int ng = chunk_groups<THREADS>(n, q, warp);
+    // Pass 1: the top 11 key bits (bin 3 collects the invalid slots).  A row
+    // of several chunks is read from memory (HBM) here: the next chunk's
+    // loads are issued before the current chunk's histogram adds.  (The later
+    // passes re-read the row from L2, where prefetching did not pay.)
+    if (nch == 1) {
+      const int ng = chunk_groups<THREADS>(n, 0, warp);
 #pragma unroll
       for (int i = 0; i < 16; ++i)
         if (i / 4 < ng) atomicAdd(&hist[key[i] >> 21], 1u);
+    } else {
+      float nx[16];
+      load_chunk_raw<THREADS>(src, n, 0, warp, lane, nx);
+      for (int q = 0; q < nch; ++q) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) key[i] = chunk_key(nx[i]);
+        if (q + 1 < nch) load_chunk_raw<THREADS>(src, n, q + 1, warp, lane, nx);
+        const int ng = chunk_groups<THREADS>(n, q, warp);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (i / 4 < ng) atomicAdd(&hist[key[i] >> 21], 1u);
+      }
     }
     __syncthreads();
     // Read before the barriers of find_bin_fast, hence before any clear.
