@@ -66,8 +66,10 @@ def parse_args(argv=None):
                     help="skip the clock-sampling load window (for profiler runs)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override T = S of the prefill workloads (smaller profiler captures)")
-    ap.add_argument("--oracle-rows", type=int, default=512,
-                    help="rows of the CPU oracle sample (cpu_baseline / reference arm)")
+    ap.add_argument("--oracle-rows", type=int, default=4096,
+                    help="rows of the CPU oracle sample for cpu_baseline (all 4096 rows of the "
+                         "default workload, a few seconds on the host's cores; the reference "
+                         "arm times an eighth of it per step)")
     return ap.parse_args(argv)
 
 
