@@ -195,18 +195,23 @@ def test_topk_edge_cases(api):
     assert (got[7] == np.arange(10, 10 + k)).all()
 
 
-# Row lengths that reach every top-k kernel variant: register-resident CTAs
-# of 4K/8K/16K/32K keys, clusters of 2/4/8 CTAs, and the streaming kernel.
-@pytest.mark.parametrize("S,k", [(100, 1), (2048, 2048), (2049, 2048), (4096, 4096),
-                                 (8000, 2048), (16384, 3000), (30000, 2048), (60000, 2048),
-                                 (131072, 2048), (200000, 5000), (300000, 2048)])
-def test_topk_row_lengths(api, S, k):
-    rng = np.random.default_rng(S + k)
-    T = 7
+# Row lengths that reach every top-k path: with few rows (7) the per-row
+# kernel's one-chunk rows (S <= 4096) and two-chunk rows, then the split path
+# (S > 16384); with more than 512 rows the per-row kernel's multi-chunk
+# bitmap path (gathered threshold bin, or digit passes when the bin is too
+# large, as in the tie-heavy rows) and, past 262144 columns, the streaming
+# kernel.
+@pytest.mark.parametrize("S,k,T", [(100, 1, 7), (2048, 2048, 7), (2049, 2048, 7),
+                                   (4096, 4096, 7), (8000, 2048, 7), (16384, 3000, 7),
+                                   (30000, 2048, 7), (60000, 2048, 7), (131072, 2048, 7),
+                                   (200000, 5000, 7), (300000, 2048, 7), (40000, 2048, 520),
+                                   (270000, 2048, 520)])
+def test_topk_row_lengths(api, S, k, T):
+    rng = np.random.default_rng(S + k + T)
     lg = (rng.standard_normal((T, S)) * 4).round().astype(np.float32)   # many ties
-    lg[6] = rng.standard_normal(S).astype(np.float32)                   # few ties
-    rs = np.array([0, 0, 0, 0, 0, 0, S // 3], np.int32)
-    re = np.array([S, S - 1, S // 2, k, k - 1, 1, S], np.int32)
+    lg[6::7] = rng.standard_normal((len(range(6, T, 7)), S)).astype(np.float32)  # few ties
+    rs = np.tile(np.array([0, 0, 0, 0, 0, 0, S // 3], np.int32), T // 7 + 1)[:T]
+    re = np.tile(np.array([S, S - 1, S // 2, k, k - 1, 1, S], np.int32), T // 7 + 1)[:T]
     got = api.topk(dev(lg), dev(rs), dev(re), k).cpu().numpy()
     assert np.array_equal(got, oracle.topk(lg, rs, re, k))
 

@@ -71,8 +71,8 @@ int topk_bitmap_words(int max_row);
 // Whether rows of up to max_row columns fit the top-k kernels.
 bool topk_supported(int max_row);
 // Few long rows take the split path: every phase runs on many CTAs per row
-// (one per 4096-key segment), exchanging per-row histograms, candidate keys,
-// the threshold and per-segment counts through global scratch of
+// (one per 4096-key unit), exchanging per-row histograms, candidate keys,
+// the threshold and per-unit offsets through global scratch of
 // topk_split_words(max_row) words per row.  Depends on the shape only, so the
 // workspace size is known on the host.
 bool topk_split_rows(int64_t rows, int64_t max_row);

@@ -23,7 +23,7 @@
 //       comes from the gathered keys, and a scan of the bitmap writes the
 //       columns out.
 //   split path         few long rows (decode): every phase on a grid of
-//       (16384-key segment, row) CTAs that talk through per-row scratch.
+//       (row, 4096-key unit) CTAs that talk through per-row scratch.
 //   topk_stream_kernel rows longer than the others take: 256 threads per
 //       row stream the row with 16-byte loads for each pass.
 // A row whose columns are all valid and that has at most k of them is
