@@ -229,6 +229,38 @@ dsa_status_t dsa_indexer_topk_noalloc(const void* q, const float* q_scale, const
                                       int topk, int32_t* out, dsa_stream_t stream);
 
 /*
+ * dsa_indexer_topk with the inputs and the result in HOST memory -- the only
+ * entry point whose tensor pointers are not device pointers.  The pages have
+ * no counterpart; it is an addition of this library for callers whose q, k
+ * and weights start on the host.
+ *   - q, q_scale, k, k_scale, weights, row_starts, row_ends, out: host
+ *     pointers, same shapes, types and meaning as dsa_indexer_topk.  Pinned
+ *     (page-locked) memory lets the copies overlap; pageable memory works but
+ *     each copy then waits for the host.  The arrays indexed by row may be
+ *     NULL when T = 0, k when S = 0.
+ *   - device_buffer: caller-owned device memory of at least
+ *     dsa_indexer_topk_host_bytes(T, S, H, D, topk, dtype) bytes, 256-byte
+ *     aligned.  It receives the inputs, the indices and one row chunk's
+ *     logits; on return from the stream's work it holds the device copy of
+ *     the inputs and of `out`.
+ *   - The rows are split into up to 8 chunks (multiples of 64 rows, about
+ *     512 or more each).  K goes up first; then chunk c's upload, chunk c-1's
+ *     scoring + top-k (on `stream`) and chunk c-2's download run at the same
+ *     time on two streams the call creates and destroys.  Work queued on
+ *     `stream` after the call sees all of `out`; host code must synchronise
+ *     `stream` before it reads `out`.
+ *   - Not capturable into a CUDA graph (it creates streams and events).
+ *   - Errors as dsa_indexer_topk; the indices are bit-identical to it.
+ */
+size_t dsa_indexer_topk_host_bytes(int T, int S, int H, int D, int topk, dsa_dtype_t dtype);
+dsa_status_t dsa_indexer_topk_host(const void* q, const float* q_scale, const void* k,
+                                   const float* k_scale, dsa_dtype_t dtype,
+                                   const float* weights, const int32_t* row_starts,
+                                   const int32_t* row_ends, int T, int S, int H, int D,
+                                   int topk, int32_t* out, void* device_buffer,
+                                   size_t device_bytes, dsa_stream_t stream);
+
+/*
  * Reorders top-k rows in place into descending order of score: the order of
  * torch.topk, which torch_dsa_topk (vime PR #502, third review comment)
  * returns, where every other entry point here writes ascending column order.

@@ -206,3 +206,29 @@ def test_topk_merge_validation(api):
     assert f(A, A, -1, 16, 8, A, NUL) == E
     assert f(A, A, 4, 16385, 8, A, NUL) == U
     assert f(A, A, 4, 16, 16385, A, NUL) == U
+
+
+def test_indexer_topk_host_validation(api):
+    E, U = api.DSA_ERR_INVALID_ARG, api.DSA_ERR_UNSUPPORTED
+    nb = api.lib.dsa_indexer_topk_host_bytes
+    need = nb(4096, 4096, 64, 128, 2048, api.DSA_BF16)
+    # inputs (q, k, weights, ranges, indices) plus one chunk's logits: up to 8
+    # chunks of at least 512 rows
+    inputs = 4096 * 64 * 128 * 2 + 4096 * 128 * 2 + 4096 * 64 * 4 * 2 + 2 * 4096 * 4 + \
+        4096 * 2048 * 4
+    assert inputs < need <= inputs + 512 * 4096 * 4 + 10 * 256
+    assert nb(-1, 8, 64, 128, 2, api.DSA_BF16) == ctypes.c_size_t(-1).value
+    assert nb(8, 8, 64, 128, 2, 7) == ctypes.c_size_t(-1).value
+    f = api.lib.dsa_indexer_topk_host
+    n = nb(8, 8, 64, 128, 2, api.DSA_BF16)
+    assert f(A, NUL, A, NUL, 0, A, A, A, 8, 8, 64, 128, 2, A, NUL, n, NUL) == E    # no buffer
+    assert f(A, NUL, A, NUL, 0, A, A, A, 8, 8, 64, 128, 2, A, A, n - 1, NUL) == E  # too small
+    assert f(A, NUL, A, NUL, 0, A, A, A, 8, 8, 64, 128, 2, A, MIS, n, NUL) == E
+    assert f(NUL, NUL, A, NUL, 0, A, A, A, 8, 8, 64, 128, 2, A, A, n, NUL) == E
+    assert f(A, NUL, A, NUL, 0, A, A, A, 8, 8, 64, 128, 2, NUL, A, n, NUL) == E
+    assert f(A, NUL, A, NUL, 0, A, A, A, 8, 8, 64, 128, 0, A, A, n, NUL) == E
+    assert f(A, NUL, A, NUL, 0, A, A, A, 8, 8, 3, 128, 2, A, A, n, NUL) == U
+    assert f(A, NUL, A, NUL, 1, A, A, A, 8, 8, 64, 128, 2, A, A, n, NUL) == E     # e4m3, no scales
+    assert f(A, NUL, A, NUL, 0, A, A, A, 0, 8, 64, 128, 2, A, A, n, NUL) == api.DSA_OK  # no rows
+    assert f(NUL, NUL, A, NUL, 0, NUL, NUL, NUL, 0, 8, 64, 128, 2, NUL, A, n, NUL) == api.DSA_OK
+    assert f(A, NUL, NUL, NUL, 0, A, A, A, 8, 8, 64, 128, 2, A, A, n, NUL) == E   # keys, no k

@@ -29,7 +29,7 @@ EXPORTS = (
     "dsa_indexer_topk_paged", "dsa_workspace_bytes", "dsa_status_string",
     "dsa_get_last_device_error", "dsa_selftest_wait_timeout", "dsa_indexer_topk_noalloc",
     "dsa_topk_sort_by_score", "dsa_q_quant_fold_weights", "dsa_k_norm_quant_insert",
-    "dsa_topk_merge",
+    "dsa_topk_merge", "dsa_indexer_topk_host_bytes", "dsa_indexer_topk_host",
 )
 
 
@@ -65,11 +65,14 @@ def _load():
     lib.dsa_q_quant_fold_weights.argtypes = [P, P, F, I, I, I, I, P, P, P]
     lib.dsa_k_norm_quant_insert.argtypes = [P, P, P, F, P, I, I, I, P, P, I, I, P]
     lib.dsa_topk_merge.argtypes = [P, P, I, I, I, P, P]
+    lib.dsa_indexer_topk_host_bytes.argtypes = [I, I, I, I, I, I]
+    lib.dsa_indexer_topk_host_bytes.restype = SZ
+    lib.dsa_indexer_topk_host.argtypes = [P, P, P, P, I, P, P, P, I, I, I, I, I, P, P, SZ, P]
     for name in ("dsa_indexer_logits", "dsa_topk", "dsa_indexer_topk",
                  "dsa_indexer_logits_paged", "dsa_indexer_topk_paged",
                  "dsa_get_last_device_error", "dsa_selftest_wait_timeout",
                  "dsa_topk_sort_by_score", "dsa_q_quant_fold_weights",
-                 "dsa_k_norm_quant_insert", "dsa_topk_merge"):
+                 "dsa_k_norm_quant_insert", "dsa_topk_merge", "dsa_indexer_topk_host"):
         getattr(lib, name).restype = I
     return lib
 
@@ -197,6 +200,58 @@ def indexer_topk(q, k, weights, row_starts, row_ends, topk_k, *, q_scale=None, k
                               _ptr(row_starts), _ptr(row_ends), T, S, H, D, topk_k, _ptr(out),
                               _ptr(ws), nbytes, _stream(dev))
     _check(st, "dsa_indexer_topk")
+    return out
+
+
+def _need_host(t, name, dtypes):
+    if t is None:
+        return
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} must have dtype in {dtypes}, got {t.dtype}")
+
+
+def indexer_topk_host_bytes(T, S, H, D, topk_k, dtype=DSA_BF16) -> int:
+    n = lib.dsa_indexer_topk_host_bytes(T, S, H, D, topk_k, dtype)
+    if n == ctypes.c_size_t(-1).value:
+        raise ValueError("dsa_indexer_topk_host_bytes: bad arguments")
+    return int(n)
+
+
+def indexer_topk_host(q, k, weights, row_starts, row_ends, topk_k, *, q_scale=None,
+                      k_scale=None, out=None, device_buffer=None, device=None):
+    """indexer_topk on HOST tensors (pin them for overlap): [T, topk_k] int32 on the host.
+
+    The library uploads the inputs in row chunks, scores and selects on the
+    GPU, and downloads the indices, overlapping the three; the call returns
+    after the current stream has finished.
+    """
+    dt = _elem_dtype(q, k)
+    T, H, D = q.shape
+    S = k.shape[0]
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else \
+        torch.device(device)
+    for t, n, d in ((q, "q", (q.dtype,)), (k, "k", (k.dtype,)), (weights, "weights", (torch.float32,)),
+                    (row_starts, "row_starts", (torch.int32,)), (row_ends, "row_ends", (torch.int32,)),
+                    (q_scale, "q_scale", (torch.float32,)), (k_scale, "k_scale", (torch.float32,))):
+        _need_host(t, n, d)
+    if out is None:
+        out = torch.empty((T, topk_k), dtype=torch.int32, pin_memory=True)
+    _need_host(out, "out", (torch.int32,))
+    nbytes = indexer_topk_host_bytes(T, S, H, D, topk_k, dt)
+    if device_buffer is None:
+        device_buffer = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+    _need(device_buffer, "device_buffer", (torch.uint8,), dev)
+    if device_buffer.numel() < nbytes:
+        raise ValueError(f"device_buffer holds {device_buffer.numel()} bytes, {nbytes} needed")
+    st = lib.dsa_indexer_topk_host(_ptr(q), _ptr(q_scale), _ptr(k), _ptr(k_scale), dt,
+                                   _ptr(weights), _ptr(row_starts), _ptr(row_ends), T, S, H, D,
+                                   topk_k, _ptr(out), _ptr(device_buffer), nbytes, _stream(dev))
+    _check(st, "dsa_indexer_topk_host")
+    torch.cuda.current_stream(dev).synchronize()
     return out
 
 

@@ -10,6 +10,9 @@
 #include <mutex>
 
 #include "dsa.h"
+
+#include <algorithm>
+#include <vector>
 #include "dsa_common.cuh"
 #include "dsa_internal.h"
 
@@ -369,6 +372,162 @@ dsa_status_t dsa_indexer_topk(const void* q, const float* q_scale, const void* k
   if (st != DSA_OK) return st;
   return run_topk(lg, ld, row_starts, row_ends, nullptr, 1, T, S, topk, out, as_stream(stream),
                   split_scratch(workspace, T, S));
+}
+
+// ---------------------------------------------------- host-buffer pipeline
+
+namespace {
+
+// Device-buffer layout of dsa_indexer_topk_host: the inputs, the indices, and
+// one chunk's workspace, each region 256-byte aligned.
+struct HostPlan {
+  int64_t chunk;  // rows per chunk
+  size_t k, ks, q, qs, w, rs, re, out, ws, total;
+};
+
+HostPlan host_plan(int T, int S, int H, int D, int topk, dsa_dtype_t dtype, bool q_scale,
+                   bool k_scale) {
+  HostPlan pl = {};
+  const size_t esz = dtype == DSA_E4M3 ? 1 : 2;
+  const int64_t nchunks = T <= 0 ? 1 : std::min<int64_t>(8, (T + 511) / 512);
+  pl.chunk = std::max<int64_t>(1, round_up((static_cast<int64_t>(T) + nchunks - 1) / nchunks, 64));
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += static_cast<size_t>(round_up(static_cast<int64_t>(bytes), 256));
+    return at;
+  };
+  pl.k = take(static_cast<size_t>(S) * D * esz);
+  pl.ks = take(k_scale ? static_cast<size_t>(S) * 4 : 0);
+  pl.q = take(static_cast<size_t>(T) * H * D * esz);
+  pl.qs = take(q_scale ? static_cast<size_t>(T) * H * 4 : 0);
+  pl.w = take(static_cast<size_t>(T) * H * 4);
+  pl.rs = take(static_cast<size_t>(T) * 4);
+  pl.re = take(static_cast<size_t>(T) * 4);
+  pl.out = take(static_cast<size_t>(T) * topk * 4);
+  // The chunks share one workspace; a short last chunk may take the split
+  // top-k path (more scratch per row) where a full one does not.
+  const int64_t full = std::min<int64_t>(pl.chunk, T > 0 ? T : 1);
+  const int64_t last = T > 0 ? T - (T - 1) / pl.chunk * pl.chunk : 1;
+  pl.ws = take(std::max(dsa_workspace_bytes(DSA_OP_INDEXER_TOPK, full, S, topk),
+                        dsa_workspace_bytes(DSA_OP_INDEXER_TOPK, last, S, topk)));
+  pl.total = off;
+  return pl;
+}
+
+}  // namespace
+
+size_t dsa_indexer_topk_host_bytes(int T, int S, int H, int D, int topk, dsa_dtype_t dtype) {
+  if (T < 0 || S < 0 || H < 1 || D < 1 || topk < 1) return static_cast<size_t>(-1);
+  if (dtype != DSA_BF16 && dtype != DSA_E4M3) return static_cast<size_t>(-1);
+  return host_plan(T, S, H, D, topk, dtype, true, dtype == DSA_E4M3).total;
+}
+
+dsa_status_t dsa_indexer_topk_host(const void* q, const float* q_scale, const void* k,
+                                   const float* k_scale, dsa_dtype_t dtype, const float* weights,
+                                   const int32_t* row_starts, const int32_t* row_ends, int T,
+                                   int S, int H, int D, int topk, int32_t* out,
+                                   void* device_buffer, size_t device_bytes,
+                                   dsa_stream_t stream) {
+  // Arrays indexed by row may be null when there are no rows, k when there
+  // are no keys.
+  if (T < 0 || S < 0 || H < 1 || D < 1 || topk < 1) return DSA_ERR_INVALID_ARG;
+  if ((T > 0 && (!q || !weights || !row_starts || !row_ends || !out)) || (S > 0 && !k))
+    return DSA_ERR_INVALID_ARG;
+  dsa_status_t st = check_elems(dtype, H, D, k_scale);
+  if (st != DSA_OK) return st;
+  if (static_cast<int64_t>(T) * H >= (int64_t(1) << 31)) return DSA_ERR_UNSUPPORTED;
+  if (!topk_supported(S)) return DSA_ERR_UNSUPPORTED;
+  // Sized as dsa_indexer_topk_host_bytes, which cannot know whether q_scale
+  // will be given: its region is always reserved.
+  const HostPlan pl = host_plan(T, S, H, D, topk, dtype, true, dtype == DSA_E4M3);
+  if (!device_buffer || device_bytes < pl.total || !aligned(device_buffer, 256))
+    return DSA_ERR_INVALID_ARG;
+  if (T == 0) return DSA_OK;
+  char* base = static_cast<char*>(device_buffer);
+  const size_t esz = dtype == DSA_E4M3 ? 1 : 2;
+  void* k_d = base + pl.k;
+  float* ks_d = k_scale ? reinterpret_cast<float*>(base + pl.ks) : nullptr;
+  char* q_d = base + pl.q;
+  float* qs_d = q_scale ? reinterpret_cast<float*>(base + pl.qs) : nullptr;
+  float* w_d = reinterpret_cast<float*>(base + pl.w);
+  int32_t* rs_d = reinterpret_cast<int32_t*>(base + pl.rs);
+  int32_t* re_d = reinterpret_cast<int32_t*>(base + pl.re);
+  int32_t* out_d = reinterpret_cast<int32_t*>(base + pl.out);
+  void* ws_d = base + pl.ws;
+  const int64_t ld = round_up(S > 0 ? S : 1, 4);
+  const int64_t nch = (T + pl.chunk - 1) / pl.chunk;
+
+  // Three streams: uploads, compute (the caller's), downloads.  Chunk c's
+  // upload overlaps chunk c-1's compute and chunk c-2's download.
+  cudaStream_t main = as_stream(stream), up = nullptr, down = nullptr;
+  std::vector<cudaEvent_t> ev;
+  auto event = [&]() {
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return e;
+    ev.push_back(e);
+    return e;
+  };
+  cudaError_t e = cudaStreamCreateWithFlags(&up, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&down, cudaStreamNonBlocking);
+  cudaEvent_t start = event(), k_in = event(), done = event();
+  if (e == cudaSuccess && (!start || !k_in || !done)) e = cudaErrorMemoryAllocation;
+  if (e == cudaSuccess) e = cudaEventRecord(start, main);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(up, start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(down, start, 0);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(k_d, k, static_cast<size_t>(S) * D * esz,
+                                            cudaMemcpyHostToDevice, up);
+  if (e == cudaSuccess && k_scale)
+    e = cudaMemcpyAsync(ks_d, k_scale, static_cast<size_t>(S) * 4, cudaMemcpyHostToDevice, up);
+  if (e == cudaSuccess) e = cudaEventRecord(k_in, up);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(main, k_in, 0);
+  for (int64_t c = 0; c < nch && e == cudaSuccess && st == DSA_OK; ++c) {
+    const int64_t r0 = c * pl.chunk, rows = std::min<int64_t>(pl.chunk, T - r0);
+    const int64_t qe = static_cast<int64_t>(H) * D;
+    cudaEvent_t in = event(), computed = event();
+    if (!in || !computed) {
+      e = cudaErrorMemoryAllocation;
+      break;
+    }
+    // upload chunk c
+    e = cudaMemcpyAsync(q_d + r0 * qe * esz, static_cast<const char*>(q) + r0 * qe * esz,
+                        rows * qe * esz, cudaMemcpyHostToDevice, up);
+    if (e == cudaSuccess && q_scale)
+      e = cudaMemcpyAsync(qs_d + r0 * H, q_scale + r0 * H, rows * H * 4, cudaMemcpyHostToDevice, up);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(w_d + r0 * H, weights + r0 * H, rows * H * 4, cudaMemcpyHostToDevice, up);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(rs_d + r0, row_starts + r0, rows * 4, cudaMemcpyHostToDevice, up);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(re_d + r0, row_ends + r0, rows * 4, cudaMemcpyHostToDevice, up);
+    if (e == cudaSuccess) e = cudaEventRecord(in, up);
+    // compute chunk c on the caller's stream
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(main, in, 0);
+    if (e != cudaSuccess) break;
+    float* lg = static_cast<float*>(ws_d);
+    st = run_logits(q_d + r0 * qe * esz, qs_d ? qs_d + r0 * H : nullptr, k_d, ks_d, dtype,
+                    w_d + r0 * H, rs_d + r0, re_d + r0, static_cast<int>(rows), S, H, D, lg, ld,
+                    main);
+    if (st == DSA_OK)
+      st = run_topk(lg, ld, rs_d + r0, re_d + r0, nullptr, 1, static_cast<int>(rows), S, topk,
+                    out_d + r0 * topk, main, split_scratch(ws_d, rows, S));
+    if (st != DSA_OK) break;
+    e = cudaEventRecord(computed, main);
+    // download chunk c
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(down, computed, 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(out + r0 * topk, out_d + r0 * topk, rows * topk * 4,
+                          cudaMemcpyDeviceToHost, down);
+  }
+  // Join: later work on the caller's stream sees every download.
+  cudaError_t j = cudaSuccess;
+  if (done && down) j = cudaEventRecord(done, down);
+  if (j == cudaSuccess && done) j = cudaStreamWaitEvent(main, done, 0);
+  if (up) cudaStreamDestroy(up);      // released once their work is done
+  if (down) cudaStreamDestroy(down);
+  for (cudaEvent_t x : ev) cudaEventDestroy(x);
+  if (st != DSA_OK) return st;
+  return from_cuda(e != cudaSuccess ? e : j);
 }
 
 dsa_status_t dsa_indexer_logits_paged(const void* q, const float* q_scale, const float* weights,
