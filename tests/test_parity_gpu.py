@@ -195,6 +195,36 @@ def test_topk_edge_cases(api):
     assert (got[7] == np.arange(10, 10 + k)).all()
 
 
+# Rows of at most 4096 columns take the persistent short-row kernel, which
+# loops over rows (more rows than its CTAs here) and prefetches two rows ahead:
+# every edge case on many rows, with ranges and garbage around them.
+@pytest.mark.parametrize("S,k", [(4096, 2048), (3000, 64), (4096, 4096), (700, 1)])
+def test_topk_short_rows_many(api, S, k):
+    rng = np.random.default_rng(S + k)
+    T = 1500
+    lg = rng.standard_normal((T, S)).astype(np.float32)
+    kind = np.arange(T) % 8
+    lg[kind == 1] = 0.0                                          # all ties
+    lg[kind == 2] = np.round(lg[kind == 2] * 2) / 2              # heavy ties
+    lg[kind == 3] = -np.inf                                      # nothing valid
+    sub = lg[kind == 4]
+    sub[rng.random(sub.shape) < 0.3] = np.nan
+    lg[kind == 4] = sub
+    lg[kind == 5, ::3] = -0.0                                    # signed zeros
+    ends = rng.integers(0, S + 1, size=T)
+    starts = (ends * rng.uniform(0, 0.5, size=T)).astype(np.int64)
+    rs = starts.astype(np.int32)
+    re = ends.astype(np.int32)
+    re[kind == 6] = S + 100                                      # clamped to S
+    rs[kind == 7] = re[kind == 7]                                # empty
+    dirty = lg.copy()
+    for t in range(T):
+        dirty[t, :max(rs[t], 0)] = 1e30
+        dirty[t, min(max(re[t], 0), S):] = np.inf
+    got = api.topk(dev(dirty), dev(rs), dev(re), k).cpu().numpy()
+    assert np.array_equal(got, oracle.topk(dirty, rs, re, k))
+
+
 # Row lengths that reach every top-k path: with few rows (7) the per-row
 # kernel's one-chunk rows (S <= 4096) and two-chunk rows, then the split path
 # (S > 16384); with more than 512 rows the per-row kernel's multi-chunk
