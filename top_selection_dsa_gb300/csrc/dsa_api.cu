@@ -460,7 +460,7 @@ dsa_status_t dsa_indexer_topk_host(const void* q, const float* q_scale, const vo
 
   // Three streams: uploads, compute (the caller's), downloads.  Chunk c's
   // upload overlaps chunk c-1's compute and chunk c-2's download.
-  cudaStream_t main = as_stream(stream), up = nullptr, down = nullptr;
+  cudaStream_t comp = as_stream(stream), up = nullptr, down = nullptr;
   std::vector<cudaEvent_t> ev;
   auto event = [&]() {
     cudaEvent_t e = nullptr;
@@ -470,17 +470,17 @@ dsa_status_t dsa_indexer_topk_host(const void* q, const float* q_scale, const vo
   };
   cudaError_t e = cudaStreamCreateWithFlags(&up, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&down, cudaStreamNonBlocking);
-  cudaEvent_t start = event(), k_in = event(), done = event();
-  if (e == cudaSuccess && (!start || !k_in || !done)) e = cudaErrorMemoryAllocation;
-  if (e == cudaSuccess) e = cudaEventRecord(start, main);
+  cudaEvent_t start = event(), k_in = event(), done = event(), up_done = event();
+  if (e == cudaSuccess && (!start || !k_in || !done || !up_done)) e = cudaErrorMemoryAllocation;
+  if (e == cudaSuccess) e = cudaEventRecord(start, comp);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(up, start, 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(down, start, 0);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(k_d, k, static_cast<size_t>(S) * D * esz,
-                                            cudaMemcpyHostToDevice, up);
-  if (e == cudaSuccess && k_scale)
+  if (e == cudaSuccess && S > 0)
+    e = cudaMemcpyAsync(k_d, k, static_cast<size_t>(S) * D * esz, cudaMemcpyHostToDevice, up);
+  if (e == cudaSuccess && S > 0 && k_scale)
     e = cudaMemcpyAsync(ks_d, k_scale, static_cast<size_t>(S) * 4, cudaMemcpyHostToDevice, up);
   if (e == cudaSuccess) e = cudaEventRecord(k_in, up);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(main, k_in, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(comp, k_in, 0);
   for (int64_t c = 0; c < nch && e == cudaSuccess && st == DSA_OK; ++c) {
     const int64_t r0 = c * pl.chunk, rows = std::min<int64_t>(pl.chunk, T - r0);
     const int64_t qe = static_cast<int64_t>(H) * D;
@@ -502,27 +502,30 @@ dsa_status_t dsa_indexer_topk_host(const void* q, const float* q_scale, const vo
       e = cudaMemcpyAsync(re_d + r0, row_ends + r0, rows * 4, cudaMemcpyHostToDevice, up);
     if (e == cudaSuccess) e = cudaEventRecord(in, up);
     // compute chunk c on the caller's stream
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(main, in, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(comp, in, 0);
     if (e != cudaSuccess) break;
     float* lg = static_cast<float*>(ws_d);
     st = run_logits(q_d + r0 * qe * esz, qs_d ? qs_d + r0 * H : nullptr, k_d, ks_d, dtype,
                     w_d + r0 * H, rs_d + r0, re_d + r0, static_cast<int>(rows), S, H, D, lg, ld,
-                    main);
+                    comp);
     if (st == DSA_OK)
       st = run_topk(lg, ld, rs_d + r0, re_d + r0, nullptr, 1, static_cast<int>(rows), S, topk,
-                    out_d + r0 * topk, main, split_scratch(ws_d, rows, S));
+                    out_d + r0 * topk, comp, split_scratch(ws_d, rows, S));
     if (st != DSA_OK) break;
-    e = cudaEventRecord(computed, main);
+    e = cudaEventRecord(computed, comp);
     // download chunk c
     if (e == cudaSuccess) e = cudaStreamWaitEvent(down, computed, 0);
     if (e == cudaSuccess)
       e = cudaMemcpyAsync(out + r0 * topk, out_d + r0 * topk, rows * topk * 4,
                           cudaMemcpyDeviceToHost, down);
   }
-  // Join: later work on the caller's stream sees every download.
+  // Join both streams, also after an error part-way: later work on the
+  // caller's stream sees every copy this call queued.
   cudaError_t j = cudaSuccess;
   if (done && down) j = cudaEventRecord(done, down);
-  if (j == cudaSuccess && done) j = cudaStreamWaitEvent(main, done, 0);
+  if (j == cudaSuccess && done) j = cudaStreamWaitEvent(comp, done, 0);
+  if (j == cudaSuccess && up_done && up) j = cudaEventRecord(up_done, up);
+  if (j == cudaSuccess && up_done) j = cudaStreamWaitEvent(comp, up_done, 0);
   if (up) cudaStreamDestroy(up);      // released once their work is done
   if (down) cudaStreamDestroy(down);
   for (cudaEvent_t x : ev) cudaEventDestroy(x);
