@@ -1,8 +1,9 @@
 """Thin ctypes binding over libdsa.so (include/dsa.h).
 
 Argument marshalling only: every function checks that its torch tensors are
-CUDA, contiguous and of the documented dtype, then passes raw device pointers,
-sizes and the current CUDA stream to the C ABI.  All arithmetic runs in the
+CUDA (host tensors for indexer_topk_host), contiguous and of the documented
+dtype, then passes raw pointers, sizes and the current CUDA stream to the C
+ABI.  All arithmetic runs in the
 library's kernels.  Importing this module loads libdsa.so and raises if it has
 not been built -- there is no fallback path.
 """
