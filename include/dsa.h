@@ -244,9 +244,10 @@ dsa_status_t dsa_indexer_topk_noalloc(const void* q, const float* q_scale, const
  *     logits; on return from the stream's work it holds the device copy of
  *     the inputs and of `out`.
  *   - The rows are split into up to 8 chunks (multiples of 64 rows, about
- *     512 or more each).  K goes up first; then chunk c's upload, chunk c-1's
- *     scoring + top-k (on `stream`) and chunk c-2's download run at the same
- *     time on two streams the call creates and destroys.  Work queued on
+ *     512 or more each).  K, the weights, the scales and the row ranges go up
+ *     first; then chunk c's queries go up while chunk c-1 is scored and
+ *     selected (on `stream`) and chunk c-2's indices come down, on two
+ *     streams the call creates and destroys.  Work queued on
  *     `stream` after the call sees all of `out`; host code must synchronise
  *     `stream` before it reads `out`.
  *   - Not capturable into a CUDA graph (it creates streams and events).

@@ -475,10 +475,18 @@ dsa_status_t dsa_indexer_topk_host(const void* q, const float* q_scale, const vo
   if (e == cudaSuccess) e = cudaEventRecord(start, comp);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(up, start, 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(down, start, 0);
+  // K and every row's small inputs first (a few large copies: each copy
+  // costs the copy engine microseconds however small it is), then q by chunk.
+  const size_t th = static_cast<size_t>(T) * H * 4, t4 = static_cast<size_t>(T) * 4;
   if (e == cudaSuccess && S > 0)
     e = cudaMemcpyAsync(k_d, k, static_cast<size_t>(S) * D * esz, cudaMemcpyHostToDevice, up);
   if (e == cudaSuccess && S > 0 && k_scale)
     e = cudaMemcpyAsync(ks_d, k_scale, static_cast<size_t>(S) * 4, cudaMemcpyHostToDevice, up);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(w_d, weights, th, cudaMemcpyHostToDevice, up);
+  if (e == cudaSuccess && q_scale)
+    e = cudaMemcpyAsync(qs_d, q_scale, th, cudaMemcpyHostToDevice, up);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(rs_d, row_starts, t4, cudaMemcpyHostToDevice, up);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(re_d, row_ends, t4, cudaMemcpyHostToDevice, up);
   if (e == cudaSuccess) e = cudaEventRecord(k_in, up);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(comp, k_in, 0);
   for (int64_t c = 0; c < nch && e == cudaSuccess && st == DSA_OK; ++c) {
@@ -489,17 +497,9 @@ dsa_status_t dsa_indexer_topk_host(const void* q, const float* q_scale, const vo
       e = cudaErrorMemoryAllocation;
       break;
     }
-    // upload chunk c
+    // upload chunk c's queries
     e = cudaMemcpyAsync(q_d + r0 * qe * esz, static_cast<const char*>(q) + r0 * qe * esz,
                         rows * qe * esz, cudaMemcpyHostToDevice, up);
-    if (e == cudaSuccess && q_scale)
-      e = cudaMemcpyAsync(qs_d + r0 * H, q_scale + r0 * H, rows * H * 4, cudaMemcpyHostToDevice, up);
-    if (e == cudaSuccess)
-      e = cudaMemcpyAsync(w_d + r0 * H, weights + r0 * H, rows * H * 4, cudaMemcpyHostToDevice, up);
-    if (e == cudaSuccess)
-      e = cudaMemcpyAsync(rs_d + r0, row_starts + r0, rows * 4, cudaMemcpyHostToDevice, up);
-    if (e == cudaSuccess)
-      e = cudaMemcpyAsync(re_d + r0, row_ends + r0, rows * 4, cudaMemcpyHostToDevice, up);
     if (e == cudaSuccess) e = cudaEventRecord(in, up);
     // compute chunk c on the caller's stream
     if (e == cudaSuccess) e = cudaStreamWaitEvent(comp, in, 0);
