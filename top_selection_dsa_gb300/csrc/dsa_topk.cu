@@ -312,7 +312,10 @@ __global__ void __launch_bounds__(THREADS, MINB) topk_rows_kernel(const TopkPara
   __shared__ uint32_t ncand;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int row = blockIdx.x;
+  // Last row first: under a causal mask the rows grow with their index, so
+  // the longest rows are scheduled first and the short ones fill the tail
+  // (causal T=4096 prefill: 0.031 -> 0.029 ms).
+  const int row = p.R - 1 - static_cast<int>(blockIdx.x);
   int lo, hi;
   row_range(p, row, &lo, &hi);
   const int n = hi - lo;
