@@ -154,14 +154,20 @@ __device__ __forceinline__ ScoreGroup score_group(const ScoreParams& p, int slot
   return g;
 }
 
-// ReLU of head h's dot product, as the epilogue takes it.  Three heads in four
-// use max(x, 0) (ALU pipe); every fourth uses x + |x| = 2 max(x, 0) (one add
-// on the FMA pipe), and its weight is staged halved, so that both forms give
-// the same products w * relu(x) bit for bit while the two pipes share the work.
-__host__ __device__ constexpr bool relu_by_add(int h) { return (h & 3) == 3; }
+// ReLU of head h's dot product, as the epilogue takes it.  Some heads use
+// max(x, 0) (ALU pipe), the others x + |x| = 2 max(x, 0) (one add on the FMA
+// pipe) with their weight staged halved, so that both forms give the same
+// products w * relu(x) bit for bit while the two pipes share the work: every
+// fourth head takes the add form for bf16, every second for e4m3 (whose
+// epilogue, with its weights in registers, leans harder on the ALU pipe).
+template <bool kFp8>
+__host__ __device__ constexpr bool relu_by_add(int h) {
+  return kFp8 ? (h & 1) == 1 : (h & 3) == 3;
+}
 
+template <bool kFp8>
 __device__ __forceinline__ float relu_term(int h, float x) {
-  return relu_by_add(h) ? x + fabsf(x) : fmaxf(x, 0.f);
+  return relu_by_add<kFp8>(h) ? x + fabsf(x) : fmaxf(x, 0.f);
 }
 
 // Snake order over work items: round r visits CTAs 0..P-1 forward when r is
@@ -450,7 +456,7 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
         }
         // Heads that take their ReLU as x + |x| (= 2 relu(x)) get a halved
         // weight: (w/2)(x + |x|) = w relu(x) exactly.
-        w_s[i] = relu_by_add(h) ? 0.5f * wv : wv;
+        w_s[i] = relu_by_add<kFp8>(h) ? 0.5f * wv : wv;
       }
       if constexpr (kPaged && kFp8) {
         const int bs = p.block_size;
@@ -566,7 +572,8 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
 #pragma unroll
               for (int hh = 0; hh < 8; hh += 2) {
                 const int h = c * 8 + hh;
-                const float2 y2 = make_float2(relu_term(h, v[hh]), relu_term(h + 1, v[hh + 1]));
+                const float2 y2 =
+                    make_float2(relu_term<kFp8>(h, v[hh]), relu_term<kFp8>(h + 1, v[hh + 1]));
                 const float2 w2 = make_float2(wr[j * H + h], wr[j * H + h + 1]);
                 part2[(h % 8) / 2] = __ffma2_rn(w2, y2, part2[(h % 8) / 2]);
               }
@@ -613,10 +620,10 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
 #pragma unroll
             for (int h = 0; h < H; h += 4) {
               const float4 w4 = *reinterpret_cast<const float4*>(wt + h);
-              const float2 y2a = make_float2(relu_term(h, v[j * H + h]),
-                                             relu_term(h + 1, v[j * H + h + 1]));
-              const float2 y2b = make_float2(relu_term(h + 2, v[j * H + h + 2]),
-                                             relu_term(h + 3, v[j * H + h + 3]));
+              const float2 y2a = make_float2(relu_term<kFp8>(h, v[j * H + h]),
+                                             relu_term<kFp8>(h + 1, v[j * H + h + 1]));
+              const float2 y2b = make_float2(relu_term<kFp8>(h + 2, v[j * H + h + 2]),
+                                             relu_term<kFp8>(h + 3, v[j * H + h + 3]));
               part2[(h % 8) / 2] = __ffma2_rn(make_float2(w4.x, w4.y), y2a, part2[(h % 8) / 2]);
               part2[(h % 8) / 2 + 1] =
                   __ffma2_rn(make_float2(w4.z, w4.w), y2b, part2[(h % 8) / 2 + 1]);
@@ -629,7 +636,8 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
           } else {
 #pragma unroll
             for (int h = 0; h < H; ++h)
-              part[h % C::NPART] = fmaf(wt[h], relu_term(h, v[j * H + h]), part[h % C::NPART]);
+              part[h % C::NPART] =
+                  fmaf(wt[h], relu_term<kFp8>(h, v[j * H + h]), part[h % C::NPART]);
           }
 #pragma unroll
           for (int w = C::NPART / 2; w > 0; w >>= 1) {
