@@ -232,3 +232,35 @@ def test_indexer_topk_host_validation(api):
     assert f(A, NUL, A, NUL, 0, A, A, A, 0, 8, 64, 128, 2, A, A, n, NUL) == api.DSA_OK  # no rows
     assert f(NUL, NUL, A, NUL, 0, NUL, NUL, NUL, 0, 8, 64, 128, 2, NUL, A, n, NUL) == api.DSA_OK
     assert f(A, NUL, NUL, NUL, 0, A, A, A, 8, 8, 64, 128, 2, A, A, n, NUL) == E   # keys, no k
+
+
+def test_indexer_topk_host_bytes_layout(api):
+    # The device buffer holds every input and the indices, then one row
+    # chunk's workspace: up to 8 chunks of a multiple of 64 rows (at least
+    # 512 rows each where T allows), sized for the larger of a full chunk and
+    # the last one (a short last chunk of long rows takes the split top-k).
+    ws = lambda rows, S, k: api.lib.dsa_workspace_bytes(api.DSA_OP_INDEXER_TOPK, rows, S, k)  # noqa: E731
+    up = lambda x: -(-x // 256) * 256  # noqa: E731
+
+    def expect(T, S, H, D, k, dtype):
+        esz = 1 if dtype == api.DSA_E4M3 else 2
+        nch = min(8, -(-T // 512)) if T > 0 else 1
+        chunk = max(1, -(-(-(-T // nch)) // 64) * 64) if T > 0 else 1
+        full = min(chunk, T) if T > 0 else 1
+        last = T - (T - 1) // chunk * chunk if T > 0 else 1
+        regions = [S * D * esz, S * 4 if dtype == api.DSA_E4M3 else 0, T * H * D * esz, T * H * 4,
+                   T * H * 4, T * 4, T * 4, T * k * 4, max(ws(full, S, k), ws(last, S, k))]
+        return sum(up(r) for r in regions)
+
+    nb = api.lib.dsa_indexer_topk_host_bytes
+    for T, S, H, D, k, dt in [(4096, 4096, 64, 128, 2048, api.DSA_BF16),
+                              (4700, 40000, 8, 64, 2048, api.DSA_BF16),
+                              (700, 700, 8, 64, 64, api.DSA_BF16),
+                              (1536, 1536, 64, 128, 512, api.DSA_E4M3),
+                              (1, 5, 1, 64, 1, api.DSA_BF16),
+                              (0, 64, 8, 64, 16, api.DSA_BF16)]:
+        assert nb(T, S, H, D, k, dt) == expect(T, S, H, D, k, dt), (T, S)
+    # 4700 rows: seven chunks of 640 and a last one of 220, which the split
+    # top-k takes (rows <= 512, columns > 16384) while the full chunks do not
+    assert api.lib.dsa_workspace_bytes(api.DSA_OP_TOPK, 220, 40000, 2048) > 0
+    assert api.lib.dsa_workspace_bytes(api.DSA_OP_TOPK, 640, 40000, 2048) == 0
