@@ -62,7 +62,9 @@ def _load():
     with _lock:
         if _lib is not None:
             return _lib
-        lib = ctypes.CDLL(build())
+        # DSA_ORACLE_LIB: a separately built copy of the same source (the
+        # sanitizer test loads one built with -fsanitize=address,undefined).
+        lib = ctypes.CDLL(os.environ.get("DSA_ORACLE_LIB") or build())
         P = ctypes.c_void_p
         i64 = ctypes.c_int64
         i32 = ctypes.c_int
