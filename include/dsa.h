@@ -42,6 +42,8 @@
  *    from a later call, or from dsa_get_last_device_error().
  *  - No C++ exception crosses this boundary.  All entry points are safe to
  *    call from several host threads at once.
+ *  - Each call that queues GPU work is wrapped in an NVTX range named after
+ *    its entry point (visible in Nsight timelines; free without a tool).
  *  - CUDA graphs: once an entry point has run on a device (its first call
  *    looks up per-device state), its calls can be captured into a CUDA graph.
  *    A capture fixes the shapes (rows, key capacity, k) and the pointers;

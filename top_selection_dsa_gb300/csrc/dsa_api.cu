@@ -11,6 +11,8 @@
 
 #include "dsa.h"
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <algorithm>
 #include <vector>
 #include "dsa_common.cuh"
@@ -82,6 +84,16 @@ bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 cudaStream_t as_stream(dsa_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
 dsa_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
+
+// An NVTX range named after the entry point around each call, so that a
+// profiler's timeline shows which library call queued which kernels.  (With
+// no tool attached an NVTX call returns at once.)
+struct CallRange {
+  explicit CallRange(const char* name) { nvtxRangePushA(name); }
+  ~CallRange() { nvtxRangePop(); }
+  CallRange(const CallRange&) = delete;
+  CallRange& operator=(const CallRange&) = delete;
+};
 
 // 128-byte-swizzled tiled map over a row-major [rows, D] matrix (2-D) or a
 // [blocks, block_rows, D] cache (3-D), box = 128 bytes of D x box_rows rows.
@@ -321,6 +333,7 @@ dsa_status_t dsa_indexer_logits(const void* q, const float* q_scale, const void*
                                 const int32_t* row_starts, const int32_t* row_ends, int T, int S,
                                 int H, int D, float* logits, int64_t ld, uint32_t flags,
                                 dsa_stream_t stream) {
+  const CallRange range("dsa_indexer_logits");
   dsa_status_t st = check_logits_args(q, q_scale, k, k_scale, dtype, weights, row_starts,
                                       row_ends, T, S, H, D);
   if (st != DSA_OK) return st;
@@ -338,6 +351,7 @@ dsa_status_t dsa_indexer_logits(const void* q, const float* q_scale, const void*
 dsa_status_t dsa_topk(const float* logits, int64_t ld, const int32_t* row_starts,
                       const int32_t* row_ends, int T, int S, int k, int32_t* out, void* workspace,
                       size_t ws_bytes, dsa_stream_t stream) {
+  const CallRange range("dsa_topk");
   if (!logits || !row_starts || !row_ends || !out) return DSA_ERR_INVALID_ARG;
   if (T < 0 || S < 0 || k < 1 || ld < S || ld < 1) return DSA_ERR_INVALID_ARG;
   if (!aligned(logits, 4) || !aligned(out, 4) || !aligned(row_starts, 4) ||
@@ -356,6 +370,7 @@ dsa_status_t dsa_indexer_topk(const void* q, const float* q_scale, const void* k
                               const int32_t* row_starts, const int32_t* row_ends, int T, int S,
                               int H, int D, int topk, int32_t* out, void* workspace,
                               size_t ws_bytes, dsa_stream_t stream) {
+  const CallRange range("dsa_indexer_topk");
   dsa_status_t st = check_logits_args(q, q_scale, k, k_scale, dtype, weights, row_starts,
                                       row_ends, T, S, H, D);
   if (st != DSA_OK) return st;
@@ -429,6 +444,7 @@ dsa_status_t dsa_indexer_topk_host(const void* q, const float* q_scale, const vo
                                    int S, int H, int D, int topk, int32_t* out,
                                    void* device_buffer, size_t device_bytes,
                                    dsa_stream_t stream) {
+  const CallRange range("dsa_indexer_topk_host");
   // Arrays indexed by row may be null when there are no rows, k when there
   // are no keys.
   if (T < 0 || S < 0 || H < 1 || D < 1 || topk < 1) return DSA_ERR_INVALID_ARG;
@@ -539,6 +555,7 @@ dsa_status_t dsa_indexer_logits_paged(const void* q, const float* q_scale, const
                                       int max_blocks, const int32_t* context_lens, int B,
                                       int next_n, int block_size, int H, int D, float* logits,
                                       int64_t ld, dsa_stream_t stream) {
+  const CallRange range("dsa_indexer_logits_paged");
   const PagedShape s = {B, next_n, block_size, max_blocks, num_blocks, H, D};
   dsa_status_t st = check_paged_args(q, q_scale, weights, k_cache, k_scale, dtype, block_table,
                                      context_lens, s);
@@ -555,6 +572,7 @@ dsa_status_t dsa_indexer_topk_paged(const void* q, const float* q_scale, const f
                                     const int32_t* context_lens, int B, int next_n,
                                     int block_size, int H, int D, int topk, int32_t* out,
                                     void* workspace, size_t ws_bytes, dsa_stream_t stream) {
+  const CallRange range("dsa_indexer_topk_paged");
   const PagedShape s = {B, next_n, block_size, max_blocks, num_blocks, H, D};
   dsa_status_t st = check_paged_args(q, q_scale, weights, k_cache, k_scale, dtype, block_table,
                                      context_lens, s);
@@ -579,6 +597,7 @@ dsa_status_t dsa_indexer_topk_paged(const void* q, const float* q_scale, const f
 
 dsa_status_t dsa_topk_sort_by_score(const float* logits, int64_t ld, int32_t* topk, int T, int k,
                                     dsa_stream_t stream) {
+  const CallRange range("dsa_topk_sort_by_score");
   if (!logits || !topk || T < 0 || k < 1 || ld < 1) return DSA_ERR_INVALID_ARG;
   if (!aligned(logits, 4) || !aligned(topk, 4)) return DSA_ERR_INVALID_ARG;
   if (k > kTopkSortMax) return DSA_ERR_UNSUPPORTED;
@@ -588,6 +607,7 @@ dsa_status_t dsa_topk_sort_by_score(const float* logits, int64_t ld, int32_t* to
 
 dsa_status_t dsa_topk_merge(const float* cand_scores, const int32_t* cand_cols, int T, int C,
                             int k, int32_t* out, dsa_stream_t stream) {
+  const CallRange range("dsa_topk_merge");
   if (!cand_scores || !cand_cols || !out || T < 0 || C < 1 || k < 1) return DSA_ERR_INVALID_ARG;
   if (!aligned(cand_scores, 4) || !aligned(cand_cols, 4) || !aligned(out, 4))
     return DSA_ERR_INVALID_ARG;
@@ -598,6 +618,7 @@ dsa_status_t dsa_topk_merge(const float* cand_scores, const int32_t* cand_cols, 
 dsa_status_t dsa_q_quant_fold_weights(const void* q, const float* weights, float weight_scale,
                                       int T, int H, int D, int padded_heads, void* q_fp8,
                                       float* weights_out, dsa_stream_t stream) {
+  const CallRange range("dsa_q_quant_fold_weights");
   if (!q || !weights || !q_fp8 || !weights_out || T < 0 || H < 1 || padded_heads < H)
     return DSA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(q_fp8, 8) || !aligned(weights, 4) || !aligned(weights_out, 4))
@@ -611,6 +632,7 @@ dsa_status_t dsa_k_norm_quant_insert(const void* k, const float* ln_weight, cons
                                      float eps, const int64_t* slot_mapping, int T, int D,
                                      dsa_dtype_t cache_dtype, void* k_cache, float* k_scale,
                                      int num_blocks, int block_size, dsa_stream_t stream) {
+  const CallRange range("dsa_k_norm_quant_insert");
   if (!k || !ln_weight || !ln_bias || !slot_mapping || !k_cache || T < 0 || num_blocks < 1 ||
       block_size < 1 || !(eps >= 0.f))
     return DSA_ERR_INVALID_ARG;
@@ -722,6 +744,7 @@ extern "C" dsa_status_t dsa_indexer_topk_noalloc(const void* q, const float* q_s
                                                  const int32_t* row_ends, int T, int S, int H,
                                                  int D, int topk, int32_t* out,
                                                  dsa_stream_t stream) {
+  const CallRange range("dsa_indexer_topk_noalloc");
   dsa_status_t st = check_logits_args(q, q_scale, k, k_scale, dtype, weights, row_starts,
                                       row_ends, T, S, H, D);
   if (st != DSA_OK) return st;
