@@ -160,6 +160,19 @@ def test_fp8_small(api):
     assert np.array_equal(got, oracle.topk(g, p.row_starts, p.row_ends, p.topk))
 
 
+@pytest.mark.parametrize("H", [32, 16, 8, 4, 1])
+def test_fp8_head_counts_ragged(api, H):
+    # e4m3 instances below 64 heads: registers-held weights (H >= 16) and the
+    # scalar head sum (H < 16), several key tiles with a ragged tail
+    T = S = 333
+    p = wl.prefill(T, S, H, 128, 16, seed=40 + H, dtype=wl.E4M3)
+    q, k, w, rs, re, ks = prefill_inputs(p)
+    g = api.indexer_logits(q, k, w, rs, re, k_scale=ks, clean=True).cpu().numpy()
+    assert_logits_close(g, oracle_logits(p), f"fp8 H={H}")
+    got = api.indexer_topk(q, k, w, rs, re, p.topk, k_scale=ks).cpu().numpy()
+    assert np.array_equal(got, oracle.topk(g, p.row_starts, p.row_ends, p.topk))
+
+
 def test_q_scale_argument(api):
     p = wl.prefill(130, 130, 16, 128, 8, seed=11)
     q, k, w, rs, re, _ = prefill_inputs(p)
