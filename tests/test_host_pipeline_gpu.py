@@ -84,6 +84,19 @@ def test_short_last_chunk_takes_split_path(api):
     assert torch.equal(run_host(api, p), run_device(api, p))
 
 
+def test_query_scales_go_up_too(api):
+    p = wl.prefill(900, 900, 16, 128, 64, seed=8, name="host_qscale")
+    qs = np.random.default_rng(8).uniform(0.5, 2.0, size=(900, 16)).astype(np.float32)
+    q, k = host_qk(p)
+    got = api.indexer_topk_host(q, k, host(p.w), host(p.row_starts), host(p.row_ends), p.topk,
+                                q_scale=host(qs))
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    want = api.indexer_topk(q.cuda(), k.cuda(), d(p.w), d(p.row_starts), d(p.row_ends), p.topk,
+                            q_scale=d(qs))
+    torch.cuda.synchronize()
+    assert torch.equal(got, want.cpu())
+
+
 def test_pageable_host_memory(api):
     p = wl.prefill(640, 640, 16, 128, 128, seed=5, name="host_pageable")
     assert torch.equal(run_host(api, p, pin=False), run_device(api, p))
