@@ -2,8 +2,8 @@
 
 Argument marshalling only: every function checks that its torch tensors are
 CUDA (host tensors for indexer_topk_host), contiguous and of the documented
-dtype, then passes raw pointers, sizes and the current CUDA stream to the C
-ABI.  All arithmetic runs in the
+dtype, then passes raw pointers, sizes and the current CUDA stream of the
+tensors' device to the C ABI, with that device current for the call.  All arithmetic runs in the
 library's kernels.  Importing this module loads libdsa.so and raises if it has
 not been built -- there is no fallback path.
 """
@@ -154,10 +154,11 @@ def indexer_logits(q, k, weights, row_starts, row_ends, *, q_scale=None, k_scale
     if logits is None:
         logits = torch.empty((T, S), dtype=torch.float32, device=dev)
     _need(logits, "logits", (torch.float32,), dev)
-    st = lib.dsa_indexer_logits(_ptr(q), _ptr(q_scale), _ptr(k), _ptr(k_scale), dt,
-                                _ptr(weights), _ptr(row_starts), _ptr(row_ends), T, S, H, D,
-                                _ptr(logits), logits.shape[1] if logits.dim() == 2 else S,
-                                DSA_LOGITS_CLEAN if clean else 0, _stream(dev))
+    with torch.cuda.device(dev):
+        st = lib.dsa_indexer_logits(_ptr(q), _ptr(q_scale), _ptr(k), _ptr(k_scale), dt,
+                                    _ptr(weights), _ptr(row_starts), _ptr(row_ends), T, S, H, D,
+                                    _ptr(logits), logits.shape[1] if logits.dim() == 2 else S,
+                                    DSA_LOGITS_CLEAN if clean else 0, _stream(dev))
     _check(st, "dsa_indexer_logits")
     return logits
 
@@ -175,8 +176,9 @@ def topk(logits, row_starts, row_ends, k, *, S=None, out=None, workspace=None):
     _need(out, "out", (torch.int32,), dev)
     nbytes = workspace_bytes(DSA_OP_TOPK, T, S, k)
     ws = _workspace(nbytes, dev, workspace)
-    st = lib.dsa_topk(_ptr(logits), ld, _ptr(row_starts), _ptr(row_ends), T, S, k, _ptr(out),
-                      _ptr(ws) if nbytes else None, nbytes, _stream(dev))
+    with torch.cuda.device(dev):
+        st = lib.dsa_topk(_ptr(logits), ld, _ptr(row_starts), _ptr(row_ends), T, S, k, _ptr(out),
+                          _ptr(ws) if nbytes else None, nbytes, _stream(dev))
     _check(st, "dsa_topk")
     return out
 
@@ -197,9 +199,10 @@ def indexer_topk(q, k, weights, row_starts, row_ends, topk_k, *, q_scale=None, k
     _need(out, "out", (torch.int32,), dev)
     nbytes = workspace_bytes(DSA_OP_INDEXER_TOPK, T, S, topk_k)
     ws = _workspace(nbytes, dev, workspace)
-    st = lib.dsa_indexer_topk(_ptr(q), _ptr(q_scale), _ptr(k), _ptr(k_scale), dt, _ptr(weights),
-                              _ptr(row_starts), _ptr(row_ends), T, S, H, D, topk_k, _ptr(out),
-                              _ptr(ws), nbytes, _stream(dev))
+    with torch.cuda.device(dev):
+        st = lib.dsa_indexer_topk(_ptr(q), _ptr(q_scale), _ptr(k), _ptr(k_scale), dt, _ptr(weights),
+                                  _ptr(row_starts), _ptr(row_ends), T, S, H, D, topk_k, _ptr(out),
+                                  _ptr(ws), nbytes, _stream(dev))
     _check(st, "dsa_indexer_topk")
     return out
 
@@ -248,9 +251,10 @@ def indexer_topk_host(q, k, weights, row_starts, row_ends, topk_k, *, q_scale=No
     _need(device_buffer, "device_buffer", (torch.uint8,), dev)
     if device_buffer.numel() < nbytes:
         raise ValueError(f"device_buffer holds {device_buffer.numel()} bytes, {nbytes} needed")
-    st = lib.dsa_indexer_topk_host(_ptr(q), _ptr(q_scale), _ptr(k), _ptr(k_scale), dt,
-                                   _ptr(weights), _ptr(row_starts), _ptr(row_ends), T, S, H, D,
-                                   topk_k, _ptr(out), _ptr(device_buffer), nbytes, _stream(dev))
+    with torch.cuda.device(dev):
+        st = lib.dsa_indexer_topk_host(_ptr(q), _ptr(q_scale), _ptr(k), _ptr(k_scale), dt,
+                                       _ptr(weights), _ptr(row_starts), _ptr(row_ends), T, S, H, D,
+                                       topk_k, _ptr(out), _ptr(device_buffer), nbytes, _stream(dev))
     _check(st, "dsa_indexer_topk_host")
     torch.cuda.current_stream(dev).synchronize()
     return out
@@ -278,10 +282,11 @@ def indexer_logits_paged(q, weights, k_cache, block_table, context_lens, *, next
     if logits is None:
         logits = torch.empty((R, max_blocks * block_size), dtype=torch.float32, device=dev)
     _need(logits, "logits", (torch.float32,), dev)
-    st = lib.dsa_indexer_logits_paged(_ptr(q), _ptr(q_scale), _ptr(weights), _ptr(k_cache),
-                                      _ptr(k_scale), num_blocks, dt, _ptr(block_table),
-                                      max_blocks, _ptr(context_lens), B, next_n, block_size, H,
-                                      D, _ptr(logits), logits.shape[1], _stream(dev))
+    with torch.cuda.device(dev):
+        st = lib.dsa_indexer_logits_paged(_ptr(q), _ptr(q_scale), _ptr(weights), _ptr(k_cache),
+                                          _ptr(k_scale), num_blocks, dt, _ptr(block_table),
+                                          max_blocks, _ptr(context_lens), B, next_n, block_size, H,
+                                          D, _ptr(logits), logits.shape[1], _stream(dev))
     _check(st, "dsa_indexer_logits_paged")
     return logits
 
@@ -298,10 +303,11 @@ def indexer_topk_paged(q, weights, k_cache, block_table, context_lens, topk_k, *
     _need(out, "out", (torch.int32,), dev)
     nbytes = workspace_bytes(DSA_OP_INDEXER_TOPK_PAGED, R, max_blocks * block_size, topk_k)
     ws = _workspace(nbytes, dev, workspace)
-    st = lib.dsa_indexer_topk_paged(_ptr(q), _ptr(q_scale), _ptr(weights), _ptr(k_cache),
-                                    _ptr(k_scale), num_blocks, dt, _ptr(block_table), max_blocks,
-                                    _ptr(context_lens), B, next_n, block_size, H, D, topk_k,
-                                    _ptr(out), _ptr(ws), nbytes, _stream(dev))
+    with torch.cuda.device(dev):
+        st = lib.dsa_indexer_topk_paged(_ptr(q), _ptr(q_scale), _ptr(weights), _ptr(k_cache),
+                                        _ptr(k_scale), num_blocks, dt, _ptr(block_table),
+                                        max_blocks, _ptr(context_lens), B, next_n, block_size, H,
+                                        D, topk_k, _ptr(out), _ptr(ws), nbytes, _stream(dev))
     _check(st, "dsa_indexer_topk_paged")
     return out
 
@@ -317,8 +323,9 @@ def topk_sort_by_score(logits, topk_idx):
     if logits.stride(1) != 1 or not topk_idx.is_contiguous():
         raise ValueError("row-major logits and a contiguous topk_idx expected")
     T, k = topk_idx.shape
-    st = lib.dsa_topk_sort_by_score(_ptr(logits), logits.stride(0), _ptr(topk_idx), T, k,
-                                    _stream(dev))
+    with torch.cuda.device(dev):
+        st = lib.dsa_topk_sort_by_score(_ptr(logits), logits.stride(0), _ptr(topk_idx), T, k,
+                                        _stream(dev))
     _check(st, "dsa_topk_sort_by_score")
     return topk_idx
 
@@ -335,8 +342,9 @@ def topk_merge(cand_scores, cand_cols, k, *, out=None):
     if out is None:
         out = torch.empty((T, k), dtype=torch.int32, device=dev)
     _need(out, "out", (torch.int32,), dev)
-    st = lib.dsa_topk_merge(_ptr(cand_scores), _ptr(cand_cols), T, C, int(k), _ptr(out),
-                            _stream(dev))
+    with torch.cuda.device(dev):
+        st = lib.dsa_topk_merge(_ptr(cand_scores), _ptr(cand_cols), T, C, int(k), _ptr(out),
+                                _stream(dev))
     _check(st, "dsa_topk_merge")
     return out
 
@@ -356,8 +364,9 @@ def q_quant_fold_weights(q, weights, weight_scale, padded_heads=None, *, q_fp8=N
         weights_out = torch.empty((T, Hp), dtype=torch.float32, device=dev)
     _need(q_fp8, "q_fp8", (torch.float8_e4m3fn, torch.uint8), dev)
     _need(weights_out, "weights_out", (torch.float32,), dev)
-    st = lib.dsa_q_quant_fold_weights(_ptr(q), _ptr(weights), float(weight_scale), T, H, D, Hp,
-                                      _ptr(q_fp8), _ptr(weights_out), _stream(dev))
+    with torch.cuda.device(dev):
+        st = lib.dsa_q_quant_fold_weights(_ptr(q), _ptr(weights), float(weight_scale), T, H, D, Hp,
+                                          _ptr(q_fp8), _ptr(weights_out), _stream(dev))
     _check(st, "dsa_q_quant_fold_weights")
     return q_fp8, weights_out
 
@@ -376,9 +385,10 @@ def k_norm_quant_insert(k, ln_weight, ln_bias, eps, slot_mapping, k_cache, k_sca
     T, D = k.shape
     num_blocks, block_size = k_cache.shape[0], k_cache.shape[1]
     dt = DSA_BF16 if k_cache.dtype == torch.bfloat16 else DSA_E4M3
-    st = lib.dsa_k_norm_quant_insert(_ptr(k), _ptr(ln_weight), _ptr(ln_bias), float(eps),
-                                     _ptr(slot_mapping), T, D, dt, _ptr(k_cache), _ptr(k_scale),
-                                     num_blocks, block_size, _stream(dev))
+    with torch.cuda.device(dev):
+        st = lib.dsa_k_norm_quant_insert(_ptr(k), _ptr(ln_weight), _ptr(ln_bias), float(eps),
+                                         _ptr(slot_mapping), T, D, dt, _ptr(k_cache), _ptr(k_scale),
+                                         num_blocks, block_size, _stream(dev))
     _check(st, "dsa_k_norm_quant_insert")
     return k_cache, k_scale
 
