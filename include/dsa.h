@@ -44,8 +44,10 @@
  *    call from several host threads at once.
  *  - Each call that queues GPU work is wrapped in an NVTX range named after
  *    its entry point (visible in Nsight timelines; free without a tool).
- *  - CUDA graphs: once an entry point has run on a device (its first call
- *    looks up per-device state), its calls can be captured into a CUDA graph.
+ *  - CUDA graphs: once one of dsa_indexer_logits, dsa_topk,
+ *    dsa_indexer_topk, the two paged calls, dsa_topk_sort_by_score or
+ *    dsa_topk_merge has run on a device (its first call looks up per-device
+ *    state), its calls can be captured into a CUDA graph.
  *    A capture fixes the shapes (rows, key capacity, k) and the pointers;
  *    row ranges, context lengths, block tables and the inputs themselves are
  *    read when the graph runs, so one graph serves every step of a decode
@@ -252,6 +254,9 @@ dsa_status_t dsa_indexer_topk_noalloc(const void* q, const float* q_scale, const
  *     streams the call creates and destroys.  Work queued on
  *     `stream` after the call sees all of `out`; host code must synchronise
  *     `stream` before it reads `out`.
+ *   - The copies are queued asynchronously and run after the call returns:
+ *     every host input must stay allocated and unchanged, and `out` must not
+ *     be read or freed, until `stream` has completed the call's work.
  *   - Not capturable into a CUDA graph (it creates streams and events).
  *   - Errors as dsa_indexer_topk; the indices are bit-identical to it.
  */
@@ -279,7 +284,12 @@ dsa_status_t dsa_indexer_topk_host(const void* q, const float* q_scale, const vo
  *   topk    [T, k] int32, read and rewritten.  An entry outside [0, ld) other
  *           than -1 is treated as padding (written back as -1, its column is
  *           never read) and reported by dsa_get_last_device_error as
- *           DSA_ERR_INVALID_ARG.
+ *           DSA_ERR_INVALID_ARG.  Entries inside [0, ld) are trusted: every
+ *           top-k entry point here writes columns below its S only, but the
+ *           columns [S, ld) of a composed call's workspace are row padding
+ *           that no call writes, so an index there (from elsewhere) sorts on
+ *           whatever that memory holds.  Pass ld = S when the indices may
+ *           come from another source and S is a multiple of 4.
  *   k       1 .. 8192 (larger k: DSA_ERR_UNSUPPORTED)
  */
 dsa_status_t dsa_topk_sort_by_score(const float* logits, int64_t ld, int32_t* topk, int T, int k,

@@ -22,6 +22,7 @@ Functions:
     f64_to_e4m3()        E4M3 encoder (nearest, ties to even, saturating)
     q_quant_fold(...)    query quantisation + weight fold (before the indexer)
     k_norm_insert(...)   key LayerNorm + quantisation + paged insert
+    k_layer_norm(...)    the key LayerNorm alone, fp64, before the bf16 cast
     bf16_to_f64 / e4m3_to_f64   element decoders
 """
 from __future__ import annotations
@@ -90,6 +91,8 @@ def _load():
         lib.dsa_oracle_k_norm_insert.argtypes = [P, P, P, ctypes.c_float, P, i32, i32, i32, i64,
                                                  P, P]
         lib.dsa_oracle_k_norm_insert.restype = i32
+        lib.dsa_oracle_k_layer_norm.argtypes = [P, P, P, ctypes.c_float, i32, i32, P]
+        lib.dsa_oracle_k_layer_norm.restype = i32
         lib.dsa_oracle_max_threads.argtypes = []
         lib.dsa_oracle_max_threads.restype = i32
         _lib = lib
@@ -283,6 +286,19 @@ def k_norm_insert(k_bf16_bits, ln_weight, ln_bias, eps, slots, cache, scale=None
     if rc != 0:
         raise ValueError("oracle k_norm_insert: bad arguments")
     return cache, scale
+
+
+def k_layer_norm(k_bf16_bits, ln_weight, ln_bias, eps) -> np.ndarray:
+    """The key LayerNorm of k [T,D] bf16 bits in fp64, before the cast back
+    to bf16 that k_norm_insert applies: [T,D] float64."""
+    k = np.ascontiguousarray(k_bf16_bits).view(np.uint16)
+    T, D = k.shape
+    g, b = _c(ln_weight, np.float32), _c(ln_bias, np.float32)
+    out = np.empty((T, D), np.float64)
+    rc = _load().dsa_oracle_k_layer_norm(_ptr(k), _ptr(g), _ptr(b), float(eps), T, D, _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle k_layer_norm: bad arguments")
+    return out
 
 
 def topk_merge(cand_scores, cand_cols, k) -> np.ndarray:

@@ -479,6 +479,38 @@ int dsa_oracle_q_quant_fold(const uint16_t* q, const float* w, float weight_scal
     return 0;
 }
 
+/* The bias-full LayerNorm of KimiK3DSAIndexerKNorm on one bf16 row of D
+ * elements, in double and not rounded: (x - mean) / sqrt(var + eps) *
+ * gamma + beta, population variance. */
+static void layer_norm_row(const uint16_t* src, const float* gamma, const float* beta, float eps,
+                           int D, double* out)
+{
+    double mean = 0.0, var = 0.0;
+    for (int d = 0; d < D; ++d)
+        mean += dsa_oracle_bf16_to_f64(src[d]);
+    mean /= D;
+    for (int d = 0; d < D; ++d) {
+        double c = dsa_oracle_bf16_to_f64(src[d]) - mean;
+        var += c * c;
+    }
+    var /= D;
+    double rstd = 1.0 / sqrt(var + (double)eps);
+    for (int d = 0; d < D; ++d)
+        out[d] = (dsa_oracle_bf16_to_f64(src[d]) - mean) * rstd * gamma[d] + beta[d];
+}
+
+/* k [T,D] bf16 -> out [T,D]: the LayerNorm values before the cast back to
+ * bf16 (what the rounding of dsa_oracle_k_norm_insert starts from). */
+int dsa_oracle_k_layer_norm(const uint16_t* k, const float* gamma, const float* beta, float eps,
+                            int T, int D, double* out)
+{
+    if (!k || !gamma || !beta || !out || T < 0 || D < 1)
+        return -1;
+    for (int64_t t = 0; t < T; ++t)
+        layer_norm_row(k + t * D, gamma, beta, eps, D, out + t * D);
+    return 0;
+}
+
 /* k [T,D] bf16 -> LayerNorm -> bf16 -> the cache row at slots[t].
  * dtype 0: cache holds bf16 (uint16) rows; 1: e4m3 codes + scale[slot]. */
 int dsa_oracle_k_norm_insert(const uint16_t* k, const float* gamma, const float* beta, float eps,
@@ -494,21 +526,9 @@ int dsa_oracle_k_norm_insert(const uint16_t* k, const float* gamma, const float*
         int64_t slot = slots[t];
         if (slot < 0 || slot >= capacity)
             continue;
-        const uint16_t* src = k + t * D;
-        double mean = 0.0, var = 0.0;
+        layer_norm_row(k + t * D, gamma, beta, eps, D, y);
         for (int d = 0; d < D; ++d)
-            mean += dsa_oracle_bf16_to_f64(src[d]);
-        mean /= D;
-        for (int d = 0; d < D; ++d) {
-            double c = dsa_oracle_bf16_to_f64(src[d]) - mean;
-            var += c * c;
-        }
-        var /= D;
-        double rstd = 1.0 / sqrt(var + (double)eps);
-        for (int d = 0; d < D; ++d) {
-            double v = (dsa_oracle_bf16_to_f64(src[d]) - mean) * rstd * gamma[d] + beta[d];
-            y[d] = dsa_oracle_bf16_to_f64(f64_to_bf16_rne(v));   /* .type_as(x) */
-        }
+            y[d] = dsa_oracle_bf16_to_f64(f64_to_bf16_rne(y[d]));   /* .type_as(x) */
         if (dtype == 0) {
             uint16_t* dst = (uint16_t*)cache + slot * D;
             for (int d = 0; d < D; ++d)

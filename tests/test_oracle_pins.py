@@ -532,6 +532,29 @@ def test_k_norm_insert_layer_norm_and_slots():
         assert np.array_equal(c8.reshape(12, D)[s], q8[0, 0]) and sc[s] == wo[0, 0]
 
 
+def test_k_layer_norm_is_torch_layer_norm_in_double():
+    # The unrounded LayerNorm the insert rounds: torch's own fp64 layer_norm
+    # on the same bf16 inputs, to double rounding; a constant row gives the
+    # bias exactly; the insert's bf16 output is within half a bf16 step of it.
+    rng = np.random.default_rng(3)
+    T, D = 9, 128
+    k = rng.standard_normal((T, D)) * rng.choice([0.01, 0.3, 20.0], (T, 1)) + 0.2
+    k[4] = -2.5                                                # constant row
+    kb = bf16(k)
+    g = (1 + 0.1 * rng.standard_normal(D)).astype(np.float32)
+    b = (0.05 * rng.standard_normal(D)).astype(np.float32)
+    got = oracle.k_layer_norm(kb, g, b, 1e-6)
+    ref = torch.nn.functional.layer_norm(torch.from_numpy(wl.bf16_bits_to_f32(kb)).double(), (D,),
+                                         torch.from_numpy(g).double(), torch.from_numpy(b).double(),
+                                         1e-6).numpy()
+    assert np.all(np.abs(got - ref) <= 1e-9 * (np.abs(ref) + 1.0))   # rows of tiny variance amplify rounding
+    assert np.array_equal(got[4], b.astype(np.float64))
+    cache = np.zeros((1, T, D), np.uint16)
+    oracle.k_norm_insert(kb, g, b, 1e-6, np.arange(T, dtype=np.int64), cache)
+    rounded = oracle.bf16_to_f64(cache.reshape(T * D)).reshape(T, D)
+    assert np.all(np.abs(rounded - got) <= np.abs(got) * 2.0 ** -8 + 1e-30)
+
+
 # ----------------------------------------------------------- rank merge
 
 def test_topk_merge_hand_example_and_whole_row():

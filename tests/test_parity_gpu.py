@@ -259,6 +259,30 @@ def test_topk_row_lengths(api, S, k, T):
     assert np.array_equal(got, oracle.topk(lg, rs, re, k))
 
 
+def test_topk_reads_ranges_written_just_before_on_the_stream(api):
+    # dsa_topk's row ranges come out of kernels queued immediately before it
+    # on the same stream (with stale zero ranges in the buffers beforehand):
+    # the top-k must see the new ranges, not the stale ones.
+    rng = np.random.default_rng(31)
+    T, S, k = 2048, 6000, 256
+    lg = rng.standard_normal((T, S)).astype(np.float32)
+    rs = rng.integers(-10, S // 2, T).astype(np.int32)
+    re = (rs + rng.integers(0, S // 2 + 20, T)).astype(np.int32)
+    lg_d, rs_src, re_src = dev(lg), dev(rs), dev(re)
+    ref = oracle.topk(lg, rs, re, k)
+    rs_d = torch.zeros(T, dtype=torch.int32, device="cuda")
+    re_d = torch.zeros(T, dtype=torch.int32, device="cuda")
+    big = torch.ones(1 << 24, device="cuda")
+    for _ in range(5):
+        rs_d.zero_()
+        re_d.zero_()
+        big.mul_(1.0)                               # a long kernel ahead of the writers
+        torch.add(rs_src, 0, out=rs_d)              # elementwise kernels, the second
+        torch.add(re_src, 0, out=re_d)              # queued right before dsa_topk
+        got = api.topk(lg_d, rs_d, re_d, k)
+        assert np.array_equal(got.cpu().numpy(), ref)
+
+
 # --------------------------------------------------------------------- paged
 
 @pytest.mark.parametrize("next_n,block_size,H,fp8", [(2, 64, 64, False), (1, 16, 64, False),
@@ -316,16 +340,59 @@ def test_paged_bad_block_id_is_reported_not_dereferenced(api):
 
 # -------------------------------------------------------- full-size workloads
 
+def edge_rows(starts, lens, n=64):
+    """The first and last n rows of every sequence (packed at the given starts)."""
+    rows = set()
+    for a, L in zip(starts, lens):
+        rows.update(range(a, a + min(n, L)))
+        rows.update(range(a + max(L - n, 0), a + L))
+    return rows
+
+
+def check_topk_all_rows(got, lg, p, chunk=2048):
+    """The GPU's top-k of every row against the oracle's top-k of the same
+    (GPU) logits, brought to the host a row chunk at a time."""
+    for r0 in range(0, p.T, chunk):
+        r1 = min(p.T, r0 + chunk)
+        g = lg[r0:r1].cpu().numpy()
+        ref = oracle.topk(g, p.row_starts[r0:r1], p.row_ends[r0:r1], p.topk, S=p.S)
+        if not np.array_equal(got[r0:r1], ref):
+            bad = np.nonzero((got[r0:r1] != ref).any(axis=1))[0]
+            raise AssertionError(f"top-k differs on {bad.size} rows of [{r0}, {r1}), "
+                                 f"first row {r0 + int(bad[0])}")
+
+
+def fused_with_logits(api, p, q, k, w, rs, re, ks=None):
+    """dsa_indexer_topk, and the logits it left at the start of its workspace."""
+    ws = torch.empty(api.workspace_bytes(api.DSA_OP_INDEXER_TOPK, p.T, p.S, p.topk),
+                     dtype=torch.uint8, device="cuda")
+    out = api.indexer_topk(q, k, w, rs, re, p.topk, k_scale=ks, workspace=ws)
+    ld = (p.S + 3) // 4 * 4
+    lg = ws[:p.T * ld * 4].view(torch.float32).view(p.T, ld)[:, :p.S]
+    return out.cpu().numpy(), lg
+
+
+def check_rows_logits(lg, p, rows, what):
+    g = lg[torch.from_numpy(rows).cuda()].cpu().numpy()
+    ref = oracle_logits(p, rows)
+    for i, t in enumerate(rows):                   # the row's own range
+        lo, hi = max(int(p.row_starts[t]), 0), min(int(p.row_ends[t]), p.S)
+        assert_logits_close(g[i, lo:hi], ref[i, lo:hi], f"{what} row {t}")
+
+
 def test_prefill_causal_4096_full_size(api):
     p = wl.prefill_causal()
     q, k, w, rs, re, _ = prefill_inputs(p)
     lg = api.indexer_logits(q, k, w, rs, re, clean=True)
     g = lg.cpu().numpy()
-    rows = sample_rows(p.T, 24, seed=1, always=(0, 1, 127, 128, 2047, 2048, 4095))
+    rows = sample_rows(p.T, 24, seed=1, always=edge_rows([0], [p.T]) | {2047, 2048})
     assert_logits_close(g[rows], oracle_logits(p, rows), "prefill 4096")
     ref = oracle.topk(g, p.row_starts, p.row_ends, p.topk)
-    fused = api.indexer_topk(q, k, w, rs, re, p.topk).cpu().numpy()
+    fused, flg = fused_with_logits(api, p, q, k, w, rs, re)
     assert np.array_equal(fused, ref)
+    cols = torch.arange(p.S, device="cuda")
+    mask = (cols[None, :] >= rs[:, None]) & (cols[None, :] < re[:, None])
+    assert torch.equal(flg[mask], lg[mask])        # the fused call's logits, bit for bit
     assert np.array_equal(api.topk(lg, rs, re, p.topk).cpu().numpy(), ref)
     assert (ref[2047:] != -1).all() and (ref[:2047, -1] == -1).all()
 
@@ -333,32 +400,28 @@ def test_prefill_causal_4096_full_size(api):
 def test_prefill_thd_full_size(api):
     p = wl.prefill_thd()
     q, k, w, rs, re, _ = prefill_inputs(p)
-    lg = api.indexer_logits(q, k, w, rs, re, clean=True)
-    g = lg.cpu().numpy()
+    fused, lg = fused_with_logits(api, p, q, k, w, rs, re)
     offs = np.cumsum([0] + p.seq_lens)
-    edges = [o + d for o in offs[:-1] for d in (0, 1, 2047, 2048)] + [int(offs[-1]) - 1]
-    rows = sample_rows(p.T, 24, seed=2, always=edges)
-    assert_logits_close(g[rows], oracle_logits(p, rows), "thd")
-    fused = api.indexer_topk(q, k, w, rs, re, p.topk).cpu().numpy()
-    ref = oracle.topk(g, p.row_starts, p.row_ends, p.topk)
-    assert np.array_equal(fused, ref)
+    rows = sample_rows(p.T, 24, seed=2, always=edge_rows(offs[:-1], p.seq_lens))
+    check_rows_logits(lg, p, rows, "thd")
+    check_topk_all_rows(fused, lg, p)
 
 
 def test_paged_decode_full_size(api):
     p = wl.paged_decode()
-    check_paged(api, p, rows=sample_rows(p.R, 12, seed=3, always=(0, 1, p.R - 1)))
+    check_paged(api, p, rows=None)                 # every row: logits and top-k
 
 
 def test_prefill_fp8_32768_full_size(api):
+    # Every row's top-k (bit-exact against the oracle's top-k of the fused
+    # call's own logits); the logits of the first and last 64 rows and a
+    # seeded sample (the oracle's fp64 logits take ~0.5 GFLOP per long row).
     p = wl.prefill_fp8()
     q, k, w, rs, re, ks = prefill_inputs(p)
-    lg = api.indexer_logits(q, k, w, rs, re, k_scale=ks)
-    rows = sample_rows(p.T, 16, seed=4, always=(0, 2047, 2048, 32767))
-    g = lg[torch.from_numpy(rows).cuda()].cpu().numpy()
-    ref = oracle_logits(p, rows)
-    for i, t in enumerate(rows):                   # written part: [0, t + 1)
-        assert_logits_close(g[i, :t + 1], ref[i, :t + 1], f"fp8 row {t}")
-    fused = api.indexer_topk(q, k, w, rs, re, p.topk, k_scale=ks)
-    got = fused[torch.from_numpy(rows).cuda()].cpu().numpy()
-    ref_idx = oracle.topk(g, p.row_starts[rows], p.row_ends[rows], p.topk)
-    assert np.array_equal(got, ref_idx)
+    fused, lg = fused_with_logits(api, p, q, k, w, rs, re, ks)
+    rows = sample_rows(p.T, 16, seed=4, always=edge_rows([0], [p.T]) | {2047, 2048})
+    check_rows_logits(lg, p, rows, "fp8")
+    check_topk_all_rows(fused, lg, p)
+    unfused = api.indexer_logits(q, k, w, rs, re, k_scale=ks)
+    for t in (0, 1000, 2047, 20000, 32767):          # the unfused call: same logits
+        assert torch.equal(unfused[t, :t + 1], lg[t, :t + 1])

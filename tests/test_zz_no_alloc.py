@@ -1,15 +1,18 @@
 """dsa_indexer_topk_noalloc, called through the C ABI (needs a GPU).
 
 This entry point serves callers that cannot allocate device memory when they
-call the indexer -- code inside CUDA-graph capture without a graph-safe
-allocator, plugins whose host framework owns every allocation, serving loops
-that cannot afford cudaMalloc's synchronisation.  It keeps the logits in a
+call the indexer: code running while its stream is captured (where cudaMalloc
+is not allowed) without a graph-safe allocator at hand, plugins whose host
+framework owns every device allocation, and serving loops that cannot afford
+cudaMalloc's implicit synchronisation.  It keeps the logits in a
 fixed 64 MiB device array of the library instead of a caller workspace.
 
 The test runs it twice in a row on different inputs (so the second call finds
 the first call's logits still in the shared array) and compares each result
 with dsa_indexer_topk, which takes a caller workspace: the indices must be
-identical.  The file is named so that pytest collects it last.
+identical.  A second case uses the shape where the workspace entry point
+splits long rows over many CTAs and the no-alloc one does not.  The file is
+named so that pytest collects it last.
 """
 import ctypes
 
@@ -63,6 +66,30 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(api):
         want = api.indexer_topk(q, k, w, rs_d, re_d, p.topk)
         torch.cuda.synchronize()
         assert torch.equal(got, want)
+    assert api.last_device_error() == api.DSA_OK
+
+
+def test_noalloc_matches_where_the_workspace_call_splits_rows(api):
+    # 256 rows of up to 32768 keys: dsa_indexer_topk takes the split top-k
+    # (many CTAs per row, scratch in its workspace), the no-alloc call the
+    # per-row kernel (its array holds only the logits: 256 * 32768 * 4 bytes
+    # = 32 MiB).  Both must select the same columns, ties and clamped or
+    # empty ranges included.
+    T, S = 256, 32768
+    rng = np.random.default_rng(23)
+    rs = rng.integers(-100, S // 2, T).astype(np.int32)
+    re = (rs + rng.integers(0, S + 200, T)).astype(np.int32)   # some past S
+    re[:4] = rs[:4]                                            # empty rows
+    rs[4:8], re[4:8] = -5, S + 9                               # whole, clamped
+    p = wl.prefill(T, S, 64, 128, 2048, rs, re, seed=24)
+    p.k[:] = p.k[np.arange(S) % 97]       # repeated key rows: exact ties
+    q, k, w, rs_d, re_d = _inputs(p)
+    for _ in range(2):
+        got = _noalloc(api, p, q, k, w, rs_d, re_d)
+        want = api.indexer_topk(q, k, w, rs_d, re_d, p.topk)
+        torch.cuda.synchronize()
+        assert torch.equal(got, want)
+    assert (got[:4] == -1).all()
     assert api.last_device_error() == api.DSA_OK
 
 

@@ -203,9 +203,11 @@ dsa_status_t run_logits(const void* q, const float* q_scale, const void* k, cons
 
 dsa_status_t run_topk(const float* logits, int64_t ld, const int32_t* row_starts,
                       const int32_t* row_ends, const int32_t* context_lens, int next_n, int R,
-                      int S, int k, int32_t* out, cudaStream_t st, uint32_t* split = nullptr) {
+                      int S, int k, int32_t* out, cudaStream_t st, uint32_t* split,
+                      bool after_score) {
   if (R == 0) return DSA_OK;
   TopkParams p = {};
+  p.after_score = after_score ? 1 : 0;
   p.logits = logits;
   p.ld = ld;
   p.row_starts = row_starts;
@@ -362,7 +364,7 @@ dsa_status_t dsa_topk(const float* logits, int64_t ld, const int32_t* row_starts
   if (need > 0 && (!workspace || ws_bytes < need || !aligned(workspace, 256)))
     return DSA_ERR_INVALID_ARG;
   return run_topk(logits, ld, row_starts, row_ends, nullptr, 1, T, S, k, out, as_stream(stream),
-                  need > 0 ? static_cast<uint32_t*>(workspace) : nullptr);
+                  need > 0 ? static_cast<uint32_t*>(workspace) : nullptr, false);
 }
 
 dsa_status_t dsa_indexer_topk(const void* q, const float* q_scale, const void* k,
@@ -386,7 +388,7 @@ dsa_status_t dsa_indexer_topk(const void* q, const float* q_scale, const void* k
                   as_stream(stream));
   if (st != DSA_OK) return st;
   return run_topk(lg, ld, row_starts, row_ends, nullptr, 1, T, S, topk, out, as_stream(stream),
-                  split_scratch(workspace, T, S));
+                  split_scratch(workspace, T, S), true);
 }
 
 // ---------------------------------------------------- host-buffer pipeline
@@ -526,7 +528,7 @@ dsa_status_t dsa_indexer_topk_host(const void* q, const float* q_scale, const vo
                     comp);
     if (st == DSA_OK)
       st = run_topk(lg, ld, rs_d + r0, re_d + r0, nullptr, 1, static_cast<int>(rows), S, topk,
-                    out_d + r0 * topk, comp, split_scratch(ws_d, rows, S));
+                    out_d + r0 * topk, comp, split_scratch(ws_d, rows, S), true);
     if (st != DSA_OK) break;
     e = cudaEventRecord(computed, comp);
     // download chunk c
@@ -592,7 +594,7 @@ dsa_status_t dsa_indexer_topk_paged(const void* q, const float* q_scale, const f
   if (st != DSA_OK) return st;
   return run_topk(lg, ld, nullptr, nullptr, context_lens, next_n, static_cast<int>(R),
                   static_cast<int>(max_ctx), topk, out, as_stream(stream),
-                  split_scratch(workspace, R, max_ctx));
+                  split_scratch(workspace, R, max_ctx), true);
 }
 
 dsa_status_t dsa_topk_sort_by_score(const float* logits, int64_t ld, int32_t* topk, int T, int k,
@@ -759,5 +761,6 @@ extern "C" dsa_status_t dsa_indexer_topk_noalloc(const void* q, const float* q_s
   st = run_logits(q, q_scale, k, k_scale, dtype, weights, row_starts, row_ends, T, S, H, D, lg, ld,
                   as_stream(stream));
   if (st != DSA_OK) return st;
-  return run_topk(lg, ld, row_starts, row_ends, nullptr, 1, T, S, topk, out, as_stream(stream));
+  return run_topk(lg, ld, row_starts, row_ends, nullptr, 1, T, S, topk, out, as_stream(stream),
+                  nullptr, true);
 }

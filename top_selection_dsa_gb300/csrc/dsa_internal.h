@@ -51,6 +51,12 @@ struct TopkParams {
   int32_t* out;      // [R, k]
   uint32_t* split;   // null, or [R, split_words] scratch of the split path (topk_split_rows)
   int split_words;   // words of split scratch per row (topk_split_words(S))
+  // 1 when the kernel queued just before on the stream is this library's own
+  // scoring kernel (the composed calls): the per-row top-k kernel may then be
+  // its programmatic dependent, since the row ranges it reads before waiting
+  // were written before that scoring kernel started.  0 for the standalone
+  // dsa_topk, whose predecessor may be the caller's kernel writing them.
+  int after_score;
 };
 
 // Launchers (return the launch error, if any).  Shapes were validated by the

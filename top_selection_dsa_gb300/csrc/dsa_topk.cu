@@ -1436,11 +1436,13 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t s) {
     cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = s;
+    // A programmatic dependent of the scoring kernel only: the kernel reads
+    // its row range before griddepcontrol.wait.
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = p.after_score ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, topk_rows_kernel<256, 5>, p, cand, words);
   }
   // Otherwise: 256-thread CTAs that stream the row (8 rows in flight per SM).
