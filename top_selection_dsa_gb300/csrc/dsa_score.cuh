@@ -432,6 +432,11 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
     const int wg = (ew >> 2) % C::EPI_WG;  // column group of this warpgroup
     const int quarter = warp & 3;  // the TMEM lane quarter this warp may access
     const int key_in_tile = quarter * 32 + lane;
+    // e4m3 with 64 heads reads the accumulator in the 16x256b shape: each
+    // thread sums 16 heads of 4 keys, a quad of threads shares those keys,
+    // and after the exchange each thread owns one of them.
+    constexpr bool kQuad = kFp8 && !kPaged && H == 64 && C::EPI_COLS == 64;
+    const int my_key = kQuad ? quarter * 32 + (lane >> 2) + 8 * (lane & 3) : key_in_tile;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const int etid = threadIdx.x - 64;  // 0 .. EPI_THREADS-1
     int tcount = 0;
@@ -456,7 +461,7 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
         }
         // Heads that take their ReLU as x + |x| (= 2 relu(x)) get a halved
         // weight: (w/2)(x + |x|) = w relu(x) exactly.
-        w_s[i] = relu_by_add<kFp8>(h) ? 0.5f * wv : wv;
+        w_s[i] = (kQuad || relu_by_add<kFp8>(h)) ? 0.5f * wv : wv;
       }
       if constexpr (kPaged && kFp8) {
         const int bs = p.block_size;
@@ -498,7 +503,14 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
       // the whole group, and the accumulator is read 8 columns at a time, so
       // that the epilogue leaves shared-memory bandwidth to the MMA operand
       // reads (an e4m3 tile takes half the MMA time of a bf16 one).
-      constexpr bool kRegW = kFp8 && H >= 16 && C::NPART == 8;
+      constexpr bool kRegW = kFp8 && H >= 16 && C::NPART == 8 && !kQuad;
+      // kQuad: this thread's 16 heads 8b + 2(lane%4) + {0,1}, b = 0..7, as pairs.
+      float2 wq[kQuad ? 8 : 1];
+      if constexpr (kQuad) {
+#pragma unroll
+        for (int b = 0; b < 8; ++b)
+          wq[b] = *reinterpret_cast<const float2*>(w_s + wg * C::EPI_COLS + 8 * b + 2 * (lane & 3));
+      }
       float wr[kRegW ? C::EPI_COLS : 1];
       if constexpr (kRegW) {
 #pragma unroll
@@ -513,7 +525,7 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
 
       // fp8: this thread's key scale, loaded one tile ahead of its use.
       auto key_scale = [&](int kt) -> float {
-        const int s = kt * C::TILE + key_in_tile;
+        const int s = kt * C::TILE + my_key;
         if constexpr (kPaged) {
           const int bs = p.block_size;
           const int nblk = (g.L + bs - 1) / bs;
@@ -545,12 +557,74 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
         tc_fence_after_sync();
         const uint32_t tcol =
             tmem_base + lane_addr + static_cast<uint32_t>(buf * N + wg * C::EPI_COLS);
-        const int s = kt * C::TILE + key_in_tile;
+        const int s = kt * C::TILE + my_key;
         const float kscale = ks_next;
         if constexpr (kFp8) {
           if (kt + C::EPI_SETS < g.kt_end) ks_next = key_scale(kt + C::EPI_SETS);
         }
         const bool col_ok = s < p.S;
+        if constexpr (kQuad) {
+          // Four chunks of 16 columns, each read as two 16-lane halves; the
+          // next chunk's loads are in flight while this one is summed.
+          // ReLU as x + |x| (one packed add, the weights staged halved).
+          const uint32_t cb = tmem_base + static_cast<uint32_t>(buf * N + wg * C::EPI_COLS);
+          const uint32_t l0 = static_cast<uint32_t>(quarter * 32) << 16;
+          const uint32_t l1 = static_cast<uint32_t>(quarter * 32 + 16) << 16;
+          float2 acc4[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc4[i] = make_float2(0.f, 0.f);
+          uint32_t cur[16], nxt[16];
+          tmem_ld16x256_x2_async(cb + l0, cur);
+          tmem_ld16x256_x2_async(cb + l1, cur + 8);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            tmem_wait_ld16(cur);
+            if (c == 3) {
+              // Every column of this tile is in registers: release it.
+              tc_fence_before_sync();
+              mbar_arrive(&acce[buf]);
+            } else {
+              tmem_ld16x256_x2_async(cb + l0 + static_cast<uint32_t>(16 * (c + 1)), nxt);
+              tmem_ld16x256_x2_async(cb + l1 + static_cast<uint32_t>(16 * (c + 1)), nxt + 8);
+            }
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+              for (int rep = 0; rep < 2; ++rep) {
+                const int r0 = 8 * hf + 4 * rep;
+                const float2 w2 = wq[2 * c + rep];
+                const float2 xa = make_float2(__uint_as_float(cur[r0]), __uint_as_float(cur[r0 + 1]));
+                const float2 xb =
+                    make_float2(__uint_as_float(cur[r0 + 2]), __uint_as_float(cur[r0 + 3]));
+                const float2 ya = __fadd2_rn(xa, make_float2(fabsf(xa.x), fabsf(xa.y)));
+                const float2 yb = __fadd2_rn(xb, make_float2(fabsf(xb.x), fabsf(xb.y)));
+                acc4[2 * hf] = __ffma2_rn(w2, ya, acc4[2 * hf]);
+                acc4[2 * hf + 1] = __ffma2_rn(w2, yb, acc4[2 * hf + 1]);
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) cur[i] = nxt[i];
+          }
+          // This thread's 16-head sums of keys +0, +8, +16, +24 (from lane/4);
+          // the quad exchanges halves twice and thread m keeps key +8m.
+          float tot[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) tot[i] = acc4[i].x + acc4[i].y;
+          const bool b0 = (lane & 1) != 0, b1 = (lane & 2) != 0;
+          float k0 = b0 ? tot[1] : tot[0], k1 = b0 ? tot[3] : tot[2];
+          const float s0 = b0 ? tot[0] : tot[1], s1 = b0 ? tot[2] : tot[3];
+          k0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+          k1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+          float acc = b1 ? k1 : k0;
+          acc += __shfl_xor_sync(0xffffffffu, b1 ? k0 : k1, 2);
+          acc *= kscale;
+          const int tok = wg;
+          if (tok < g.ntok && col_ok) {
+            const float val = (s >= rlo[0] && s < rhi[0]) ? acc : -INFINITY;
+            p.logits[static_cast<int64_t>(g.row0 + tok) * p.ld + s] = val;
+          }
+          continue;
+        }
         if constexpr (kRegW) {
 #pragma unroll
           for (int j = 0; j < C::EPI_TOK; ++j) {
