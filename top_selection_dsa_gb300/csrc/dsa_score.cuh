@@ -570,9 +570,9 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
           const uint32_t cb = tmem_base + static_cast<uint32_t>(buf * N + wg * C::EPI_COLS);
           const uint32_t l0 = static_cast<uint32_t>(quarter * 32) << 16;
           const uint32_t l1 = static_cast<uint32_t>(quarter * 32 + 16) << 16;
-          float2 acc4[4];
+          float2 acc4[4], acc4b[4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) acc4[i] = make_float2(0.f, 0.f);
+          for (int i = 0; i < 4; ++i) acc4[i] = acc4b[i] = make_float2(0.f, 0.f);
           uint32_t cur[16], nxt[16];
           tmem_ld16x256_x2_async(cb + l0, cur);
           tmem_ld16x256_x2_async(cb + l1, cur + 8);
@@ -598,8 +598,13 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
                     make_float2(__uint_as_float(cur[r0 + 2]), __uint_as_float(cur[r0 + 3]));
                 const float2 ya = __fadd2_rn(xa, make_float2(fabsf(xa.x), fabsf(xa.y)));
                 const float2 yb = __fadd2_rn(xb, make_float2(fabsf(xb.x), fabsf(xb.y)));
-                acc4[2 * hf] = __ffma2_rn(w2, ya, acc4[2 * hf]);
-                acc4[2 * hf + 1] = __ffma2_rn(w2, yb, acc4[2 * hf + 1]);
+                if (rep == 0) {
+                  acc4[2 * hf] = __ffma2_rn(w2, ya, acc4[2 * hf]);
+                  acc4[2 * hf + 1] = __ffma2_rn(w2, yb, acc4[2 * hf + 1]);
+                } else {
+                  acc4b[2 * hf] = __ffma2_rn(w2, ya, acc4b[2 * hf]);
+                  acc4b[2 * hf + 1] = __ffma2_rn(w2, yb, acc4b[2 * hf + 1]);
+                }
               }
             }
 #pragma unroll
@@ -609,7 +614,10 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
           // the quad exchanges halves twice and thread m keeps key +8m.
           float tot[4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) tot[i] = acc4[i].x + acc4[i].y;
+          for (int i = 0; i < 4; ++i) {
+            const float2 t2 = __fadd2_rn(acc4[i], acc4b[i]);
+            tot[i] = t2.x + t2.y;
+          }
           const bool b0 = (lane & 1) != 0, b1 = (lane & 2) != 0;
           float k0 = b0 ? tot[1] : tot[0], k1 = b0 ? tot[3] : tot[2];
           const float s0 = b0 ? tot[0] : tot[1], s1 = b0 ? tot[2] : tot[3];
