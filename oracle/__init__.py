@@ -14,6 +14,7 @@ it with gcc on first use and wraps it for numpy arrays.
 Functions:
     logits(...)          dense prefill logits, fp64          (indexer score)
     logits_paged(...)    paged-decode logits, fp64           (indexer score)
+    logits_mxfp4(...)    prefill logits of MXFP4 q/k (E2M1 + E8M0 block scales)
     paged_row_ranges()   the row ranges of paged decode
     topk(...)            masked per-row top-k of given fp32 logits
                          (torch_dsa_topk, vime PR #502, third review comment)
@@ -23,7 +24,7 @@ Functions:
     q_quant_fold(...)    query quantisation + weight fold (before the indexer)
     k_norm_insert(...)   key LayerNorm + quantisation + paged insert
     k_layer_norm(...)    the key LayerNorm alone, fp64, before the bf16 cast
-    bf16_to_f64 / e4m3_to_f64   element decoders
+    bf16_to_f64 / e4m3_to_f64 / e2m1_to_f64 / e8m0_to_f64   element decoders
 """
 from __future__ import annotations
 
@@ -92,6 +93,13 @@ def _load():
                                                  P, P]
         lib.dsa_oracle_k_norm_insert.restype = i32
         lib.dsa_oracle_k_layer_norm.argtypes = [P, P, P, ctypes.c_float, i32, i32, P]
+        lib.dsa_oracle_e2m1_to_f64.argtypes = [ctypes.c_uint8]
+        lib.dsa_oracle_e2m1_to_f64.restype = ctypes.c_double
+        lib.dsa_oracle_e8m0_to_f64.argtypes = [ctypes.c_uint8]
+        lib.dsa_oracle_e8m0_to_f64.restype = ctypes.c_double
+        lib.dsa_oracle_logits_mxfp4.argtypes = [P, P, P, P, P, P, P, i64, i64, i32, i32, P, i64,
+                                                P, i32]
+        lib.dsa_oracle_logits_mxfp4.restype = i32
         lib.dsa_oracle_k_layer_norm.restype = i32
         lib.dsa_oracle_max_threads.argtypes = []
         lib.dsa_oracle_max_threads.restype = i32
@@ -158,6 +166,48 @@ def logits(q, k, w, row_starts, row_ends, *, dtype=BF16, q_scale=None,
                                    _ptr(rr), n, _ptr(out), nthreads)
     if rc != 0:
         raise ValueError("oracle logits: bad arguments")
+    return out
+
+
+def e2m1_to_f64(codes) -> np.ndarray:
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8).ravel()
+    return np.array([lib.dsa_oracle_e2m1_to_f64(int(v)) for v in c])
+
+
+def e8m0_to_f64(codes) -> np.ndarray:
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8).ravel()
+    return np.array([lib.dsa_oracle_e8m0_to_f64(int(v)) for v in c])
+
+
+def logits_mxfp4(q, q_sf, k, k_sf, w, row_starts, row_ends, *, rows=None,
+                 nthreads=0) -> np.ndarray:
+    """fp64 index logits [len(rows) or T, S] of MXFP4 operands.
+
+    q: [T, H, D/2] packed E2M1 (uint8, the low nibble is the even element),
+    q_sf: [T, H, D/32] E8M0 codes, k: [S, D/2], k_sf: [S, D/32], w: [T, H].
+    """
+    qe = np.ascontiguousarray(q, dtype=np.uint8)
+    ke = np.ascontiguousarray(k, dtype=np.uint8)
+    T, H, D2 = qe.shape
+    D = 2 * D2
+    S = ke.shape[0]
+    assert ke.shape[1] == D2
+    qs = np.ascontiguousarray(q_sf, dtype=np.uint8)
+    ks = np.ascontiguousarray(k_sf, dtype=np.uint8)
+    assert qs.shape == (T, H, D // 32) and ks.shape == (S, D // 32)
+    wf = _c(w, np.float32)
+    rs = _c(row_starts, np.int32)
+    re_ = _c(row_ends, np.int32)
+    rr = _c(rows, np.int64)
+    n = T if rr is None else rr.shape[0]
+    out = np.empty((n, S), dtype=np.float64)
+    rc = _load().dsa_oracle_logits_mxfp4(_ptr(qe), _ptr(qs), _ptr(ke), _ptr(ks), _ptr(wf),
+                                         _ptr(rs), _ptr(re_), T, S, H, D, _ptr(rr), n,
+                                         _ptr(out), nthreads)
+    if rc != 0:
+        raise ValueError("oracle logits_mxfp4: bad arguments")
     return out
 
 

@@ -28,6 +28,9 @@
  *               score is -inf, -1 padding when k exceeds the row).
  *   [OCP-FP8]   the OCP 8-bit floating point specification, E4M3 encoding
  *               (bias 7, no infinities, S.1111.111 is NaN, max 448).
+ *   [OCP-MX]    the OCP Microscaling Formats (MX) specification: MXFP4 =
+ *               E2M1 elements (bias 1, max 6) in blocks of 32 sharing one
+ *               E8M0 scale 2^(e-127).
  *
  * The index score itself is the DeepSeek sparse-attention lightning indexer:
  *     logit[t,s] = sum_h w[t,h] * max(0, sum_d q[t,h,d] * k[s,d])
@@ -188,6 +191,94 @@ int dsa_oracle_logits(const void* q, const float* q_scale, const void* k,
             int lo = clamp64(row_starts[t], 0, S);
             int hi = clamp64(row_ends[t], 0, S);
             load_query(q, q_scale, dtype, t, H, D, qrow);
+            for (int64_t s = 0; s < S; ++s) {
+                if (s >= lo && s < hi)
+                    o[s] = index_score(qrow, kd + s * D, w + t * H, H, D);
+                else
+                    o[s] = -INFINITY;
+            }
+        }
+        free(qrow);
+    }
+    free(kd);
+    return bad ? -1 : 0;
+}
+
+/* ---------------------------------------------------- MXFP4 (OCP MX) */
+
+/* E2M1 per [OCP-MX]: a 4-bit code S.EE.M, exponent bias 1.  E = 0 is
+ * subnormal (M/2); otherwise (1 + M/2) * 2^(E-1).  Magnitudes 0, 0.5, 1, 1.5,
+ * 2, 3, 4, 6; no infinities or NaN.  Only the low 4 bits of `code` count. */
+double dsa_oracle_e2m1_to_f64(uint8_t code)
+{
+    int sign = (code >> 3) & 1;
+    int e = (code >> 1) & 3;
+    int m = code & 1;
+    double mag = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return sign ? -mag : mag;
+}
+
+/* E8M0 (UE8M0) scale per [OCP-MX]: 2^(code - 127); code 255 is NaN. */
+double dsa_oracle_e8m0_to_f64(uint8_t code)
+{
+    if (code == 255)
+        return NAN;
+    return ldexp(1.0, (int)code - 127);
+}
+
+/* Element i of a packed E2M1 array: byte i/2, the low nibble for even i. */
+static double mxfp4_elem(const uint8_t* packed, const uint8_t* scales, int64_t i)
+{
+    uint8_t byte = packed[i / 2];
+    uint8_t code = (i & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
+    return dsa_oracle_e2m1_to_f64(code) * dsa_oracle_e8m0_to_f64(scales[i / 32]);
+}
+
+/*
+ * Dense index logits with MXFP4 queries and keys ([vLLM-dsa]: MXFP4 keys with
+ * MXFP4 queries, mxfp4_q_quant returning a separate q_scale): every block of
+ * 32 consecutive elements of a row shares one E8M0 scale.
+ *   q     [T, H, D/2] packed E2M1, q_sf [T, H, D/32] E8M0 codes
+ *   k     [S, D/2]    packed E2M1, k_sf [S, D/32]    E8M0 codes
+ *   w     [T, H] fp32 (the query scale is NOT folded in: it is in q_sf)
+ * The rest as dsa_oracle_logits.  D must be a multiple of 32.
+ */
+int dsa_oracle_logits_mxfp4(const uint8_t* q, const uint8_t* q_sf, const uint8_t* k,
+                            const uint8_t* k_sf, const float* w, const int32_t* row_starts,
+                            const int32_t* row_ends, int64_t T, int64_t S, int H, int D,
+                            const int64_t* rows, int64_t nrows, double* out, int nthreads)
+{
+    if (!q || !q_sf || !k || !k_sf || !w || !row_starts || !row_ends || !out || T < 0 ||
+        S < 0 || H < 1 || D < 32 || D % 32 != 0)
+        return -1;
+    if (!rows)
+        nrows = T;
+    double* kd = (double*)malloc(sizeof(double) * (size_t)(S * D + 1));
+    if (!kd)
+        return -1;
+    for (int64_t s = 0; s < S; ++s)
+        for (int d = 0; d < D; ++d)
+            kd[s * D + d] = mxfp4_elem(k + s * (D / 2), k_sf + s * (D / 32), d);
+    int bad = 0;
+    set_threads(nthreads);
+#pragma omp parallel
+    {
+        double* qrow = (double*)malloc(sizeof(double) * (size_t)H * D);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < nrows; ++i) {
+            int64_t t = rows ? rows[i] : i;
+            double* o = out + i * S;
+            if (t < 0 || t >= T || !qrow) {
+                bad = 1;
+                continue;
+            }
+            int lo = clamp64(row_starts[t], 0, S);
+            int hi = clamp64(row_ends[t], 0, S);
+            for (int h = 0; h < H; ++h) {
+                int64_t r = t * H + h;
+                for (int d = 0; d < D; ++d)
+                    qrow[(int64_t)h * D + d] = mxfp4_elem(q + r * (D / 2), q_sf + r * (D / 32), d);
+            }
             for (int64_t s = 0; s < S; ++s) {
                 if (s >= lo && s < hi)
                     o[s] = index_score(qrow, kd + s * D, w + t * H, H, D);

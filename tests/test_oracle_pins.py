@@ -591,3 +591,99 @@ def test_topk_merge_of_interleaved_local_topk_is_the_global_topk():
             cand_c.append(g)
         merged = oracle.topk_merge(np.concatenate(cand_s, 1), np.concatenate(cand_c, 1), k)
         assert np.array_equal(merged, oracle.topk(lg, np.zeros(T, np.int32), L, k))
+
+
+# ------------------------------------------------------------------ MXFP4
+
+def _golden_json(name):
+    import json
+    import os
+    with open(os.path.join(os.path.dirname(__file__), "golden", name)) as f:
+        return json.load(f)
+
+
+def test_e2m1_and_e8m0_decoders_match_the_mx_definition():
+    g = _golden_json("e2m1_codes.json")
+    got = oracle.e2m1_to_f64(range(16))
+    for c in range(16):
+        want = g["e2m1"][str(c)]
+        assert got[c] == want and np.signbit(got[c]) == np.signbit(want), c
+    codes = [int(c) for c in g["e8m0"]]
+    got = oracle.e8m0_to_f64(codes)
+    assert np.array_equal(got, np.array([g["e8m0"][str(c)] for c in codes]))
+    assert np.isnan(oracle.e8m0_to_f64([255])[0])
+    # every code: the value doubles with the exponent field
+    assert np.array_equal(oracle.e8m0_to_f64(range(1, 255)), 2.0 * oracle.e8m0_to_f64(range(0, 254)))
+
+
+def test_mxfp4_logits_hand_example():
+    g = _golden_json("mxfp4_hand_example.json")
+    q = np.zeros((1, 1, 32), np.uint8)
+    k = np.zeros((2, 32), np.uint8)
+    for i, v in g["q_bytes"].items():
+        q[0, 0, int(i)] = v
+    for row, key in ((0, "k0_bytes"), (1, "k1_bytes")):
+        for i, v in g[key].items():
+            k[row, int(i)] = v
+    q_sf = np.array(g["q_sf"], np.uint8).reshape(1, 1, 2)
+    k_sf = np.array([g["k0_sf"], g["k1_sf"]], np.uint8)
+    w = np.full((1, 1), g["w"], np.float32)
+    got = oracle.logits_mxfp4(q, q_sf, k, k_sf, w, np.zeros(1, np.int32), np.full(1, 2, np.int32))
+    assert got.tolist() == [g["logits"]]
+
+
+def _decode_mx_with_table(packed, sf):
+    """Decoded values from the golden E2M1 table (independent of the oracle)."""
+    g = _golden_json("e2m1_codes.json")
+    table = np.array([g["e2m1"][str(c)] for c in range(16)])
+    codes = np.empty(packed.shape[:-1] + (2 * packed.shape[-1],), np.uint8)
+    codes[..., 0::2] = packed & 15
+    codes[..., 1::2] = packed >> 4
+    scale = np.ldexp(1.0, sf.astype(np.int64) - 127)
+    return table[codes] * np.repeat(scale, 32, axis=-1)
+
+
+def test_mxfp4_logits_equal_the_bf16_oracle_on_the_decoded_values():
+    # E2M1 values times powers of two near 1 are exact in bf16: the MXFP4
+    # logits must equal the (separately pinned) bf16 oracle's on those values,
+    # bit for bit (same fp64 sums in the same order).
+    rng = np.random.default_rng(21)
+    T, S, H, D = 9, 70, 4, 64
+    q = rng.integers(0, 256, (T, H, D // 2)).astype(np.uint8)
+    k = rng.integers(0, 256, (S, D // 2)).astype(np.uint8)
+    q_sf = rng.integers(120, 135, (T, H, D // 32)).astype(np.uint8)
+    k_sf = rng.integers(120, 135, (S, D // 32)).astype(np.uint8)
+    w = rng.standard_normal((T, H)).astype(np.float32)
+    rs = rng.integers(-3, 40, T).astype(np.int32)
+    re = (rs + rng.integers(0, 50, T)).astype(np.int32)
+    qv = _decode_mx_with_table(q, q_sf)
+    kv = _decode_mx_with_table(k, k_sf)
+    assert np.array_equal(wl.bf16_bits_to_f32(bf16(qv)), qv)      # exact in bf16
+    assert np.array_equal(wl.bf16_bits_to_f32(bf16(kv)), kv)
+    ref = oracle.logits(bf16(qv), bf16(kv), w, rs, re)
+    got = oracle.logits_mxfp4(q, q_sf, k, k_sf, w, rs, re)
+    assert np.array_equal(got, ref)
+
+
+def test_mxfp4_quantiser_of_the_input_generator():
+    # Encoding only (the generator's job): the decoded block is the nearest
+    # E2M1 value times the block scale, ties to the even code, and the scale
+    # is the smallest power of two with amax <= 6 * scale.
+    rng = np.random.default_rng(22)
+    x = rng.standard_normal((40, 128)) * rng.choice([1e-3, 0.1, 3.0, 500.0], (40, 1))
+    x[0, :32] = 0.0                                   # an all-zero block
+    x[1, :32] = 6.0                                   # amax exactly 6 -> scale 1
+    x[2, :4] = [0.25, 0.75, 1.25, 2.5]                # ties (with amax 6 below)
+    x[2, 4] = 6.0
+    packed, sf = wl.quantize_mxfp4_blocks(x)
+    dec = _decode_mx_with_table(packed, sf)
+    scale = np.ldexp(1.0, sf.astype(np.int64) - 127)
+    amax = np.abs(x.reshape(40, 4, 32)).max(-1)
+    assert np.all(amax <= 6 * scale) and np.all((amax == 0) | (amax > 3 * scale))
+    assert sf[0, 0] == 127 and sf[1, 0] == 127
+    assert dec[2, :4].tolist() == [0.0, 1.0, 1.0, 2.0]  # ties go to the even code
+    grid = np.concatenate([-wl.E2M1_GRID[::-1], wl.E2M1_GRID])
+    y = x / np.repeat(scale, 32, axis=1)
+    nearest = grid[np.abs(y[..., None] - grid).argmin(-1)]
+    err_best = np.abs(y - nearest)
+    assert np.all(np.abs(dec / np.repeat(scale, 32, axis=1) - y) <= err_best + 1e-12)

@@ -12,6 +12,8 @@ Workloads (shapes and distributions of the lightning-indexer configurations):
   paged_decode     64 requests x 2 query tokens, contexts log-U[4096, 131072],
                    bf16 K cache in 64-token blocks behind a permuted block table
   prefill_fp8      T=S=32768, H=64, D=128, k=2048, e4m3 q/k with UE8M0 scales
+  prefill_mxfp4    T=S=32768, H=64, D=128, k=2048, MXFP4 q/k (E2M1 elements,
+                   one E8M0 scale per 32-element block)
 
 Distributions: q, k ~ N(0, 1/D) rounded to bf16; weights ~ N(0,1)/sqrt(H),
 times D^-0.5 for every workload but the tiny one (the index softmax scale that
@@ -36,7 +38,12 @@ import torch
 
 BF16 = 0
 E4M3 = 1
+MXFP4 = 2
 E4M3_MAX = 448.0
+E2M1_MAX = 6.0
+MX_BLOCK = 32
+# E2M1 magnitudes of codes 0..7 (OCP Microscaling Formats, E2M1: bias 1).
+E2M1_GRID = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
 
 
 @dataclass
@@ -64,6 +71,46 @@ class Prefill:
     @property
     def D(self):
         return self.q.shape[2]
+
+    @property
+    def S(self):
+        return self.k.shape[0]
+
+    def valid_pairs(self) -> int:
+        lo = np.clip(self.row_starts.astype(np.int64), 0, self.S)
+        hi = np.clip(self.row_ends.astype(np.int64), 0, self.S)
+        return int(np.maximum(hi - lo, 0).sum())
+
+
+@dataclass
+class PrefillMX:
+    """Contiguous-key workload with MXFP4 operands: packed E2M1 q [T,H,D/2]
+    and k [S,D/2] (uint8, low nibble = even element), E8M0 block scales
+    q_sf [T,H,D/32] and k_sf [S,D/32] (uint8), fp32 weights [T,H] without
+    the query scale (it stays in q_sf)."""
+    name: str
+    q: np.ndarray
+    q_sf: np.ndarray
+    k: np.ndarray
+    k_sf: np.ndarray
+    w: np.ndarray
+    row_starts: np.ndarray
+    row_ends: np.ndarray
+    topk: int
+    dtype: int = MXFP4
+    seq_lens: list = field(default_factory=list)
+
+    @property
+    def T(self):
+        return self.q.shape[0]
+
+    @property
+    def H(self):
+        return self.q.shape[1]
+
+    @property
+    def D(self):
+        return 2 * self.q.shape[2]
 
     @property
     def S(self):
@@ -157,6 +204,32 @@ def quantize_e4m3_blocks(x: np.ndarray):
     return codes, scale
 
 
+def quantize_mxfp4_blocks(x: np.ndarray):
+    """Quantise rows of x [rows, D] (D a multiple of 32) to MXFP4: per block
+    of 32 elements the E8M0 scale 2^e, e = ceil(log2(amax / 6)) (0 for an
+    all-zero block), and each element x / 2^e rounded to the nearest E2M1
+    value, ties to the even code (|x / 2^e| <= 6, so nothing saturates).
+    Returns (packed [rows, D/2] uint8 with the even element in the low
+    nibble, scales [rows, D/32] uint8)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    rows, D = x.shape
+    blocks = x.reshape(rows, D // MX_BLOCK, MX_BLOCK)
+    amax = np.abs(blocks).max(axis=-1)
+    m, e = np.frexp(amax / E2M1_MAX)
+    e = np.where(m == 0.5, e - 1, e)
+    e = np.where(amax > 0, e, 0)
+    e = np.clip(e, -127, 127)
+    y = blocks / np.ldexp(1.0, e)[..., None]
+    mag = np.abs(y)
+    hi = np.clip(np.searchsorted(E2M1_GRID, mag, side="left"), 0, 7)
+    lo = np.clip(hi - 1, 0, 7)
+    dlo, dhi = mag - E2M1_GRID[lo], E2M1_GRID[hi] - mag
+    code = np.where(dlo < dhi, lo, np.where(dhi < dlo, hi, np.where(lo % 2 == 0, lo, hi)))
+    code = (code | np.where(np.signbit(y), 8, 0)).astype(np.uint8).reshape(rows, D)
+    packed = (code[:, 0::2] | (code[:, 1::2] << 4)).astype(np.uint8)
+    return packed, (e + 127).astype(np.uint8)
+
+
 def _normal_bf16(rng, shape, std, chunk_rows=1 << 16):
     """N(0, std^2) rounded to bf16, generated in row chunks to bound memory."""
     rows = shape[0]
@@ -219,6 +292,30 @@ def prefill(T, S, H, D, topk, row_starts=None, row_ends=None, *, seed=0,
     return Prefill(name, E4M3, q8.reshape(T, H, D), k8, w,
                    np.asarray(row_starts, np.int32), np.asarray(row_ends, np.int32),
                    topk, k_scale=sk)
+
+
+def prefill_mx(T, S, H, D, topk, row_starts=None, row_ends=None, *, seed=0,
+               name="prefill_mxfp4") -> PrefillMX:
+    """MXFP4 workload: q, k ~ N(0, 1/D) rounded to bf16, then quantised to
+    MXFP4 by blocks of 32; w ~ N(0,1)/sqrt(H) * D^-0.5 (the softmax scale;
+    the query's block scales stay separate, as mxfp4_q_quant returns them)."""
+    rng = _rng(seed)
+    if row_starts is None:
+        assert T == S, "default ranges are causal and need T == S"
+        row_starts, row_ends = causal_ranges(T)
+    std = 1.0 / math.sqrt(D)
+    w = _weights(rng, T, H, D)
+    qsrc = bf16_bits_to_f32(_normal_bf16(rng, (T * H, D), std))
+    ksrc = bf16_bits_to_f32(_normal_bf16(rng, (S, D), std))
+    q4, qsf = quantize_mxfp4_blocks(qsrc)
+    del qsrc
+    k4, ksf = quantize_mxfp4_blocks(ksrc)
+    return PrefillMX(name, q4.reshape(T, H, D // 2), qsf.reshape(T, H, D // MX_BLOCK), k4, ksf,
+                     w, np.asarray(row_starts, np.int32), np.asarray(row_ends, np.int32), topk)
+
+
+def prefill_mxfp4(T=32768, H=64, D=128, topk=2048, seed=0) -> PrefillMX:
+    return prefill_mx(T, T, H, D, topk, seed=seed, name=f"prefill_mxfp4_T{T}_H{H}_D{D}_k{topk}")
 
 
 def tiny_causal(seed=0) -> Prefill:
@@ -300,4 +397,5 @@ WORKLOADS = {
     "prefill_thd": prefill_thd,
     "paged_decode": paged_decode,
     "prefill_fp8": prefill_fp8,
+    "prefill_mxfp4": prefill_mxfp4,
 }
