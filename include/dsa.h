@@ -45,7 +45,7 @@
  *  - Each call that queues GPU work is wrapped in an NVTX range named after
  *    its entry point (visible in Nsight timelines; free without a tool).
  *  - CUDA graphs: once one of dsa_indexer_logits, dsa_topk,
- *    dsa_indexer_topk, the two paged calls, dsa_topk_sort_by_score or
+ *    dsa_indexer_topk, the paged and MXFP4 calls, dsa_topk_sort_by_score or
  *    dsa_topk_merge has run on a device (its first call looks up per-device
  *    state), its calls can be captured into a CUDA graph.
  *    A capture fixes the shapes (rows, key capacity, k) and the pointers;
@@ -148,6 +148,46 @@ dsa_status_t dsa_indexer_topk(const void* q, const float* q_scale, const void* k
                               const int32_t* row_ends, int T, int S, int H, int D,
                               int topk, int32_t* out, void* workspace, size_t ws_bytes,
                               dsa_stream_t stream);
+
+/*
+ * Index logits with MXFP4 queries and keys (KimiK3DSAIndexer on the vLLM page
+ * "vllm.models.kimi_k3.nvidia.dsa": MXFP4 keys with MXFP4 queries on an
+ * explicit indexer_kv_dtype='mxfp4', where mxfp4_q_quant returns the query,
+ * its block scales and the weights).  Element format (OCP Microscaling):
+ * E2M1 codes (bias 1, magnitudes 0 .. 6) packed two per byte, the even
+ * element in the low nibble; every 32 consecutive elements of a row share one
+ * E8M0 scale byte, value 2^(code - 127).  The scales enter the tensor-core
+ * contraction (tcgen05 kind::mxf4 with block scales), so
+ *   logit[t,s] = sum_h w[t,h] * max(0, sum_d q[t,h,d] * k[s,d])
+ * with q and k their decoded values.
+ *
+ *   q         [T, H, D/2] packed E2M1, 16-byte aligned
+ *   q_sf      [T, H, D/32] E8M0 scale bytes, 4-byte aligned
+ *   k         [S, D/2] packed E2M1, 16-byte aligned
+ *   k_sf      [S, D/32] E8M0 scale bytes, 4-byte aligned
+ *   weights   [T, H] fp32 (the query scales are in q_sf, not folded in)
+ *   row_starts, row_ends, logits, ld, flags: as dsa_indexer_logits
+ *   H = 64 and D = 128 only (else DSA_ERR_UNSUPPORTED).
+ * Errors as dsa_indexer_logits.  The head sum runs in one fixed order, so
+ * dsa_indexer_topk_mxfp4's selection equals dsa_topk on these logits.
+ */
+dsa_status_t dsa_indexer_logits_mxfp4(const void* q, const uint8_t* q_sf, const void* k,
+                                      const uint8_t* k_sf, const float* weights,
+                                      const int32_t* row_starts, const int32_t* row_ends, int T,
+                                      int S, int H, int D, float* logits, int64_t ld,
+                                      uint32_t flags, dsa_stream_t stream);
+
+/*
+ * MXFP4 index logits + masked top-k in one call: arguments as
+ * dsa_indexer_logits_mxfp4 plus k/out of dsa_topk; `workspace` must hold
+ * dsa_workspace_bytes(DSA_OP_INDEXER_TOPK, T, S, k) bytes, 256-byte aligned.
+ * The result equals dsa_topk(dsa_indexer_logits_mxfp4(...)) bit for bit.
+ */
+dsa_status_t dsa_indexer_topk_mxfp4(const void* q, const uint8_t* q_sf, const void* k,
+                                    const uint8_t* k_sf, const float* weights,
+                                    const int32_t* row_starts, const int32_t* row_ends, int T,
+                                    int S, int H, int D, int topk, int32_t* out, void* workspace,
+                                    size_t ws_bytes, dsa_stream_t stream);
 
 /*
  * Index logits of paged decode (the paged indexer K cache of

@@ -24,7 +24,7 @@ def api():
 def declared_symbols():
     src = open(os.path.join(ROOT, "include", "dsa.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(dsa_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(dsa_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_header_declares_the_boundary():
@@ -264,3 +264,27 @@ def test_indexer_topk_host_bytes_layout(api):
     # top-k takes (rows <= 512, columns > 16384) while the full chunks do not
     assert api.lib.dsa_workspace_bytes(api.DSA_OP_TOPK, 220, 40000, 2048) > 0
     assert api.lib.dsa_workspace_bytes(api.DSA_OP_TOPK, 640, 40000, 2048) == 0
+
+
+def mx_call(api, q=A, qsf=A, k=A, ksf=A, w=A, rs=A, re=A, T=8, S=8, H=64, D=128, lg=A, ld=8,
+            flags=0):
+    return api.lib.dsa_indexer_logits_mxfp4(q, qsf, k, ksf, w, rs, re, T, S, H, D, lg, ld, flags,
+                                            None)
+
+
+def test_mxfp4_argument_errors(api):
+    assert mx_call(api, q=NUL) == api.DSA_ERR_INVALID_ARG
+    assert mx_call(api, qsf=NUL) == api.DSA_ERR_INVALID_ARG
+    assert mx_call(api, ksf=NUL) == api.DSA_ERR_INVALID_ARG
+    assert mx_call(api, q=MIS) == api.DSA_ERR_INVALID_ARG          # TMA needs 16 B
+    assert mx_call(api, qsf=ctypes.c_void_p(0x10002)) == api.DSA_ERR_INVALID_ARG
+    assert mx_call(api, H=32) == api.DSA_ERR_UNSUPPORTED             # 64 heads only
+    assert mx_call(api, D=64) == api.DSA_ERR_UNSUPPORTED             # D = 128 only
+    assert mx_call(api, ld=7) == api.DSA_ERR_INVALID_ARG             # ld < S
+    assert mx_call(api, flags=4) == api.DSA_ERR_INVALID_ARG
+    assert mx_call(api, T=-1) == api.DSA_ERR_INVALID_ARG
+    assert mx_call(api, T=0) == api.DSA_OK                           # nothing to do, no launch
+    f = api.lib.dsa_indexer_topk_mxfp4
+    assert f(A, A, A, A, A, A, A, 8, 8, 64, 128, 0, A, A, 4096, None) == api.DSA_ERR_INVALID_ARG
+    assert f(A, A, A, A, A, A, A, 8, 8, 64, 128, 4, NUL, A, 4096, None) == api.DSA_ERR_INVALID_ARG
+    assert f(A, A, A, A, A, A, A, 8, 8, 64, 128, 4, A, NUL, 0, None) == api.DSA_ERR_INVALID_ARG

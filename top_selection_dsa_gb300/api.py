@@ -31,6 +31,7 @@ EXPORTS = (
     "dsa_get_last_device_error", "dsa_selftest_wait_timeout", "dsa_indexer_topk_noalloc",
     "dsa_topk_sort_by_score", "dsa_q_quant_fold_weights", "dsa_k_norm_quant_insert",
     "dsa_topk_merge", "dsa_indexer_topk_host_bytes", "dsa_indexer_topk_host",
+    "dsa_indexer_logits_mxfp4", "dsa_indexer_topk_mxfp4",
 )
 
 
@@ -69,6 +70,10 @@ def _load():
     lib.dsa_indexer_topk_host_bytes.argtypes = [I, I, I, I, I, I]
     lib.dsa_indexer_topk_host_bytes.restype = SZ
     lib.dsa_indexer_topk_host.argtypes = [P, P, P, P, I, P, P, P, I, I, I, I, I, P, P, SZ, P]
+    lib.dsa_indexer_logits_mxfp4.argtypes = [P, P, P, P, P, P, P, I, I, I, I, P, I64, U32, P]
+    lib.dsa_indexer_topk_mxfp4.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P, P, SZ, P]
+    for name in ("dsa_indexer_logits_mxfp4", "dsa_indexer_topk_mxfp4"):
+        getattr(lib, name).restype = I
     for name in ("dsa_indexer_logits", "dsa_topk", "dsa_indexer_topk",
                  "dsa_indexer_logits_paged", "dsa_indexer_topk_paged",
                  "dsa_get_last_device_error", "dsa_selftest_wait_timeout",
@@ -204,6 +209,53 @@ def indexer_topk(q, k, weights, row_starts, row_ends, topk_k, *, q_scale=None, k
                                   _ptr(row_starts), _ptr(row_ends), T, S, H, D, topk_k, _ptr(out),
                                   _ptr(ws), nbytes, _stream(dev))
     _check(st, "dsa_indexer_topk")
+    return out
+
+
+def _mx_common(q, q_sf, k, k_sf, weights, row_starts, row_ends):
+    dev = q.device
+    for t, n, d in ((q, "q", (torch.uint8,)), (q_sf, "q_sf", (torch.uint8,)),
+                    (k, "k", (torch.uint8,)), (k_sf, "k_sf", (torch.uint8,)),
+                    (weights, "weights", (torch.float32,)),
+                    (row_starts, "row_starts", (torch.int32,)),
+                    (row_ends, "row_ends", (torch.int32,))):
+        _need(t, n, d, dev)
+    T, H, D2 = q.shape
+    return dev, T, H, 2 * D2, k.shape[0]
+
+
+def indexer_logits_mxfp4(q, q_sf, k, k_sf, weights, row_starts, row_ends, *, logits=None,
+                         clean=False):
+    """fp32 index logits [T, ld] of MXFP4 operands: q [T,H,D/2] and k [S,D/2]
+    packed E2M1 (uint8), q_sf [T,H,D/32] and k_sf [S,D/32] E8M0 scale bytes."""
+    dev, T, H, D, S = _mx_common(q, q_sf, k, k_sf, weights, row_starts, row_ends)
+    if logits is None:
+        logits = torch.empty((T, S), dtype=torch.float32, device=dev)
+    _need(logits, "logits", (torch.float32,), dev)
+    with torch.cuda.device(dev):
+        st = lib.dsa_indexer_logits_mxfp4(_ptr(q), _ptr(q_sf), _ptr(k), _ptr(k_sf),
+                                          _ptr(weights), _ptr(row_starts), _ptr(row_ends), T, S,
+                                          H, D, _ptr(logits),
+                                          logits.shape[1] if logits.dim() == 2 else S,
+                                          DSA_LOGITS_CLEAN if clean else 0, _stream(dev))
+    _check(st, "dsa_indexer_logits_mxfp4")
+    return logits
+
+
+def indexer_topk_mxfp4(q, q_sf, k, k_sf, weights, row_starts, row_ends, topk_k, *, out=None,
+                       workspace=None):
+    """MXFP4 index logits + masked top-k in one library call: [T, topk_k] int32."""
+    dev, T, H, D, S = _mx_common(q, q_sf, k, k_sf, weights, row_starts, row_ends)
+    if out is None:
+        out = torch.empty((T, topk_k), dtype=torch.int32, device=dev)
+    _need(out, "out", (torch.int32,), dev)
+    nbytes = workspace_bytes(DSA_OP_INDEXER_TOPK, T, S, topk_k)
+    ws = _workspace(nbytes, dev, workspace)
+    with torch.cuda.device(dev):
+        st = lib.dsa_indexer_topk_mxfp4(_ptr(q), _ptr(q_sf), _ptr(k), _ptr(k_sf), _ptr(weights),
+                                        _ptr(row_starts), _ptr(row_ends), T, S, H, D, topk_k,
+                                        _ptr(out), _ptr(ws), nbytes, _stream(dev))
+    _check(st, "dsa_indexer_topk_mxfp4")
     return out
 
 

@@ -128,6 +128,20 @@ bool encode_map(CUtensorMap* map, const void* base, dsa_dtype_t dtype, int D, in
   return r == CUDA_SUCCESS;
 }
 
+// 64-byte-swizzled tiled map over packed E2M1 rows [rows, 64 bytes], box =
+// 64 bytes x box_rows rows (the MXFP4 operands, D = 128).
+bool encode_map_e2m1(CUtensorMap* map, const void* base, int64_t rows, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {64, static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {64};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
 // Workspace of the composed calls: the fp32 logits [rows, round_up(cols, 4)],
@@ -199,6 +213,42 @@ dsa_status_t run_logits(const void* q, const float* q_scale, const void* k, cons
   cudaError_t e = dtype == DSA_BF16 ? launch_score_prefill_bf16(p, H, D, st)
                                     : launch_score_prefill_fp8(p, H, D, st);
   return from_cuda(e);
+}
+
+dsa_status_t check_mx_args(const void* q, const uint8_t* q_sf, const void* k, const uint8_t* k_sf,
+                           const float* weights, const int32_t* row_starts,
+                           const int32_t* row_ends, int T, int S, int H, int D) {
+  if (!q || !q_sf || !k || !k_sf || !weights || !row_starts || !row_ends)
+    return DSA_ERR_INVALID_ARG;
+  if (T < 0 || S < 0 || H < 1 || D < 1) return DSA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(q_sf, 4) || !aligned(k_sf, 4) ||
+      !aligned(weights, 4) || !aligned(row_starts, 4) || !aligned(row_ends, 4))
+    return DSA_ERR_INVALID_ARG;
+  if (!score_mx_supported(H, D)) return DSA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(T) * H >= (int64_t(1) << 31)) return DSA_ERR_UNSUPPORTED;
+  return DSA_OK;
+}
+
+// Validated, unchecked launch of the MXFP4 prefill scoring kernel.
+dsa_status_t run_logits_mx(const void* q, const uint8_t* q_sf, const void* k,
+                           const uint8_t* k_sf, const float* weights, const int32_t* row_starts,
+                           const int32_t* row_ends, int T, int S, int H, float* logits,
+                           int64_t ld, cudaStream_t st) {
+  if (T == 0 || S == 0) return DSA_OK;
+  ScoreParams p = {};
+  if (!encode_map_e2m1(&p.tmap_q, q, static_cast<int64_t>(T) * H, 128) ||
+      !encode_map_e2m1(&p.tmap_k, k, S, 128))
+    return DSA_ERR_CUDA;
+  p.weights = weights;
+  p.row_starts = row_starts;
+  p.row_ends = row_ends;
+  p.logits = logits;
+  p.ld = ld;
+  p.R = T;
+  p.S = S;
+  p.err = error_word();
+  if (!p.err) return DSA_ERR_CUDA;
+  return from_cuda(launch_score_mx(p, q_sf, k_sf, st));
 }
 
 dsa_status_t run_topk(const float* logits, int64_t ld, const int32_t* row_starts,
@@ -386,6 +436,50 @@ dsa_status_t dsa_indexer_topk(const void* q, const float* q_scale, const void* k
   float* lg = static_cast<float*>(workspace);
   st = run_logits(q, q_scale, k, k_scale, dtype, weights, row_starts, row_ends, T, S, H, D, lg, ld,
                   as_stream(stream));
+  if (st != DSA_OK) return st;
+  return run_topk(lg, ld, row_starts, row_ends, nullptr, 1, T, S, topk, out, as_stream(stream),
+                  split_scratch(workspace, T, S), true);
+}
+
+dsa_status_t dsa_indexer_logits_mxfp4(const void* q, const uint8_t* q_sf, const void* k,
+                                      const uint8_t* k_sf, const float* weights,
+                                      const int32_t* row_starts, const int32_t* row_ends, int T,
+                                      int S, int H, int D, float* logits, int64_t ld,
+                                      uint32_t flags, dsa_stream_t stream) {
+  const CallRange range("dsa_indexer_logits_mxfp4");
+  dsa_status_t st =
+      check_mx_args(q, q_sf, k, k_sf, weights, row_starts, row_ends, T, S, H, D);
+  if (st != DSA_OK) return st;
+  if (!logits || !aligned(logits, 4) || ld < S || ld < 1) return DSA_ERR_INVALID_ARG;
+  if (flags & ~DSA_LOGITS_CLEAN) return DSA_ERR_INVALID_ARG;
+  if (T == 0) return DSA_OK;
+  if (flags & DSA_LOGITS_CLEAN) {
+    st = from_cuda(launch_fill(logits, T, S, ld, -INFINITY, as_stream(stream)));
+    if (st != DSA_OK) return st;
+  }
+  return run_logits_mx(q, q_sf, k, k_sf, weights, row_starts, row_ends, T, S, H, logits, ld,
+                       as_stream(stream));
+}
+
+dsa_status_t dsa_indexer_topk_mxfp4(const void* q, const uint8_t* q_sf, const void* k,
+                                    const uint8_t* k_sf, const float* weights,
+                                    const int32_t* row_starts, const int32_t* row_ends, int T,
+                                    int S, int H, int D, int topk, int32_t* out, void* workspace,
+                                    size_t ws_bytes, dsa_stream_t stream) {
+  const CallRange range("dsa_indexer_topk_mxfp4");
+  dsa_status_t st =
+      check_mx_args(q, q_sf, k, k_sf, weights, row_starts, row_ends, T, S, H, D);
+  if (st != DSA_OK) return st;
+  if (!out || !aligned(out, 4) || topk < 1) return DSA_ERR_INVALID_ARG;
+  if (!topk_supported(S)) return DSA_ERR_UNSUPPORTED;
+  const size_t need = dsa_workspace_bytes(DSA_OP_INDEXER_TOPK, T, S, topk);
+  if (need > 0 && (!workspace || ws_bytes < need || !aligned(workspace, 256)))
+    return DSA_ERR_INVALID_ARG;
+  if (T == 0) return DSA_OK;
+  const int64_t ld = round_up(S > 0 ? S : 1, 4);
+  float* lg = static_cast<float*>(workspace);
+  st = run_logits_mx(q, q_sf, k, k_sf, weights, row_starts, row_ends, T, S, H, lg, ld,
+                     as_stream(stream));
   if (st != DSA_OK) return st;
   return run_topk(lg, ld, row_starts, row_ends, nullptr, 1, T, S, topk, out, as_stream(stream),
                   split_scratch(workspace, T, S), true);

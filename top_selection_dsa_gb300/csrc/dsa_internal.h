@@ -69,6 +69,11 @@ bool score_paged_supported(bool fp8, int H, int D, int next_n);
 // MMA columns (and q-tile rows) of the paged kernel: next_n*H rounded up to 64/128/256.
 int score_paged_cols(int H, int next_n);
 cudaError_t launch_score_paged(const ScoreParams& p, bool fp8, int H, int D, cudaStream_t s);
+// MXFP4 prefill (packed E2M1 q [R*H, D/2], k [S, D/2]; E8M0 scales q_sf
+// [R*H, D/32], k_sf [S, D/32]); H = 64, D = 128 only.
+bool score_mx_supported(int H, int D);
+cudaError_t launch_score_mx(const ScoreParams& p, const uint8_t* q_sf, const uint8_t* k_sf,
+                            cudaStream_t s);
 // Tokens (query rows) per prefill tile group for a head count.
 int score_tokens_per_group(int H);
 
