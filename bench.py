@@ -64,7 +64,11 @@ PROFILES = {
 # Rows of the CPU oracle sample for cpu_baseline (about 10-30 s of the host's
 # cores); the reference arm times an eighth of it per step.
 ORACLE_ROWS = {"prefill_fp8": 2048, "prefill_causal": 4096, "prefill_thd": 4096,
-               "paged_decode": 128, "tiny_causal": 256}
+               "paged_decode": 128, "tiny_causal": 256, "prefill_mxfp4": 2048}
+# Dense tensor peak per element type, as a multiple of the measured bf16 one
+# (the nominal ratios: e4m3 2x, E2M1 with block scales 6x).
+PEAK_RATIO = {0: 1.0, 1: 2.0, 2: 6.0}
+DTYPE_NAME = {0: "bf16", 1: "e4m3", 2: "mxfp4 (e2m1 + e8m0 per 32)"}
 
 
 def parse_args(argv=None):
@@ -75,7 +79,7 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="prefill_fp8",
                     choices=("prefill_causal", "prefill_thd", "prefill_fp8", "paged_decode",
-                             "tiny_causal"))
+                             "tiny_causal", "prefill_mxfp4"))
     ap.add_argument("--prologue", action="store_true",
                     help="time the steps before the indexer (query quantisation + weight "
                          "fold, key LayerNorm + e4m3 paged insert) at the e4m3 workload's "
@@ -231,7 +235,7 @@ def barrier(world):
 
 def make_workload(name, tokens=0):
     from top_selection_dsa_gb300 import workloads as wl
-    if tokens and name in ("prefill_causal", "prefill_fp8"):
+    if tokens and name in ("prefill_causal", "prefill_fp8", "prefill_mxfp4"):
         return wl.WORKLOADS[name](T=tokens)
     return wl.WORKLOADS[name]()
 
@@ -249,8 +253,12 @@ def oracle_sample_rate(p, nrows, seed=0):
     if hasattr(p, "row_starts"):
         rows = np.sort(rng.choice(p.T, size=min(nrows, p.T), replace=False)).astype(np.int64)
         t0 = time.perf_counter()
-        lg = oracle.logits(p.q, p.k, p.w, p.row_starts, p.row_ends, dtype=p.dtype,
-                           k_scale=p.k_scale, rows=rows)
+        if p.dtype == 2:
+            lg = oracle.logits_mxfp4(p.q, p.q_sf, p.k, p.k_sf, p.w, p.row_starts, p.row_ends,
+                                     rows=rows)
+        else:
+            lg = oracle.logits(p.q, p.k, p.w, p.row_starts, p.row_ends, dtype=p.dtype,
+                               k_scale=p.k_scale, rows=rows)
         oracle.topk(lg.astype(np.float32), p.row_starts[rows], p.row_ends[rows], p.topk,
                     S=p.S)
         dt = time.perf_counter() - t0
@@ -278,7 +286,8 @@ def workload_config(p, world):
     rows = p.R if paged else p.T
     return {"workload": p.name, "rows_per_step": rows, "valid_pairs": p.valid_pairs(),
             "index_topk": p.topk, "H": p.H, "D": p.D,
-            "elements": "bf16" if p.dtype == 0 else "e4m3 + UE8M0 per-row scales",
+            "elements": {0: "bf16", 1: "e4m3 + UE8M0 per-row scales",
+                         2: "MXFP4: E2M1 + E8M0 per 32 elements"}[p.dtype],
             "parallelism": f"replicas x{world}"}
 
 
@@ -332,7 +341,29 @@ def run_ours(args):
 
     stream = torch.cuda.current_stream(device)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
-    if not paged:
+    mx = (not paged) and p.dtype == 2
+    if mx:
+        q, qsf, k, ksf, w = cuda(p.q), cuda(p.q_sf), cuda(p.k), cuda(p.k_sf), cuda(p.w)
+        rs, re_ = cuda(p.row_starts), cuda(p.row_ends)
+        rows_per_step = p.T
+        ld = (p.S + 3) // 4 * 4
+        ws = torch.empty(api.workspace_bytes(api.DSA_OP_INDEXER_TOPK, p.T, p.S, p.topk),
+                         dtype=torch.uint8, device=device)
+        lg_bytes = (p.T * ld * 4 + 255) // 256 * 256
+        logits = ws[:p.T * ld * 4].view(torch.float32).view(p.T, ld)
+        ws_topk = ws[lg_bytes:]
+        out = torch.empty((p.T, p.topk), dtype=torch.int32, device=device)
+
+        def score():
+            api.indexer_logits_mxfp4(q, qsf, k, ksf, w, rs, re_, logits=logits)
+
+        def select():
+            api.topk(logits, rs, re_, p.topk, S=p.S, out=out, workspace=ws_topk)
+
+        def fused(o):
+            return api.indexer_topk_mxfp4(q, qsf, k, ksf, w, rs, re_, p.topk, out=o,
+                                          workspace=ws)
+    elif not paged:
         q, k, w = elems(p.q), elems(p.k), cuda(p.w)
         rs, re_ = cuda(p.row_starts), cuda(p.row_ends)
         ks = cuda(p.k_scale) if p.k_scale is not None else None
@@ -466,7 +497,16 @@ def run_ours(args):
     if not args.no_e2e:
         pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
         host_out = torch.empty(out.shape, dtype=torch.int32).pin_memory()
-        if not paged:
+        if mx:
+            host_in = [pin(a) for a in (p.q, p.q_sf, p.k, p.k_sf, p.w, p.row_starts, p.row_ends)]
+            dev_in = [q, qsf, k, ksf, w, rs, re_]
+
+            def e2e_step():
+                for d, h in zip(dev_in, host_in):
+                    d.view(-1).copy_(h.view(-1), non_blocking=True)
+                fused(out)
+                host_out.copy_(out, non_blocking=True)
+        elif not paged:
             if p.dtype == 0:
                 hq, hk = pin(p.q.view(np.int16)).view(torch.bfloat16), \
                     pin(p.k.view(np.int16)).view(torch.bfloat16)
@@ -537,8 +577,9 @@ def run_ours(args):
                                  statistics.mean(d2h_ms)], world, device)
         e2e = {"value": world * rows_per_step / (em / 1e3), "unit": "rows/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": em,
-               "entry_point": "dsa_indexer_topk_host" if not paged else
-                              "copies + dsa_indexer_topk_paged + copy",
+               "entry_point": ("copies + dsa_indexer_topk_mxfp4 + copy" if mx else
+                               "dsa_indexer_topk_host" if not paged else
+                               "copies + dsa_indexer_topk_paged + copy"),
                "copies_alone_ms": {"h2d": hm, "d2h": dm,
                                    "h2d_gbs": h2d / hm / 1e6, "d2h_gbs": d2h / dm / 1e6}}
 
@@ -548,18 +589,20 @@ def run_ours(args):
     peaks, peak_src = measured_peaks()
     flops = step_flops(p)
     if not paged:
-        fp8 = p.dtype == 1
-        peak = peaks["bf16_tflops"] * (2.0 if fp8 else 1.0)
+        ratio = PEAK_RATIO[p.dtype]
+        peak = peaks["bf16_tflops"] * ratio
         achieved = flops / (s_ms / 1e3) / 1e12
         traffic, traffic_src = profiled_traffic(args.workload if not args.tokens else "")
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
                 "traffic_source": traffic_src,
-                "kernel": "score_kernel (tcgen05 scoring, writes fp32 logits)",
+                "kernel": ("score_mx_kernel (tcgen05 kind::mxf4 block-scaled scoring)" if mx else
+                           "score_kernel (tcgen05 scoring, writes fp32 logits)"),
                 "algorithmic_flops_per_launch": flops,
                 "duration_ms": s_ms,
-                "peak_source": f"{peak_src} " + ("bf16 burst x2 (the nominal fp8:bf16 dense "
-                                                 "ratio)" if fp8 else "bf16 burst")}
+                "peak_source": f"{peak_src} bf16 burst" + (
+                    f" x{ratio:g} (the nominal {DTYPE_NAME[p.dtype]}:bf16 dense ratio)"
+                    if ratio != 1.0 else "")}
     else:
         kbytes = int(sum(int(L) for L in p.context_lens)) * p.D * (2 if p.dtype == 0 else 1)
         other = p.R * p.H * p.D * (2 if p.dtype == 0 else 1) + p.R * p.H * 4 \
@@ -577,8 +620,9 @@ def run_ours(args):
     topk_bytes = p.valid_pairs() * 4 + rows_per_step * p.topk * 4
     launches = launches_per_step(p)
     cfg = workload_config(p, world)
-    cfg.update({"step": "one dsa_indexer_topk call" if not paged
-                else "one dsa_indexer_topk_paged call",
+    cfg.update({"step": ("one dsa_indexer_topk_mxfp4 call" if mx else
+                         "one dsa_indexer_topk call" if not paged
+                         else "one dsa_indexer_topk_paged call"),
                 "l2": "flushed before every step (256 MiB write, outside the step events)",
                 "clock_window": "nvidia-smi every 100 ms over a 1 s window of the same "
                                 "steps right before the timed ones, and over both timed "
@@ -594,7 +638,7 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16" if p.dtype == 0 else "e4m3",
+        "dtype": {0: "bf16", 1: "e4m3", 2: "mxfp4"}[p.dtype],
         "data": "synthetic",
         "config": cfg,
         "tflops": flops / (ms / 1e3) / 1e12,
