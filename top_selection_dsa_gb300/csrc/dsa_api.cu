@@ -236,7 +236,7 @@ dsa_status_t run_logits_mx(const void* q, const uint8_t* q_sf, const void* k,
                            int64_t ld, cudaStream_t st) {
   if (T == 0 || S == 0) return DSA_OK;
   ScoreParams p = {};
-  if (!encode_map_e2m1(&p.tmap_q, q, static_cast<int64_t>(T) * H, 128) ||
+  if (!encode_map_e2m1(&p.tmap_q, q, static_cast<int64_t>(T) * H, score_mx_q_rows()) ||
       !encode_map_e2m1(&p.tmap_k, k, S, 128))
     return DSA_ERR_CUDA;
   p.weights = weights;

@@ -72,6 +72,9 @@ cudaError_t launch_score_paged(const ScoreParams& p, bool fp8, int H, int D, cud
 // MXFP4 prefill (packed E2M1 q [R*H, D/2], k [S, D/2]; E8M0 scales q_sf
 // [R*H, D/32], k_sf [S, D/32]); H = 64, D = 128 only.
 bool score_mx_supported(int H, int D);
+// Rows of q ([R*H, D/2] packed) the MXFP4 kernel loads per group: the TMA box
+// height of its q map.
+int score_mx_q_rows();
 cudaError_t launch_score_mx(const ScoreParams& p, const uint8_t* q_sf, const uint8_t* k_sf,
                             cudaStream_t s);
 // Tokens (query rows) per prefill tile group for a head count.

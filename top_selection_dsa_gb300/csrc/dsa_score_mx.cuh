@@ -213,16 +213,24 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
         tma_load_2d(q_s + qb * C::Q_BYTES, &p.tmap_q, &qfull[qb], 0, g.row0 * C::H);
         ++qissued;
       }
-      for (int kt = g.kt_begin; kt < g.kt_end; ++kt) {
-        const int stage = kiter % C::NST;
-        const uint32_t phase = static_cast<uint32_t>(kiter / C::NST) & 1u;
-        // Key scales of the tile, loaded before the wait for the stage.
-        uint32_t kv[4];
+      // Key scale words of a tile (one per key), loaded a tile ahead of use
+      // so that their latency stays off the producer's per-tile path.
+      auto load_kv = [&](int kt, uint32_t (&kv)[4]) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int key = kt * C::TILE + 32 * j + lane;
-          kv[j] = key < p.S ? __ldg(k_sf + key) : 0x7F7F7F7Fu;
+          kv[j] = (kt < g.kt_end && key < p.S) ? __ldg(k_sf + key) : 0x7F7F7F7Fu;
         }
+      };
+      uint32_t kv_next[4];
+      load_kv(g.kt_begin, kv_next);
+      for (int kt = g.kt_begin; kt < g.kt_end; ++kt) {
+        const int stage = kiter % C::NST;
+        const uint32_t phase = static_cast<uint32_t>(kiter / C::NST) & 1u;
+        uint32_t kv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) kv[j] = kv_next[j];
+        load_kv(kt + 1, kv_next);
         if (lane == 0) ok = mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag);
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;

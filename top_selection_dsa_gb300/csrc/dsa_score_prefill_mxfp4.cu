@@ -7,6 +7,8 @@ namespace dsa {
 
 bool score_mx_supported(int H, int D) { return H == MxCfg::H && D == MxCfg::D; }
 
+int score_mx_q_rows() { return MxCfg::N; }
+
 cudaError_t launch_score_mx(const ScoreParams& p, const uint8_t* q_sf, const uint8_t* k_sf,
                             cudaStream_t s) {
   using C = MxCfg;
