@@ -259,6 +259,43 @@ def test_topk_row_lengths(api, S, k, T):
     assert np.array_equal(got, oracle.topk(lg, rs, re, k))
 
 
+# The split path (few rows, some longer than 16384 columns) over rows of every
+# kind: empty, one key, exactly one or two 4096-key units, all ties, nothing
+# valid, NaN, signed zeros, ranges starting mid-row or clamped, and more rows
+# (40) than one unit each, so that each resident CTA walks several units.
+def test_topk_split_path_edge_rows(api):
+    rng = np.random.default_rng(77)
+    T, S, k = 40, 50000, 2048
+    lg = rng.standard_normal((T, S)).astype(np.float32)
+    kind = np.arange(T) % 10
+    lg[kind == 1] = 0.0                                           # all ties
+    lg[kind == 2] = np.round(lg[kind == 2] * 2) / 2               # heavy ties
+    lg[kind == 3] = -np.inf                                       # nothing valid
+    sub = lg[kind == 4]
+    sub[rng.random(sub.shape) < 0.4] = np.nan
+    lg[kind == 4] = sub
+    lg[kind == 5, ::2] = -0.0                                     # signed zeros
+    lg[kind == 5, 1::2] = 0.0
+    starts = np.zeros(T, np.int64)
+    ends = np.full(T, S, np.int64)
+    ends[kind == 6] = 4096                                        # one whole unit
+    ends[kind == 7] = 8192 + 1                                    # two units and a key
+    starts[kind == 8] = 12345                                     # mid-row start
+    ends[kind == 8] = S + 1000                                    # clamped end
+    ends[0] = 0                                                   # empty
+    starts[10], ends[10] = 777, 778                               # one key
+    starts[20], ends[20] = 100, 100 + k                           # exactly k keys
+    rs, re = starts.astype(np.int32), ends.astype(np.int32)
+    dirty = lg.copy()
+    for t in range(T):
+        dirty[t, :max(rs[t], 0)] = 1e30
+        dirty[t, min(max(re[t], 0), S):] = np.inf
+    got = api.topk(dev(dirty), dev(rs), dev(re), k).cpu().numpy()
+    assert np.array_equal(got, oracle.topk(dirty, rs, re, k))
+    assert (got[0] == -1).all() and got[10, 0] == 777 and (got[10, 1:] == -1).all()
+    assert (got[20] == np.arange(100, 100 + k)).all()
+
+
 def test_topk_reads_ranges_written_just_before_on_the_stream(api):
     # dsa_topk's row ranges come out of kernels queued immediately before it
     # on the same stream (with stale zero ranges in the buffers beforehand):

@@ -872,6 +872,7 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamThreads >= 1024 ? 1 : 8
 constexpr int kUnitThreads = 256;
 constexpr int kUnitKeys = kUnitThreads * 16;  // 4096
 constexpr int kSplitUnits = 256;              // rows of up to 256 * 4096 keys
+constexpr int kSplitMaxRows = 512;
 constexpr int kSplitCand = 16384;
 constexpr int kStateWords = 16;
 constexpr int kStHist = 0, kStState = kHistBins, kStAbove = kStState + kStateWords,
@@ -905,15 +906,61 @@ __device__ __forceinline__ bool last_to_arrive(uint32_t* counter, uint32_t total
   return last;
 }
 
+// The split path's work items: every (row, unit) whose unit holds keys, and
+// unit 0 of each empty row (whose state and -1 row still have to be
+// written), row-major.  Each phase runs a grid of resident CTAs that take
+// items blockIdx.x, blockIdx.x + gridDim.x, ... so that no CTA is spent on
+// the empty tail units of short rows.  pre[r] (shared, R + 1 entries) = the
+// items of rows before r; returns their total.  Every thread must call it.
+__device__ __forceinline__ int split_items(const TopkParams& p, int* pre, uint2* warp_sums) {
+  const int tid = threadIdx.x;
+  int cnt[2] = {0, 0};
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int row = 2 * tid + j;
+    if (row < p.R) {
+      int lo, hi;
+      row_range(p, row, &lo, &hi);
+      cnt[j] = hi > lo ? (hi - lo + kUnitKeys - 1) / kUnitKeys : 1;
+    }
+  }
+  uint2 total;
+  const uint32_t before =
+      block_scan2<kUnitThreads>(make_uint2(static_cast<uint32_t>(cnt[0] + cnt[1]), 0u),
+                                warp_sums, &total).x;
+  if (2 * tid < p.R) pre[2 * tid] = static_cast<int>(before);
+  if (2 * tid + 1 < p.R) pre[2 * tid + 1] = static_cast<int>(before) + cnt[0];
+  if (tid == 0) pre[p.R] = static_cast<int>(total.x);
+  __syncthreads();
+  return static_cast<int>(total.x);
+}
+
+// Item -> (row, unit): the largest row with pre[row] <= item.
+__device__ __forceinline__ void split_item(const int* pre, int R, int item, int* row, int* unit) {
+  int lo_r = 0, hi_r = R;
+  while (hi_r - lo_r > 1) {
+    const int mid = (lo_r + hi_r) >> 1;
+    if (pre[mid] <= item) lo_r = mid; else hi_r = mid;
+  }
+  *row = lo_r;
+  *unit = item - pre[lo_r];
+}
+
 __global__ void __launch_bounds__(kUnitThreads, 5) topk_unit_hist_kernel(const TopkParams p) {
   constexpr int NW = kUnitThreads / 32;
   __shared__ __align__(16) uint32_t hist[kHistBins];
   __shared__ __align__(16) uint32_t wsum[NW];
   __shared__ uint32_t sel[4];
   __shared__ uint32_t flag;
-  const int row = blockIdx.x, unit = blockIdx.y;
+  __shared__ int pre[kSplitMaxRows + 1];
+  __shared__ uint2 scan_sums[NW];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   launch_dependents();
+  const int items = split_items(p, pre, scan_sums);
+  for (int item = blockIdx.x; item < items; item += gridDim.x) {
+  int row, unit;
+  split_item(pre, p.R, item, &row, &unit);
+  __syncthreads();  // the previous item's readers of shared memory are done
   int lo, hi;
   row_range(p, row, &lo, &hi);
   const int n = hi - lo;
@@ -921,11 +968,11 @@ __global__ void __launch_bounds__(kUnitThreads, 5) topk_unit_hist_kernel(const T
   const int cnt = min(n - c0, kUnitKeys);
   uint32_t* w = split_row(p, row);
   if (cnt <= 0) {
-    if (unit == 0 && tid == 0) {  // empty row: nothing to select
+    if (tid == 0) {  // empty row: nothing to select
       w[kStState + kSMode] = kModeIota;
       w[kStState + kSValid] = 0u;
     }
-    return;
+    continue;
   }
   uint32_t key[16];
   load_chunk<kUnitThreads>(p.logits + static_cast<int64_t>(row) * p.ld + lo + c0, cnt, 0, warp,
@@ -945,7 +992,7 @@ __global__ void __launch_bounds__(kUnitThreads, 5) topk_unit_hist_kernel(const T
     if (v && i != 3) atomicAdd(&g[i], v);
   }
   const uint32_t nunits = static_cast<uint32_t>((n + kUnitKeys - 1) / kUnitKeys);
-  if (!last_to_arrive(&w[kStState + kSDoneHist], nunits, &flag)) return;
+  if (!last_to_arrive(&w[kStState + kSDoneHist], nunits, &flag)) continue;
   // The row's histogram is complete: find the threshold bin once.
   for (int i = tid; i < kHistBins; i += kUnitThreads) hist[i] = __ldcg(&g[i]);
   __syncthreads();
@@ -970,6 +1017,7 @@ __global__ void __launch_bounds__(kUnitThreads, 5) topk_unit_hist_kernel(const T
       }
     }
   }
+  }
 }
 
 __global__ void __launch_bounds__(kUnitThreads, 4) topk_unit_gather_kernel(const TopkParams p) {
@@ -981,22 +1029,27 @@ __global__ void __launch_bounds__(kUnitThreads, 4) topk_unit_gather_kernel(const
   __shared__ uint32_t flag, cta_hits, cta_base;
   __shared__ uint32_t stage[kUnitKeys];  // this unit's candidates
   __shared__ uint32_t unit_gt[kSplitUnits], unit_eq[kSplitUnits];
-  const int row = blockIdx.x, unit = blockIdx.y;
+  __shared__ int pre[kSplitMaxRows + 1];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  launch_dependents();
+  const int items = split_items(p, pre, warp_sums);
+  for (int item = blockIdx.x; item < items; item += gridDim.x) {
+  int row, unit;
+  split_item(pre, p.R, item, &row, &unit);
+  __syncthreads();  // the previous item's readers of shared memory are done
   int lo, hi;
   row_range(p, row, &lo, &hi);
   const int n = hi - lo;
   const int c0 = unit * kUnitKeys;
   const int cnt = min(n - c0, kUnitKeys);
-  launch_dependents();
-  if (cnt <= 0) return;
+  if (cnt <= 0) continue;
   uint32_t* w = split_row(p, row);
   const float* row_src = p.logits + static_cast<int64_t>(row) * p.ld + lo;
   uint32_t key[16];
   load_chunk<kUnitThreads>(row_src + c0, cnt, 0, warp, lane, key);
   grid_dependency_wait();  // the histogram phase is complete
   const uint32_t mode = w[kStState + kSMode];
-  if (mode == kModeIota) return;
+  if (mode == kModeIota) continue;
   const uint32_t b1 = w[kStState + kSB1];
   // Keys above `thr` are taken whatever the refinement finds; keys of bin
   // `want` (none unless gathering) are the candidates.
@@ -1040,7 +1093,7 @@ __global__ void __launch_bounds__(kUnitThreads, 4) topk_unit_gather_kernel(const
       if (base + i < static_cast<uint32_t>(kSplitCand)) cand[base + i] = stage[i];
   }
   const uint32_t nunits = static_cast<uint32_t>((n + kUnitKeys - 1) / kUnitKeys);
-  if (!last_to_arrive(&w[kStState + kSDoneGather], nunits, &flag)) return;
+  if (!last_to_arrive(&w[kStState + kSDoneGather], nunits, &flag)) continue;
 
   // Last gather CTA of the row: tau / need_eq, then the offsets of every
   // unit's selected columns.
@@ -1143,13 +1196,20 @@ __global__ void __launch_bounds__(kUnitThreads, 4) topk_unit_gather_kernel(const
     w[kStState + kSNeed] = need_eq;
     w[kStState + kSMode] = kModeSelect;
   }
+  }
 }
 
 __global__ void __launch_bounds__(kUnitThreads, 5) topk_unit_write_kernel(const TopkParams p) {
   constexpr int NW = kUnitThreads / 32;
   __shared__ uint2 warp_cnt[NW];
-  const int row = blockIdx.x, unit = blockIdx.y;
+  __shared__ uint2 scan_sums[NW];
+  __shared__ int pre[kSplitMaxRows + 1];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int items = split_items(p, pre, scan_sums);
+  for (int item = blockIdx.x; item < items; item += gridDim.x) {
+  int row, unit;
+  split_item(pre, p.R, item, &row, &unit);
+  __syncthreads();  // the previous item's readers of warp_cnt are done
   int lo, hi;
   row_range(p, row, &lo, &hi);
   const int n = hi - lo;
@@ -1167,11 +1227,11 @@ __global__ void __launch_bounds__(kUnitThreads, 5) topk_unit_write_kernel(const 
     const int nsel = nvalid < static_cast<uint32_t>(p.k) ? static_cast<int>(nvalid) : p.k;
     for (int i = nsel + tid; i < p.k; i += kUnitThreads) dst[i] = -1;
   }
-  if (cnt <= 0) return;
+  if (cnt <= 0) continue;
   const uint32_t mode = w[kStState + kSMode];
   if (mode == kModeIota) {
     for (int i = tid; i < cnt; i += kUnitThreads) dst[c0 + i] = lo + c0 + i;
-    return;
+    continue;
   }
   const uint32_t tau = w[kStState + kSTau], need_eq = w[kStState + kSNeed];
   const int ng = chunk_groups<kUnitThreads>(cnt, 0, warp);
@@ -1224,6 +1284,7 @@ __global__ void __launch_bounds__(kUnitThreads, 5) topk_unit_write_kernel(const 
         erun += __popc(me);
       }
     }
+  }
   }
 }
 
@@ -1366,7 +1427,7 @@ bool topk_supported(int max_row) {
 
 bool topk_split_rows(int64_t rows, int64_t max_row) {
   return max_row > 16384 && max_row <= static_cast<int64_t>(kSplitUnits) * kUnitKeys &&
-         rows <= 512;
+         rows <= kSplitMaxRows;
 }
 
 int topk_split_words(int64_t) {
@@ -1397,16 +1458,20 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t s) {
                                       0, kStZeroWords * sizeof(uint32_t),
                                       static_cast<size_t>(p.R), s);
     if (e != cudaSuccess) return e;
-    // Rows vary fastest: every row's first unit is scheduled before any
-    // second one, and the empty tail units of short rows come last.
-    const dim3 grid(static_cast<unsigned>(p.R), (S + kUnitKeys - 1) / kUnitKeys);
-    topk_unit_hist_kernel<<<grid, kUnitThreads, 0, s>>>(p);
+    // Each phase: at most as many CTAs as are resident at once (their launch
+    // bounds), each walking the row-major list of units that hold keys.
+    const int64_t units = static_cast<int64_t>(p.R) * ((S + kUnitKeys - 1) / kUnitKeys);
+    const int sms = device_sm_count() > 0 ? device_sm_count() : 1;
+    auto grid_of = [&](int per_sm) {
+      return dim3(static_cast<unsigned>(std::min<int64_t>(units, static_cast<int64_t>(sms) * per_sm)));
+    };
+    topk_unit_hist_kernel<<<grid_of(5), kUnitThreads, 0, s>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // The later phases start early (their loads overlap the previous
     // phase's tail) and wait for it in hardware before reading its results.
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
+    cfg.gridDim = grid_of(4);
     cfg.blockDim = dim3(kUnitThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
@@ -1417,6 +1482,7 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t s) {
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, topk_unit_gather_kernel, p);
     if (e != cudaSuccess) return e;
+    cfg.gridDim = grid_of(5);
     return cudaLaunchKernelEx(&cfg, topk_unit_write_kernel, p);
   }
   // One 256-thread CTA per row, the row in 4096-key chunks.
