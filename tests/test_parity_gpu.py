@@ -334,6 +334,20 @@ def test_paged_small(api, next_n, block_size, H, fp8):
     check_paged(api, p, rows=None)
 
 
+# Paged rows long enough for the split top-k (a context above 16384 keys),
+# one to five query tokens a request: empty and one-key rows, contexts ending
+# inside a 4096-key unit and inside a block, e4m3 and bf16, 8 to 64 heads.
+@pytest.mark.parametrize("next_n,block_size,H,fp8", [(1, 16, 64, False), (2, 64, 64, True),
+                                                     (4, 32, 8, False), (3, 128, 16, True),
+                                                     (5, 64, 32, False)])
+def test_paged_split_topk(api, next_n, block_size, H, fp8):
+    ctx = np.array([0, 1, next_n, 4097, 16385, 20003, 33000, 40960], np.int32)
+    p = wl.paged_decode(next_n=next_n, block_size=block_size, H=H, D=128, topk=2048,
+                        ctx_hi=40960, seed=7 * next_n + H, context_lens=ctx,
+                        dtype=wl.E4M3 if fp8 else wl.BF16)
+    check_paged(api, p, rows=None)
+
+
 def paged_tensors(p):
     if p.dtype == wl.BF16:
         q = dev(p.q.view(np.int16)).view(torch.bfloat16)
