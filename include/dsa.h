@@ -357,6 +357,47 @@ dsa_status_t dsa_topk_merge(const float* cand_scores, const int32_t* cand_cols, 
                             int k, int32_t* out, dsa_stream_t stream);
 
 /*
+ * dsa_topk_merge over candidates laid out rank-major, [W, T, kr] (rank w's
+ * [T, kr] block at offset w * T * kr), as an all-gather of every rank's
+ * dsa_topk_dcp_candidates output into one buffer leaves them: row t's
+ * candidates are the W * kr entries (w, t, 0 .. kr-1).  Same result as
+ * dsa_topk_merge on those candidates in any order.
+ *
+ *   cand_scores [W, T, kr] fp32, cand_cols [W, T, kr] int32 global columns
+ *               (negative = empty slot; distinct within a row)
+ *   out         [T, k] int32
+ *   W * kr, k <= 16384 (else DSA_ERR_UNSUPPORTED)
+ */
+dsa_status_t dsa_topk_merge_ranks(const float* cand_scores, const int32_t* cand_cols, int W,
+                                  int T, int kr, int k, int32_t* out, dsa_stream_t stream);
+
+/*
+ * One rank's candidates for the merge under decode context parallelism
+ * (KimiK3DSAIndexer.__init__ on the vLLM page: the key cache is dealt to the
+ * W ranks in runs of `interleave` consecutive positions, cp_kv_cache_
+ * interleave_size, so rank r owns the positions p with (p / interleave) % W
+ * == r, in order).  Per row, dsa_topk of the rank's local logits, written as
+ * pairs: cand_cols[t, i] = the global position of the i-th selected local
+ * column j, ((j / interleave) * W + rank) * interleave + j % interleave, and
+ * cand_scores[t, i] = logits[t, j]; empty slots get -1 and -inf.  The pairs
+ * follow the local columns' ascending order, so the global positions ascend
+ * too.
+ *
+ *   logits      [T, ld] fp32 scores over the rank's own keys (local columns)
+ *   row_starts, row_ends  [T] int32 local column ranges, as dsa_topk
+ *   rank, world 0 <= rank < world
+ *   interleave  >= 1
+ *   cand_scores [T, k] fp32 out; cand_cols [T, k] int32 out
+ *   workspace   dsa_workspace_bytes(DSA_OP_TOPK, T, S, k) bytes, as dsa_topk
+ * A global position past INT32_MAX gives DSA_ERR_UNSUPPORTED.
+ */
+dsa_status_t dsa_topk_dcp_candidates(const float* logits, int64_t ld, const int32_t* row_starts,
+                                     const int32_t* row_ends, int T, int S, int k, int rank,
+                                     int world, int interleave, float* cand_scores,
+                                     int32_t* cand_cols, void* workspace, size_t ws_bytes,
+                                     dsa_stream_t stream);
+
+/*
  * The query side of the e4m3 path, before dsa_indexer_logits / _topk /
  * _topk_paged: indexer_q_quant_fold_weights of KimiK3DSAIndexer.score (vLLM
  * API docs, "vllm.models.kimi_k3.nvidia.dsa").  Every (t, h) row of D query

@@ -208,6 +208,38 @@ def test_topk_merge_validation(api):
     assert f(A, A, 4, 16, 16385, A, NUL) == U
 
 
+def test_topk_merge_ranks_validation(api):
+    E, U = api.DSA_ERR_INVALID_ARG, api.DSA_ERR_UNSUPPORTED
+    f = api.lib.dsa_topk_merge_ranks                        # (s, c, W, T, kr, k, out, stream)
+    assert f(NUL, A, 2, 4, 16, 8, A, NUL) == E
+    assert f(A, A, 0, 4, 16, 8, A, NUL) == E                 # no rank
+    assert f(A, A, 2, -1, 16, 8, A, NUL) == E
+    assert f(A, A, 2, 4, 0, 8, A, NUL) == E
+    assert f(A, A, 2, 4, 16, 0, A, NUL) == E
+    assert f(A, A, 2, 4, 16, 8, ctypes.c_void_p(0x10002), NUL) == E   # out not 4-byte aligned
+    assert f(A, A, 2, 4, 8193, 8, A, NUL) == U               # W * kr > 16384
+    assert f(A, A, 2, 4, 16, 16385, A, NUL) == U
+
+
+def test_topk_dcp_candidates_validation(api):
+    E, U = api.DSA_ERR_INVALID_ARG, api.DSA_ERR_UNSUPPORTED
+    f = api.lib.dsa_topk_dcp_candidates
+    # (logits, ld, rs, re, T, S, k, rank, world, interleave, scores, cols, ws, ws_bytes, stream)
+    assert f(NUL, 8, A, A, 4, 8, 2, 0, 2, 64, A, A, NUL, 0, NUL) == E
+    assert f(A, 8, A, A, 4, 8, 2, 2, 2, 64, A, A, NUL, 0, NUL) == E    # rank >= world
+    assert f(A, 8, A, A, 4, 8, 2, -1, 2, 64, A, A, NUL, 0, NUL) == E
+    assert f(A, 8, A, A, 4, 8, 2, 0, 0, 64, A, A, NUL, 0, NUL) == E    # world < 1
+    assert f(A, 8, A, A, 4, 8, 2, 0, 2, 0, A, A, NUL, 0, NUL) == E     # interleave < 1
+    assert f(A, 8, A, A, 4, 8, 0, 0, 2, 64, A, A, NUL, 0, NUL) == E    # k < 1
+    assert f(A, 4, A, A, 4, 8, 2, 0, 2, 64, A, A, NUL, 0, NUL) == E    # ld < S
+    assert f(A, 8, A, A, 4, 8, 2, 0, 2, 64, NUL, A, NUL, 0, NUL) == E
+    assert f(A, 8, A, A, 4, 8, 2, 0, 2, 64, A, ctypes.c_void_p(0x10002), NUL, 0, NUL) == E
+    need = api.lib.dsa_workspace_bytes(api.DSA_OP_TOPK, 4, 100000, 8)
+    assert f(A, 100000, A, A, 4, 100000, 8, 0, 2, 64, A, A, NUL, 0, NUL) == E   # needs scratch
+    # global positions past INT32_MAX
+    assert f(A, 100000, A, A, 4, 100000, 8, 0, 1 << 16, 64, A, A, A, need, NUL) == U
+
+
 def test_indexer_topk_host_validation(api):
     E, U = api.DSA_ERR_INVALID_ARG, api.DSA_ERR_UNSUPPORTED
     nb = api.lib.dsa_indexer_topk_host_bytes

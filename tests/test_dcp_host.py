@@ -58,8 +58,11 @@ def _worker(rank, world, port, out):
     sc = np.where(top >= 0, np.take_along_axis(loc, np.maximum(top, 0), 1), -np.inf)
     gc = d.local_to_global(torch.from_numpy(top), rank, world, inter)
     all_s, all_c = d.gather_candidates(torch.from_numpy(sc.astype(np.float32)), gc)
-    assert tuple(all_s.shape) == (T, world * k)
-    merged = oracle.topk_merge(all_s.numpy(), all_c.numpy(), k)
+    assert tuple(all_s.shape) == (world, T, k) and tuple(all_c.shape) == (world, T, k)
+    assert torch.equal(all_c[rank], gc)                     # rank-major: this rank's block
+    flat_s = all_s.permute(1, 0, 2).reshape(T, world * k)   # row t: every rank's candidates
+    flat_c = all_c.permute(1, 0, 2).reshape(T, world * k)
+    merged = oracle.topk_merge(flat_s.numpy(), flat_c.numpy(), k)
     out[rank] = bool(np.array_equal(merged, oracle.topk(lg, np.zeros(T, np.int32), L, k)))
     dist.destroy_process_group()
 

@@ -31,7 +31,8 @@ EXPORTS = (
     "dsa_get_last_device_error", "dsa_selftest_wait_timeout", "dsa_indexer_topk_noalloc",
     "dsa_topk_sort_by_score", "dsa_q_quant_fold_weights", "dsa_k_norm_quant_insert",
     "dsa_topk_merge", "dsa_indexer_topk_host_bytes", "dsa_indexer_topk_host",
-    "dsa_indexer_logits_mxfp4", "dsa_indexer_topk_mxfp4",
+    "dsa_indexer_logits_mxfp4", "dsa_indexer_topk_mxfp4", "dsa_topk_merge_ranks",
+    "dsa_topk_dcp_candidates",
 )
 
 
@@ -67,6 +68,8 @@ def _load():
     lib.dsa_q_quant_fold_weights.argtypes = [P, P, F, I, I, I, I, P, P, P]
     lib.dsa_k_norm_quant_insert.argtypes = [P, P, P, F, P, I, I, I, P, P, I, I, P]
     lib.dsa_topk_merge.argtypes = [P, P, I, I, I, P, P]
+    lib.dsa_topk_merge_ranks.argtypes = [P, P, I, I, I, I, P, P]
+    lib.dsa_topk_dcp_candidates.argtypes = [P, I64, P, P, I, I, I, I, I, I, P, P, P, SZ, P]
     lib.dsa_indexer_topk_host_bytes.argtypes = [I, I, I, I, I, I]
     lib.dsa_indexer_topk_host_bytes.restype = SZ
     lib.dsa_indexer_topk_host.argtypes = [P, P, P, P, I, P, P, P, I, I, I, I, I, P, P, SZ, P]
@@ -399,6 +402,52 @@ def topk_merge(cand_scores, cand_cols, k, *, out=None):
                                 _stream(dev))
     _check(st, "dsa_topk_merge")
     return out
+
+
+def topk_merge_ranks(cand_scores, cand_cols, k, *, out=None):
+    """[W, T, kr] rank-major (score, global column) candidates -> the [T, k]
+    global top-k, ascending columns, -1 padding."""
+    dev = cand_scores.device
+    _need(cand_scores, "cand_scores", (torch.float32,), dev)
+    _need(cand_cols, "cand_cols", (torch.int32,), dev)
+    W, T, kr = cand_scores.shape
+    if tuple(cand_cols.shape) != (W, T, kr):
+        raise ValueError("cand_scores and cand_cols must have the same [W, T, kr] shape")
+    if out is None:
+        out = torch.empty((T, k), dtype=torch.int32, device=dev)
+    _need(out, "out", (torch.int32,), dev)
+    with torch.cuda.device(dev):
+        st = lib.dsa_topk_merge_ranks(_ptr(cand_scores), _ptr(cand_cols), W, T, kr, int(k),
+                                      _ptr(out), _stream(dev))
+    _check(st, "dsa_topk_merge_ranks")
+    return out
+
+
+def topk_dcp_candidates(logits, row_starts, row_ends, k, rank, world, interleave, *, S=None,
+                        scores=None, cols=None, workspace=None):
+    """A rank's masked top-k of its local logits [T, ld] as (score, global
+    position) pairs, [T, k] each (-inf / -1 in empty slots)."""
+    T, ld = logits.shape
+    S = ld if S is None else S
+    dev = logits.device
+    _need(logits, "logits", (torch.float32,), dev)
+    _need(row_starts, "row_starts", (torch.int32,), dev)
+    _need(row_ends, "row_ends", (torch.int32,), dev)
+    if scores is None:
+        scores = torch.empty((T, k), dtype=torch.float32, device=dev)
+    if cols is None:
+        cols = torch.empty((T, k), dtype=torch.int32, device=dev)
+    _need(scores, "scores", (torch.float32,), dev)
+    _need(cols, "cols", (torch.int32,), dev)
+    nbytes = workspace_bytes(DSA_OP_TOPK, T, S, k)
+    ws = _workspace(nbytes, dev, workspace)
+    with torch.cuda.device(dev):
+        st = lib.dsa_topk_dcp_candidates(_ptr(logits), ld, _ptr(row_starts), _ptr(row_ends), T, S,
+                                         int(k), int(rank), int(world), int(interleave),
+                                         _ptr(scores), _ptr(cols), _ptr(ws) if nbytes else None,
+                                         nbytes, _stream(dev))
+    _check(st, "dsa_topk_dcp_candidates")
+    return scores, cols
 
 
 def q_quant_fold_weights(q, weights, weight_scale, padded_heads=None, *, q_fp8=None,

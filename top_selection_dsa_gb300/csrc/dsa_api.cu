@@ -708,7 +708,50 @@ dsa_status_t dsa_topk_merge(const float* cand_scores, const int32_t* cand_cols, 
   if (!aligned(cand_scores, 4) || !aligned(cand_cols, 4) || !aligned(out, 4))
     return DSA_ERR_INVALID_ARG;
   if (C > kTopkMergeMax || k > kTopkMergeMax) return DSA_ERR_UNSUPPORTED;
-  return from_cuda(launch_topk_merge(cand_scores, cand_cols, T, C, k, out, as_stream(stream)));
+  return from_cuda(launch_topk_merge(cand_scores, cand_cols, T, 1, C, k, out, as_stream(stream)));
+}
+
+dsa_status_t dsa_topk_merge_ranks(const float* cand_scores, const int32_t* cand_cols, int W,
+                                  int T, int kr, int k, int32_t* out, dsa_stream_t stream) {
+  const CallRange range("dsa_topk_merge_ranks");
+  if (!cand_scores || !cand_cols || !out || W < 1 || T < 0 || kr < 1 || k < 1)
+    return DSA_ERR_INVALID_ARG;
+  if (!aligned(cand_scores, 4) || !aligned(cand_cols, 4) || !aligned(out, 4))
+    return DSA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(W) * kr > kTopkMergeMax || k > kTopkMergeMax)
+    return DSA_ERR_UNSUPPORTED;
+  return from_cuda(launch_topk_merge(cand_scores, cand_cols, T, W, kr, k, out, as_stream(stream)));
+}
+
+dsa_status_t dsa_topk_dcp_candidates(const float* logits, int64_t ld, const int32_t* row_starts,
+                                     const int32_t* row_ends, int T, int S, int k, int rank,
+                                     int world, int interleave, float* cand_scores,
+                                     int32_t* cand_cols, void* workspace, size_t ws_bytes,
+                                     dsa_stream_t stream) {
+  const CallRange range("dsa_topk_dcp_candidates");
+  if (!logits || !row_starts || !row_ends || !cand_scores || !cand_cols) return DSA_ERR_INVALID_ARG;
+  if (T < 0 || S < 0 || k < 1 || ld < S || ld < 1 || world < 1 || rank < 0 || rank >= world ||
+      interleave < 1)
+    return DSA_ERR_INVALID_ARG;
+  if (!aligned(logits, 4) || !aligned(cand_scores, 4) || !aligned(cand_cols, 4) ||
+      !aligned(row_starts, 4) || !aligned(row_ends, 4))
+    return DSA_ERR_INVALID_ARG;
+  if (!topk_supported(S)) return DSA_ERR_UNSUPPORTED;
+  // The largest global position a local column can map to must fit int32.
+  if (S > 0) {
+    const int64_t runs = (static_cast<int64_t>(S) - 1) / interleave;
+    const int64_t gmax = (runs * world + (world - 1)) * interleave + (interleave - 1);
+    if (gmax > INT32_MAX) return DSA_ERR_UNSUPPORTED;
+  }
+  const size_t need = dsa_workspace_bytes(DSA_OP_TOPK, T, S, k);
+  if (need > 0 && (!workspace || ws_bytes < need || !aligned(workspace, 256)))
+    return DSA_ERR_INVALID_ARG;
+  dsa_status_t st = run_topk(logits, ld, row_starts, row_ends, nullptr, 1, T, S, k, cand_cols,
+                             as_stream(stream),
+                             need > 0 ? static_cast<uint32_t*>(workspace) : nullptr, false);
+  if (st != DSA_OK) return st;
+  return from_cuda(launch_dcp_pairs(logits, ld, T, k, rank, world, interleave, cand_scores,
+                                    cand_cols, as_stream(stream)));
 }
 
 dsa_status_t dsa_q_quant_fold_weights(const void* q, const float* weights, float weight_scale,

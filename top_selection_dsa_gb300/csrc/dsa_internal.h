@@ -99,8 +99,10 @@ constexpr int kTopkSortMax = 8192;
 // Merge of C (score, global column) candidates per row into the k best,
 // ascending columns, -1 padding (C, k <= kTopkMergeMax).
 constexpr int kTopkMergeMax = 16384;
-cudaError_t launch_topk_merge(const float* scores, const int32_t* cols, int T, int C, int k,
-                              int32_t* out, cudaStream_t s);
+cudaError_t launch_topk_merge(const float* scores, const int32_t* cols, int T, int W, int kr,
+                              int k, int32_t* out, cudaStream_t s);
+cudaError_t launch_dcp_pairs(const float* logits, int64_t ld, int T, int k, int rank, int W,
+                             int inter, float* scores, int32_t* cols, cudaStream_t s);
 cudaError_t launch_topk_sort(const float* logits, int64_t ld, int32_t* topk, int T, int k,
                              uint32_t* err, cudaStream_t s);
 cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint64_t timeout_ns, cudaStream_t s);

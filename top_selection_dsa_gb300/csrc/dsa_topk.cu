@@ -1374,13 +1374,14 @@ __device__ __forceinline__ void bitonic_desc(K* a, int n) {
   }
 }
 
+// Candidates of row `row`: C = W * kr of them, candidate i at
+// (i / kr) * rank_stride + row * kr + i % kr (W = 1, kr = C: a [T, C] array;
+// rank_stride = T * kr: [W, T, kr] rank-major, as an all-gather leaves them).
 __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(
-    const float* __restrict__ scores, const int32_t* __restrict__ cols, int C, int n, int k,
-    int m, int32_t* __restrict__ out) {
+    const float* __restrict__ scores, const int32_t* __restrict__ cols, int C, int kr,
+    int64_t rank_stride, int n, int k, int m, int32_t* __restrict__ out) {
   extern __shared__ __align__(16) unsigned long long mk[];  // n composites
   const int row = blockIdx.x;
-  const float* sr = scores + static_cast<int64_t>(row) * C;
-  const int32_t* cr = cols + static_cast<int64_t>(row) * C;
   __shared__ uint32_t nvalid;
   if (threadIdx.x == 0) nvalid = 0u;
   __syncthreads();
@@ -1388,8 +1389,10 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(
   for (int i = threadIdx.x; i < n; i += kMergeThreads) {
     unsigned long long v = 0ull;
     if (i < C) {
-      const int c = __ldg(cr + i);
-      const uint32_t key = c >= 0 ? order_key(__ldg(sr + i)) : 0u;  // -inf / NaN: never taken
+      const int w = i / kr;
+      const int64_t off = w * rank_stride + static_cast<int64_t>(row) * kr + (i - w * kr);
+      const int c = __ldg(cols + off);
+      const uint32_t key = c >= 0 ? order_key(__ldg(scores + off)) : 0u;  // -inf / NaN: never taken
       if (key != 0u) {
         v = (static_cast<unsigned long long>(key) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(c));
         ++mine;
@@ -1528,9 +1531,10 @@ cudaError_t launch_topk_sort(const float* logits, int64_t ld, int32_t* topk, int
   return cudaGetLastError();
 }
 
-cudaError_t launch_topk_merge(const float* scores, const int32_t* cols, int T, int C, int k,
-                              int32_t* out, cudaStream_t s) {
+cudaError_t launch_topk_merge(const float* scores, const int32_t* cols, int T, int W, int kr,
+                              int k, int32_t* out, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
+  const int C = W * kr;
   int n = 1;
   while (n < C) n <<= 1;
   int m = 1;
@@ -1540,7 +1544,42 @@ cudaError_t launch_topk_merge(const float* scores, const int32_t* cols, int T, i
   cudaError_t e = cudaFuncSetAttribute(topk_merge_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  topk_merge_kernel<<<T, kMergeThreads, smem, s>>>(scores, cols, C, n, k, m, out);
+  topk_merge_kernel<<<T, kMergeThreads, smem, s>>>(scores, cols, C, kr,
+                                                   static_cast<int64_t>(T) * kr, n, k, m, out);
+  return cudaGetLastError();
+}
+
+// Decode context parallelism: a rank's top-k indices (local columns, in
+// place in cols) become (local score, global position) pairs.  The rank owns
+// the runs of `inter` positions p with (p / inter) % W == rank, in order, so
+// local column j is global ((j / inter) * W + rank) * inter + j % inter.
+__global__ void dcp_pairs_kernel(const float* __restrict__ logits, int64_t ld, int T, int k,
+                                 int rank, int W, int inter, float* __restrict__ scores,
+                                 int32_t* __restrict__ cols) {
+  const int64_t total = static_cast<int64_t>(T) * k;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int j = cols[i];
+    if (j >= 0) {
+      const int64_t t = i / k;
+      scores[i] = logits[t * ld + j];
+      const int64_t run = j / inter;
+      cols[i] = static_cast<int32_t>((run * W + rank) * inter + (j - run * inter));
+    } else {
+      scores[i] = -INFINITY;
+      cols[i] = -1;
+    }
+  }
+}
+
+cudaError_t launch_dcp_pairs(const float* logits, int64_t ld, int T, int k, int rank, int W,
+                             int inter, float* scores, int32_t* cols, cudaStream_t s) {
+  const int64_t total = static_cast<int64_t>(T) * k;
+  if (total <= 0) return cudaSuccess;
+  const int sms = device_sm_count() > 0 ? device_sm_count() : 1;
+  const int64_t blocks = std::min<int64_t>((total + 255) / 256, static_cast<int64_t>(sms) * 8);
+  dcp_pairs_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(logits, ld, T, k, rank, W, inter,
+                                                                 scores, cols);
   return cudaGetLastError();
 }
 
