@@ -285,6 +285,19 @@ __device__ __forceinline__ void tmem_ld16x256_x2_async(uint32_t taddr, uint32_t*
       : "memory");
 }
 
+// The same shape four blocks of 8 columns wide (32 columns): registers
+// 4b .. 4b+3 of block b as for the two-block form.
+__device__ __forceinline__ void tmem_ld16x256_x4_async(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
 // Wait for this thread's outstanding TMEM loads; the 16 registers are tied
 // to the wait so that no use of them moves above it.
 __device__ __forceinline__ void tmem_wait_ld16(uint32_t (&r)[16]) {

@@ -564,8 +564,10 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
         }
         const bool col_ok = s < p.S;
         if constexpr (kQuad) {
-          // Four chunks of 16 columns, each read as two 16-lane halves; the
-          // next chunk's loads are in flight while this one is summed.
+          // Four chunks, each one 16x256b.x4 load (16 lanes x 32 columns:
+          // lanes +16(c & 1), heads 32(c >> 1) ..); the next chunk's load is
+          // in flight while this one is summed.  Per key the heads still
+          // alternate between two accumulators in ascending 8-head blocks.
           // ReLU as x + |x| (one packed add, the weights staged halved).
           const uint32_t cb = tmem_base + static_cast<uint32_t>(buf * N + wg * C::EPI_COLS);
           const uint32_t l0 = static_cast<uint32_t>(quarter * 32) << 16;
@@ -574,8 +576,7 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 4; ++i) acc4[i] = acc4b[i] = make_float2(0.f, 0.f);
           uint32_t cur[16], nxt[16];
-          tmem_ld16x256_x2_async(cb + l0, cur);
-          tmem_ld16x256_x2_async(cb + l1, cur + 8);
+          tmem_ld16x256_x4_async(cb + l0, cur);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             tmem_wait_ld16(cur);
@@ -584,15 +585,17 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
               tc_fence_before_sync();
               mbar_arrive(&acce[buf]);
             } else {
-              tmem_ld16x256_x2_async(cb + l0 + static_cast<uint32_t>(16 * (c + 1)), nxt);
-              tmem_ld16x256_x2_async(cb + l1 + static_cast<uint32_t>(16 * (c + 1)), nxt + 8);
+              const int cn = c + 1;
+              tmem_ld16x256_x4_async(
+                  cb + ((cn & 1) ? l1 : l0) + static_cast<uint32_t>(32 * (cn >> 1)), nxt);
             }
+            {
+              const int hf = c & 1;
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-#pragma unroll
-              for (int rep = 0; rep < 2; ++rep) {
-                const int r0 = 8 * hf + 4 * rep;
-                const float2 w2 = wq[2 * c + rep];
+              for (int jj = 0; jj < 4; ++jj) {
+                const int rep = jj & 1;
+                const int r0 = 4 * jj;
+                const float2 w2 = wq[4 * (c >> 1) + jj];
                 const float2 xa = make_float2(__uint_as_float(cur[r0]), __uint_as_float(cur[r0 + 1]));
                 const float2 xb =
                     make_float2(__uint_as_float(cur[r0 + 2]), __uint_as_float(cur[r0 + 3]));
