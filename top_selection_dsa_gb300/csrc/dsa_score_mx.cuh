@@ -377,8 +377,8 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc4[i] = acc4b[i] = make_float2(0.f, 0.f);
         uint32_t cur[16], nxt[16];
-        tmem_ld16x256_x2_async(cb + l0, cur);
-        tmem_ld16x256_x2_async(cb + l1, cur + 8);
+        // Chunk c: one 16x256b.x4 load, lanes +16(c & 1), heads 32(c >> 1) ..
+        tmem_ld16x256_x4_async(cb + l0, cur);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           tmem_wait_ld16(cur);
@@ -387,15 +387,17 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&acce[buf]);
           } else {
-            tmem_ld16x256_x2_async(cb + l0 + static_cast<uint32_t>(16 * (c + 1)), nxt);
-            tmem_ld16x256_x2_async(cb + l1 + static_cast<uint32_t>(16 * (c + 1)), nxt + 8);
+            const int cn = c + 1;
+            tmem_ld16x256_x4_async(
+                cb + ((cn & 1) ? l1 : l0) + static_cast<uint32_t>(32 * (cn >> 1)), nxt);
           }
+          {
+            const int hf = c & 1;
 #pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-#pragma unroll
-            for (int rep = 0; rep < 2; ++rep) {
-              const int r0 = 8 * hf + 4 * rep;
-              const float2 w2 = wq[2 * c + rep];
+            for (int jj = 0; jj < 4; ++jj) {
+              const int rep = jj & 1;
+              const int r0 = 4 * jj;
+              const float2 w2 = wq[4 * (c >> 1) + jj];
               const float2 xa = make_float2(__uint_as_float(cur[r0]), __uint_as_float(cur[r0 + 1]));
               const float2 xb =
                   make_float2(__uint_as_float(cur[r0 + 2]), __uint_as_float(cur[r0 + 3]));
