@@ -162,6 +162,14 @@ uint32_t* split_scratch(void* workspace, int64_t rows, int64_t cols) {
                                      logits_scratch_bytes(rows, cols));
 }
 
+// The composed calls clear the split path's scratch (when they use it)
+// before their scoring kernel, so that the top-k's first phase can start as
+// that kernel's programmatic dependent.
+cudaError_t clear_split(uint32_t* split, int64_t rows, int64_t cols, cudaStream_t st) {
+  if (!split || rows == 0) return cudaSuccess;
+  return topk_split_clear(split, topk_split_words(cols), static_cast<int>(rows), st);
+}
+
 // ---------------------------------------------------------------- validation
 
 dsa_status_t check_elems(dsa_dtype_t dtype, int H, int D, const void* k_scale) {
@@ -434,11 +442,14 @@ dsa_status_t dsa_indexer_topk(const void* q, const float* q_scale, const void* k
   if (T == 0) return DSA_OK;
   const int64_t ld = round_up(S > 0 ? S : 1, 4);
   float* lg = static_cast<float*>(workspace);
+  uint32_t* split = split_scratch(workspace, T, S);
+  st = from_cuda(clear_split(split, T, S, as_stream(stream)));
+  if (st != DSA_OK) return st;
   st = run_logits(q, q_scale, k, k_scale, dtype, weights, row_starts, row_ends, T, S, H, D, lg, ld,
                   as_stream(stream));
   if (st != DSA_OK) return st;
   return run_topk(lg, ld, row_starts, row_ends, nullptr, 1, T, S, topk, out, as_stream(stream),
-                  split_scratch(workspace, T, S), true);
+                  split, true);
 }
 
 dsa_status_t dsa_indexer_logits_mxfp4(const void* q, const uint8_t* q_sf, const void* k,
@@ -478,11 +489,14 @@ dsa_status_t dsa_indexer_topk_mxfp4(const void* q, const uint8_t* q_sf, const vo
   if (T == 0) return DSA_OK;
   const int64_t ld = round_up(S > 0 ? S : 1, 4);
   float* lg = static_cast<float*>(workspace);
+  uint32_t* split = split_scratch(workspace, T, S);
+  st = from_cuda(clear_split(split, T, S, as_stream(stream)));
+  if (st != DSA_OK) return st;
   st = run_logits_mx(q, q_sf, k, k_sf, weights, row_starts, row_ends, T, S, H, lg, ld,
                      as_stream(stream));
   if (st != DSA_OK) return st;
   return run_topk(lg, ld, row_starts, row_ends, nullptr, 1, T, S, topk, out, as_stream(stream),
-                  split_scratch(workspace, T, S), true);
+                  split, true);
 }
 
 // ---------------------------------------------------- host-buffer pipeline
@@ -617,12 +631,15 @@ dsa_status_t dsa_indexer_topk_host(const void* q, const float* q_scale, const vo
     if (e == cudaSuccess) e = cudaStreamWaitEvent(comp, in, 0);
     if (e != cudaSuccess) break;
     float* lg = static_cast<float*>(ws_d);
-    st = run_logits(q_d + r0 * qe * esz, qs_d ? qs_d + r0 * H : nullptr, k_d, ks_d, dtype,
-                    w_d + r0 * H, rs_d + r0, re_d + r0, static_cast<int>(rows), S, H, D, lg, ld,
-                    comp);
+    uint32_t* split = split_scratch(ws_d, rows, S);
+    st = from_cuda(clear_split(split, rows, S, comp));
+    if (st == DSA_OK)
+      st = run_logits(q_d + r0 * qe * esz, qs_d ? qs_d + r0 * H : nullptr, k_d, ks_d, dtype,
+                      w_d + r0 * H, rs_d + r0, re_d + r0, static_cast<int>(rows), S, H, D, lg,
+                      ld, comp);
     if (st == DSA_OK)
       st = run_topk(lg, ld, rs_d + r0, re_d + r0, nullptr, 1, static_cast<int>(rows), S, topk,
-                    out_d + r0 * topk, comp, split_scratch(ws_d, rows, S), true);
+                    out_d + r0 * topk, comp, split, true);
     if (st != DSA_OK) break;
     e = cudaEventRecord(computed, comp);
     // download chunk c
@@ -683,12 +700,14 @@ dsa_status_t dsa_indexer_topk_paged(const void* q, const float* q_scale, const f
   if (B == 0) return DSA_OK;
   const int64_t ld = round_up(max_ctx, 4);
   float* lg = static_cast<float*>(workspace);
+  uint32_t* split = split_scratch(workspace, R, max_ctx);
+  st = from_cuda(clear_split(split, R, max_ctx, as_stream(stream)));
+  if (st != DSA_OK) return st;
   st = run_logits_paged(q, q_scale, weights, k_cache, k_scale, dtype, block_table, context_lens, s,
                         lg, ld, as_stream(stream));
   if (st != DSA_OK) return st;
   return run_topk(lg, ld, nullptr, nullptr, context_lens, next_n, static_cast<int>(R),
-                  static_cast<int>(max_ctx), topk, out, as_stream(stream),
-                  split_scratch(workspace, R, max_ctx), true);
+                  static_cast<int>(max_ctx), topk, out, as_stream(stream), split, true);
 }
 
 dsa_status_t dsa_topk_sort_by_score(const float* logits, int64_t ld, int32_t* topk, int T, int k,

@@ -52,10 +52,12 @@ struct TopkParams {
   uint32_t* split;   // null, or [R, split_words] scratch of the split path (topk_split_rows)
   int split_words;   // words of split scratch per row (topk_split_words(S))
   // 1 when the kernel queued just before on the stream is this library's own
-  // scoring kernel (the composed calls): the per-row top-k kernel may then be
+  // scoring kernel (the composed calls): the first top-k kernel may then be
   // its programmatic dependent, since the row ranges it reads before waiting
-  // were written before that scoring kernel started.  0 for the standalone
-  // dsa_topk, whose predecessor may be the caller's kernel writing them.
+  // were written before that scoring kernel started; the split path's
+  // scratch was then cleared before the scoring kernel (topk_split_clear).
+  // 0 for the standalone dsa_topk, whose predecessor may be the caller's
+  // kernel writing the ranges.
   int after_score;
 };
 
@@ -91,6 +93,8 @@ bool topk_supported(int max_row);
 // workspace size is known on the host.
 bool topk_split_rows(int64_t rows, int64_t max_row);
 int topk_split_words(int64_t max_row);
+// Zeroes each split-path row's histogram and state words (before its first phase).
+cudaError_t topk_split_clear(uint32_t* split, int split_words, int rows, cudaStream_t s);
 cudaError_t launch_fill(float* dst, int64_t rows, int64_t cols, int64_t ld, float value,
                         cudaStream_t s);
 // Rows of k top-k indices reordered by descending score in place (k <=

@@ -955,8 +955,13 @@ __global__ void __launch_bounds__(kUnitThreads, 5) topk_unit_hist_kernel(const T
   __shared__ int pre[kSplitMaxRows + 1];
   __shared__ uint2 scan_sums[NW];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  launch_dependents();
   const int items = split_items(p, pre, scan_sums);
+  // After the library's scoring kernel this phase is its programmatic
+  // dependent: the logits (and the scratch cleared before it) are read only
+  // once it has completed (a no-op for a plain launch).  The gather phase,
+  // which loads logits before its own wait, may start only after that.
+  grid_dependency_wait();
+  launch_dependents();
   for (int item = blockIdx.x; item < items; item += gridDim.x) {
   int row, unit;
   split_item(pre, p.R, item, &row, &unit);
@@ -1437,6 +1442,11 @@ int topk_split_words(int64_t) {
   return (kStWords + 63) / 64 * 64;  // rows stay 256-byte aligned
 }
 
+cudaError_t topk_split_clear(uint32_t* split, int split_words, int rows, cudaStream_t s) {
+  return cudaMemset2DAsync(split, static_cast<size_t>(split_words) * sizeof(uint32_t), 0,
+                           kStZeroWords * sizeof(uint32_t), static_cast<size_t>(rows), s);
+}
+
 template <int THREADS>
 cudaError_t launch_stream(const TopkParams& p, cudaStream_t s) {
   const size_t cand = THREADS >= 1024 ? 8192 : 2048;
@@ -1456,11 +1466,14 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t s) {
   const int S = p.S;
   if (p.split) {
     // Few long rows: every phase on (row, unit) grids, see the split path.
-    // Only each row's histogram and state words start at zero.
-    cudaError_t e = cudaMemset2DAsync(p.split, static_cast<size_t>(p.split_words) * sizeof(uint32_t),
-                                      0, kStZeroWords * sizeof(uint32_t),
-                                      static_cast<size_t>(p.R), s);
-    if (e != cudaSuccess) return e;
+    // Only each row's histogram and state words start at zero: cleared here,
+    // or, in the composed calls, before the scoring kernel, so that the first
+    // phase can start as that kernel's programmatic dependent.
+    cudaError_t e = cudaSuccess;
+    if (!p.after_score) {
+      e = topk_split_clear(p.split, p.split_words, p.R, s);
+      if (e != cudaSuccess) return e;
+    }
     // Each phase: at most as many CTAs as are resident at once (their launch
     // bounds), each walking the row-major list of units that hold keys.
     const int64_t units = static_cast<int64_t>(p.R) * ((S + kUnitKeys - 1) / kUnitKeys);
@@ -1468,13 +1481,11 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t s) {
     auto grid_of = [&](int per_sm) {
       return dim3(static_cast<unsigned>(std::min<int64_t>(units, static_cast<int64_t>(sms) * per_sm)));
     };
-    topk_unit_hist_kernel<<<grid_of(5), kUnitThreads, 0, s>>>(p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    // The later phases start early (their loads overlap the previous
-    // phase's tail) and wait for it in hardware before reading its results.
+    // The later phases (and the first one after the library's own scoring
+    // kernel) start early and wait for the previous kernel in hardware
+    // before reading what it wrote.
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid_of(4);
+    cfg.gridDim = grid_of(5);
     cfg.blockDim = dim3(kUnitThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
@@ -1482,6 +1493,10 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t s) {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
+    cfg.numAttrs = p.after_score ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, topk_unit_hist_kernel, p);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = grid_of(4);
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, topk_unit_gather_kernel, p);
     if (e != cudaSuccess) return e;
