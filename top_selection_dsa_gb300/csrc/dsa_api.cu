@@ -507,6 +507,7 @@ namespace {
 // one chunk's workspace, each region 256-byte aligned.
 struct HostPlan {
   int64_t chunk;  // rows per chunk
+  int64_t first;  // rows of the first chunk (the remainder)
   size_t k, ks, q, qs, w, rs, re, out, ws, total;
 };
 
@@ -515,7 +516,17 @@ HostPlan host_plan(int T, int S, int H, int D, int topk, dsa_dtype_t dtype, bool
   HostPlan pl = {};
   const size_t esz = dtype == DSA_E4M3 ? 1 : 2;
   const int64_t nchunks = T <= 0 ? 1 : std::min<int64_t>(8, (T + 511) / 512);
-  pl.chunk = std::max<int64_t>(1, round_up((static_cast<int64_t>(T) + nchunks - 1) / nchunks, 64));
+  // Chunks of whole rounds of the persistent scoring kernel (its rows per
+  // group times this device's SM count), so that no chunk's kernel ends on a
+  // partial round of its longest groups; the remainder is the first chunk,
+  // whose rows are the shortest under a causal mask.  Rows in multiples of
+  // 64 where a round is larger than a chunk (or there is no device).
+  const int64_t even = (static_cast<int64_t>(T) + nchunks - 1) / nchunks;
+  const int64_t round_rows =
+      static_cast<int64_t>(score_tokens_per_group(H)) * std::max(device_sm_count(), 0);
+  pl.chunk = std::max<int64_t>(
+      1, round_up(even, round_rows > 0 && round_rows <= even ? round_rows : 64));
+  pl.first = T > 0 ? T - (T - 1) / pl.chunk * pl.chunk : 1;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t at = off;
@@ -533,9 +544,8 @@ HostPlan host_plan(int T, int S, int H, int D, int topk, dsa_dtype_t dtype, bool
   // The chunks share one workspace; a short last chunk may take the split
   // top-k path (more scratch per row) where a full one does not.
   const int64_t full = std::min<int64_t>(pl.chunk, T > 0 ? T : 1);
-  const int64_t last = T > 0 ? T - (T - 1) / pl.chunk * pl.chunk : 1;
   pl.ws = take(std::max(dsa_workspace_bytes(DSA_OP_INDEXER_TOPK, full, S, topk),
-                        dsa_workspace_bytes(DSA_OP_INDEXER_TOPK, last, S, topk)));
+                        dsa_workspace_bytes(DSA_OP_INDEXER_TOPK, pl.first, S, topk)));
   pl.total = off;
   return pl;
 }
@@ -616,7 +626,8 @@ dsa_status_t dsa_indexer_topk_host(const void* q, const float* q_scale, const vo
   if (e == cudaSuccess) e = cudaEventRecord(k_in, up);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(comp, k_in, 0);
   for (int64_t c = 0; c < nch && e == cudaSuccess && st == DSA_OK; ++c) {
-    const int64_t r0 = c * pl.chunk, rows = std::min<int64_t>(pl.chunk, T - r0);
+    const int64_t r0 = c == 0 ? 0 : pl.first + (c - 1) * pl.chunk;
+    const int64_t rows = c == 0 ? pl.first : pl.chunk;
     const int64_t qe = static_cast<int64_t>(H) * D;
     cudaEvent_t in = event(), computed = event();
     if (!in || !computed) {
