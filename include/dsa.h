@@ -287,12 +287,12 @@ dsa_status_t dsa_indexer_topk_noalloc(const void* q, const float* q_scale, const
  *     aligned.  It receives the inputs, the indices and one row chunk's
  *     logits; on return from the stream's work it holds the device copy of
  *     the inputs and of `out`.
- *   - The rows are split into up to 8 chunks (whole rounds of the scoring
+ *   - The rows are split into up to 12 chunks (whole rounds of the scoring
  *     kernel, 256/H rows times the current device's SM count, where a chunk
  *     holds one; else multiples of 64 rows; about 512 or more each), the
  *     remainder first; so dsa_indexer_topk_host_bytes is for the current
- *     device.  K, the weights, the scales and the row ranges go up
- *     first; then chunk c's queries go up while chunk c-1 is scored and
+ *     device.  K, the key scales and the row ranges go up first;
+ *     then chunk c's queries and weights go up while chunk c-1 is scored and
  *     selected (on `stream`) and chunk c-2's indices come down, on two
  *     streams the call creates and destroys.  Work queued on
  *     `stream` after the call sees all of `out`; host code must synchronise

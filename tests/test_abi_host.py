@@ -268,15 +268,16 @@ def test_indexer_topk_host_validation(api):
 
 def test_indexer_topk_host_bytes_layout(api):
     # The device buffer holds every input and the indices, then one row
-    # chunk's workspace: up to 8 chunks of a multiple of 64 rows (at least
-    # 512 rows each where T allows), sized for the larger of a full chunk and
-    # the last one (a short last chunk of long rows takes the split top-k).
+    # chunk's workspace: up to 12 chunks of a multiple of 64 rows with no
+    # device (whole scoring rounds on one), at least 512 rows each where T
+    # allows, sized for the larger of a full chunk and the first one, which
+    # holds the remainder (a short chunk of long rows takes the split top-k).
     ws = lambda rows, S, k: api.lib.dsa_workspace_bytes(api.DSA_OP_INDEXER_TOPK, rows, S, k)  # noqa: E731
     up = lambda x: -(-x // 256) * 256  # noqa: E731
 
     def expect(T, S, H, D, k, dtype):
         esz = 1 if dtype == api.DSA_E4M3 else 2
-        nch = min(8, -(-T // 512)) if T > 0 else 1
+        nch = min(12, -(-T // 512)) if T > 0 else 1
         chunk = max(1, -(-(-(-T // nch)) // 64) * 64) if T > 0 else 1
         full = min(chunk, T) if T > 0 else 1
         last = T - (T - 1) // chunk * chunk if T > 0 else 1
@@ -292,10 +293,10 @@ def test_indexer_topk_host_bytes_layout(api):
                               (1, 5, 1, 64, 1, api.DSA_BF16),
                               (0, 64, 8, 64, 16, api.DSA_BF16)]:
         assert nb(T, S, H, D, k, dt) == expect(T, S, H, D, k, dt), (T, S)
-    # 4700 rows: seven chunks of 640 and a last one of 220, which the split
-    # top-k takes (rows <= 512, columns > 16384) while the full chunks do not
-    assert api.lib.dsa_workspace_bytes(api.DSA_OP_TOPK, 220, 40000, 2048) > 0
-    assert api.lib.dsa_workspace_bytes(api.DSA_OP_TOPK, 640, 40000, 2048) == 0
+    # 4700 rows: a first chunk of 92 and nine of 512, which the split top-k
+    # takes (rows <= 512, columns > 16384), all of them
+    assert api.lib.dsa_workspace_bytes(api.DSA_OP_TOPK, 92, 40000, 2048) > 0
+    assert api.lib.dsa_workspace_bytes(api.DSA_OP_TOPK, 512, 40000, 2048) > 0
 
 
 def mx_call(api, q=A, qsf=A, k=A, ksf=A, w=A, rs=A, re=A, T=8, S=8, H=64, D=128, lg=A, ld=8,

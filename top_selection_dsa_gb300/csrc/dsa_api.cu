@@ -515,7 +515,7 @@ HostPlan host_plan(int T, int S, int H, int D, int topk, dsa_dtype_t dtype, bool
                    bool k_scale) {
   HostPlan pl = {};
   const size_t esz = dtype == DSA_E4M3 ? 1 : 2;
-  const int64_t nchunks = T <= 0 ? 1 : std::min<int64_t>(8, (T + 511) / 512);
+  const int64_t nchunks = T <= 0 ? 1 : std::min<int64_t>(12, (T + 511) / 512);
   // Chunks of whole rounds of the persistent scoring kernel (its rows per
   // group times this device's SM count), so that no chunk's kernel ends on a
   // partial round of its longest groups; the remainder is the first chunk,
@@ -611,16 +611,20 @@ dsa_status_t dsa_indexer_topk_host(const void* q, const float* q_scale, const vo
   if (e == cudaSuccess) e = cudaEventRecord(start, comp);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(up, start, 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(down, start, 0);
-  // K and every row's small inputs first (a few large copies: each copy
-  // costs the copy engine microseconds however small it is), then q by chunk.
-  const size_t th = static_cast<size_t>(T) * H * 4, t4 = static_cast<size_t>(T) * 4;
+  // K and the row ranges first, then each chunk's queries; the weights (and
+  // query scales) go with their chunk when a chunk's share is large enough
+  // to be worth a copy of its own (every copy costs the copy engine a few
+  // microseconds however small it is), else all at once up front.
+  const size_t t4 = static_cast<size_t>(T) * 4, th = static_cast<size_t>(T) * H * 4;
+  const bool w_by_chunk = static_cast<size_t>(pl.chunk) * H * 4 >= (512u << 10);
+  if (e == cudaSuccess && !w_by_chunk)
+    e = cudaMemcpyAsync(w_d, weights, th, cudaMemcpyHostToDevice, up);
+  if (e == cudaSuccess && !w_by_chunk && q_scale)
+    e = cudaMemcpyAsync(qs_d, q_scale, th, cudaMemcpyHostToDevice, up);
   if (e == cudaSuccess && S > 0)
     e = cudaMemcpyAsync(k_d, k, static_cast<size_t>(S) * D * esz, cudaMemcpyHostToDevice, up);
   if (e == cudaSuccess && S > 0 && k_scale)
     e = cudaMemcpyAsync(ks_d, k_scale, static_cast<size_t>(S) * 4, cudaMemcpyHostToDevice, up);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(w_d, weights, th, cudaMemcpyHostToDevice, up);
-  if (e == cudaSuccess && q_scale)
-    e = cudaMemcpyAsync(qs_d, q_scale, th, cudaMemcpyHostToDevice, up);
   if (e == cudaSuccess) e = cudaMemcpyAsync(rs_d, row_starts, t4, cudaMemcpyHostToDevice, up);
   if (e == cudaSuccess) e = cudaMemcpyAsync(re_d, row_ends, t4, cudaMemcpyHostToDevice, up);
   if (e == cudaSuccess) e = cudaEventRecord(k_in, up);
@@ -634,9 +638,15 @@ dsa_status_t dsa_indexer_topk_host(const void* q, const float* q_scale, const vo
       e = cudaErrorMemoryAllocation;
       break;
     }
-    // upload chunk c's queries
+    // upload chunk c's queries and weights
     e = cudaMemcpyAsync(q_d + r0 * qe * esz, static_cast<const char*>(q) + r0 * qe * esz,
                         rows * qe * esz, cudaMemcpyHostToDevice, up);
+    if (e == cudaSuccess && w_by_chunk)
+      e = cudaMemcpyAsync(w_d + r0 * H, weights + r0 * H, static_cast<size_t>(rows) * H * 4,
+                          cudaMemcpyHostToDevice, up);
+    if (e == cudaSuccess && w_by_chunk && q_scale)
+      e = cudaMemcpyAsync(qs_d + r0 * H, q_scale + r0 * H, static_cast<size_t>(rows) * H * 4,
+                          cudaMemcpyHostToDevice, up);
     if (e == cudaSuccess) e = cudaEventRecord(in, up);
     // compute chunk c on the caller's stream
     if (e == cudaSuccess) e = cudaStreamWaitEvent(comp, in, 0);
