@@ -432,10 +432,11 @@ __global__ void __launch_bounds__(ScoreCfg<H, N, D, kFp8, kPaged>::THREADS, 1)
     const int wg = (ew >> 2) % C::EPI_WG;  // column group of this warpgroup
     const int quarter = warp & 3;  // the TMEM lane quarter this warp may access
     const int key_in_tile = quarter * 32 + lane;
-    // e4m3 with 64 heads reads the accumulator in the 16x256b shape: each
-    // thread sums 16 heads of 4 keys, a quad of threads shares those keys,
-    // and after the exchange each thread owns one of them.
-    constexpr bool kQuad = kFp8 && !kPaged && H == 64 && C::EPI_COLS == 64;
+    // 64 heads, one token per warpgroup (prefill and paged, bf16 and e4m3):
+    // the accumulator is read in the 16x256b shape: each thread sums 16
+    // heads of 4 keys, a quad of threads shares those keys, and after the
+    // exchange each thread owns one of them.
+    constexpr bool kQuad = H == 64 && C::EPI_COLS == 64;
     const int my_key = kQuad ? quarter * 32 + (lane >> 2) + 8 * (lane & 3) : key_in_tile;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const int etid = threadIdx.x - 64;  // 0 .. EPI_THREADS-1
