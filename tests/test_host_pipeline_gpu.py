@@ -61,7 +61,10 @@ def test_small_case_matches_oracle_topk_of_gpu_logits(api):
     assert np.array_equal(got.numpy(), want)
 
 
-@pytest.mark.parametrize("T", [4096, 1000])
+# 4096 and 1000 rows: chunks of whole multiples of 64 rows; 8192 rows at 64
+# heads: chunks of whole scoring rounds (4 rows x the SM count) after a
+# shorter first chunk.
+@pytest.mark.parametrize("T", [4096, 1000, 8192])
 def test_causal_bf16_equals_device_entry_point(api, T):
     p = wl.prefill_causal(T=T, H=64, D=128, topk=2048, seed=1)
     assert torch.equal(run_host(api, p), run_device(api, p))
@@ -73,9 +76,9 @@ def test_e4m3_with_key_scales_equals_device_entry_point(api):
 
 
 def test_short_last_chunk_takes_split_path(api):
-    # 4700 rows of up to 40000 keys: 7 chunks of 640 rows (bitmap top-k) and
-    # a last chunk of 220 rows, which the split top-k takes; the device entry
-    # point runs all 4700 rows without the split path.
+    # 4700 rows of up to 40000 keys in chunks of at most 512 rows (a short
+    # first one), which the split top-k takes; the device entry point runs all
+    # 4700 rows without the split path.
     T, S = 4700, 40000
     rng = np.random.default_rng(7)
     ends = rng.integers(1, S + 1, size=T).astype(np.int32)
