@@ -128,8 +128,9 @@ dsa_status_t dsa_indexer_logits(const void* q, const float* q_scale, const void*
  *   out        [T, k] int32 output
  *   workspace  dsa_workspace_bytes(DSA_OP_TOPK, T, S, k) bytes, 256-byte aligned.
  *              That is 0 (workspace may be NULL) except for few long rows
- *              (T <= 512 and S > 16384), where many CTAs per row share
- *              per-row scratch there (about 75 KiB per row).
+ *              (S > 16384 and T < 32, or S > 262144 and T <= 512), where
+ *              many CTAs per row share per-row scratch there (about 75 KiB
+ *              per row).
  */
 dsa_status_t dsa_topk(const float* logits, int64_t ld, const int32_t* row_starts,
                       const int32_t* row_ends, int T, int S, int k, int32_t* out,

@@ -61,11 +61,14 @@ def test_workspace_bytes(api):
     def split(rows, S):
         words = 2048 + 16 + 3 * 256 + 16384
         return rows * (-(-words // 64) * 64) * 4
-    assert wb(api.DSA_OP_TOPK, 128, 131072, 2048) == split(128, 131072)
+    assert wb(api.DSA_OP_TOPK, 16, 131072, 2048) == split(16, 131072)   # fewer than 32 rows
+    assert wb(api.DSA_OP_TOPK, 128, 131072, 2048) == 0        # 32-512 rows: a CTA per row
+    assert wb(api.DSA_OP_TOPK, 128, 300000, 2048) == split(128, 300000)  # rows past 262144
     assert wb(api.DSA_OP_TOPK, 4096, 131072, 2048) == 0       # many rows: no scratch
     assert wb(api.DSA_OP_TOPK, 128, 16384, 2048) == 0         # short rows: no scratch
-    assert wb(api.DSA_OP_INDEXER_TOPK_PAGED, 128, 131072, 2048) == \
-        128 * 131072 * 4 + split(128, 131072)
+    assert wb(api.DSA_OP_INDEXER_TOPK_PAGED, 128, 131072, 2048) == 128 * 131072 * 4
+    assert wb(api.DSA_OP_INDEXER_TOPK_PAGED, 16, 131072, 2048) == \
+        16 * 131072 * 4 + split(16, 131072)
     assert wb(api.DSA_OP_INDEXER_TOPK, 0, 100, 1) == 0
     bad = ctypes.c_size_t(-1).value
     assert wb(api.DSA_OP_INDEXER_TOPK, -1, 5, 1) == bad
@@ -293,10 +296,12 @@ def test_indexer_topk_host_bytes_layout(api):
                               (1, 5, 1, 64, 1, api.DSA_BF16),
                               (0, 64, 8, 64, 16, api.DSA_BF16)]:
         assert nb(T, S, H, D, k, dt) == expect(T, S, H, D, k, dt), (T, S)
-    # 4700 rows: a first chunk of 92 and nine of 512, which the split top-k
-    # takes (rows <= 512, columns > 16384), all of them
-    assert api.lib.dsa_workspace_bytes(api.DSA_OP_TOPK, 92, 40000, 2048) > 0
-    assert api.lib.dsa_workspace_bytes(api.DSA_OP_TOPK, 512, 40000, 2048) > 0
+    # 4700 rows: a first chunk of 92 and nine of 512, which the top-k takes
+    # with one 1024-thread CTA per row (32-512 rows, columns > 16384): no
+    # split scratch
+    assert api.lib.dsa_workspace_bytes(api.DSA_OP_TOPK, 92, 40000, 2048) == 0
+    assert api.lib.dsa_workspace_bytes(api.DSA_OP_TOPK, 512, 40000, 2048) == 0
+    assert api.lib.dsa_workspace_bytes(api.DSA_OP_TOPK, 20, 40000, 2048) > 0
 
 
 def mx_call(api, q=A, qsf=A, k=A, ksf=A, w=A, rs=A, re=A, T=8, S=8, H=64, D=128, lg=A, ld=8,

@@ -259,13 +259,15 @@ def test_topk_row_lengths(api, S, k, T):
     assert np.array_equal(got, oracle.topk(lg, rs, re, k))
 
 
-# The split path (few rows, some longer than 16384 columns) over rows of every
-# kind: empty, one key, exactly one or two 4096-key units, all ties, nothing
-# valid, NaN, signed zeros, ranges starting mid-row or clamped, and more rows
-# (40) than one unit each, so that each resident CTA walks several units.
-def test_topk_split_path_edge_rows(api):
-    rng = np.random.default_rng(77)
-    T, S, k = 40, 50000, 2048
+# Few long rows (some longer than 16384 columns) over rows of every kind:
+# empty, one key, exactly one or two 4096-key units, all ties, nothing valid,
+# NaN, signed zeros, ranges starting mid-row or clamped.  24 rows take the
+# split path (each resident CTA walking several units), 40 rows one
+# 1024-thread CTA per row.
+@pytest.mark.parametrize("T", [24, 40])
+def test_topk_few_long_rows_edge_rows(api, T):
+    rng = np.random.default_rng(77 + T)
+    S, k = 50000, 2048
     lg = rng.standard_normal((T, S)).astype(np.float32)
     kind = np.arange(T) % 10
     lg[kind == 1] = 0.0                                           # all ties
@@ -294,6 +296,8 @@ def test_topk_split_path_edge_rows(api):
     assert np.array_equal(got, oracle.topk(dirty, rs, re, k))
     assert (got[0] == -1).all() and got[10, 0] == 777 and (got[10, 1:] == -1).all()
     assert (got[20] == np.arange(100, 100 + k)).all()
+    ws = api.workspace_bytes(api.DSA_OP_TOPK, T, S, k)
+    assert (ws > 0) == (T < 32)                    # split scratch for the split path only
 
 
 def test_topk_reads_ranges_written_just_before_on_the_stream(api):
@@ -334,9 +338,11 @@ def test_paged_small(api, next_n, block_size, H, fp8):
     check_paged(api, p, rows=None)
 
 
-# Paged rows long enough for the split top-k (a context above 16384 keys),
-# one to five query tokens a request: empty and one-key rows, contexts ending
-# inside a 4096-key unit and inside a block, e4m3 and bf16, 8 to 64 heads.
+# Paged rows long enough for the few-long-rows top-k (a context above 16384
+# keys; 8 to 40 rows: the split path below 32 rows, a 1024-thread CTA per row
+# from 32), one to five query tokens a request: empty and one-key rows,
+# contexts ending inside a 4096-key unit and inside a block, e4m3 and bf16, 8
+# to 64 heads.
 @pytest.mark.parametrize("next_n,block_size,H,fp8", [(1, 16, 64, False), (2, 64, 64, True),
                                                      (4, 32, 8, False), (3, 128, 16, True),
                                                      (5, 64, 32, False)])
