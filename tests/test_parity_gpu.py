@@ -208,6 +208,50 @@ def test_topk_edge_cases(api):
     assert (got[7] == np.arange(10, 10 + k)).all()
 
 
+# Rows of several chunks whose threshold bin (top 11 key bits) sits at an
+# edge of the value order, where the bin's bounds are compared as floats:
+# the +0 bin with -0 and positive subnormals, the bin just below it
+# (negative subnormals, with the zeros above it), the +inf bin, the bin of
+# -FLT_MAX, and a NaN-heavy row.  Every bin holds more keys than are still
+# needed, so each row lists its bin's keys and refines them.  Both row
+# kernels: 256 threads (3 chunks of 4096) and 1024 threads (4 of 16384).
+@pytest.mark.parametrize("S,T", [(10000, 10), (50000, 40)])
+def test_topk_threshold_bin_at_value_edges(api, S, T):
+    rng = np.random.default_rng(S + T)
+    k = 80
+    f = lambda bits: np.array(bits, np.uint32).view(np.float32)
+    lg = np.full((T, S), -1.0, np.float32)
+    kind = np.arange(T) % 5
+    for t in range(T):
+        cols = rng.permutation(S)
+        big, mid = cols[:30], cols[30:30 + 150]
+        if kind[t] == 0:    # bin of +0: zeros of both signs and positive subnormals
+            lg[t, big] = 1.0
+            lg[t, mid[:50]] = f(rng.integers(1, 0x200000, 50))
+            lg[t, mid[50:100:2]] = 0.0
+            lg[t, mid[51:100:2]] = -0.0
+        elif kind[t] == 1:  # bin below it: negative subnormals under 20 zeros
+            lg[t, big] = 1.0
+            lg[t, mid[:20]] = -0.0
+            lg[t, mid[20:90]] = f(0x80000000 + rng.integers(1, 0x200000, 70))
+            lg[t, mid[90:95]] = f(0x80000001)          # -(smallest subnormal)
+        elif kind[t] == 2:  # bin of +inf
+            lg[t, mid[:100]] = np.inf
+        elif kind[t] == 3:  # bin of -FLT_MAX, the rest -inf
+            lg[t] = -np.inf
+            lg[t, big] = 3.0e38
+            lg[t, mid[:90]] = f(0xFF7FFFFF - rng.integers(0, 0x100000, 90))
+            lg[t, mid[90:100]] = f(0xFF7FFFFF)
+        else:               # NaN everywhere but 150 tied keys and 30 larger ones
+            lg[t] = np.nan
+            lg[t, big] = 2.0
+            lg[t, mid] = 1.5
+    rs = np.zeros(T, np.int32)
+    re = np.full(T, S, np.int32)
+    got = api.topk(dev(lg), dev(rs), dev(re), k).cpu().numpy()
+    assert np.array_equal(got, oracle.topk(lg, rs, re, k))
+
+
 # Rows of at most 4096 columns take the persistent short-row kernel, which
 # loops over rows (more rows than its CTAs here) and prefetches two rows ahead:
 # every edge case on many rows, with ranges and garbage around them.

@@ -219,7 +219,9 @@ __device__ __forceinline__ void grid_dependency_wait() {
 //
 //   pass 1   histogram of the top 11 key bits -> the bin b1 holding rank k;
 //   pass 2   keys above bin b1 are selected (bitmap words written by
-//            ballot); the keys of bin b1 are gathered with their columns;
+//            ballot of float compares against the bin's bounds); the keys
+//            of bin b1 are marked in a second bitmap, whose columns a scan
+//            then lists, and their keys are read again by column;
 //   refine   bits 20..10, then 9..0, of the gathered keys -> tau and the
 //            number need_eq of keys == tau to take; the selected candidates
 //            are added to the bitmap (keys == tau to a second bitmap);
@@ -239,6 +241,19 @@ __device__ __forceinline__ uint32_t chunk_key(float x) {
   const float y = fmaxf(x, -INFINITY) + 0.0f;  // NaN -> -inf, -0 -> +0
   const uint32_t u = __float_as_uint(y);
   return u ^ (static_cast<uint32_t>(static_cast<int32_t>(u) >> 31) | 0x80000000u);
+}
+
+// The float whose chunk_key is `key`.  For x not NaN, x > key_float(t) holds
+// exactly when chunk_key(x) > t, for any t but 0x7FFFFFFF (the key -0.0
+// would have: no key takes that value, so 0x7FFFFFFE stands in for it), and
+// x == key_float(t) exactly when chunk_key(x) == t, for t the key of some
+// value.  A NaN compares false, as its key, kNoKey, is below every bound.
+// Past the key of +inf the result is a NaN, which no x exceeds.
+__device__ __forceinline__ float key_float(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+__device__ __forceinline__ float key_float_gt(uint32_t key) {
+  return key_float(key == 0x7FFFFFFFu ? 0x7FFFFFFEu : key);
 }
 
 // Keys of chunk q for this thread: key[4g + j].
@@ -402,38 +417,56 @@ __global__ void __launch_bounds__(THREADS, MINB) topk_rows_kernel(const TopkPara
       uint32_t rem = static_cast<uint32_t>(p.k) - above;
       if (rem == c1) {
         tau = (b1 << 21) - 1u;  // the whole bin is taken
-      } else if (nch > 2 && c1 <= static_cast<uint32_t>(cand_cap)) {
-        // Pass 2: keys above bin b1 are selected straight into the bitmap;
-        // the keys of bin b1 are gathered with their columns.
+      } else if (nch > 1 && c1 <= static_cast<uint32_t>(cand_cap)) {
+        // Pass 2, by float compares against the bounds of bin b1 (no key
+        // transform): keys above the bin go straight into the selection
+        // bitmap, the bin's own keys into a second one (eq_bits for now).
         const uint32_t thr = ((b1 + 1u) << 21) - 1u;
+        const float f_hi = key_float_gt(thr), f_lo = key_float(b1 << 21);
         for (int q = 0; q < nch; ++q) {
-          load_chunk<THREADS>(src, n, q, warp, lane, key);
+          float x[16];
+          load_chunk_raw<THREADS>(src, n, q, warp, lane, x);
           const int ng = chunk_groups<THREADS>(n, q, warp);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             if (i / 4 >= ng) continue;  // words of later groups lie past the row
-            const uint32_t kk = key[i];
-            const uint32_t g = __ballot_sync(0xffffffffu, kk > thr);
+            const bool up = x[i] > f_hi;
+            const uint32_t g = __ballot_sync(0xffffffffu, up);
+            const uint32_t e = __ballot_sync(0xffffffffu, !up && x[i] >= f_lo);
             if (lane == 0) {
               sel_bits[chunk_word<THREADS>(q, warp, i)] = g;
-              eq_bits[chunk_word<THREADS>(q, warp, i)] = 0u;
-            }
-            const bool hit = (kk >> 21) == b1;
-            const uint32_t m = __ballot_sync(0xffffffffu, hit);
-            if (m) {
-              uint32_t slot = 0u;
-              if (lane == 0) slot = atomicAdd(&ncand, static_cast<uint32_t>(__popc(m)));
-              slot = __shfl_sync(0xffffffffu, slot, 0) + __popc(m & lt);
-              if (hit) {
-                cand_key[slot] = kk & 0x1FFFFFu;
-                cand_col[slot] = static_cast<uint32_t>(q * CH + warp * 512 + i * 32 + lane);
-              }
+              eq_bits[chunk_word<THREADS>(q, warp, i)] = e;
             }
           }
         }
         __syncthreads();
+        // The bin's columns to the candidate list in column order: thread t
+        // takes a run of words (and clears them for the marks below), a scan
+        // gives its first slot.  Then their keys, read again by column.
+        const int nwords = (n + 31) >> 5;
+        const int per = (nwords + THREADS - 1) / THREADS;
+        const int w0 = min(tid * per, nwords), w1 = min(w0 + per, nwords);
+        uint32_t mine = 0u;
+        for (int w = w0; w < w1; ++w) mine += __popc(eq_bits[w]);
+        uint2 gathered;
+        uint32_t slot = block_scan2<THREADS>(make_uint2(mine, 0u), warp_sums, &gathered).x;
+        for (int w = w0; w < w1; ++w) {
+          uint32_t f = eq_bits[w];
+          eq_bits[w] = 0u;
+          while (f) {
+            const int b = __ffs(static_cast<int>(f)) - 1;
+            if (slot < static_cast<uint32_t>(cand_cap))
+              cand_col[slot] = static_cast<uint32_t>(w * 32 + b);
+            ++slot;
+            f &= f - 1u;
+          }
+        }
+        const int nc = min(static_cast<int>(gathered.x), cand_cap);
+        __syncthreads();
+#pragma unroll 4
+        for (int i = tid; i < nc; i += THREADS)
+          cand_key[i] = chunk_key(__ldg(src + cand_col[i])) & 0x1FFFFFu;
         // Refine over the c1 gathered keys: bits 20..10, then 9..0.
-        const int nc = static_cast<int>(c1);
         for (int i = tid; i < kHistBins / 4; i += THREADS)
           reinterpret_cast<uint4*>(hist)[i] = make_uint4(0u, 0u, 0u, 0u);
         __syncthreads();
@@ -573,14 +606,18 @@ __global__ void __launch_bounds__(THREADS, MINB) topk_rows_kernel(const TopkPara
   // Several chunks: bitmaps (unless the gather path filled them), then the
   // emit.  Words of groups past the row are never read.
   if (!marked) {
+    // Float compares against tau's value (tau is a key of the row whenever
+    // need_eq > 0).
+    const float f_gt = key_float_gt(tau), f_eq = key_float(tau);
     for (int q = 0; q < nch; ++q) {
-      load_chunk<THREADS>(src, n, q, warp, lane, key);
+      float x[16];
+      load_chunk_raw<THREADS>(src, n, q, warp, lane, x);
       const int ng = chunk_groups<THREADS>(n, q, warp);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         if (i / 4 < ng) {
-          const uint32_t g = __ballot_sync(0xffffffffu, key[i] > tau);
-          const uint32_t e = need_eq ? __ballot_sync(0xffffffffu, key[i] == tau) : 0u;
+          const uint32_t g = __ballot_sync(0xffffffffu, x[i] > f_gt);
+          const uint32_t e = need_eq ? __ballot_sync(0xffffffffu, x[i] == f_eq) : 0u;
           if (lane == 0) {
             sel_bits[chunk_word<THREADS>(q, warp, i)] = g;
             eq_bits[chunk_word<THREADS>(q, warp, i)] = e;
