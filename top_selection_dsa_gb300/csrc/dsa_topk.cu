@@ -288,6 +288,34 @@ __device__ __forceinline__ void load_chunk_raw(const float* src, int n, int q, i
   }
 }
 
+// Lines of this warp's share of chunk q into L1 (lanes 0-15, one 128-byte
+// line each), ahead of its loads.
+template <int THREADS>
+__device__ __forceinline__ void prefetch_chunk_l1(const float* src, int n, int q, int warp, int lane) {
+  constexpr int CH = THREADS * 16;
+  const int c = q * CH + warp * 512 + lane * 32;
+  if (lane < 16 && c < n)
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<uint64_t>(src + c)));
+}
+
+// As load_chunk_raw, without per-element checks on whole chunks.
+template <int THREADS>
+__device__ __forceinline__ void load_chunk_f(const float* src, int n, int q, int warp, int lane,
+                                             float (&x)[16]) {
+  constexpr int CH = THREADS * 16;
+  const int c0 = q * CH + warp * 512 + lane;
+  if ((q + 1) * CH <= n) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[i] = __ldg(src + c0 + i * 32);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int c = c0 + i * 32;
+      x[i] = c < n ? __ldg(src + c) : -INFINITY;
+    }
+  }
+}
+
 // Groups of this warp in chunk q that hold a column of the row (warp-uniform).
 template <int THREADS>
 __device__ __forceinline__ int chunk_groups(int n, int q, int warp) {
@@ -425,7 +453,8 @@ __global__ void __launch_bounds__(THREADS, MINB) topk_rows_kernel(const TopkPara
         const float f_hi = key_float_gt(thr), f_lo = key_float(b1 << 21);
         for (int q = 0; q < nch; ++q) {
           float x[16];
-          load_chunk_raw<THREADS>(src, n, q, warp, lane, x);
+          load_chunk_f<THREADS>(src, n, q, warp, lane, x);
+          if (q + 1 < nch) prefetch_chunk_l1<THREADS>(src, n, q + 1, warp, lane);
           const int ng = chunk_groups<THREADS>(n, q, warp);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
@@ -611,7 +640,8 @@ __global__ void __launch_bounds__(THREADS, MINB) topk_rows_kernel(const TopkPara
     const float f_gt = key_float_gt(tau), f_eq = key_float(tau);
     for (int q = 0; q < nch; ++q) {
       float x[16];
-      load_chunk_raw<THREADS>(src, n, q, warp, lane, x);
+      load_chunk_f<THREADS>(src, n, q, warp, lane, x);
+      if (q + 1 < nch) prefetch_chunk_l1<THREADS>(src, n, q + 1, warp, lane);
       const int ng = chunk_groups<THREADS>(n, q, warp);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -1578,11 +1608,11 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t s) {
   }
   // One 256-thread CTA per row, the row in 4096-key chunks.
   if (S <= kChunkMax * 4096) {
-    // 1024 candidates (the threshold bin of a row rarely holds more; a larger
-    // bin takes the digit passes): 24 KB of shared memory per CTA up to 32768
-    // columns, so the register limit of five CTAs per SM is the binding one.
-    // 2048 or 4096 candidates cost THD rows 13 % and 32768-column rows 12 %.
-    const int cand = 1024;
+    // 2048 candidates (the threshold bin of a 32768-key row holds up to about
+    // 2 K keys; a larger bin takes the digit passes): 32 KB of shared memory
+    // per CTA up to 32768 columns, so the register limit of five CTAs per SM
+    // is the binding one.
+    const int cand = 2048;
     const int words = bitmap_row_words<256>(S);
     const int smem = (kHistBins + 2 * cand + 2 * words) * static_cast<int>(sizeof(uint32_t));
     cudaError_t e = cudaFuncSetAttribute(topk_rows_kernel<256, 5>,
