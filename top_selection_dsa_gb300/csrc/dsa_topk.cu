@@ -704,7 +704,21 @@ __global__ void __launch_bounds__(THREADS, MINB) topk_rows_kernel(const TopkPara
   }
   if (staged) {
     __syncthreads();
-    for (int i = tid; i < p.k; i += THREADS) dst[i] = i < nsel ? static_cast<int>(stage[i]) : -1;
+    if ((p.k & 3) == 0 && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+      // Four columns a store (the output row is 16-byte aligned).
+      for (int i = 4 * tid; i < p.k; i += 4 * THREADS) {
+        uint4 v = *reinterpret_cast<const uint4*>(stage + i);
+        if (i + 3 >= nsel) {
+          v.x = i < nsel ? v.x : 0xFFFFFFFFu;
+          v.y = i + 1 < nsel ? v.y : 0xFFFFFFFFu;
+          v.z = i + 2 < nsel ? v.z : 0xFFFFFFFFu;
+          v.w = i + 3 < nsel ? v.w : 0xFFFFFFFFu;
+        }
+        *reinterpret_cast<uint4*>(dst + i) = v;
+      }
+    } else {
+      for (int i = tid; i < p.k; i += THREADS) dst[i] = i < nsel ? static_cast<int>(stage[i]) : -1;
+    }
   } else {
     for (int i = nsel + tid; i < p.k; i += THREADS) dst[i] = -1;
   }
