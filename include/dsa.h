@@ -245,10 +245,9 @@ dsa_status_t dsa_indexer_topk_paged(const void* q, const float* q_scale,
  * have no counterpart to this entry point; it is an addition of this library.
  *
  * Some callers have no way to obtain a scratch buffer when they need one:
- * code that runs while a stream is being captured into a CUDA graph without a
- * graph-safe allocator, plugins inside a host framework that owns every
- * device allocation, or latency-critical serving loops that must not pay for
- * cudaMalloc's implicit synchronisation.  This variant keeps its fp32 logits
+ * plugins inside a host framework that owns every device allocation, or
+ * latency-critical serving loops that must not pay for cudaMalloc's implicit
+ * synchronisation.  This variant keeps its fp32 logits
  * in a fixed device array inside the library instead of a caller workspace;
  * it calls no allocator of any kind.
  *   - The array holds DSA_NOALLOC_SCRATCH_BYTES (64 MiB) on every GPU that
@@ -257,8 +256,7 @@ dsa_status_t dsa_indexer_topk_paged(const void* q, const float* q_scale,
  *     DSA_NOALLOC_SCRATCH_BYTES / 4 of them (T = S = 4096 fits); a larger
  *     request returns DSA_ERR_UNSUPPORTED before anything is launched.
  *   - The first call on a device looks up the array's device address (once
- *     per device, under a lock); make that first call before capturing a
- *     stream.
+ *     per device, under a lock).
  *   - Every call on a device uses the same array and leaves its logits there.
  *     Calls whose work overlaps on the GPU (several streams, or several host
  *     threads) race on it and corrupt each other's results: order them on one

@@ -1,10 +1,8 @@
 """dsa_indexer_topk_noalloc, called through the C ABI (needs a GPU).
 
 This entry point serves callers that cannot allocate device memory when they
-call the indexer: code running while its stream is captured (where cudaMalloc
-is not allowed) without a graph-safe allocator at hand, plugins whose host
-framework owns every device allocation, and serving loops that cannot afford
-cudaMalloc's implicit synchronisation.  It keeps the logits in a
+call the indexer: plugins whose host framework owns every device allocation,
+and serving loops that cannot afford cudaMalloc's implicit synchronisation.  It keeps the logits in a
 fixed 64 MiB device array of the library instead of a caller workspace.
 
 The test runs it twice in a row on different inputs (so the second call finds
@@ -69,13 +67,15 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(api):
     assert api.last_device_error() == api.DSA_OK
 
 
-def test_noalloc_matches_where_the_workspace_call_splits_rows(api):
-    # 256 rows of up to 32768 keys: dsa_indexer_topk takes the split top-k
+@pytest.mark.parametrize("T", [24, 256])
+def test_noalloc_matches_where_the_workspace_call_splits_rows(api, T):
+    # 24 rows of up to 32768 keys: dsa_indexer_topk takes the split top-k
     # (many CTAs per row, scratch in its workspace), the no-alloc call the
-    # per-row kernel (its array holds only the logits: 256 * 32768 * 4 bytes
-    # = 32 MiB).  Both must select the same columns, ties and clamped or
-    # empty ranges included.
-    T, S = 256, 32768
+    # 256-thread per-row kernel (its array holds only the logits).  256 rows:
+    # both take one 1024-thread CTA per row (256 * 32768 * 4 bytes = 32 MiB of
+    # logits).  Both must select the same columns, ties and clamped or empty
+    # ranges included.
+    S = 32768
     rng = np.random.default_rng(23)
     rs = rng.integers(-100, S // 2, T).astype(np.int32)
     re = (rs + rng.integers(0, S + 200, T)).astype(np.int32)   # some past S
