@@ -12,21 +12,23 @@
 // needs no scale in the epilogue.
 //
 // Layout of the contraction as in dsa_score.cuh: keys on M (128 TMEM lanes),
-// a group of TOK = 2 query rows x 64 heads on N = 128.  Tensor memory holds
-// two 128-column accumulators and the scale factors of the MMAs in flight:
+// a group of TOK = 3 query rows x 64 heads on N = 192 (four rows would need
+// two 256-column accumulators, all of tensor memory, with no room left for
+// the scales).  Tensor memory holds two 192-column accumulators and the scale
+// factors of the MMAs in flight:
 //   A (keys)     a row's four scale bytes, copied to 4 columns of its lane
 //   B (queries)  lane 32q + i, column j holds row 32j + i's four scale bytes
-//                for every lane quarter q
+//                for every lane quarter q (columns 0-5: two copies of 4)
 // (the layouts the block-scaled MMA reads; the copies come from shared-memory
 // rows that the producer warp fills with tcgen05.cp.128x128b).
 //
-// Roles (576 threads):
+// Roles (448 threads: 14 warps, so 128 registers a thread):
 //   warp 0      producer: scale rows (plain loads + shared stores) and TMA
 //               boxes of packed E2M1 rows (64-byte swizzle) for q and K
 //   warp 1      TMEM allocator; one thread copies the scale factors and
 //               issues two K=64 block-scaled MMAs per 128-key tile
-//   warps 2-17  two epilogue sets of two warpgroups (one per token); the sets
-//               take alternate tiles, each on its own accumulator
+//   warps 2-13  three epilogue warpgroups (one per token) on the same tile,
+//               the MMA of the next tile filling the other accumulator
 #pragma once
 
 #include "dsa_score.cuh"
@@ -36,12 +38,12 @@ namespace dsa {
 struct MxCfg {
   static constexpr int H = 64;
   static constexpr int D = 128;
-  static constexpr int TOK = 2;
+  static constexpr int TOK = 3;
   static constexpr int N = TOK * H;            // 128 MMA columns
   static constexpr int TILE = 128;             // keys per tile (MMA M)
   static constexpr int ROW_BYTES = D / 2;      // packed E2M1
   static constexpr int KSTEPS = D / 64;        // K = 64 elements per MMA
-  static constexpr int SETS = 2;               // epilogue sets (alternate tiles)
+  static constexpr int SETS = 1;               // epilogue sets (alternate tiles)
   static constexpr int EPI_WARPS = 4 * TOK * SETS;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   static constexpr int Q_BYTES = N * ROW_BYTES;          // 8 KB
@@ -50,14 +52,15 @@ struct MxCfg {
   // tensor memory columns
   static constexpr uint32_t COL_ACC = 0;                 // two accumulators of N
   static constexpr uint32_t COL_SFA = 2 * N;             // two 4-column blocks
-  static constexpr uint32_t COL_SFB = COL_SFA + 8;       // two 4-column blocks
+  static constexpr int NSFB = (N + 127) / 128;           // B-scale copies per q buffer
+  static constexpr uint32_t COL_SFB = COL_SFA + 8;       // two blocks of NSFB x 4 columns
   static constexpr uint32_t TMEM_COLS = 512;
   // shared memory: q[2] | K stages | sfb[2] | sfa stages | misc
   static constexpr int NST = 8;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
   static constexpr int OFF_SFB = OFF_K + NST * STAGE_BYTES;
-  static constexpr int OFF_SFA = OFF_SFB + 2 * SF_BYTES;
+  static constexpr int OFF_SFA = OFF_SFB + 2 * NSFB * SF_BYTES;
   static constexpr int OFF_W = OFF_SFA + NST * SF_BYTES;     // N floats
   static constexpr int OFF_RANGE = OFF_W + N * 4;            // TOK lo, TOK hi
   static constexpr int OFF_BARS = OFF_RANGE + 64;
@@ -67,7 +70,7 @@ struct MxCfg {
 
   static_assert(Q_BYTES % 1024 == 0 && STAGE_BYTES % 1024 == 0, "swizzle atoms");
   static_assert(SMEM <= 232448, "shared memory");
-  static_assert(COL_SFB + 8 <= TMEM_COLS, "tensor memory");
+  static_assert(COL_SFB + 8 * NSFB <= TMEM_COLS, "tensor memory");
 };
 
 // Shared-memory matrix descriptor of a K-major operand in the 64-byte
@@ -196,15 +199,20 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
       {
         // Query scales: lane 32q + i, column j <- q row 32j + i, for every q.
         const int64_t r0 = static_cast<int64_t>(g.row0) * C::H;
-        uint32_t wv[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int64_t row = r0 + 32 * j + lane;
-          wv[j] = row < qrows ? __ldg(q_sf + row) : 0x7F7F7F7Fu;
+        for (int cc = 0; cc < C::NSFB; ++cc) {
+          uint32_t wv[4];
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const int n = 128 * cc + 32 * jj + lane;
+            const int64_t row = r0 + n;
+            wv[jj] = (n < C::N && row < qrows) ? __ldg(q_sf + row) : 0x7F7F7F7Fu;
+          }
+          uint4* dst = reinterpret_cast<uint4*>(sfb_s + (qb * C::NSFB + cc) * C::SF_BYTES);
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq)
+            dst[32 * qq + lane] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
         }
-        uint4* dst = reinterpret_cast<uint4*>(sfb_s + qb * C::SF_BYTES);
-#pragma unroll
-        for (int qq = 0; qq < 4; ++qq) dst[32 * qq + lane] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
@@ -272,7 +280,7 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
         const int qb = ngroups & 1;
         ok = mbar_wait_bounded(&qfull[qb], static_cast<uint32_t>(ngroups >> 1) & 1u, abort_flag);
         const uint32_t q_addr = smem_u32(q_s + qb * C::Q_BYTES);
-        const uint32_t sfb_t = tmem_base + C::COL_SFB + static_cast<uint32_t>(4 * qb);
+        const uint32_t sfb_t = tmem_base + C::COL_SFB + static_cast<uint32_t>(4 * C::NSFB * qb);
         bool first = true;
         for (int kt = g.kt_begin; ok && kt < g.kt_end; ++kt) {
           const int stage = kiter % C::NST;
@@ -288,7 +296,10 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
           const uint32_t sfa_t = tmem_base + C::COL_SFA + static_cast<uint32_t>(4 * buf);
           tmem_cp_128x128b(sfa_t, rows16_desc(smem_u32(sfa_s + stage * C::SF_BYTES)));
           if (first) {
-            tmem_cp_128x128b(sfb_t, rows16_desc(smem_u32(sfb_s + qb * C::SF_BYTES)));
+#pragma unroll
+            for (int cc = 0; cc < C::NSFB; ++cc)
+              tmem_cp_128x128b(sfb_t + 4u * cc,
+                               rows16_desc(smem_u32(sfb_s + (qb * C::NSFB + cc) * C::SF_BYTES)));
             first = false;
           }
           const uint32_t d_tmem = tmem_base + C::COL_ACC + static_cast<uint32_t>(buf * C::N);
@@ -361,7 +372,7 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
       int tc = tcount + skip;
       tcount += ntile;
       for (int kt = g.kt_begin + skip; ok && kt < g.kt_end; kt += C::SETS, tc += C::SETS) {
-        const int buf = tc & 1;  // == set
+        const int buf = tc & 1;  // the accumulator of this tile
         ok = __all_sync(0xffffffffu,
                         mbar_wait_bounded(&accf[buf], static_cast<uint32_t>(tc >> 1) & 1u,
                                           abort_flag)
@@ -376,45 +387,44 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
         float2 acc4[4], acc4b[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc4[i] = acc4b[i] = make_float2(0.f, 0.f);
-        uint32_t cur[16], nxt[16];
-        // Chunk c: one 16x256b.x4 load, lanes +16(c & 1), heads 32(c >> 1) ..
-        tmem_ld16x256_x4_async(cb + l0, cur);
+        auto sum_chunk = [&](const uint32_t* v, int c) {
+          const int hf = c & 1;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          tmem_wait_ld16(cur);
-          if (c == 3) {
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acce[buf]);
-          } else {
-            const int cn = c + 1;
-            tmem_ld16x256_x4_async(
-                cb + ((cn & 1) ? l1 : l0) + static_cast<uint32_t>(32 * (cn >> 1)), nxt);
-          }
-          {
-            const int hf = c & 1;
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-              const int rep = jj & 1;
-              const int r0 = 4 * jj;
-              const float2 w2 = wq[4 * (c >> 1) + jj];
-              const float2 xa = make_float2(__uint_as_float(cur[r0]), __uint_as_float(cur[r0 + 1]));
-              const float2 xb =
-                  make_float2(__uint_as_float(cur[r0 + 2]), __uint_as_float(cur[r0 + 3]));
-              const float2 ya = __fadd2_rn(xa, make_float2(fabsf(xa.x), fabsf(xa.y)));
-              const float2 yb = __fadd2_rn(xb, make_float2(fabsf(xb.x), fabsf(xb.y)));
-              if (rep == 0) {
-                acc4[2 * hf] = __ffma2_rn(w2, ya, acc4[2 * hf]);
-                acc4[2 * hf + 1] = __ffma2_rn(w2, yb, acc4[2 * hf + 1]);
-              } else {
-                acc4b[2 * hf] = __ffma2_rn(w2, ya, acc4b[2 * hf]);
-                acc4b[2 * hf + 1] = __ffma2_rn(w2, yb, acc4b[2 * hf + 1]);
-              }
+          for (int jj = 0; jj < 4; ++jj) {
+            const int rep = jj & 1;
+            const int r0 = 4 * jj;
+            const float2 w2 = wq[4 * (c >> 1) + jj];
+            const float2 xa = make_float2(__uint_as_float(v[r0]), __uint_as_float(v[r0 + 1]));
+            const float2 xb = make_float2(__uint_as_float(v[r0 + 2]), __uint_as_float(v[r0 + 3]));
+            const float2 ya = __fadd2_rn(xa, make_float2(fabsf(xa.x), fabsf(xa.y)));
+            const float2 yb = __fadd2_rn(xb, make_float2(fabsf(xb.x), fabsf(xb.y)));
+            if (rep == 0) {
+              acc4[2 * hf] = __ffma2_rn(w2, ya, acc4[2 * hf]);
+              acc4[2 * hf + 1] = __ffma2_rn(w2, yb, acc4[2 * hf + 1]);
+            } else {
+              acc4b[2 * hf] = __ffma2_rn(w2, ya, acc4b[2 * hf]);
+              acc4b[2 * hf + 1] = __ffma2_rn(w2, yb, acc4b[2 * hf + 1]);
             }
           }
-#pragma unroll
-          for (int i = 0; i < 16; ++i) cur[i] = nxt[i];
-        }
+        };
+        // Chunk c: one 16x256b.x4 load, lanes +16(c & 1), heads 32(c >> 1) ..;
+        // two chunks a batch: chunks 2-3 load while 0-1 are summed.
+        uint32_t va[16], vb[16], vc[16], vd[16];
+        tmem_ld16x256_x4_async(cb + l0, va);
+        tmem_ld16x256_x4_async(cb + l1, vb);
+        tmem_wait_ld16(va);
+        tmem_tie16(vb);
+        tmem_ld16x256_x4_async(cb + l0 + 32u, vc);
+        tmem_ld16x256_x4_async(cb + l1 + 32u, vd);
+        sum_chunk(va, 0);
+        sum_chunk(vb, 1);
+        tmem_wait_ld16(vc);
+        tmem_tie16(vd);
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acce[buf]);
+        sum_chunk(vc, 2);
+        sum_chunk(vd, 3);
         float tot[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
