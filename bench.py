@@ -60,6 +60,11 @@ PROFILES = {
                        ("top_selection_dsa_gb300/csrc/dsa_score.cuh",
                         "top_selection_dsa_gb300/csrc/dsa_common.cuh",
                         "top_selection_dsa_gb300/csrc/dsa_score_prefill_bf16.cu")),
+    "prefill_mxfp4": ("score_prefill_mxfp4_T32768_H64_D128.md",
+                      ("top_selection_dsa_gb300/csrc/dsa_score_mx.cuh",
+                       "top_selection_dsa_gb300/csrc/dsa_score.cuh",
+                       "top_selection_dsa_gb300/csrc/dsa_common.cuh",
+                       "top_selection_dsa_gb300/csrc/dsa_score_prefill_mxfp4.cu")),
 }
 # Rows of the CPU oracle sample for cpu_baseline (about 10-30 s of the host's
 # cores); the reference arm times an eighth of it per step.
