@@ -289,8 +289,9 @@ dsa_status_t dsa_indexer_topk_noalloc(const void* q, const float* q_scale, const
  *   - The rows are split into up to 12 chunks (whole rounds of the scoring
  *     kernel, 256/H rows times the current device's SM count, where a chunk
  *     holds one; else multiples of 64 rows; about 512 or more each), the
- *     remainder first; so dsa_indexer_topk_host_bytes is for the current
- *     device.  K, the key scales and the row ranges go up first;
+ *     remainder first; with three or more, the first and the last are cut
+ *     down to one round (or 64 rows) each, the rest of each a chunk of its
+ *     own.  So dsa_indexer_topk_host_bytes is for the current device.  K, the key scales and the row ranges go up first;
  *     then chunk c's queries and weights go up while chunk c-1 is scored and
  *     selected (on `stream`) and chunk c-2's indices come down, on two
  *     streams the call creates and destroys.  Work queued on

@@ -269,23 +269,48 @@ def test_indexer_topk_host_validation(api):
     assert f(A, NUL, NUL, NUL, 0, A, A, A, 8, 8, 64, 128, 2, A, A, n, NUL) == E   # keys, no k
 
 
+def host_chunks(T, unit=64):
+    """Row chunks of dsa_indexer_topk_host with no device: up to 12 chunks of
+    a multiple of 64 rows, at least 512 rows each where T allows, the
+    remainder first; with three or more, the first and the last cut down to
+    one unit (the rest of each a chunk of its own)."""
+    if T <= 0:
+        return []
+    nch = min(12, -(-T // 512))
+    chunk = max(1, -(-(-(-T // nch)) // unit) * unit)
+    first = T - (T - 1) // chunk * chunk
+    nfull = (T - first) // chunk
+    cut = nfull >= 2
+    bounds = [0] + ([unit] if cut and first > unit else []) + [first]
+    for c in range(1, nfull + 1):
+        if cut and c == nfull and chunk > unit:
+            bounds.append(T - unit)
+        bounds.append(first + c * chunk)
+    return [b - a for a, b in zip(bounds, bounds[1:])]
+
+
+def test_host_chunks_cover_the_rows():
+    for T in (1, 63, 64, 511, 512, 700, 1536, 4096, 4700, 32768, 100000):
+        sizes = host_chunks(T)
+        assert sum(sizes) == T and min(sizes) > 0 and len(sizes) <= 14
+        if len(sizes) >= 4:
+            assert sizes[0] == 64 and sizes[-1] == 64
+    assert host_chunks(32768) == [64, 2496 - 64] + [2752] * 10 + [2752 - 64, 64]
+    assert host_chunks(32768, unit=608) == [608, 2368 - 608] + [3040] * 9 + [3040 - 608, 608]
+
+
 def test_indexer_topk_host_bytes_layout(api):
     # The device buffer holds every input and the indices, then one row
-    # chunk's workspace: up to 12 chunks of a multiple of 64 rows with no
-    # device (whole scoring rounds on one), at least 512 rows each where T
-    # allows, sized for the larger of a full chunk and the first one, which
-    # holds the remainder (a short chunk of long rows takes the split top-k).
+    # chunk's workspace, sized for the largest need over the chunks (a short
+    # chunk of long rows can take the split top-k).
     ws = lambda rows, S, k: api.lib.dsa_workspace_bytes(api.DSA_OP_INDEXER_TOPK, rows, S, k)  # noqa: E731
     up = lambda x: -(-x // 256) * 256  # noqa: E731
 
     def expect(T, S, H, D, k, dtype):
         esz = 1 if dtype == api.DSA_E4M3 else 2
-        nch = min(12, -(-T // 512)) if T > 0 else 1
-        chunk = max(1, -(-(-(-T // nch)) // 64) * 64) if T > 0 else 1
-        full = min(chunk, T) if T > 0 else 1
-        last = T - (T - 1) // chunk * chunk if T > 0 else 1
+        need = max([ws(1, S, k)] + [ws(r, S, k) for r in host_chunks(T)])
         regions = [S * D * esz, S * 4 if dtype == api.DSA_E4M3 else 0, T * H * D * esz, T * H * 4,
-                   T * H * 4, T * 4, T * 4, T * k * 4, max(ws(full, S, k), ws(last, S, k))]
+                   T * H * 4, T * 4, T * 4, T * k * 4, need]
         return sum(up(r) for r in regions)
 
     nb = api.lib.dsa_indexer_topk_host_bytes
@@ -296,12 +321,13 @@ def test_indexer_topk_host_bytes_layout(api):
                               (1, 5, 1, 64, 1, api.DSA_BF16),
                               (0, 64, 8, 64, 16, api.DSA_BF16)]:
         assert nb(T, S, H, D, k, dt) == expect(T, S, H, D, k, dt), (T, S)
-    # 4700 rows: a first chunk of 92 and nine of 512, which the top-k takes
-    # with one 1024-thread CTA per row (32-512 rows, columns > 16384): no
-    # split scratch
-    assert api.lib.dsa_workspace_bytes(api.DSA_OP_TOPK, 92, 40000, 2048) == 0
+    # 4700 rows: chunks of 64, 28, 8 x 512, 448 and 64 rows, which the
+    # top-k takes with one 1024-thread CTA per row (32-512 rows, columns >
+    # 16384), except the 28-row chunk: split scratch
+    assert host_chunks(4700) == [64, 28] + [512] * 8 + [448, 64]
+    assert api.lib.dsa_workspace_bytes(api.DSA_OP_TOPK, 64, 40000, 2048) == 0
     assert api.lib.dsa_workspace_bytes(api.DSA_OP_TOPK, 512, 40000, 2048) == 0
-    assert api.lib.dsa_workspace_bytes(api.DSA_OP_TOPK, 20, 40000, 2048) > 0
+    assert api.lib.dsa_workspace_bytes(api.DSA_OP_TOPK, 28, 40000, 2048) > 0
 
 
 def mx_call(api, q=A, qsf=A, k=A, ksf=A, w=A, rs=A, re=A, T=8, S=8, H=64, D=128, lg=A, ld=8,

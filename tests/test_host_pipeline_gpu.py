@@ -76,9 +76,10 @@ def test_e4m3_with_key_scales_equals_device_entry_point(api):
 
 
 def test_chunks_of_few_long_rows(api):
-    # 4700 rows of up to 40000 keys in chunks of at most 512 rows (a short
-    # first one), which the top-k takes with one 1024-thread CTA per row; the
-    # device entry point runs all 4700 rows on 256-thread CTAs.
+    # 4700 rows of up to 40000 keys in chunks of at most 512 rows, which the
+    # top-k takes with one 1024-thread CTA per row, but for a 28-row chunk
+    # that takes the split top-k; the device entry point runs all 4700 rows
+    # on 256-thread CTAs.
     T, S = 4700, 40000
     rng = np.random.default_rng(7)
     ends = rng.integers(1, S + 1, size=T).astype(np.int32)

@@ -506,8 +506,8 @@ namespace {
 // Device-buffer layout of dsa_indexer_topk_host: the inputs, the indices, and
 // one chunk's workspace, each region 256-byte aligned.
 struct HostPlan {
-  int64_t chunk;  // rows per chunk
-  int64_t first;  // rows of the first chunk (the remainder)
+  int64_t chunk;                // rows per full chunk
+  std::vector<int64_t> bounds;  // chunk c holds rows [bounds[c], bounds[c+1])
   size_t k, ks, q, qs, w, rs, re, out, ws, total;
 };
 
@@ -524,9 +524,25 @@ HostPlan host_plan(int T, int S, int H, int D, int topk, dsa_dtype_t dtype, bool
   const int64_t even = (static_cast<int64_t>(T) + nchunks - 1) / nchunks;
   const int64_t round_rows =
       static_cast<int64_t>(score_tokens_per_group(H)) * std::max(device_sm_count(), 0);
-  pl.chunk = std::max<int64_t>(
-      1, round_up(even, round_rows > 0 && round_rows <= even ? round_rows : 64));
-  pl.first = T > 0 ? T - (T - 1) / pl.chunk * pl.chunk : 1;
+  const int64_t unit = round_rows > 0 && round_rows <= even ? round_rows : 64;
+  pl.chunk = std::max<int64_t>(1, round_up(even, unit));
+  // The remainder first, then full chunks; with three or more chunks the
+  // first and the last are cut down to one unit each (the rest of each
+  // becomes a chunk of its own): the pipeline waits for the first chunk's
+  // upload before anything is scored and for the last chunk's download after
+  // everything is, so both are kept short.
+  const int64_t first = T > 0 ? T - (T - 1) / pl.chunk * pl.chunk : 1;
+  pl.bounds.push_back(0);
+  if (T > 0) {
+    const int64_t nfull = (T - first) / pl.chunk;
+    const bool cut = nfull >= 2;
+    if (cut && first > unit) pl.bounds.push_back(unit);
+    pl.bounds.push_back(first);
+    for (int64_t c = 1; c <= nfull; ++c) {
+      if (cut && c == nfull && pl.chunk > unit) pl.bounds.push_back(T - unit);
+      pl.bounds.push_back(first + c * pl.chunk);
+    }
+  }
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t at = off;
@@ -543,9 +559,12 @@ HostPlan host_plan(int T, int S, int H, int D, int topk, dsa_dtype_t dtype, bool
   pl.out = take(static_cast<size_t>(T) * topk * 4);
   // The chunks share one workspace; a short last chunk may take the split
   // top-k path (more scratch per row) where a full one does not.
-  const int64_t full = std::min<int64_t>(pl.chunk, T > 0 ? T : 1);
-  pl.ws = take(std::max(dsa_workspace_bytes(DSA_OP_INDEXER_TOPK, full, S, topk),
-                        dsa_workspace_bytes(DSA_OP_INDEXER_TOPK, pl.first, S, topk)));
+  size_t ws = dsa_workspace_bytes(DSA_OP_INDEXER_TOPK, 1, S, topk);
+  for (size_t c = 0; c + 1 < pl.bounds.size(); ++c)
+    ws = std::max(ws, dsa_workspace_bytes(DSA_OP_INDEXER_TOPK,
+                                          static_cast<int>(pl.bounds[c + 1] - pl.bounds[c]), S,
+                                          topk));
+  pl.ws = take(ws);
   pl.total = off;
   return pl;
 }
@@ -592,7 +611,7 @@ dsa_status_t dsa_indexer_topk_host(const void* q, const float* q_scale, const vo
   int32_t* out_d = reinterpret_cast<int32_t*>(base + pl.out);
   void* ws_d = base + pl.ws;
   const int64_t ld = round_up(S > 0 ? S : 1, 4);
-  const int64_t nch = (T + pl.chunk - 1) / pl.chunk;
+  const int64_t nch = static_cast<int64_t>(pl.bounds.size()) - 1;
 
   // Three streams: uploads, compute (the caller's), downloads.  Chunk c's
   // upload overlaps chunk c-1's compute and chunk c-2's download.
@@ -630,8 +649,8 @@ dsa_status_t dsa_indexer_topk_host(const void* q, const float* q_scale, const vo
   if (e == cudaSuccess) e = cudaEventRecord(k_in, up);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(comp, k_in, 0);
   for (int64_t c = 0; c < nch && e == cudaSuccess && st == DSA_OK; ++c) {
-    const int64_t r0 = c == 0 ? 0 : pl.first + (c - 1) * pl.chunk;
-    const int64_t rows = c == 0 ? pl.first : pl.chunk;
+    const int64_t r0 = pl.bounds[c];
+    const int64_t rows = pl.bounds[c + 1] - r0;
     const int64_t qe = static_cast<int64_t>(H) * D;
     cudaEvent_t in = event(), computed = event();
     if (!in || !computed) {
