@@ -248,7 +248,9 @@ __device__ __forceinline__ uint32_t chunk_key(float x) {
 // would have: no key takes that value, so 0x7FFFFFFE stands in for it), and
 // x == key_float(t) exactly when chunk_key(x) == t, for t the key of some
 // value.  A NaN compares false, as its key, kNoKey, is below every bound.
-// Past the key of +inf the result is a NaN, which no x exceeds.
+// Past the key of +inf the result is a NaN, which no x exceeds.  Subnormal
+// bounds and values compare exactly because this file is built without
+// flush-to-zero (no -ftz / --use_fast_math).
 __device__ __forceinline__ float key_float(uint32_t key) {
   return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
