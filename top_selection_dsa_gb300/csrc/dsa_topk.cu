@@ -354,7 +354,6 @@ __global__ void __launch_bounds__(THREADS, MINB) topk_rows_kernel(const TopkPara
   __shared__ __align__(16) uint32_t wsum[NW];
   __shared__ uint2 warp_sums[NW];
   __shared__ uint32_t sel[4];
-  __shared__ uint32_t ncand;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // Last row first: under a causal mask the rows grow with their index, so
@@ -407,7 +406,6 @@ __global__ void __launch_bounds__(THREADS, MINB) topk_rows_kernel(const TopkPara
   } else {
     for (int i = tid; i < kHistBins / 4; i += THREADS)
       reinterpret_cast<uint4*>(hist)[i] = make_uint4(0u, 0u, 0u, 0u);
-    if (tid == 0) ncand = 0u;
     __syncthreads();
     // Pass 1: the top 11 key bits (bin 3 collects the invalid slots).  A row
     // of several chunks is read from memory (HBM) here: the next chunk's
