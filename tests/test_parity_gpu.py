@@ -252,6 +252,28 @@ def test_topk_threshold_bin_at_value_edges(api, S, T):
     assert np.array_equal(got, oracle.topk(lg, rs, re, k))
 
 
+# A row of several chunks goes out from shared memory four columns a store
+# when k is a multiple of 4 and the output row is 16-byte aligned, else one
+# column a store: k = 6 and 2050, and k = 2048 into an output that starts 4
+# bytes past a 16-byte boundary, each with rows shorter than k (padding) and
+# a NaN-heavy row.
+@pytest.mark.parametrize("k,offset", [(6, 0), (2050, 0), (2048, 1), (2048, 0)])
+def test_topk_output_store_widths(api, k, offset):
+    rng = np.random.default_rng(k + offset)
+    T, S = 40, 10000
+    lg = rng.standard_normal((T, S)).astype(np.float32)
+    lg[5] = np.round(lg[5] * 2) / 2                       # ties
+    lg[6, rng.random(S) < 0.9] = np.nan                   # about 1000 valid keys
+    rs = np.zeros(T, np.int32)
+    re = np.full(T, S, np.int32)
+    re[7], rs[9], re[11] = 3000, 5000, 1500               # 1500 keys: fewer than k
+    flat = torch.full((T * k + 4,), 7, dtype=torch.int32, device="cuda")
+    out = flat[offset:offset + T * k].view(T, k)
+    got = api.topk(dev(lg), dev(rs), dev(re), k, out=out).cpu().numpy()
+    assert np.array_equal(got, oracle.topk(lg, rs, re, k))
+    assert (flat[:offset] == 7).all() and (flat[offset + T * k:] == 7).all()
+
+
 # Rows of at most 4096 columns take the persistent short-row kernel, which
 # loops over rows (more rows than its CTAs here) and prefetches two rows ahead:
 # every edge case on many rows, with ranges and garbage around them.
