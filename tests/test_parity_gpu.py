@@ -411,7 +411,7 @@ def test_paged_small(api, next_n, block_size, H, fp8):
 # to 64 heads.
 @pytest.mark.parametrize("next_n,block_size,H,fp8", [(1, 16, 64, False), (2, 64, 64, True),
                                                      (4, 32, 8, False), (3, 128, 16, True),
-                                                     (5, 64, 32, False)])
+                                                     (5, 64, 32, False), (4, 64, 64, True)])
 def test_paged_split_topk(api, next_n, block_size, H, fp8):
     ctx = np.array([0, 1, next_n, 4097, 16385, 20003, 33000, 40960], np.int32)
     p = wl.paged_decode(next_n=next_n, block_size=block_size, H=H, D=128, topk=2048,
